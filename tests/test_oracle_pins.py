@@ -1,0 +1,393 @@
+"""Pins for the float64 oracle: page-printed values, closed forms, invariants, brute force.
+
+Every pin is a function of the oracle module ``O`` so that ``test_oracle_mutations``
+can run the same checks against copies of the oracle with a planted mistake and show
+that each mistake is caught.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import gptq_oracle as ORACLE
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_example_4x4.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    return {k: (np.array(v["value"], dtype=float) if isinstance(v, dict) else v)
+            for k, v in g.items()}
+
+
+def page_column_quantizer(seen=None):
+    """The 4x4 example's grid: one symmetric scale per column, max|col| / 7, codes in
+    [-7, 7] ("Same Ruler", section 1.11), in the page's (float64) hand arithmetic."""
+    def q(col_idx, w):
+        if seen is not None:
+            seen[col_idx] = w.copy()
+        delta = np.max(np.abs(w)) / 7.0
+        c = np.rint(w / delta)
+        return c.astype(np.int64), c * delta
+    return q
+
+
+def spd(rng, d, n=None):
+    n = 4 * d if n is None else n
+    X = rng.standard_normal((n, d)) * np.exp(rng.standard_normal(d))
+    return 2.0 / n * X.T @ X, X
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_worked_example(O):
+    g = golden()
+    W = g["W_columns"].T.copy()
+    sX = g["s_X"]
+    assert np.allclose(W @ sX, g["y_true"], atol=6e-4)
+    for B in (1, 2, 4):
+        seen = {}
+        res = O.gptq_sweep(W, g["Hinv_2dp"], blocksize=B,
+                           column_quantizer=page_column_quantizer(seen))
+        assert np.array_equal(res["codes"].T, g["codes_per_column"]), B
+        # the column each step sees, against W^(1), W^(2) and the adjusted column 3
+        assert np.allclose(seen[1], g["W1"][:, 1], atol=1.5e-4)
+        assert np.allclose(seen[2], g["W2"][:, 2], atol=1.5e-4)
+        assert np.allclose(seen[3], [0.1084, -0.0696, 0.1023, 0.0066], atol=1.5e-4)
+        assert np.allclose(res["Q"], g["W_hat_gptq"], atol=1.5e-4)
+        yhat = res["Q"] @ sX
+        assert np.allclose(yhat, g["y_hat_gptq"], atol=1.5e-3)
+        loss = float(np.sum((yhat - W @ sX) ** 2))
+        assert abs(loss - g["loss_gptq_text"]) < 1e-3
+
+
+def pin_rtn_per_column():
+    g = golden()
+    W = g["W_columns"].T.copy()
+    q = page_column_quantizer()
+    Q = np.stack([q(j, W[:, j])[1] for j in range(4)], axis=1)
+    yhat = Q @ g["s_X"]
+    assert np.allclose(yhat, g["y_hat_rtn_col"], atol=1e-3)
+    assert abs(np.sum((yhat - W @ g["s_X"]) ** 2) - g["loss_rtn_col"]) < 1e-3
+
+
+def pin_conditioned_example(O):
+    """True GPTQ on the printed H (conditioned inverse) differs from the page's
+    illustration at one code only: column 3, row 2 becomes 6."""
+    g = golden()
+    W = g["W_columns"].T.copy()
+    for Hd in (g["H"], O.damping(g["H"], 0.01)[0]):
+        U = O.inverse_cholesky_upper(Hd)
+        a = O.gptq_sweep(W, U, blocksize=4, column_quantizer=page_column_quantizer())
+        b = O.gptq_sweep_obs(W, Hd, column_quantizer=page_column_quantizer())
+        assert np.array_equal(a["codes"], b["codes"])
+        assert np.allclose(a["loss_rows"], b["loss_rows"], rtol=1e-10, atol=1e-14)
+        expect = g["codes_per_column"].T.copy()
+        expect[2, 3] = 6
+        assert np.array_equal(a["codes"], expect)
+
+
+def pin_two_weight_closed_form(O):
+    """d_in = 2: after quantising column 0, w1 moves by (w0 - what0) H01 / H11 and the
+    column-0 loss is (w0 - what0)^2 / (2 [H^-1]_00) ("Same Ruler", section 1.5;
+    "04 - GPTQ", section 2); column 1 then has conditional inverse 1 / H11."""
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        H, _ = spd(rng, 2)
+        W = rng.standard_normal((5, 2)) * 0.3
+        delta = 0.05
+
+        def quant(q, w):
+            c = np.rint(w / delta)
+            return c.astype(np.int64), c * delta
+
+        seen = {}
+
+        def rec(q, w):
+            seen[q] = w.copy()
+            return quant(q, w)
+
+        for res in (O.gptq_sweep(W, O.inverse_cholesky_upper(H), blocksize=1,
+                                 column_quantizer=rec),
+                    O.gptq_sweep_obs(W, H, column_quantizer=rec)):
+            e0 = W[:, 0] - np.rint(W[:, 0] / delta) * delta
+            w1 = W[:, 1] + e0 * H[0, 1] / H[1, 1]
+            assert np.allclose(seen[1], w1, rtol=1e-12, atol=1e-14)
+            hinv00 = H[1, 1] / (H[0, 0] * H[1, 1] - H[0, 1] ** 2)
+            e1 = w1 - np.rint(w1 / delta) * delta
+            loss = e0 ** 2 / (2 * hinv00) + e1 ** 2 * H[1, 1] / 2
+            assert np.allclose(res["loss_rows"], loss, rtol=1e-10, atol=1e-16)
+
+
+def pin_cholesky_2x2(O):
+    """U for a 2x2 H^-1 = [[a, b], [b, c]]: u00 = sqrt(a), u01 = b / sqrt(a),
+    u11 = sqrt(c - b^2 / a) ("Same Ruler", section 1.7)."""
+    rng = np.random.default_rng(3)
+    for _ in range(10):
+        H, _ = spd(rng, 2)
+        Hinv = np.linalg.inv(H)
+        a, b, c = Hinv[0, 0], Hinv[0, 1], Hinv[1, 1]
+        U = O.inverse_cholesky_upper(H)
+        assert np.allclose(U, [[np.sqrt(a), b / np.sqrt(a)], [0.0, np.sqrt(c - b * b / a)]],
+                           rtol=1e-12)
+
+
+def pin_cholesky_general(O):
+    """Row q of U carries the conditional inverse at step q: u_qq^2 = [H_c^-1]_qq and
+    u_qj / u_qq = [H_c^-1]_qj / [H_c^-1]_qq ("Same Ruler", section 1.7, 'The general
+    pattern'); U agrees with the reversed-order Cholesky route U = J chol(J H J)^-1 J."""
+    rng = np.random.default_rng(11)
+    d = 24
+    H, _ = spd(rng, d)
+    Hd, _ = O.damping(H, 0.01)
+    U = O.inverse_cholesky_upper(Hd)
+    assert np.allclose(np.tril(U, -1), 0)
+    assert np.all(np.diag(U) > 0)
+    assert np.allclose(U.T @ U @ Hd, np.eye(d), atol=1e-10)
+    Hc = np.linalg.inv(Hd)
+    for q in range(d):
+        assert np.isclose(U[q, q] ** 2, Hc[0, 0], rtol=1e-10)
+        assert np.allclose(U[q, q + 1:] / U[q, q], Hc[0, 1:] / Hc[0, 0], rtol=1e-9, atol=1e-12)
+        Hc = Hc[1:, 1:] - np.outer(Hc[1:, 0], Hc[0, 1:]) / Hc[0, 0]
+    J = np.eye(d)[::-1]
+    Lr = np.linalg.cholesky(J @ Hd @ J)
+    assert np.allclose(J @ np.linalg.inv(Lr) @ J, U, rtol=1e-9, atol=1e-12)
+
+
+def _small_layer(rng, m, d, n=None):
+    H, X = spd(rng, d, n)
+    W = rng.standard_normal((m, d)) * 0.02
+    return W, H, X
+
+
+def pin_obs_equals_cholesky(O):
+    """The OBQ-style explicit-inverse loop and the Cholesky-row loop agree."""
+    rng = np.random.default_rng(5)
+    for bits, group, sym in [(4, -1, False), (3, 4, False), (4, 8, True), (2, 4, True)]:
+        W, H, _ = _small_layer(rng, 6, 16)
+        Hd, _ = O.damping(H, 0.01)
+        U = O.inverse_cholesky_upper(Hd)
+        a = O.gptq_sweep(W, U, bits, group, sym, blocksize=10 ** 9)
+        b = O.gptq_sweep_obs(W, Hd, bits, group, sym)
+        assert np.array_equal(a["codes"], b["codes"])
+        assert np.allclose(a["loss_rows"], b["loss_rows"], rtol=1e-10)
+        assert np.allclose(a["scales"], b["scales"], rtol=1e-6)
+
+
+def pin_blocked_equals_unblocked(O):
+    """Lazy batching changes only when updates are applied ("Same Ruler", section 1.8)."""
+    rng = np.random.default_rng(9)
+    for bits, group, sym in [(4, -1, False), (4, 8, False), (3, 4, True), (4, 16, False)]:
+        W, H, _ = _small_layer(rng, 7, 48)
+        U = O.inverse_cholesky_upper(O.damping(H, 0.01)[0])
+        ref = O.gptq_sweep(W, U, bits, group, sym, blocksize=10 ** 9)
+        for B in (1, 4, 8, 16, 128):
+            if group != -1 and group % B and B % group:
+                continue
+            r = O.gptq_sweep(W, U, bits, group, sym, blocksize=B)
+            assert np.array_equal(r["codes"], ref["codes"]), (B, group)
+            assert np.allclose(r["loss_rows"], ref["loss_rows"], rtol=1e-10)
+            assert np.array_equal(r["zeros"], ref["zeros"])
+
+
+def pin_loss_identity(O):
+    """sum e^2/2 over a row equals 1/2 delta^T H_damp delta with delta = what - w."""
+    rng = np.random.default_rng(13)
+    for bits, group, sym in [(4, 8, False), (3, -1, True)]:
+        W, H, _ = _small_layer(rng, 5, 32)
+        Hd, _ = O.damping(H, 0.01)
+        r = O.gptq_sweep(W, O.inverse_cholesky_upper(Hd), bits, group, sym, blocksize=8)
+        assert np.allclose(r["loss_rows"], O.quadratic_loss(r["Q"] - W, Hd), rtol=1e-9)
+
+
+def pin_brute_force_optimum(O):
+    """d_in <= 6: the exhaustive minimum of the layer loss ||W X - What X||^2 over every
+    assignment on GPTQ's own grid is never above GPTQ's loss."""
+    rng = np.random.default_rng(17)
+    d, bits = 5, 3
+    maxq = (1 << bits) - 1
+    grid_codes = np.stack(np.meshgrid(*[np.arange(maxq + 1)] * d, indexing="ij"), -1)
+    grid_codes = grid_codes.reshape(-1, d)
+    for trial in range(6):
+        W, H, X = _small_layer(rng, 3, d, n=12)
+        r = O.gptq_layer(W, H, bits=bits, group=-1, sym=False, actorder=bool(trial % 2),
+                         damp=0.01, blocksize=128)
+        for row in range(W.shape[0]):
+            s = float(r["scales"][0, row])
+            z = int(r["zeros"][0, row])
+            cand = s * (grid_codes - z)                       # all grid points, [N, d]
+            err = cand - W[row][None, :]
+            layer = np.sum((err @ X.T) ** 2, axis=1)          # ||(what - w) X^T||^2
+            mine = float(np.sum(((((r["codes"][row] - z) * s) - W[row]) @ X.T) ** 2))
+            assert layer.min() <= mine * (1 + 1e-12) + 1e-18
+
+
+def pin_gptq_beats_rtn_on_average(O):
+    """Over 200 seeds, GPTQ's mean layer loss is below round-to-nearest on the same
+    groups ("Same Ruler", section 2; spec: RTN never better on average)."""
+    g_loss, r_loss = [], []
+    for seed in range(200):
+        rng = np.random.default_rng(1000 + seed)
+        W, H, X = _small_layer(rng, 4, 16, n=40)
+        r = O.gptq_layer(W, H, bits=3, group=8, sym=False, actorder=True, damp=0.01)
+        perm = r["perm"]
+        rt = O.rtn_quantize(W[:, perm], bits=3, group=8)
+        Qr = np.empty_like(W)
+        Qr[:, perm] = rt["Q"]
+        Qg = np.empty_like(W)
+        Qg[:, perm] = r["Q"]
+        g_loss.append(np.sum(O.quadratic_loss(Qg - W, H)))
+        r_loss.append(np.sum(O.quadratic_loss(Qr - W, H)))
+    assert np.mean(g_loss) < np.mean(r_loss)
+
+
+def pin_act_order(O):
+    """perm sorts diag(H) descending ("GPTQ > ActOrder"); ties keep index order."""
+    rng = np.random.default_rng(19)
+    H, _ = spd(rng, 30)
+    perm = O.act_order(H)
+    dg = np.diag(H)[perm]
+    assert np.all(np.diff(dg) <= 0)
+    assert sorted(perm.tolist()) == list(range(30))
+    Ht = np.diag([1.0, 3.0, 1.0, 3.0, 2.0, 1.0])
+    assert O.act_order(Ht).tolist() == [1, 3, 4, 0, 2, 5]
+    prep = O.gptq_prepare(Ht, 0.01, actorder=True)
+    assert np.all(np.diff(np.diag(prep["Hd"])) <= 0)
+
+
+def pin_damping(O):
+    """Every eigenvalue moves up by lambda = 0.01 mean(diag H) and each diagonal entry
+    of H_damp^-1 is at most 1 / lambda ("Same Ruler", section 1.6)."""
+    rng = np.random.default_rng(23)
+    H, _ = spd(rng, 20, n=8)           # rank-deficient: n < d
+    Hd, lam = O.damping(H, 0.01)
+    assert np.isclose(lam, 0.01 * np.trace(H) / 20)
+    assert np.allclose(np.linalg.eigvalsh(Hd), np.linalg.eigvalsh(H) + lam, atol=1e-10)
+    assert np.all(np.diag(np.linalg.inv(Hd)) <= 1.0 / lam * (1 + 1e-12))
+
+
+def pin_dead_columns(O):
+    rng = np.random.default_rng(29)
+    X = rng.standard_normal((50, 6))
+    X[:, 2] = 0.0
+    H = O.hessian(X)
+    W = rng.standard_normal((3, 6))
+    Hf, Wf, dead = O.fix_dead(H, W)
+    assert dead.tolist() == [False, False, True, False, False, False]
+    assert Hf[2, 2] == 1.0 and np.all(Wf[:, 2] == 0.0)
+    assert np.allclose(np.delete(np.delete(Hf, 2, 0), 2, 1), np.delete(np.delete(H, 2, 0), 2, 1))
+    r = O.gptq_layer(W, H, bits=4, group=-1, actorder=True)
+    assert r["dead"][2] and np.isfinite(r["loss"])
+
+
+def pin_hessian(O):
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((7, 4))
+    brute = np.zeros((4, 4))
+    for t in range(7):
+        for i in range(4):
+            for j in range(4):
+                brute[i, j] += 2.0 / 7 * X[t, i] * X[t, j]
+    assert np.allclose(O.hessian(X), brute, rtol=1e-14)
+    X = rng.standard_normal((300, 9))
+    Hs, n = O.hessian_streaming([X[:100], X[100:101], X[101:250], X[250:]])
+    assert n == 300 and np.allclose(Hs, O.hessian(X), rtol=1e-12)
+    assert np.allclose(np.diag(O.hessian(X)), 2.0 / 300 * np.sum(X * X, axis=0), rtol=1e-13)
+    assert np.allclose(O.hessian_block(X, slice(2, 5), slice(4, 9)), O.hessian(X)[2:5, 4:9])
+
+
+def pin_fit_and_round(O):
+    # asymmetric, 4 bits: lo=-1, hi=2, s=3/15=0.2, z=round(5)=5
+    s, z = O.fit_group(np.array([[-1.0, 0.5, 2.0]]), 4, False)
+    assert np.isclose(s[0], np.float32(0.2)) and z[0] == 5
+    # -lo/s = 0.9 / (2.9/15) = 4.655 rounds to 5
+    s, z = O.fit_group(np.array([[-0.9, 2.0, 0.1]]), 4, False)
+    assert np.isclose(s[0], np.float32(2.9 / 15)) and z[0] == 5
+    # all positive: lo clamps to 0 so z = 0
+    s, z = O.fit_group(np.array([[0.5, 1.5]]), 4, False)
+    assert np.isclose(s[0], np.float32(0.1)) and z[0] == 0
+    # all-zero group: s = 1e-8, z = 0
+    s, z = O.fit_group(np.zeros((1, 4)), 4, False)
+    assert s[0] == np.float32(1e-8) and z[0] == 0
+    # symmetric, 4 bits: s = max|w| / 7, zero 8
+    s, z = O.fit_group(np.array([[-0.7, 0.35]]), 4, True)
+    assert np.isclose(s[0], np.float32(0.1)) and z[0] == 8
+    # rounding: half to even, clamp to the grid
+    c, q = O.round_to_grid(np.array([0.25, 0.35, 10.0, -10.0]), np.float32([0.1] * 4),
+                           np.array([0, 0, 0, 0]), 4, False)
+    assert c.tolist() == [2, 4, 15, 0]
+    c, q = O.round_to_grid(np.array([-10.0, 10.0]), np.float32([0.1] * 2),
+                           np.array([8, 8]), 4, True)
+    assert c.tolist() == [1, 15]
+
+
+def pin_pack(O):
+    codes = np.arange(1, 9)[None, :]
+    w = O.pack_bitstream(codes, 4)
+    assert w.view(np.uint32)[0, 0] == 0x87654321
+    # 3 bits: 32 codes in 3 words, code 10 straddles words 0 and 1
+    codes = np.zeros((1, 32), dtype=np.int64)
+    codes[0, 10] = 0b111
+    w = O.pack_bitstream(codes, 3).view(np.uint32)
+    assert w[0, 0] == 0b11 << 30 and w[0, 1] == 0b1 and w[0, 2] == 0
+    assert O.pack_bitstream(np.array([[0x12, 0x34, 0x56, 0x78]]), 8).view(np.uint32)[0, 0] \
+        == 0x78563412
+    rng = np.random.default_rng(37)
+    for bits in (2, 3, 4, 8):
+        v = rng.integers(0, 1 << bits, size=(5, 64))
+        assert np.array_equal(O.unpack_bitstream(O.pack_bitstream(v, bits), bits, 64), v)
+
+
+def pin_checkpoint_format(O):
+    """"04 - GPTQ", section 8: 4096x4096 at g128 is out*in/2 + out*in/g*2 + out*in/(2g)
+    + 4*in = 8,732,672 bytes; the tensors the oracle packs have exactly these sizes."""
+    assert O.checkpoint_bytes(4096, 4096, 128) == 8732672
+    # "GPTQ Architecture, in depth", worked example: 4 + (16 + 4)/128 bits per weight
+    assert np.isclose((O.checkpoint_bytes(4096, 4096, 128) - 4 * 4096) * 8 / 4096 ** 2,
+                      4 + 20 / 128)
+    rng = np.random.default_rng(41)
+    m, d, g = 32, 256, 128
+    W, H, _ = _small_layer(rng, m, d)
+    r = O.gptq_layer(W, H, bits=4, group=g, actorder=True)
+    nbytes = (r["qweight"].nbytes + r["scales"].astype(np.float16).nbytes
+              + r["qzeros"].nbytes + r["g_idx"].nbytes)
+    assert r["qweight"].shape == (d // 8, m) and r["qzeros"].shape == (d // g, m // 8)
+    assert nbytes == O.checkpoint_bytes(m, d, g)
+
+
+def pin_format_roundtrip(O):
+    """qweight/qzeros/scales/g_idx dequantise to the loop's Q, un-permuted
+    ("GPTQ Architecture, in depth": Q[:, argsort(perm)], g_idx per original column)."""
+    rng = np.random.default_rng(43)
+    m, d = 32, 64
+    for bits, group, sym in [(4, 16, False), (3, 32, True), (4, -1, False)]:
+        W, H, _ = _small_layer(rng, m, d)
+        r = O.gptq_layer(W, H, bits=bits, group=group, sym=sym, actorder=True, blocksize=16)
+        codes = O.unpack_bitstream(r["qweight"].T.copy(), bits, d)
+        zeros = O.unpack_bitstream(r["qzeros"], bits, m)
+        gi = r["g_idx"]
+        deq = r["scales"][gi].T.astype(float) * (codes - zeros[gi].T)
+        Q = np.empty_like(W)
+        Q[:, r["perm"]] = r["Q"]
+        assert np.allclose(deq, Q, rtol=0, atol=1e-15)
+        assert np.array_equal(codes, r["codes"])
+
+
+PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
+        pin_cholesky_2x2, pin_cholesky_general, pin_obs_equals_cholesky,
+        pin_blocked_equals_unblocked, pin_loss_identity, pin_brute_force_optimum,
+        pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
+        pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
+        pin_format_roundtrip]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin(ORACLE)
+
+
+def test_rtn_per_column_row_of_table():
+    pin_rtn_per_column()
