@@ -1,0 +1,197 @@
+/*
+ * gptq.h -- C ABI of the GB300 GPTQ layer-quantization engine (libgptq_gb300.so).
+ *
+ * The engine quantises one linear layer with GPTQ.  Three calls follow the method's
+ * statement of the problem:
+ *
+ *   gptq_hessian_accumulate  H = 2/n * sum x x^T over calibration tokens, streamed
+ *   gptq_prepare             dead-column fix, act-order permutation, damping and the
+ *                            upper Cholesky factor U of H_damp^-1
+ *   gptq_quantize_layer      the fixed-order column loop in 128-column blocks with the
+ *                            lazy trailing update, group scales / zeros, g_idx and
+ *                            bit packing
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Device pointers are CUDA device memory on the current device, allocated and owned by
+ *   the caller.  The library never allocates device memory; scratch comes from the
+ *   caller's workspace `ws` of `ws_bytes` bytes (size it with gptq_workspace_size; the
+ *   base must be 256-byte aligned).  Host pointers are named as such below.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *   call enqueues its kernels on `stream`, then synchronises `stream` and returns the
+ *   status of the work it enqueued (device-side failures such as a non-positive-definite
+ *   matrix are reported this way).
+ * - Matrices are row-major.  Indices and sizes are 32-bit unless stated.
+ * - On any status other than GPTQ_OK, gptq_last_error() (thread-local) describes it.
+ *   Invalid arguments are detected before anything is enqueued; outputs are then
+ *   untouched.
+ */
+#ifndef GPTQ_GB300_H
+#define GPTQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned buffer       */
+  GPTQ_ERR_UNSUPPORTED = 2,   /* a valid value this engine does not implement          */
+  GPTQ_ERR_NOT_PD = 3,        /* H_damp is not positive definite (Cholesky pivot <= 0) */
+  GPTQ_ERR_NONFINITE = 4,     /* NaN or Inf in an input                                */
+  GPTQ_ERR_CUDA = 5,          /* a CUDA runtime call failed                            */
+  GPTQ_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out                    */
+  GPTQ_ERR_WORKSPACE = 7      /* ws too small (see gptq_workspace_size)                */
+} gptq_status;
+
+typedef enum { GPTQ_F32 = 0, GPTQ_BF16 = 1 } gptq_dtype;
+
+typedef enum { GPTQ_OP_HESSIAN = 0, GPTQ_OP_PREPARE = 1, GPTQ_OP_QUANTIZE = 2 } gptq_op;
+
+/*
+ * gptq_workspace_size -- bytes of workspace the call `op` wants for these sizes on the
+ * current device.  Arguments that do not apply to `op` are ignored.  For GPTQ_OP_HESSIAN
+ * the value is the size that lets the call split the token axis as it prefers; any ws of
+ * at least d_in*d_in*4 + 4096 bytes is accepted (fewer splits).  Returns 0 for invalid
+ * sizes.
+ */
+size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, int bits,
+                           int group);
+
+/*
+ * gptq_hessian_accumulate -- one step of the streaming Hessian hook.
+ *
+ * Defined by "GPTQ Architecture, in depth", "The algorithm in code" (HessianHook) and
+ * "Same Ruler, Smarter Placement: GPTQ" section 1.4 (H = 2 X X^T): for a chunk of t =
+ * ntok tokens and n = *nseen tokens seen so far,
+ *     H <- H * n/(n+t) + 2/(n+t) * X^T X ,   *nseen <- n + t .
+ * When *nseen == 0 the previous contents of H are ignored (H may be uninitialised).
+ *
+ * H      device float32 [d_in, d_in], in/out.  Only the upper triangle, at the
+ *        granularity of 128x128 tiles (every element (i, j) with i/128 <= j/128), is
+ *        written and is authoritative; the rest is left as it was.
+ * nseen  host int64, in/out: the running token count n.
+ * X      device [ntok, d_in] row-major (token-major: a Linear's input flattened to
+ *        [tokens, cols]), element type `xdtype` (GPTQ_BF16: bfloat16, computed on the
+ *        tensor cores with float32 accumulation; GPTQ_F32: float32, computed in float32
+ *        FMA).  Row stride d_in elements; d_in must be a multiple of 8.
+ * ntok   >= 0; ntok == 0 is a no-op.
+ * Errors: INVALID_ARG, UNSUPPORTED (d_in % 8 != 0), WORKSPACE, CUDA, TIMEOUT.
+ */
+gptq_status gptq_hessian_accumulate(float* H, int64_t* nseen, const void* X, int xdtype,
+                                    int64_t ntok, int32_t d_in, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/*
+ * gptq_prepare -- everything GPTQ does to H before the column loop.
+ *
+ * Defined by "GPTQ Architecture, in depth", "The algorithm in code" and "Groups,
+ * act-order and other knobs", "Same Ruler, Smarter Placement: GPTQ" sections 1.6, 1.7
+ * and 1.9, "GPTQ > ActOrder: Activation-Based Column Ordering":
+ *   dead[j]   = (H_jj == 0); such channels get H_jj = 1 (their weights are zeroed later)
+ *   perm      = columns by descending diagonal (after the dead fix), ties by ascending
+ *               index; identity when actorder == 0
+ *   H_damp    = H[perm][:, perm] + lambda I, lambda = damp * mean(diag H)
+ *   Hinv_chol = U, upper triangular, H_damp^-1 = U^T U (the upper Cholesky factor of the
+ *               inverse), in permuted order.
+ *
+ * H          device float32 [d_in, d_in], read only; the upper 128-tile triangle (as
+ *            written by gptq_hessian_accumulate) is read, the rest ignored.
+ * damp       relative damping, >= 0 (0.01 on the pages).
+ * perm       device int32 [d_in], out: perm[k] = original column processed k-th.
+ * dead       device uint8 [d_in], out: 1 for dead channels (original order).
+ * Hinv_chol  device float32 [d_in, d_in], out: U (strict lower triangle written as 0).
+ * info       host int32, out, may be NULL: 0, or for GPTQ_ERR_NOT_PD the 1-based
+ *            position in processing order of the first column whose pivot failed.
+ * Errors: INVALID_ARG, WORKSPACE, NOT_PD (raise damp; the pages suggest up to 0.1),
+ *         NONFINITE, CUDA, TIMEOUT.
+ */
+gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
+                         int32_t* perm, uint8_t* dead, float* Hinv_chol, int32_t* info,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * gptq_quantize_layer -- the GPTQ column loop and the packed checkpoint tensors.
+ *
+ * Defined by "GPTQ Architecture, in depth", "The algorithm in code" (gptq, fit_group)
+ * and "Packing, tooling and serving", "Same Ruler, Smarter Placement: GPTQ" sections
+ * 1.5 and 1.8, "04 - GPTQ" section 8.  With W' = W with dead columns zeroed, in
+ * processing order, for each column q in order: at a group start fit (s, z) per row on
+ * the current W'[:, q:q+g] (asymmetric: lo = min(w,0), hi = max(w,0),
+ * s = max((hi-lo)/maxq, 1e-8), z = round(-lo/s); symmetric: s = max(max|w| /
+ * (2^(bits-1)-1), 1e-8), z = 2^(bits-1)); code = clamp(round(w/s) + z, lowest, maxq)
+ * (lowest = 0 asymmetric, 1 symmetric; round half to even; w/s in float32);
+ * e = (w - s(code - z)) / U_qq; every later column j: w_j -= e U_qj.  Results equal the
+ * unblocked loop up to float32 rounding; the engine applies updates inside 128-column
+ * blocks at once and pushes each block's errors to later columns as one matrix product.
+ *
+ * W          device [d_out, d_in] row-major, `wdtype` (float32 or bfloat16); read only.
+ * Hinv_chol  device float32 [d_in, d_in], U from gptq_prepare (upper triangle read).
+ * perm       device int32 [d_in], or NULL for natural order.
+ * dead       device uint8 [d_in], or NULL for no dead channels.
+ * d_out      >= 0 (0: only g_idx and *loss = 0 are written); multiple of 32.
+ * d_in       >= 1, multiple of 32.
+ * bits       2, 3, 4 or 8.   group: -1 (one group per row), 16, 32, 64, or a multiple
+ *            of 128.   sym: 0 asymmetric, 1 symmetric.
+ * blocksize  1..128.  Results do not depend on it (beyond rounding); it is accepted for
+ *            the pages' interface.  With group != -1, group and blocksize must divide
+ *            one another, else GPTQ_ERR_UNSUPPORTED.
+ * qweight    device int32 [bits*d_in/32, d_out], out: codes in original column order
+ *            packed along d_in as a little-endian bit stream (code k of output row r at
+ *            bits [bits*k, bits*k+bits) of column r's stream).
+ * scales     device float32 [G, d_out], out; G = ceil(d_in/group) (1 when group=-1),
+ *            groups in processing order.
+ * qzeros     device int32 [G, bits*d_out/32], out: zero points packed along d_out.
+ * g_idx      device int32 [d_in], out: g_idx[c] = (position of c in perm) / group.
+ * loss       device float64 scalar, out: sum over rows and columns of e^2 / 2, the OBS
+ *            loss (w - what)^2 / (2 [H_cond^-1]_qq) ("04 - GPTQ", section 2).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, NONFINITE (W), CUDA, TIMEOUT.
+ */
+gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_chol,
+                                const int32_t* perm, const uint8_t* dead, int32_t d_out,
+                                int32_t d_in, int bits, int group, int sym, int blocksize,
+                                int32_t* qweight, float* scales, int32_t* qzeros,
+                                int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* gptq_last_error(void);
+
+/* Name of a gptq_status value. */
+const char* gptq_status_string(int status);
+
+/* ABI version of this header: 1. */
+int gptq_abi_version(void);
+
+/*
+ * Tracing.  gptq_profile_enable(1) makes every later call bracket each of its kernel
+ * launches with CUDA events on the call's stream and accumulate the device time per
+ * kernel kind; gptq_profile_read(kind, &ms, &launches) returns the totals and
+ * gptq_profile_reset() clears them.  Kinds are the gptq_kernel_kind values; the name of
+ * a kind is gptq_kernel_name(kind).  gptq_launch_count() counts every kernel launched by
+ * the library since load (profiling or not).
+ */
+typedef enum {
+  GPTQ_K_SYRK_TC = 0, GPTQ_K_SYRK_SIMT, GPTQ_K_SYRK_REDUCE,
+  GPTQ_K_PREP_DIAG, GPTQ_K_PREP_RANK, GPTQ_K_PREP_MIRROR, GPTQ_K_PREP_GATHER,
+  GPTQ_K_POTRF_PANEL, GPTQ_K_POTRF_TRSM, GPTQ_K_POTRF_UPDATE,
+  GPTQ_K_TRTRI_DIAG, GPTQ_K_TRTRI_UPDATE, GPTQ_K_PREP_REVERSE,
+  GPTQ_K_QUANT_GATHER, GPTQ_K_QUANT_FIT, GPTQ_K_QUANT_LOOP, GPTQ_K_QUANT_LAZY,
+  GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT,
+  GPTQ_K_COUNT
+} gptq_kernel_kind;
+
+void gptq_profile_enable(int on);
+int gptq_profile_read(int kind, double* ms_total, int64_t* launches);
+void gptq_profile_reset(void);
+const char* gptq_kernel_name(int kind);
+int64_t gptq_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_GB300_H */

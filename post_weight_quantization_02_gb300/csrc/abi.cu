@@ -1,0 +1,372 @@
+// The C ABI: argument checks, workspace layout, split choice and call orchestration.
+// Every entry point enqueues its kernels on the caller's stream, synchronises that
+// stream and returns the status of the work (see include/gptq.h).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace gptq {
+namespace {
+
+template <typename F>
+gptq_status guarded(F&& f) {
+  try {
+    f();
+    set_last_error("");
+    return GPTQ_OK;
+  } catch (const Error& e) {
+    trace_discard();
+    set_last_error(e.msg);
+    return e.status;
+  } catch (const std::exception& e) {
+    trace_discard();
+    set_last_error(std::string("internal error: ") + e.what());
+    return GPTQ_ERR_CUDA;
+  } catch (...) {
+    trace_discard();
+    set_last_error("internal error");
+    return GPTQ_ERR_CUDA;
+  }
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void require(bool ok, gptq_status s, const char* msg) {
+  if (!ok) fail(s, "%s", msg);
+}
+
+void begin_call(DevStatus* st, cudaStream_t s) {
+  GPTQ_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+}
+
+// Synchronise, read the device status word, fold in the tracing events.
+DevStatus finish_call(DevStatus* st, cudaStream_t s) {
+  DevStatus h;
+  std::memset(&h, 0, sizeof(h));
+  GPTQ_CUDA(cudaMemcpyAsync(&h, st, 3 * sizeof(int), cudaMemcpyDeviceToHost, s));
+  GPTQ_CUDA(cudaStreamSynchronize(s));
+  trace_flush();
+  return h;
+}
+
+void raise_device_status(const DevStatus& h, const char* call) {
+  switch (h.code) {
+    case 0:
+      return;
+    case GPTQ_ERR_NOT_PD:
+      fail(GPTQ_ERR_NOT_PD, "%s: H_damp is not positive definite (pivot at processing position %d);"
+           " raise damp", call, h.info);
+    case GPTQ_ERR_NONFINITE:
+      fail(GPTQ_ERR_NONFINITE, "%s: NaN or Inf in the input (detail %d)", call, h.info);
+    case GPTQ_ERR_TIMEOUT:
+      fail(GPTQ_ERR_TIMEOUT, "%s: %d device-side wait(s) ran out", call, h.timeouts);
+    default:
+      fail(static_cast<gptq_status>(h.code), "%s: device reported status %d", call, h.code);
+  }
+}
+
+// ------------------------------------------------------------------ Hessian
+
+bool use_tensor_cores(int xdtype) {
+  if (xdtype != GPTQ_BF16) return false;
+  const char* e = std::getenv("GPTQ_SYRK");
+  return !(e != nullptr && std::strcmp(e, "simt") == 0);
+}
+
+int planning_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+    return n;
+  }
+  cudaGetLastError();
+  return 152;  // sizing only: GB300
+}
+
+struct SplitPlan {
+  int splits;
+  int64_t tok_per_split;
+};
+
+// Splits of the token axis: enough units to fill the SMs evenly, at least 8 token
+// stages per unit, and no more partials than the workspace holds.
+SplitPlan plan_splits(int64_t ntok, int d, bool tc, int64_t max_splits, int nsm) {
+  const int granule = tc ? syrk_tc_token_granule() : 16;
+  const int64_t tiles = tc ? syrk_tc_tiles(d) : syrk_simt_tiles(d);
+  const int64_t slots = tc ? nsm : 4LL * nsm;  // the SIMT kernel keeps ~4 CTAs per SM
+  int64_t smax = ntok / (8LL * granule);
+  if (smax < 1) smax = 1;
+  if (smax > 16) smax = 16;
+  if (smax > max_splits) smax = max_splits;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= smax; ++s) {
+    const int64_t units = tiles * s;
+    const int64_t waves = (units + slots - 1) / slots;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * slots);
+    if (eff > best_eff + 0.03) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff >= 0.9) break;
+  }
+  int64_t tps = (ntok + best - 1) / best;
+  tps = (tps + granule - 1) / granule * granule;
+  SplitPlan p;
+  p.tok_per_split = tps;
+  p.splits = static_cast<int>((ntok + tps - 1) / tps);
+  return p;
+}
+
+size_t hessian_ws_bytes(int d, int splits) {
+  WsPlan w;
+  w.add<DevStatus>(1);
+  w.add<float>(static_cast<size_t>(splits) * d * d);
+  return w.bytes;
+}
+
+size_t prepare_ws_bytes(int d) {
+  WsPlan w;
+  w.add<DevStatus>(1);
+  w.add<float>(static_cast<size_t>(d) * d);  // symmetric copy, then the inverse
+  w.add<float>(static_cast<size_t>(d) * d);  // reversed, permuted, damped H -> factor
+  w.add<float>(d);                           // fixed diagonal
+  w.add<float>(1);                           // lambda
+  return w.bytes;
+}
+
+size_t quantize_ws_bytes(int m, int d, int G) {
+  WsPlan w;
+  w.add<DevStatus>(1);
+  w.add<float>(static_cast<size_t>(m) * d);    // Wp
+  w.add<uint8_t>(static_cast<size_t>(m) * d);  // codesT
+  w.add<float>(static_cast<size_t>(128) * m);  // errT
+  w.add<int32_t>(static_cast<size_t>(G) * m);  // zeros
+  w.add<double>(m);                            // loss_rows
+  w.add<int32_t>(d);                           // pos
+  return w.bytes;
+}
+
+int groups_of(int d, int group) { return group == -1 ? 1 : static_cast<int>(ceil_div(d, group)); }
+
+bool group_supported(int group) {
+  return group == -1 || group == 16 || group == 32 || group == 64 || (group > 0 && group % 128 == 0);
+}
+
+}  // namespace
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" {
+
+size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, int bits,
+                           int group) {
+  (void)bits;
+  if (d_in <= 0) return 0;
+  switch (op) {
+    case GPTQ_OP_HESSIAN: {
+      if (ntok < 0) return 0;
+      const int64_t t = ntok > 0 ? ntok : 1;
+      SplitPlan p = plan_splits(t, d_in, true, 16, planning_sm_count());
+      SplitPlan q = plan_splits(t, d_in, false, 16, planning_sm_count());
+      return hessian_ws_bytes(d_in, p.splits > q.splits ? p.splits : q.splits);
+    }
+    case GPTQ_OP_PREPARE:
+      return prepare_ws_bytes(d_in);
+    case GPTQ_OP_QUANTIZE:
+      if (d_out < 0 || !group_supported(group)) return 0;
+      return quantize_ws_bytes(d_out, d_in, groups_of(d_in, group));
+    default:
+      return 0;
+  }
+}
+
+gptq_status gptq_hessian_accumulate(float* H, int64_t* nseen, const void* X, int xdtype,
+                                    int64_t ntok, int32_t d_in, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  return guarded([&] {
+    require(H != nullptr && nseen != nullptr && ws != nullptr, GPTQ_ERR_INVALID_ARG,
+            "gptq_hessian_accumulate: null H, nseen or ws");
+    require(d_in > 0 && ntok >= 0 && *nseen >= 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_hessian_accumulate: need d_in > 0, ntok >= 0, *nseen >= 0");
+    require(xdtype == GPTQ_F32 || xdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
+            "gptq_hessian_accumulate: xdtype must be GPTQ_F32 or GPTQ_BF16");
+    require(d_in % 8 == 0, GPTQ_ERR_UNSUPPORTED, "gptq_hessian_accumulate: d_in must be a multiple of 8");
+    require(ntok == 0 || X != nullptr, GPTQ_ERR_INVALID_ARG, "gptq_hessian_accumulate: null X");
+    require(aligned(H, 16) && aligned(X, 16) && aligned(ws, 256), GPTQ_ERR_INVALID_ARG,
+            "gptq_hessian_accumulate: H and X must be 16-byte aligned, ws 256-byte aligned");
+    require(ntok < (int64_t(1) << 31), GPTQ_ERR_UNSUPPORTED,
+            "gptq_hessian_accumulate: at most 2^31 - 1 tokens per call");
+    const int64_t one = hessian_ws_bytes(d_in, 1);
+    require(ws_bytes >= static_cast<size_t>(one), GPTQ_ERR_WORKSPACE,
+            "gptq_hessian_accumulate: workspace smaller than d_in*d_in*4 + 256 bytes");
+    if (ntok == 0) return;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool tc = use_tensor_cores(xdtype);
+    const size_t per = static_cast<size_t>(d_in) * d_in * sizeof(float);
+    const int64_t cap = static_cast<int64_t>((ws_bytes - 256) / per);
+    SplitPlan p = plan_splits(ntok, d_in, tc, cap, sm_count());
+
+    WsCarver wc(ws, ws_bytes);
+    DevStatus* st = wc.take<DevStatus>(1);
+    float* P = wc.take<float>(static_cast<size_t>(p.splits) * d_in * d_in);
+
+    const int64_t n_old = *nseen;
+    const double n_new = static_cast<double>(n_old) + static_cast<double>(ntok);
+    const float alpha = static_cast<float>(2.0 / n_new);
+    const float beta = static_cast<float>(static_cast<double>(n_old) / n_new);
+
+    begin_call(st, s);
+    if (tc) launch_syrk_tc(X, ntok, d_in, p.splits, p.tok_per_split, P, st, s);
+    else launch_syrk_simt(X, xdtype == GPTQ_BF16, ntok, d_in, p.splits, p.tok_per_split, P, s);
+    launch_syrk_reduce(H, P, d_in, p.splits, alpha, beta, n_old == 0, s);
+    raise_device_status(finish_call(st, s), "gptq_hessian_accumulate");
+    *nseen = n_old + ntok;
+  });
+}
+
+gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
+                         int32_t* perm, uint8_t* dead, float* Hinv_chol, int32_t* info,
+                         void* ws, size_t ws_bytes, void* stream) {
+  if (info != nullptr) *info = 0;
+  int32_t pivot = 0;
+  gptq_status st_code = guarded([&] {
+    require(H != nullptr && perm != nullptr && dead != nullptr && Hinv_chol != nullptr &&
+                ws != nullptr,
+            GPTQ_ERR_INVALID_ARG, "gptq_prepare: null pointer argument");
+    require(d_in > 0, GPTQ_ERR_INVALID_ARG, "gptq_prepare: d_in must be positive");
+    require(std::isfinite(damp) && damp >= 0.0f, GPTQ_ERR_INVALID_ARG,
+            "gptq_prepare: damp must be finite and >= 0");
+    require(d_in % 8 == 0, GPTQ_ERR_UNSUPPORTED, "gptq_prepare: d_in must be a multiple of 8");
+    require(aligned(H, 16) && aligned(Hinv_chol, 16) && aligned(ws, 256), GPTQ_ERR_INVALID_ARG,
+            "gptq_prepare: H and Hinv_chol must be 16-byte aligned, ws 256-byte aligned");
+    require(ws_bytes >= prepare_ws_bytes(d_in), GPTQ_ERR_WORKSPACE,
+            "gptq_prepare: workspace too small (see gptq_workspace_size)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsCarver wc(ws, ws_bytes);
+    DevStatus* st = wc.take<DevStatus>(1);
+    float* S = wc.take<float>(static_cast<size_t>(d_in) * d_in);
+    float* Hr = wc.take<float>(static_cast<size_t>(d_in) * d_in);
+    float* diag = wc.take<float>(d_in);
+    float* lam = wc.take<float>(1);
+    begin_call(st, s);
+    launch_prepare(H, d_in, damp, actorder ? 1 : 0, perm, dead, Hinv_chol, S, Hr, diag, lam, st,
+                   s);
+    DevStatus h = finish_call(st, s);
+    if (h.code == GPTQ_ERR_NOT_PD) pivot = h.info;
+    raise_device_status(h, "gptq_prepare");
+  });
+  if (info != nullptr) *info = pivot;
+  return st_code;
+}
+
+gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_chol,
+                                const int32_t* perm, const uint8_t* dead, int32_t d_out,
+                                int32_t d_in, int bits, int group, int sym, int blocksize,
+                                int32_t* qweight, float* scales, int32_t* qzeros,
+                                int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
+                                void* stream) {
+  return guarded([&] {
+    require(d_in > 0 && d_out >= 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: need d_in > 0 and d_out >= 0");
+    require(Hinv_chol != nullptr && g_idx != nullptr && loss != nullptr && ws != nullptr,
+            GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer: null Hinv_chol, g_idx, loss or ws");
+    require(d_out == 0 || (W != nullptr && qweight != nullptr && scales != nullptr &&
+                           qzeros != nullptr),
+            GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer: null W or output");
+    require(wdtype == GPTQ_F32 || wdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: wdtype must be GPTQ_F32 or GPTQ_BF16");
+    require(sym == 0 || sym == 1, GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer: sym must be 0 or 1");
+    require(blocksize >= 1 && blocksize <= 128, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: blocksize must be in 1..128");
+    require(group == -1 || group > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: group must be -1 or positive");
+    require(bits == 2 || bits == 3 || bits == 4 || bits == 8, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer: bits must be 2, 3, 4 or 8");
+    require(group_supported(group), GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer: group must be -1, 16, 32, 64 or a multiple of 128");
+    require(group == -1 || group % blocksize == 0 || blocksize % group == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer: group and blocksize must divide one another");
+    require(d_in % 32 == 0 && d_out % 32 == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer: d_in and d_out must be multiples of 32");
+    require(aligned(W, 16) && aligned(Hinv_chol, 16) && aligned(ws, 256), GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: W and Hinv_chol must be 16-byte aligned, ws 256-byte aligned");
+    const int G = groups_of(d_in, group);
+    require(ws_bytes >= quantize_ws_bytes(d_out, d_in, G), GPTQ_ERR_WORKSPACE,
+            "gptq_quantize_layer: workspace too small (see gptq_workspace_size)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsCarver wc(ws, ws_bytes);
+    QuantArgs q;
+    q.st = wc.take<DevStatus>(1);
+    q.Wp = wc.take<float>(static_cast<size_t>(d_out) * d_in);
+    q.codesT = wc.take<uint8_t>(static_cast<size_t>(d_out) * d_in);
+    q.errT = wc.take<float>(static_cast<size_t>(128) * d_out);
+    q.zeros = wc.take<int32_t>(static_cast<size_t>(G) * d_out);
+    q.loss_rows = wc.take<double>(d_out);
+    q.pos = wc.take<int32_t>(d_in);
+    q.W = W;
+    q.w_bf16 = (wdtype == GPTQ_BF16);
+    q.U = Hinv_chol;
+    q.perm = perm;
+    q.dead = dead;
+    q.m = d_out;
+    q.d = d_in;
+    q.bits = bits;
+    q.group = group;
+    q.sym = sym;
+    q.G = G;
+    q.qweight = qweight;
+    q.scales = scales;
+    q.qzeros = qzeros;
+    q.g_idx = g_idx;
+    q.loss = loss;
+    begin_call(q.st, s);
+    launch_quantize(q, s);
+    raise_device_status(finish_call(q.st, s), "gptq_quantize_layer");
+  });
+}
+
+const char* gptq_last_error(void) { return last_error().c_str(); }
+
+const char* gptq_status_string(int status) {
+  switch (status) {
+    case GPTQ_OK: return "GPTQ_OK";
+    case GPTQ_ERR_INVALID_ARG: return "GPTQ_ERR_INVALID_ARG";
+    case GPTQ_ERR_UNSUPPORTED: return "GPTQ_ERR_UNSUPPORTED";
+    case GPTQ_ERR_NOT_PD: return "GPTQ_ERR_NOT_PD";
+    case GPTQ_ERR_NONFINITE: return "GPTQ_ERR_NONFINITE";
+    case GPTQ_ERR_CUDA: return "GPTQ_ERR_CUDA";
+    case GPTQ_ERR_TIMEOUT: return "GPTQ_ERR_TIMEOUT";
+    case GPTQ_ERR_WORKSPACE: return "GPTQ_ERR_WORKSPACE";
+    default: return "GPTQ_ERR_UNKNOWN";
+  }
+}
+
+int gptq_abi_version(void) { return 1; }
+
+void gptq_profile_enable(int on) { profile_enable(on != 0); }
+int gptq_profile_read(int kind, double* ms_total, int64_t* launches) {
+  return profile_read(kind, ms_total, launches) ? 0 : -1;
+}
+void gptq_profile_reset(void) { profile_reset(); }
+
+const char* gptq_kernel_name(int kind) {
+  static const char* names[GPTQ_K_COUNT] = {
+      "syrk_tc", "syrk_simt", "syrk_reduce", "prep_diag", "prep_rank", "prep_mirror",
+      "prep_gather", "potrf_panel", "potrf_trsm", "potrf_update", "trtri_diag", "trtri_update",
+      "prep_reverse", "quant_gather", "quant_fit", "quant_loop", "quant_lazy", "quant_pack",
+      "quant_loss", "quant_split"};
+  if (kind < 0 || kind >= GPTQ_K_COUNT) return "";
+  return names[kind];
+}
+
+int64_t gptq_launch_count(void) { return launch_count(); }
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Shared host and device helpers of the GPTQ engine: errors, workspace carving, the
+// device status word, bounded waits and launch tracing.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdio>
+#include <string>
+
+#include "../../include/gptq.h"
+
+namespace gptq {
+
+// ------------------------------------------------------------------ host-side errors
+
+struct Error {
+  gptq_status status;
+  std::string msg;
+};
+
+[[noreturn]] void fail(gptq_status s, const char* fmt, ...);
+void cuda_check(cudaError_t e, const char* what);
+void set_last_error(const std::string& msg);
+
+#define GPTQ_CUDA(call) ::gptq::cuda_check((call), #call)
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Carves 256-byte aligned sub-buffers out of the caller's workspace.
+class WsCarver {
+ public:
+  WsCarver(void* base, size_t bytes) : base_(static_cast<char*>(base)), size_(bytes) {}
+  template <typename T>
+  T* take(size_t count) {
+    size_t need = align_up(count * sizeof(T), 256);
+    if (off_ + need > size_) {
+      fail(GPTQ_ERR_WORKSPACE, "workspace too small: need more than %zu bytes", size_);
+    }
+    T* p = reinterpret_cast<T*>(base_ + off_);
+    off_ += need;
+    return p;
+  }
+  size_t used() const { return off_; }
+
+ private:
+  char* base_;
+  size_t size_;
+  size_t off_ = 0;
+};
+
+// Counts bytes the way WsCarver lays them out.
+struct WsPlan {
+  size_t bytes = 0;
+  template <typename T>
+  void add(size_t count) { bytes += align_up(count * sizeof(T), 256); }
+};
+
+// ------------------------------------------------------------------ device status
+
+// The first 256 bytes of every workspace: written by kernels, read after the call's
+// stream synchronisation.
+struct DevStatus {
+  int code;      // gptq_status of the first device-side failure (0 = none)
+  int info;      // failing pivot (1-based) or other detail
+  int timeouts;  // number of bounded waits that ran out
+  int pad[61];
+};
+
+__device__ __forceinline__ void dev_fail(DevStatus* st, int code, int info) {
+  if (atomicCAS(&st->code, 0, code) == 0) st->info = info;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every spin-wait in the library gives up after this long and records a timeout.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ------------------------------------------------------------------ launch tracing
+
+void trace_begin(int kind, cudaStream_t s);
+void trace_end(int kind, cudaStream_t s);
+void trace_flush();    // after the call's stream is synchronised
+void trace_discard();  // on failure: drop this thread's pending events
+void profile_enable(bool on);
+void profile_reset();
+bool profile_read(int kind, double* ms, int64_t* n);
+int64_t launch_count();
+const std::string& last_error();
+
+#define GPTQ_LAUNCH(kind, stream, kernel, grid, block, smem, ...)                 \
+  do {                                                                            \
+    ::gptq::trace_begin((kind), (stream));                                        \
+    kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);                   \
+    ::gptq::cuda_check(cudaGetLastError(), #kernel);                              \
+    ::gptq::trace_end((kind), (stream));                                          \
+  } while (0)
+
+// Number of SMs of the current device.
+int sm_count();
+
+}  // namespace gptq

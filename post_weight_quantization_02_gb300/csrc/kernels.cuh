@@ -1,0 +1,54 @@
+// Host-side launchers of the engine's kernels (one translation unit each).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gptq {
+
+// hessian_simt.cu
+int syrk_simt_tiles(int d);
+void launch_syrk_simt(const void* X, bool bf16, int64_t ntok, int d, int splits,
+                      int64_t tok_per_split, float* P, cudaStream_t s);
+void launch_syrk_reduce(float* H, const float* P, int d, int splits, float alpha, float beta,
+                        bool overwrite, cudaStream_t s);
+
+// hessian_tc.cu
+int syrk_tc_tiles(int d);
+int syrk_tc_token_granule();
+void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
+                    float* P, DevStatus* st, cudaStream_t s);
+
+// prepare.cu
+void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
+                    uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
+                    float* lam, DevStatus* st, cudaStream_t s);
+
+// quantize.cu
+struct QuantArgs {
+  const void* W;
+  bool w_bf16;
+  const float* U;
+  const int32_t* perm;  // may be null
+  const uint8_t* dead;  // may be null
+  int m, d, bits, group, sym, G;
+  // workspace
+  float* Wp;
+  uint8_t* codesT;
+  float* errT;
+  int32_t* zeros;
+  double* loss_rows;
+  int32_t* pos;
+  // outputs
+  int32_t* qweight;
+  float* scales;
+  int32_t* qzeros;
+  int32_t* g_idx;
+  double* loss;
+  DevStatus* st;
+};
+void launch_quantize(const QuantArgs& q, cudaStream_t s);
+
+}  // namespace gptq

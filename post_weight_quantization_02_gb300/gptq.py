@@ -1,0 +1,210 @@
+"""Thin ctypes binding of libgptq_gb300.so, with the C ABI's names.
+
+Argument marshalling only: torch tensors are passed as raw device pointers plus sizes,
+every step of the computation runs in the library's CUDA kernels.  A missing or
+unloadable library raises ``GptqLibraryError``; there is no other code path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "GPTQ_OK", "GPTQ_ERR_INVALID_ARG", "GPTQ_ERR_UNSUPPORTED", "GPTQ_ERR_NOT_PD",
+    "GPTQ_ERR_NONFINITE", "GPTQ_ERR_CUDA", "GPTQ_ERR_TIMEOUT", "GPTQ_ERR_WORKSPACE",
+    "GPTQ_F32", "GPTQ_BF16", "GPTQ_OP_HESSIAN", "GPTQ_OP_PREPARE", "GPTQ_OP_QUANTIZE",
+    "GptqError", "GptqLibraryError", "lib", "library_path",
+    "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_prepare", "gptq_quantize_layer",
+    "gptq_last_error", "gptq_status_string", "gptq_abi_version",
+    "gptq_profile_enable", "gptq_profile_read", "gptq_profile_reset", "gptq_kernel_name",
+    "gptq_launch_count", "KERNEL_KINDS", "workspace",
+]
+
+GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 3
+GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 6, 7
+GPTQ_F32, GPTQ_BF16 = 0, 1
+GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE = 0, 1, 2
+KERNEL_KINDS = 20
+
+
+class GptqLibraryError(RuntimeError):
+    """The CUDA library is missing or cannot be loaded."""
+
+
+class GptqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{gptq_status_string(status)}: {message}")
+        self.status = status
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_c = ctypes
+_vp, _sz, _i64, _i32, _f32 = _c.c_void_p, _c.c_size_t, _c.c_int64, _c.c_int32, _c.c_float
+_SIGS = {
+    "gptq_workspace_size": (_sz, [_c.c_int, _i64, _i32, _i32, _c.c_int, _c.c_int]),
+    "gptq_hessian_accumulate": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int, _i64, _i32,
+                                           _vp, _sz, _vp]),
+    "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
+                                _vp, _sz, _vp]),
+    "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
+                                       _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp,
+                                       _vp, _sz, _vp]),
+    "gptq_last_error": (_c.c_char_p, []),
+    "gptq_status_string": (_c.c_char_p, [_c.c_int]),
+    "gptq_abi_version": (_c.c_int, []),
+    "gptq_profile_enable": (None, [_c.c_int]),
+    "gptq_profile_read": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_double), _c.POINTER(_i64)]),
+    "gptq_profile_reset": (None, []),
+    "gptq_kernel_name": (_c.c_char_p, [_c.c_int]),
+    "gptq_launch_count": (_i64, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building in-tree if needed) and return the library."""
+    global _lib
+    if _lib is None:
+        try:
+            path = _build.ensure_built()
+            handle = ctypes.CDLL(path)
+        except Exception as e:  # no nvcc, failed build, wrong architecture
+            raise GptqLibraryError(f"libgptq_gb300.so unavailable: {e}") from e
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int):
+    if status != GPTQ_OK:
+        raise GptqError(status, gptq_last_error())
+
+
+def gptq_last_error() -> str:
+    return lib().gptq_last_error().decode()
+
+
+def gptq_status_string(status: int) -> str:
+    return lib().gptq_status_string(int(status)).decode()
+
+
+def gptq_abi_version() -> int:
+    return lib().gptq_abi_version()
+
+
+def gptq_workspace_size(op: int, ntok: int, d_out: int, d_in: int, bits: int = 4,
+                        group: int = 128) -> int:
+    return int(lib().gptq_workspace_size(op, ntok, d_out, d_in, bits, group))
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Caller-owned workspace (torch allocates; the library never does)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GPTQ_BF16
+    if t.dtype == torch.float32:
+        return GPTQ_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def gptq_hessian_accumulate(H: torch.Tensor, nseen: int, X: torch.Tensor,
+                            ws: Optional[torch.Tensor] = None, stream=None) -> int:
+    """One hook step on device tensors H [d, d] float32 and X [t, d]; returns the new n."""
+    d = H.shape[0]
+    if X.dim() != 2 or X.shape[1] != d:
+        raise ValueError("X must be [ntok, d_in]")
+    if ws is None:
+        ws = workspace(gptq_workspace_size(GPTQ_OP_HESSIAN, X.shape[0], 0, d), H.device)
+    n = ctypes.c_int64(int(nseen))
+    _check(lib().gptq_hessian_accumulate(_ptr(H), ctypes.byref(n), _ptr(X) if X.numel() else None,
+                                         _dtype_code(X), X.shape[0], d, _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return int(n.value)
+
+
+def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tensor,
+                 dead: torch.Tensor, Hinv_chol: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                 stream=None) -> int:
+    """Dead fix, act-order, damping, U; returns info (0, or the failing pivot)."""
+    d = H.shape[0]
+    if ws is None:
+        ws = workspace(gptq_workspace_size(GPTQ_OP_PREPARE, 0, 0, d), H.device)
+    info = ctypes.c_int32(0)
+    st = lib().gptq_prepare(_ptr(H), d, float(damp), int(bool(actorder)), _ptr(perm), _ptr(dead),
+                            _ptr(Hinv_chol), ctypes.byref(info), _ptr(ws), ws.numel(),
+                            _stream(stream))
+    if st != GPTQ_OK:
+        err = GptqError(st, gptq_last_error())
+        err.info = int(info.value)
+        raise err
+    return int(info.value)
+
+
+def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional[torch.Tensor],
+                        dead: Optional[torch.Tensor], bits: int, group: int, sym: bool,
+                        blocksize: int, qweight: torch.Tensor, scales: torch.Tensor,
+                        qzeros: torch.Tensor, g_idx: torch.Tensor, loss: torch.Tensor,
+                        ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    m, d = W.shape
+    if ws is None:
+        ws = workspace(gptq_workspace_size(GPTQ_OP_QUANTIZE, 0, m, d, bits, group), W.device)
+    _check(lib().gptq_quantize_layer(_ptr(W), _dtype_code(W), _ptr(Hinv_chol), _ptr(perm),
+                                     _ptr(dead), m, d, bits, group, int(bool(sym)), blocksize,
+                                     _ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx),
+                                     _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def gptq_profile_enable(on: bool) -> None:
+    lib().gptq_profile_enable(int(bool(on)))
+
+
+def gptq_profile_reset() -> None:
+    lib().gptq_profile_reset()
+
+
+def gptq_profile_read(kind: int):
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int64(0)
+    if lib().gptq_profile_read(kind, ctypes.byref(ms), ctypes.byref(n)) != 0:
+        raise ValueError(kind)
+    return float(ms.value), int(n.value)
+
+
+def gptq_kernel_name(kind: int) -> str:
+    return lib().gptq_kernel_name(kind).decode()
+
+
+def gptq_launch_count() -> int:
+    return int(lib().gptq_launch_count())

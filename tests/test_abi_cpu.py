@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and exports
+every declared entry point; sizes and argument checks answer without touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from post_weight_quantization_02_gb300 import gptq as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gptq_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = G.lib()
+    names = declared_functions()
+    assert "gptq_hessian_accumulate" in names and len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert G.gptq_abi_version() == 1
+
+
+def test_status_names():
+    assert G.gptq_status_string(G.GPTQ_ERR_NOT_PD) == "GPTQ_ERR_NOT_PD"
+    assert G.gptq_kernel_name(0) == "syrk_tc"
+
+
+def test_workspace_sizes():
+    d, m = 4096, 4096
+    assert G.gptq_workspace_size(G.GPTQ_OP_PREPARE, 0, 0, d) >= 2 * d * d * 4
+    q = G.gptq_workspace_size(G.GPTQ_OP_QUANTIZE, 0, m, d, 4, 128)
+    assert q >= m * d * 5 + 128 * m * 4
+    h = G.gptq_workspace_size(G.GPTQ_OP_HESSIAN, 262144, 0, d)
+    assert h >= d * d * 4 + 256
+    assert G.gptq_workspace_size(G.GPTQ_OP_QUANTIZE, 0, m, d, 4, 96) == 0
+    assert G.gptq_workspace_size(9, 0, m, d, 4, 128) == 0
+
+
+# Fake, aligned, never-dereferenced addresses: every call below fails its argument
+# checks before anything reaches CUDA.
+P = 1 << 20
+
+
+def _call_q(**kw):
+    a = dict(W=P, wdtype=1, U=P, perm=None, dead=None, m=64, d=256, bits=4, group=128, sym=0,
+             block=128, qw=P, sc=P, qz=P, gi=P, loss=P, ws=P, wsb=1 << 30)
+    a.update(kw)
+    return G.lib().gptq_quantize_layer(a["W"], a["wdtype"], a["U"], a["perm"], a["dead"],
+                                       a["m"], a["d"], a["bits"], a["group"], a["sym"],
+                                       a["block"], a["qw"], a["sc"], a["qz"], a["gi"],
+                                       a["loss"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=5), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(group=96), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(group=128, block=96), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(d=250), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(m=48), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(U=None), G.GPTQ_ERR_INVALID_ARG),
+    (dict(block=0), G.GPTQ_ERR_INVALID_ARG),
+    (dict(sym=2), G.GPTQ_ERR_INVALID_ARG),
+    (dict(wdtype=7), G.GPTQ_ERR_INVALID_ARG),
+    (dict(W=P + 4), G.GPTQ_ERR_INVALID_ARG),
+    (dict(m=-1), G.GPTQ_ERR_INVALID_ARG),
+    (dict(wsb=1024), G.GPTQ_ERR_WORKSPACE),
+])
+def test_quantize_argument_checks(kw, status):
+    assert _call_q(**kw) == status
+    assert G.gptq_last_error() != ""
+
+
+def test_prepare_and_hessian_argument_checks():
+    lib = G.lib()
+    info = ctypes.c_int32(-5)
+    assert lib.gptq_prepare(P, 0, 0.01, 1, P, P, P, ctypes.byref(info), P, 1 << 30, None) \
+        == G.GPTQ_ERR_INVALID_ARG
+    assert info.value == 0
+    assert lib.gptq_prepare(P, 100, 0.01, 1, P, P, P, None, P, 1 << 30, None) == \
+        G.GPTQ_ERR_UNSUPPORTED
+    assert lib.gptq_prepare(P, 128, -1.0, 1, P, P, P, None, P, 1 << 30, None) == \
+        G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_prepare(P, 128, 0.01, 1, P, P, P, None, P, 1000, None) == \
+        G.GPTQ_ERR_WORKSPACE
+    n = ctypes.c_int64(0)
+    assert lib.gptq_hessian_accumulate(P, ctypes.byref(n), P, 3, 10, 128, P, 1 << 30, None) \
+        == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_accumulate(P, ctypes.byref(n), P, 1, 10, 100, P, 1 << 30, None) \
+        == G.GPTQ_ERR_UNSUPPORTED
+    assert lib.gptq_hessian_accumulate(P, ctypes.byref(n), P, 1, 10, 128, P, 100, None) \
+        == G.GPTQ_ERR_WORKSPACE
+    assert lib.gptq_hessian_accumulate(None, ctypes.byref(n), P, 1, 10, 128, P, 1 << 30, None) \
+        == G.GPTQ_ERR_INVALID_ARG
+    assert n.value == 0

@@ -1,0 +1,108 @@
+"""Parity of gptq_hessian_accumulate (through the C ABI) with the float64 oracle."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as O
+from tests.parity import H_REL_FRO, rel_fro, to_np, upper_tile_mask
+from workloads import CONFIGS, make_tokens, make_tokens_chunk, channel_multipliers
+
+pytestmark = pytest.mark.gpu
+
+
+def _accumulate(lib, chunks, d, dev):
+    H = torch.full((d, d), float("nan"), dtype=torch.float32, device=dev)
+    n = 0
+    for X in chunks:
+        n = lib.gptq_hessian_accumulate(H, n, X.to(dev))
+    torch.cuda.synchronize()
+    return to_np(H), n
+
+
+@pytest.mark.parametrize("impl", ["tc", "simt"])
+@pytest.mark.parametrize("d,ntok", [(256, 128), (296, 1000), (1024, 4160)])
+def test_hessian_bf16_small(lib, cuda_device, impl, d, ntok, monkeypatch):
+    """Ragged column tiles (296) and token tails (1000, 4160) against the f64 oracle."""
+    if impl == "simt":
+        monkeypatch.setenv("GPTQ_SYRK", "simt")
+    else:
+        monkeypatch.delenv("GPTQ_SYRK", raising=False)
+    g = torch.Generator().manual_seed(d + ntok)
+    X = (torch.randn(ntok, d, generator=g) * torch.exp(torch.randn(d, generator=g))).bfloat16()
+    H, n = _accumulate(lib, [X], d, cuda_device)
+    ref = O.hessian(X.float().numpy())
+    mask = upper_tile_mask(d)
+    assert n == ntok
+    assert rel_fro(H[mask], ref[mask]) <= H_REL_FRO
+    assert np.all(np.isfinite(H[mask]))
+
+
+def test_hessian_streaming_chunks(lib, cuda_device):
+    """Three uneven calls follow the hook's recurrence (H <- H n/(n+t) + 2/(n+t) X^T X)."""
+    d = 384
+    g = torch.Generator().manual_seed(5)
+    X = (torch.randn(3000, d, generator=g) * 3.0).bfloat16()
+    parts = [X[:700], X[700:701], X[701:]]
+    H, n = _accumulate(lib, parts, d, cuda_device)
+    ref, nref = O.hessian_streaming([p.float().numpy() for p in parts])
+    mask = upper_tile_mask(d)
+    assert n == nref == 3000
+    assert rel_fro(H[mask], ref[mask]) <= H_REL_FRO
+
+
+def test_hessian_fp32_layer_256(lib, cuda_device):
+    """The 256x256 layer's float32 calibration stream (2048 tokens)."""
+    cfg = CONFIGS["layer_256x256"]
+    X = make_tokens(cfg)
+    H, n = _accumulate(lib, [X], cfg.d_in, cuda_device)
+    ref = O.hessian(X.numpy())
+    mask = upper_tile_mask(cfg.d_in)
+    assert n == cfg.n_tokens
+    assert rel_fro(H[mask], ref[mask]) <= H_REL_FRO
+
+
+def test_hessian_zero_tokens_is_noop(lib, cuda_device):
+    d = 64
+    H = torch.ones(d, d, device=cuda_device)
+    n = lib.gptq_hessian_accumulate(H, 5, torch.empty(0, d, dtype=torch.bfloat16, device=cuda_device))
+    assert n == 5 and bool(torch.all(H == 1))
+
+
+@pytest.mark.slow
+def test_hessian_q_proj_full(lib, cuda_device):
+    """q_proj 4096x4096, 262,144 bf16 tokens with outlier channels, in one call: sampled
+    128x128 blocks against the f64 oracle, the diagonal closed form, and v^T H v =
+    2/n ||X v||^2 for random v."""
+    cfg = CONFIGS["q_proj_4096x4096"]
+    dev = cuda_device
+    mult = channel_multipliers(cfg, dev)
+    nch = cfg.n_tokens // cfg.chunk
+    X = torch.cat([make_tokens_chunk(cfg, i, dev, mult) for i in range(nch)])
+    d, n = cfg.d_in, cfg.n_tokens
+    H = torch.empty(d, d, dtype=torch.float32, device=dev)
+    assert lib.gptq_hessian_accumulate(H, 0, X) == n
+    torch.cuda.synchronize()
+    Hn = to_np(H)
+    rng = np.random.default_rng(0)
+    blocks = [(i, j) for i in range(32) for j in range(i, 32)]
+    for bi, bj in [blocks[k] for k in rng.choice(len(blocks), 12, replace=False)] + [(0, 0), (31, 31)]:
+        a = X[:, bi * 128:(bi + 1) * 128].float().cpu().numpy()
+        b = X[:, bj * 128:(bj + 1) * 128].float().cpu().numpy()
+        ref = 2.0 / n * (a.astype(np.float64).T @ b.astype(np.float64))
+        got = Hn[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+        assert rel_fro(got, ref) <= H_REL_FRO, (bi, bj, rel_fro(got, ref))
+    # diagonal: 2/n sum x^2 in float64 on the device
+    diag_ref = (2.0 / n) * (X.double() ** 2).sum(0).cpu().numpy()
+    assert np.max(np.abs(np.diag(Hn) - diag_ref) / diag_ref) <= 1e-5
+    # quadratic forms with the symmetric H built from the upper triangle
+    Hs = np.triu(Hn) + np.triu(Hn, 1).T
+    for s in range(3):
+        v = torch.randn(d, generator=torch.Generator().manual_seed(s), dtype=torch.float64)
+        xv = X.double() @ v.to(dev)
+        ref = float(2.0 / n * (xv * xv).sum())
+        got = float(v.numpy() @ Hs @ v.numpy())
+        assert abs(got - ref) <= 1e-5 * abs(ref)
+    del X
