@@ -9,9 +9,14 @@
 //   warp 0      TMA producer: X tiles [64 tokens x 128 | 256 columns] into a 4-stage ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, both operands
 //               MN-major (the column index of X is contiguous in memory)
-//   warps 2..5  epilogue: tcgen05.ld of a finished accumulator, float32 stores of P[s]
-// Two 256-column accumulators in TMEM let the epilogue of one unit overlap the main
-// loop of the next.  A unit is (row tile I of 128, column tile J of 256, token split s).
+//   warps 2..9  epilogue: drain finished TMEM accumulators into float32 registers, then
+//               store the unit's tile of P[s]
+// A unit is (row tile I of 128, column tile J of 256, token split s).  The tensor core's
+// float32 accumulation does not round to nearest, so its error grows with the length of
+// an accumulation chain; each chain therefore covers only CHAIN stages (256 tokens) and
+// is then added, with round-to-nearest float32 adds in a fixed order, into the epilogue
+// warps' registers.  Two 256-column TMEM accumulators alternate between chains, so the
+// MMAs of one chain overlap the drain of the previous one.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -31,6 +36,9 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * BK * 2;  // one TMA box: 64 columns x 64 tokens
 constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024 + 256;
+constexpr int CHAIN = 4;            // stages per TMEM accumulation chain (256 tokens)
+constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, 128 columns each
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, true, true);
 
 struct SyrkArgs {
@@ -55,7 +63,7 @@ __device__ __forceinline__ void decode_tile(int tile, int n_i, int n_j, int& I, 
   I = 0;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(THREADS, 1)
     syrk_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SyrkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -78,7 +86,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
-      tc::mbar_init(&accempty[b], 4);
+      tc::mbar_init(&accempty[b], EPI_WARPS);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -130,10 +138,13 @@ __global__ void __launch_bounds__(192, 1)
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
-      if (!tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag)) { ok = false; break; }
-      tc::fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < nk; ++kb) {
+        const int kc = kb % CHAIN;
+        if (kc == 0) {
+          if (!tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag)) { ok = false; break; }
+          tc::fence_after();
+        }
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         if (!tc::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
         tc::fence_after();
         const uint32_t abase = tc::smem_u32(smem + stage * STAGE_BYTES);
@@ -144,53 +155,67 @@ __global__ void __launch_bounds__(192, 1)
           // (8192 B) apart.
           const uint64_t ad = tc::smem_desc(abase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
           const uint64_t bd = tc::smem_desc(bbase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
-          tc::mma_f16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          tc::mma_f16(d_tmem, ad, bd, IDESC, (kc | kk) != 0 ? 1u : 0u);
         }
         tc::mma_commit(&empty[stage]);
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+        if (kc == CHAIN - 1 || kb == nk - 1) {
+          tc::mma_commit(&accfull[acc]);
+          acc ^= 1;
+          if (acc == 0) accphase ^= 1u;
+        }
       }
-      if (!ok) break;
-      tc::mma_commit(&accfull[acc]);
-      acc ^= 1;
-      if (acc == 0) accphase ^= 1u;
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp % 4;  // TMEM lane quarter this warp may access
+    const int q = warp % 4;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) / 4;   // which 128 of the 256 columns
     int acc = 0;
     uint32_t accphase = 0;
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int s = static_cast<int>(u / a.n_tiles);
       int I, J;
       decode_tile(static_cast<int>(u % a.n_tiles), a.n_i, a.n_j, I, J);
-      if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag)) { ok = false; break; }
-      tc::fence_after();
-      const int row = I * BM + 32 * q + lane;
-      float* prow = a.P + static_cast<size_t>(s) * a.d * a.d + static_cast<size_t>(row) * a.d;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                               static_cast<uint32_t>(acc * BN + c * 32);
-        tc::tmem_ld_32x32b_x32(taddr, r);
-        tc::tmem_ld_wait();
-        const int col0 = J * BN + c * 32;
-        if (row < a.d) {
+      const int64_t t0 = s * a.tok_per_split;
+      const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
+      const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
+      const int nchain = (nk + CHAIN - 1) / CHAIN;
+      float sum[128];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (col0 + 4 * k < a.d) {
-              float4 v = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                     __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-              *reinterpret_cast<float4*>(prow + col0 + 4 * k) = v;
-            }
+      for (int k = 0; k < 128; ++k) sum[k] = 0.0f;
+      for (int ch = 0; ch < nchain; ++ch) {
+        if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                               static_cast<uint32_t>(acc * BN + half * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tc::tmem_ld_32x32b_x16(tbase + c * 16, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            sum[c * 16 + k] = __fadd_rn(sum[c * 16 + k], __uint_as_float(r[k]));
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+        acc ^= 1;
+        if (acc == 0) accphase ^= 1u;
+      }
+      if (!ok) break;
+      const int row = I * BM + 32 * q + lane;
+      if (row < a.d) {
+        float* prow = a.P + static_cast<size_t>(s) * a.d * a.d + static_cast<size_t>(row) * a.d;
+        const int col0 = J * BN + half * 128;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (col0 + 4 * k < a.d) {
+            *reinterpret_cast<float4*>(prow + col0 + 4 * k) =
+                make_float4(sum[4 * k], sum[4 * k + 1], sum[4 * k + 2], sum[4 * k + 3]);
           }
         }
       }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&accempty[acc]);
-      acc ^= 1;
-      if (acc == 0) accphase ^= 1u;
     }
   }
 
@@ -249,7 +274,7 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.st = st;
   const int64_t units = static_cast<int64_t>(a.n_tiles) * splits;
   const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel, grid, 192, SMEM_BYTES, tmap, a);
+  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel, grid, THREADS, SMEM_BYTES, tmap, a);
 }
 
 }  // namespace gptq

@@ -126,6 +126,15 @@ __global__ void __launch_bounds__(256) fit_kernel(const float* __restrict__ Wp, 
 
 // ---------------------------------------------------------------- the column loop
 
+// 4-byte asynchronous global -> shared copy; with valid == false it writes zero and
+// reads nothing.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+
 struct LoopArgs {
   float* Wp;
   const float* U;
@@ -213,14 +222,18 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
   float(*ush)[BLK] = reinterpret_cast<float(*)[BLK]>(smem_f);
   float* udiag = smem_f + BLK * BLK;
   const int i1 = a.i1, nb = a.nb;
-  for (int q = 0; q < nb; ++q) {
-    const float* urow = a.U + static_cast<size_t>(i1 + q) * a.d + i1 + q + 1;
-    for (int j = threadIdx.x; j < BLK; j += blockDim.x)
-      ush[q][j] = (q + 1 + j < nb) ? urow[j] : 0.0f;
-    if (threadIdx.x == 0) udiag[q] = a.U[static_cast<size_t>(i1 + q) * a.d + i1 + q];
+  // The U block goes to shared memory through cp.async, so that all of its loads are in
+  // flight at once; entries past the block's end are zero-filled.
+  for (int q = 0; q < BLK; ++q) {
+    const float* urow = a.U + static_cast<size_t>(i1 + (q < nb ? q : 0)) * a.d + i1 + q + 1;
+    for (int j = threadIdx.x; j < BLK; j += blockDim.x) {
+      const bool valid = (q + 1 + j < nb);
+      cp_async4(&ush[q][j], valid ? urow + j : a.U, valid);
+    }
   }
-  for (int q = nb; q < BLK; ++q)
-    for (int j = threadIdx.x; j < BLK; j += blockDim.x) ush[q][j] = 0.0f;
+  for (int q = threadIdx.x; q < nb; q += blockDim.x)
+    cp_async4(&udiag[q], a.U + static_cast<size_t>(i1 + q) * a.d + i1 + q, true);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
 
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
