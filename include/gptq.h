@@ -86,6 +86,31 @@ gptq_status gptq_hessian_accumulate(float* H, int64_t* nseen, const void* X, int
                                     void* stream);
 
 /*
+ * gptq_hessian_accumulate_noalloc -- gptq_hessian_accumulate for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an interface addition.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator while it feeds
+ * calibration batches -- a host framework that owns the device pool and forbids
+ * allocations after start-up, a plug-in living inside another program's memory manager,
+ * or a loop that must not take an allocation's implicit device synchronisation.  The
+ * caller still owns and passes H, nseen and X; the scratch (status word and token-split
+ * partials) comes from a fixed 16 MiB (+256 B) array in device memory that the library
+ * holds on every GPU that loads it, until the process exits.
+ *
+ * Same arguments, semantics and errors as gptq_hessian_accumulate, without ws/ws_bytes.
+ * Limit: d_in * d_in * 4 <= 16 MiB, i.e. d_in <= 2048; larger d_in returns
+ * GPTQ_ERR_UNSUPPORTED without touching anything.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (each call clears its status word and rewrites the partials it
+ * reads), so calls whose work overlaps on the GPU -- from two streams or two threads --
+ * race and must be serialised by the caller.
+ */
+gptq_status gptq_hessian_accumulate_noalloc(float* H, int64_t* nseen, const void* X,
+                                            int xdtype, int64_t ntok, int32_t d_in,
+                                            void* stream);
+
+/*
  * gptq_prepare -- everything GPTQ does to H before the column loop.
  *
  * Defined by "GPTQ Architecture, in depth", "The algorithm in code" and "Groups,

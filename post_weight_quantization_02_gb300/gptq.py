@@ -51,6 +51,8 @@ _SIGS = {
     "gptq_workspace_size": (_sz, [_c.c_int, _i64, _i32, _i32, _c.c_int, _c.c_int]),
     "gptq_hessian_accumulate": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int, _i64, _i32,
                                            _vp, _sz, _vp]),
+    "gptq_hessian_accumulate_noalloc": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int,
+                                                   _i64, _i32, _vp]),
     "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
                                 _vp, _sz, _vp]),
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
