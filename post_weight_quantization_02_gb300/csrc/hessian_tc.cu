@@ -13,11 +13,13 @@
 //               store the unit's tile of P[s]
 // A unit is (row tile I of 128, column tile J of 256, token split s).  The tensor core's
 // float32 accumulation does not round to nearest, so its error grows with the length of
-// an accumulation chain; each chain therefore covers only CHAIN stages (256 tokens) and
+// an accumulation chain; each chain therefore covers only a few stages (512 tokens) and
 // is then added, with round-to-nearest float32 adds in a fixed order, into the epilogue
 // warps' registers.  Two 256-column TMEM accumulators alternate between chains, so the
 // MMAs of one chain overlap the drain of the previous one.
 #include <cuda_bf16.h>
+
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -36,7 +38,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * BK * 2;  // one TMA box: 64 columns x 64 tokens
 constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024 + 256;
-constexpr int CHAIN = 4;            // stages per TMEM accumulation chain (256 tokens)
+constexpr int CHAIN_DEFAULT = 8;    // stages per TMEM accumulation chain (512 tokens)
 constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, 128 columns each
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, true, true);
@@ -49,6 +51,7 @@ struct SyrkArgs {
   int n_j;       // column tiles of 256
   int n_tiles;   // tiles intersecting the upper 128-tile triangle
   int splits;
+  int chain;     // stages per accumulation chain
   float* P;      // [splits][d][d]
   DevStatus* st;
 };
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
       for (int kb = 0; kb < nk; ++kb) {
-        const int kc = kb % CHAIN;
+        const int kc = kb % a.chain;
         if (kc == 0) {
           if (!tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag)) { ok = false; break; }
           tc::fence_after();
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc::mma_commit(&empty[stage]);
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
-        if (kc == CHAIN - 1 || kb == nk - 1) {
+        if (kc == a.chain - 1 || kb == nk - 1) {
           tc::mma_commit(&accfull[acc]);
           acc ^= 1;
           if (acc == 0) accphase ^= 1u;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
-      const int nchain = (nk + CHAIN - 1) / CHAIN;
+      const int nchain = (nk + a.chain - 1) / a.chain;
       float sum[128];
 #pragma unroll
       for (int k = 0; k < 128; ++k) sum[k] = 0.0f;
@@ -270,6 +273,11 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.n_j = (d + BN - 1) / BN;
   a.n_tiles = syrk_tc_tiles(d);
   a.splits = splits;
+  a.chain = CHAIN_DEFAULT;
+  if (const char* e = std::getenv("GPTQ_SYRK_CHAIN")) {  // tuning knob: stages per chain
+    const int c = std::atoi(e);
+    if (c >= 1 && c <= 1024) a.chain = c;
+  }
   a.P = P;
   a.st = st;
   const int64_t units = static_cast<int64_t>(a.n_tiles) * splits;

@@ -1,6 +1,8 @@
 // Host-side launchers of the engine's kernels (one translation unit each).
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +26,7 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, DevStatus* st, cudaStream_t s);
+                    float* lam, float* DI, DevStatus* st, cudaStream_t s);
 
 // quantize.cu
 struct QuantArgs {
@@ -37,10 +39,14 @@ struct QuantArgs {
   // workspace
   float* Wp;
   uint8_t* codesT;
-  float* errT;
+  __nv_bfloat16* ehi;   // [128][m] bf16 split of the block's errors
+  __nv_bfloat16* elo;
+  __nv_bfloat16* uhi;   // [d][d] bf16 split of U's strict upper triangle
+  __nv_bfloat16* ulo;
   int32_t* zeros;
   double* loss_rows;
   int32_t* pos;
+  float* Ublk;  // [ceil(d/128)][128*128 + 128]
   // outputs
   int32_t* qweight;
   float* scales;
@@ -50,5 +56,16 @@ struct QuantArgs {
   DevStatus* st;
 };
 void launch_quantize(const QuantArgs& q, cudaStream_t s);
+constexpr int kLoopUblkFloats = 128 * 144 + 128;  // floats of one block's loop layout of U
+
+// lazy_tc.cu
+struct LazyMaps {
+  CUtensorMap ehi, elo, uhi, ulo;
+};
+LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo,
+                        const __nv_bfloat16* uhi, const __nv_bfloat16* ulo, int m, int d);
+void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s);
+void launch_lazy_tc(const LazyMaps& mp, float* W, int m, int d, int i1, DevStatus* st,
+                    cudaStream_t s);
 
 }  // namespace gptq

@@ -12,13 +12,14 @@
 // Hr = J H_damp J directly, so both factorisations run on Hr and the last kernel
 // reverses the inverse into U.
 #include "common.cuh"
+#include "gemm_simt.cuh"
 #include "kernels.cuh"
 
 namespace gptq {
 
 namespace {
 
-constexpr int NB = 64;  // panel width of the blocked factorisation and inverse
+constexpr int NB = 128;  // panel width of the blocked factorisation and inverse
 
 // ---------------------------------------------------------------- diagonal statistics
 
@@ -138,211 +139,120 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 
 // ---------------------------------------------------------------- blocked Cholesky
 
-// Factor the NB x NB diagonal block at (k, k) in place (lower).  One CTA.
-__global__ void __launch_bounds__(256) potf2_kernel(float* __restrict__ A, int d, int k,
-                                                    DevStatus* st, int32_t info_base) {
-  __shared__ float s[NB][NB + 1];
-  __shared__ int bad;
+// Factor the NB x NB diagonal block at (k, k) in place (lower).  One CTA of NB threads;
+// thread r holds row r in registers.  Right-looking with a rolling register window: at
+// step c the window holds the row's columns c .. NB-1 in w[0 ..], so the pivot column is
+// always w[0] and every register index is static; the update writes each compensated
+// column one slot down.  Per step: the pivot's owner publishes it, every later row
+// publishes l_rc, and all rows update.
+__global__ void __launch_bounds__(NB) chol_diag_kernel(float* __restrict__ A, int d, int k,
+                                                       DevStatus* st, int32_t info_base) {
+  __shared__ __align__(16) float col[NB + 4];
+  __shared__ float piv_s;
   if (st->code != 0) return;
   const int nb = min(NB, d - k);
-  for (int e = threadIdx.x; e < NB * NB; e += 256) {
-    const int r = e / NB, c = e % NB;
-    s[r][c] = (r < nb && c <= r) ? A[static_cast<size_t>(k + r) * d + k + c] : 0.0f;
+  const int r = threadIdx.x;
+  float w[NB];
+  const float* arow = A + static_cast<size_t>(k + (r < nb ? r : 0)) * d + k;
+#pragma unroll
+  for (int j = 0; j < NB; j += 4) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nb && j < nb) v = *reinterpret_cast<const float4*>(arow + j);
+    w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
   }
-  if (threadIdx.x == 0) bad = 0;
-  __syncthreads();
+  float lrow_c = 0.0f;  // this row's finished entry of the current column
+#pragma unroll 1
   for (int c = 0; c < nb; ++c) {
-    if (threadIdx.x == 0) {
-      const float piv = s[c][c];
-      if (!(piv > 0.0f) || !isfinite(piv)) {
-        bad = 1;
-        dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c));
-      } else {
-        s[c][c] = sqrtf(piv);
+    if (r == c) piv_s = w[0];
+    __syncthreads();
+    const float piv = piv_s;
+    if (!(piv > 0.0f) || !isfinite(piv)) {
+      if (r == 0) dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c));
+      return;
+    }
+    const float sq = sqrtf(piv);
+    if (r >= c) {
+      lrow_c = (r == c) ? sq : w[0] / sq;
+      if (r < nb) A[static_cast<size_t>(k + r) * d + k + c] = lrow_c;
+    }
+    // col[j'] = l_{c+1+j', c}
+    if (r > c) col[r - c - 1] = lrow_c;
+    __syncthreads();
+    if (r > c) {
+#pragma unroll
+      for (int j = 0; j < NB - 1; j += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(col + j);
+        w[j] = fmaf(-lrow_c, l4.x, w[j + 1]);
+        if (j + 1 < NB - 1) w[j + 1] = fmaf(-lrow_c, l4.y, w[j + 2]);
+        if (j + 2 < NB - 1) w[j + 2] = fmaf(-lrow_c, l4.z, w[j + 3]);
+        if (j + 3 < NB - 1) w[j + 3] = fmaf(-lrow_c, l4.w, w[j + 4 < NB ? j + 4 : NB - 1]);
       }
     }
-    __syncthreads();
-    if (bad) return;
-    const float inv = 1.0f / s[c][c];
-    for (int r = c + 1 + threadIdx.x; r < nb; r += 256) s[r][c] *= inv;
-    __syncthreads();
-    const int m = nb - c - 1;
-    for (int e = threadIdx.x; e < m * m; e += 256) {
-      const int r = c + 1 + e / m, cc = c + 1 + e % m;
-      if (cc <= r) s[r][cc] -= s[r][c] * s[cc][c];
+  }
+}
+
+// Forward substitution L y = b for one right-hand side per thread, L = the NB x NB lower
+// factor at (k, k).  Used twice:
+//   panel (ident == 0): b = row r of A[k+NB:, k:k+NB]; y overwrites it, giving
+//                        L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T;
+//   inverse (ident == 1): b = e_c for c = threadIdx.x, one CTA per diagonal block
+//                        (blockIdx.x), y = column c of L_bb^-1 written to DI[b].
+// Right-looking with the same rolling register window as the factorisation; column t of
+// L below its diagonal is staged in shared memory as lt[t][j'] = L[t+1+j'][t].
+__global__ void __launch_bounds__(NB) trsv_rows_kernel(float* __restrict__ A, int d, int k,
+                                                       int ident, float* __restrict__ DI,
+                                                       const DevStatus* st) {
+  extern __shared__ __align__(16) float smem_f[];
+  float(*lt)[NB] = reinterpret_cast<float(*)[NB]>(smem_f);
+  float* inv = smem_f + NB * NB;
+  if (st->code != 0) return;
+  const int kb = ident ? blockIdx.x * NB : k;
+  const int nb = min(NB, d - kb);
+  for (int e = threadIdx.x; e < NB * NB; e += NB) {
+    const int t = e / NB, j = e % NB;   // lt[t][j] = L[t+1+j][t]
+    lt[t][j] = (t < nb && t + 1 + j < nb) ? A[static_cast<size_t>(kb + t + 1 + j) * d + kb + t] : 0.0f;
+  }
+  for (int t = threadIdx.x; t < NB; t += NB)
+    inv[t] = (t < nb) ? 1.0f / A[static_cast<size_t>(kb + t) * d + kb + t] : 1.0f;
+  __syncthreads();
+  float w[NB];
+  float* yrow = nullptr;
+  if (ident) {
+#pragma unroll
+    for (int j = 0; j < NB; ++j) w[j] = (j == static_cast<int>(threadIdx.x)) ? 1.0f : 0.0f;
+  } else {
+    const int r = k + NB + blockIdx.x * NB + threadIdx.x;
+    if (r >= d) return;
+    yrow = A + static_cast<size_t>(r) * d + k;
+#pragma unroll
+    for (int j = 0; j < NB; j += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(yrow + j);
+      w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
     }
-    __syncthreads();
   }
-  for (int e = threadIdx.x; e < nb * nb; e += 256) {
-    const int r = e / nb, c = e % nb;
-    if (c <= r) A[static_cast<size_t>(k + r) * d + k + c] = s[r][c];
-  }
-}
-
-// Panel below the diagonal block: L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T, one thread per row.
-__global__ void __launch_bounds__(128) trsm_panel_kernel(float* __restrict__ A, int d, int k,
-                                                         const DevStatus* st) {
-  __shared__ float l[NB][NB + 1];
-  __shared__ float inv[NB];
-  if (st->code != 0) return;
-  for (int e = threadIdx.x; e < NB * NB; e += 128) {
-    const int r = e / NB, c = e % NB;
-    l[r][c] = (c <= r) ? A[static_cast<size_t>(k + r) * d + k + c] : 0.0f;
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < NB; c += 128) inv[c] = 1.0f / l[c][c];
-  __syncthreads();
-  const int r = k + NB + blockIdx.x * 128 + threadIdx.x;
-  if (r >= d) return;
-  float* row = A + static_cast<size_t>(r) * d + k;
-  float x[NB];
+  float* dcol = ident ? DI + static_cast<size_t>(blockIdx.x) * NB * NB + threadIdx.x : nullptr;
+#pragma unroll 1
+  for (int t = 0; t < NB; ++t) {
+    const float y = w[0] * inv[t];
+    if (ident) dcol[static_cast<size_t>(t) * NB] = y;
+    else yrow[t] = y;
+    const float* l = lt[t];
 #pragma unroll
-  for (int c = 0; c < NB; c += 4) {
-    float4 v = *reinterpret_cast<const float4*>(row + c);
-    x[c] = v.x; x[c + 1] = v.y; x[c + 2] = v.z; x[c + 3] = v.w;
-  }
-#pragma unroll
-  for (int c = 0; c < NB; ++c) {
-#pragma unroll
-    for (int cp = 0; cp < c; ++cp) x[c] = fmaf(-x[cp], l[c][cp], x[c]);
-    x[c] *= inv[c];
-  }
-#pragma unroll
-  for (int c = 0; c < NB; c += 4)
-    *reinterpret_cast<float4*>(row + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
-}
-
-// C[i][j] -= sum_c A1[i][c] * A2[j][c] over a 64x64 tile, K = NB.  Shared by the
-// Cholesky trailing update (A1 = A2 = panel, lower tiles) and the triangular-inverse
-// update.  Operands are staged transposed: sa[c][i], sb[c][j].
-struct TileOperands {
-  float sa[NB][68];
-  float sb[NB][68];
-};
-
-__device__ __forceinline__ void tile_update(TileOperands& t, int tx, int ty, float (&acc)[4][4]) {
-#pragma unroll 8
-  for (int c = 0; c < NB; ++c) {
-    const float4 a = *reinterpret_cast<const float4*>(&t.sa[c][ty * 4]);
-    const float4 b = *reinterpret_cast<const float4*>(&t.sb[c][tx * 4]);
-    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-  }
-}
-
-// Trailing update of the Cholesky: A[i][j] -= L[i][k:k+NB] . L[j][k:k+NB] for
-// k+NB <= j <= i.  blockIdx.x enumerates 64-tiles (bi >= bj) of the trailing matrix.
-__global__ void __launch_bounds__(256) potrf_update_kernel(float* __restrict__ A, int d, int k,
-                                                           const DevStatus* st) {
-  __shared__ TileOperands t;
-  if (st->code != 0) return;
-  const int base = k + NB;
-  int rem = blockIdx.x, bi = 0;
-  while (rem > bi) { rem -= bi + 1; ++bi; }
-  const int bj = rem;
-  const int i0 = base + bi * 64, j0 = base + bj * 64;
-  for (int e = threadIdx.x; e < 64 * NB; e += 256) {
-    const int r = e / NB, c = e % NB;
-    t.sa[c][r] = (i0 + r < d) ? A[static_cast<size_t>(i0 + r) * d + k + c] : 0.0f;
-    t.sb[c][r] = (j0 + r < d) ? A[static_cast<size_t>(j0 + r) * d + k + c] : 0.0f;
-  }
-  __syncthreads();
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  tile_update(t, tx, ty, acc);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = i0 + ty * 4 + u;
-    if (i >= d) continue;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int j = j0 + tx * 4 + v;
-      if (j <= i) A[static_cast<size_t>(i) * d + j] -= acc[u][v];
+    for (int j = 0; j < NB - 1; j += 4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(l + j);
+      w[j] = fmaf(-y, l4.x, w[j + 1]);
+      if (j + 1 < NB - 1) w[j + 1] = fmaf(-y, l4.y, w[j + 2]);
+      if (j + 2 < NB - 1) w[j + 2] = fmaf(-y, l4.z, w[j + 3]);
+      if (j + 3 < NB - 1) w[j + 3] = fmaf(-y, l4.w, w[j + 4 < NB ? j + 4 : NB - 1]);
     }
   }
 }
 
-// ---------------------------------------------------------------- triangular inverse
-
-// Xb (lower part) = 0 before the inverse.
-__global__ void zero_lower_kernel(float* __restrict__ X, int d) {
+// S = I (the right-hand side of L X = I; updates accumulate into it).
+__global__ void identity_kernel(float* __restrict__ S, int d) {
   const int i = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j <= i && i < d) X[static_cast<size_t>(i) * d + j] = 0.0f;
-}
-
-// Block row i of X = L^-1: X[rows of block i][c] = L_ii^-1 R[rows of block i][c] for
-// every c < (i+1) NB, one thread per column; inside the diagonal block R is the
-// identity, left of it R holds what the updates accumulated.
-__global__ void __launch_bounds__(128) trtri_rows_kernel(const float* __restrict__ L,
-                                                         float* __restrict__ X, int d, int i0,
-                                                         const DevStatus* st) {
-  __shared__ float l[NB][NB + 1];
-  __shared__ float inv[NB];
-  if (st->code != 0) return;
-  const int nb = min(NB, d - i0);
-  for (int e = threadIdx.x; e < NB * NB; e += 128) {
-    const int r = e / NB, c = e % NB;
-    l[r][c] = (r < nb && c <= r) ? L[static_cast<size_t>(i0 + r) * d + i0 + c] : 0.0f;
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < NB; c += 128) inv[c] = (c < nb) ? 1.0f / l[c][c] : 0.0f;
-  __syncthreads();
-  const int c = blockIdx.x * 128 + threadIdx.x;
-  if (c >= i0 + nb) return;
-  float y[NB];
-#pragma unroll
-  for (int r = 0; r < NB; ++r) {
-    float v;
-    if (c >= i0) v = (c - i0 == r) ? 1.0f : 0.0f;
-    else v = (r < nb) ? X[static_cast<size_t>(i0 + r) * d + c] : 0.0f;
-    y[r] = v;
-  }
-#pragma unroll
-  for (int r = 0; r < NB; ++r) {
-#pragma unroll
-    for (int rp = 0; rp < r; ++rp) y[r] = fmaf(-l[r][rp], y[rp], y[r]);
-    y[r] *= inv[r];
-  }
-  // inside the diagonal block the entries above its diagonal come out as exact zeros;
-  // they are written too because the update reads the whole block row
-#pragma unroll
-  for (int r = 0; r < NB; ++r)
-    if (r < nb) X[static_cast<size_t>(i0 + r) * d + c] = y[r];
-}
-
-// X[r][c] -= sum_t L[r][i0+t] X[i0+t][c] for r >= i0+NB, c < i0+NB (64x64 tiles).
-__global__ void __launch_bounds__(256) trtri_update_kernel(const float* __restrict__ L,
-                                                           float* __restrict__ X, int d, int i0,
-                                                           const DevStatus* st) {
-  __shared__ TileOperands t;
-  if (st->code != 0) return;
-  const int r0 = i0 + NB + blockIdx.y * 64;
-  const int c0 = blockIdx.x * 64;
-  for (int e = threadIdx.x; e < 64 * NB; e += 256) {
-    const int r = e / NB, c = e % NB;
-    t.sa[c][r] = (r0 + r < d) ? L[static_cast<size_t>(r0 + r) * d + i0 + c] : 0.0f;
-    // sb[t][col] = X[i0 + t][c0 + col]
-    const int tt = e / 64, col = e % 64;
-    t.sb[tt][col] = (c0 + col < i0 + NB) ? X[static_cast<size_t>(i0 + tt) * d + c0 + col] : 0.0f;
-  }
-  __syncthreads();
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  tile_update(t, tx, ty, acc);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int r = r0 + ty * 4 + u;
-    if (r >= d) continue;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int c = c0 + tx * 4 + v;
-      if (c < i0 + NB) X[static_cast<size_t>(r) * d + c] -= acc[u][v];
-    }
-  }
+  if (j < d) S[static_cast<size_t>(i) * d + j] = (i == j) ? 1.0f : 0.0f;
 }
 
 // U[i][j] = X[d-1-i][d-1-j] for j >= i, 0 below the diagonal.
@@ -358,7 +268,7 @@ __global__ void reverse_kernel(const float* __restrict__ X, int d, float* __rest
 
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, DevStatus* st, cudaStream_t s) {
+                    float* lam, float* DI, DevStatus* st, cudaStream_t s) {
   GPTQ_LAUNCH(GPTQ_K_PREP_DIAG, s, prep_diag_kernel, 1, 1024, 0, H, d, damp, dead, diag_fixed,
               lam, st);
   GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 256), 256, 0,
@@ -375,32 +285,47 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_LAUNCH(GPTQ_K_PREP_GATHER, s, prep_gather_kernel, d, 256, row_smem, S, d, perm, dead, lam,
               Hr);
 
-  // Cholesky of Hr (lower, in place).  A failing pivot at reversed position a reports
-  // processing position d - a (1-based).
+  // Cholesky of Hr (lower, in place), NB-wide panels.  A failing pivot at reversed
+  // position a reports processing position d - a (1-based).
+  const int trsv_smem = (NB * NB + NB) * static_cast<int>(sizeof(float));
+  static bool trsv_attr = false;
+  if (!trsv_attr) {
+    GPTQ_CUDA(cudaFuncSetAttribute(trsv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   trsv_smem));
+    trsv_attr = true;
+  }
   for (int k = 0; k < d; k += NB) {
-    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, s, potf2_kernel, 1, 256, 0, Hr, d, k, st, d);
+    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, s, chol_diag_kernel, 1, NB, 0, Hr, d, k, st, d);
     const int rest = d - k - NB;
     if (rest <= 0) break;
-    GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, s, trsm_panel_kernel, (unsigned)ceil_div(rest, 128), 128, 0,
-                Hr, d, k, st);
-    const int T = static_cast<int>(ceil_div(rest, 64));
-    GPTQ_LAUNCH(GPTQ_K_POTRF_UPDATE, s, potrf_update_kernel, T * (T + 1) / 2, 256, 0, Hr, d, k,
-                st);
+    GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, s, trsv_rows_kernel, (unsigned)ceil_div(rest, NB), NB, trsv_smem,
+                Hr, d, k, 0, DI, st);
+    GemmArgs upd{Hr + static_cast<size_t>(k + NB) * d + k + NB, d,
+                 Hr + static_cast<size_t>(k + NB) * d + k, d,
+                 Hr + static_cast<size_t>(k + NB) * d + k, d, rest, rest, NB, -1.0f, 1.0f};
+    launch_gemm_tile<true, true, true>(GPTQ_K_POTRF_UPDATE, upd, s);
   }
+  // inverses of all diagonal blocks at once
+  GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, s, trsv_rows_kernel, (unsigned)ceil_div(d, NB), NB, trsv_smem, Hr,
+              d, 0, 1, DI, st);
 
-  // X = Hr^-1 (lower) into S, then U = J X J.
+  // X = Hr^-1 (lower) into S: block rows in order, X[i] = DI[i] R[i], then the later rows'
+  // right-hand sides lose L[r, i] X[i].  Then U = J X J.
   {
     dim3 grid((unsigned)ceil_div(d, 256), d);
-    GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, zero_lower_kernel, grid, 256, 0, S, d);
+    GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, identity_kernel, grid, 256, 0, S, d);
   }
   for (int i0 = 0; i0 < d; i0 += NB) {
-    const int ncols = (i0 + NB < d) ? i0 + NB : d;
-    GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, s, trtri_rows_kernel, (unsigned)ceil_div(ncols, 128), 128, 0,
-                Hr, S, d, i0, st);
+    const int nbi = (d - i0 < NB) ? d - i0 : NB;
+    const float* DIi = DI + static_cast<size_t>(i0 / NB) * NB * NB;
+    GemmArgs rows{S + static_cast<size_t>(i0) * d, d, DIi, NB, S + static_cast<size_t>(i0) * d, d,
+                  nbi, i0 + nbi, nbi, 1.0f, 0.0f};
+    launch_gemm_tile<true, false, false>(GPTQ_K_TRTRI_DIAG, rows, s);
     const int rest = d - i0 - NB;
     if (rest <= 0) break;
-    dim3 grid((unsigned)ceil_div(i0 + NB, 64), (unsigned)ceil_div(rest, 64));
-    GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, trtri_update_kernel, grid, 256, 0, Hr, S, d, i0, st);
+    GemmArgs upd{S + static_cast<size_t>(i0 + NB) * d, d, Hr + static_cast<size_t>(i0 + NB) * d + i0,
+                 d, S + static_cast<size_t>(i0) * d, d, rest, i0 + NB, NB, -1.0f, 1.0f};
+    launch_gemm_tile<true, false, false>(GPTQ_K_TRTRI_UPDATE, upd, s);
   }
   {
     dim3 grid((unsigned)ceil_div(d, 256), d);

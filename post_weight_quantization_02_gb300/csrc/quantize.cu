@@ -21,7 +21,6 @@ namespace gptq {
 namespace {
 
 constexpr int BLK = 128;   // columns per block of the loop
-constexpr int CHUNK = 16;  // columns per register-shift chunk
 
 // ---------------------------------------------------------------- permuted copy
 
@@ -126,125 +125,110 @@ __global__ void __launch_bounds__(256) fit_kernel(const float* __restrict__ Wp, 
 
 // ---------------------------------------------------------------- the column loop
 
-// 4-byte asynchronous global -> shared copy; with valid == false it writes zero and
-// reads nothing.
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+// 16-byte asynchronous global -> shared copy.
+__device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
-               "r"(valid ? 4 : 0)
-               : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+// The column loop gives each output row a quad of four lanes; lane t of the quad owns the
+// block's columns c = 4i + t (i = 0..31).  Column q is quantised by its owner (lane q%4),
+// which broadcasts e to the quad; every lane then updates its own later columns.  Each
+// lane keeps a rolling window of 32 registers: during group g (steps 4g .. 4g+3) w[i] is
+// column 4(i+g)+t, and the last step of a group writes every compensated value one slot
+// down, so the window's first slot always holds the lane's next column and every register
+// index is static.  The U rows are laid out so that each (step, lane) reads 32
+// consecutive floats:
+//   Ulay[b][q][t][i] = U[i1+q][i1+c], c = 4(i + g + (q%4 == 3)) + t, if q < c < nb else 0
+// (i < 32, padded to 36 floats per lane), followed by the 128 reciprocals 1/U[i1+q][i1+q].
+constexpr int QUAD = 4;
+constexpr int WIN = BLK / QUAD;                     // 32 columns per lane
+constexpr int LANE_STRIDE = WIN + 4;                // padded: the quad's float4 reads hit
+                                                    // four different bank groups
+constexpr int ROW_STRIDE = QUAD * LANE_STRIDE;      // floats per step q
+constexpr int kUlayFloats = BLK * ROW_STRIDE + BLK;
+static_assert(kUlayFloats == kLoopUblkFloats, "workspace sizing of the loop's U layout");
+
+__global__ void ulayout_kernel(const float* __restrict__ U, int d, float* __restrict__ Ulay) {
+  const int b = blockIdx.x, q = blockIdx.y;
+  const int i1 = b * BLK;
+  const int nb = min(BLK, d - i1);
+  float* out = Ulay + static_cast<size_t>(b) * kUlayFloats;
+  const float* urow = U + static_cast<size_t>(i1 + (q < nb ? q : 0)) * d + i1;
+  const int g = q / QUAD + ((q % QUAD) == QUAD - 1 ? 1 : 0);
+  for (int e = threadIdx.x; e < ROW_STRIDE; e += blockDim.x) {
+    const int t = e / LANE_STRIDE, i = e % LANE_STRIDE;
+    const int c = QUAD * (i + g) + t;
+    out[q * ROW_STRIDE + e] = (i < WIN && q < nb && c > q && c < nb) ? urow[c] : 0.0f;
+  }
+  if (threadIdx.x == 0) out[BLK * ROW_STRIDE + q] = (q < nb) ? 1.0f / urow[q] : 1.0f;
 }
 
 struct LoopArgs {
   float* Wp;
-  const float* U;
+  const float* Ulay;
   int m, d;
   int i1, nb;          // block start and width (nb <= 128)
   int group;           // in-kernel fit width (16, 32, 64 or 128), or 0: fitted outside
-  int gi_outer;        // group index of the outside fit (group 0 == -1 or wide groups)
+  int gi_outer;        // group index of the outside fit (group -1 or wide groups)
   Grid g;
   float* scales;       // [G][m]
   int32_t* zeros;      // [G][m]
   uint8_t* codesT;     // [d][m]
-  float* errT;         // [128][m]
+  __nv_bfloat16* ehi;  // [128][m]: e = hi + lo, both bf16
+  __nv_bfloat16* elo;
   double* loss_rows;   // [m]
 };
 
-// Fit over the first `width` live columns of the rolling row (static width).
-template <int WIDTH>
-__device__ __forceinline__ void fit_regs(const float (&w)[BLK], int live, const Grid& g,
-                                         float& s, float& z) {
+// Group fit over the first NW window slots of each lane of the quad (warp-shuffle
+// min / max across the quad), masking columns past the block's end.
+template <int NW>
+__device__ __forceinline__ void fit_quad(const float (&w)[WIN], int g, int t, int nb,
+                                         const Grid& gr, float& s, float& z) {
   float mn = INFINITY, mx = -INFINITY, am = 0.0f;
 #pragma unroll
-  for (int j = 0; j < WIDTH; ++j) {
-    if (j < live) {
-      mn = fminf(mn, w[j]);
-      mx = fmaxf(mx, w[j]);
-      am = fmaxf(am, fabsf(w[j]));
+  for (int i = 0; i < NW; ++i) {
+    if (QUAD * (i + g) + t < nb) {
+      mn = fminf(mn, w[i]);
+      mx = fmaxf(mx, w[i]);
+      am = fmaxf(am, fabsf(w[i]));
     }
   }
-  fit_from_range(g, mn, mx, am, s, z);
-}
-
-// One chunk of 16 columns.  On entry w[0] is column q0 = 16*C of the block and the row's
-// live columns are w[0 .. nb-q0); each step quantises w[0], then writes the compensated
-// later columns one slot down (w[j] <- w[j+1] - e u_{q, q+1+j}), so that w[0] is always
-// the next column and every register index is static.
-template <int C>
-__device__ __forceinline__ void loop_chunk(float (&w)[BLK], const float (*ush)[BLK],
-                                           const float* udiag, const LoopArgs& a, int r,
-                                           bool active, float& s, float& z, double& loss) {
-  constexpr int LEN = BLK - C * CHUNK;
-  const int q0 = C * CHUNK;
-  if (q0 >= a.nb) return;
-  if (a.group > 0 && (q0 % a.group) == 0) {
-    const int live = a.nb - q0;
-    const int gi = (a.i1 + q0) / a.group;
-    if (a.group == 16) fit_regs<(LEN < 16 ? LEN : 16)>(w, live, a.g, s, z);
-    else if (a.group == 32) fit_regs<(LEN < 32 ? LEN : 32)>(w, live, a.g, s, z);
-    else if (a.group == 64) fit_regs<(LEN < 64 ? LEN : 64)>(w, live, a.g, s, z);
-    else fit_regs<LEN>(w, live, a.g, s, z);
-    if (active) {
-      a.scales[static_cast<size_t>(gi) * a.m + r] = s;
-      a.zeros[static_cast<size_t>(gi) * a.m + r] = static_cast<int32_t>(z);
-    }
-  }
-  const int steps = min(CHUNK, a.nb - q0);
-#pragma unroll 1
-  for (int t = 0; t < steps; ++t) {
-    const int q = q0 + t;
-    const float wq = w[0];
-    const float v = __fdiv_rn(wq, s);
-    const float code = fminf(fmaxf(rintf(v) + z, a.g.lowest), a.g.maxq);
-    const float what = s * (code - z);
-    const float e = __fdiv_rn(wq - what, udiag[q]);
-    if (active) {
-      a.codesT[static_cast<size_t>(a.i1 + q) * a.m + r] = static_cast<uint8_t>(code);
-      a.errT[static_cast<size_t>(q) * a.m + r] = e;
-      loss += 0.5 * static_cast<double>(e) * static_cast<double>(e);
-    }
-    const float* u = ush[q];
 #pragma unroll
-    for (int j = 0; j < LEN - 1; j += 4) {
-      const float4 u4 = *reinterpret_cast<const float4*>(u + j);
-      w[j] = fmaf(-e, u4.x, w[j + 1]);
-      if (j + 1 < LEN - 1) w[j + 1] = fmaf(-e, u4.y, w[j + 2]);
-      if (j + 2 < LEN - 1) w[j + 2] = fmaf(-e, u4.z, w[j + 3]);
-      if (j + 3 < LEN - 1) w[j + 3] = fmaf(-e, u4.w, w[j + 4 < BLK ? j + 4 : BLK - 1]);
-    }
+  for (int o = 1; o < QUAD; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
   }
+  fit_from_range(gr, mn, mx, am, s, z);
 }
 
-// One CTA per 128 rows; the block's U rows (shifted: ush[q][j] = U[i1+q][i1+q+1+j]) and
-// diagonal sit in shared memory, each thread keeps its row's 128 columns in registers.
 __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
   extern __shared__ __align__(16) float smem_f[];
-  float(*ush)[BLK] = reinterpret_cast<float(*)[BLK]>(smem_f);
-  float* udiag = smem_f + BLK * BLK;
+  const float* ulay = smem_f;
+  const float* urinv = smem_f + BLK * ROW_STRIDE;
   const int i1 = a.i1, nb = a.nb;
-  // The U block goes to shared memory through cp.async, so that all of its loads are in
-  // flight at once; entries past the block's end are zero-filled.
-  for (int q = 0; q < BLK; ++q) {
-    const float* urow = a.U + static_cast<size_t>(i1 + (q < nb ? q : 0)) * a.d + i1 + q + 1;
-    for (int j = threadIdx.x; j < BLK; j += blockDim.x) {
-      const bool valid = (q + 1 + j < nb);
-      cp_async4(&ush[q][j], valid ? urow + j : a.U, valid);
-    }
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
+    float4* dst = reinterpret_cast<float4*>(smem_f);
+    for (int e = threadIdx.x; e < kUlayFloats / 4; e += blockDim.x) cp_async16(dst + e, src + e);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   }
-  for (int q = threadIdx.x; q < nb; q += blockDim.x)
-    cp_async4(&udiag[q], a.U + static_cast<size_t>(i1 + q) * a.d + i1 + q, true);
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
 
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x % 32;
+  const int t = lane % QUAD;
+  const int qbase = lane & ~(QUAD - 1);
+  const int r = blockIdx.x * (blockDim.x / QUAD) + threadIdx.x / QUAD;
   const bool active = r < a.m;
-  float w[BLK];
-  const float* wrow = a.Wp + static_cast<size_t>(active ? r : 0) * a.d + i1;
+  float w[WIN];
+  {
+    const float* wrow = a.Wp + static_cast<size_t>(active ? r : 0) * a.d + i1;
 #pragma unroll
-  for (int j = 0; j < BLK; j += 4) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active && j < nb) v = *reinterpret_cast<const float4*>(wrow + j);
-    w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+    for (int i = 0; i < WIN; ++i) {
+      const int c = QUAD * i + t;
+      w[i] = (active && c < nb) ? wrow[c] : 0.0f;
+    }
   }
   float s = 1.0f, z = 0.0f;
   if (a.group == 0 && active) {
@@ -252,63 +236,65 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
   }
   double loss = 0.0;
-  loop_chunk<0>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<1>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<2>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<3>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<4>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<5>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<6>(w, ush, udiag, a, r, active, s, z, loss);
-  loop_chunk<7>(w, ush, udiag, a, r, active, s, z, loss);
-  if (active) a.loss_rows[r] += loss;
-}
-
-// ---------------------------------------------------------------- lazy update (FMA)
-
-// Wp[r][c] -= sum_k ErrT[k][r] U[i1+k][c] for c >= i2 = i1 + nb.  64x64 output tiles,
-// K in chunks of 32.
-__global__ void __launch_bounds__(256) lazy_update_kernel(float* __restrict__ Wp,
-                                                          const float* __restrict__ U,
-                                                          const float* __restrict__ errT,
-                                                          int m, int d, int i1, int nb) {
-  __shared__ __align__(16) float se[32][64];
-  __shared__ __align__(16) float su[32][64];
-  const int i2 = i1 + nb;
-  const int c0 = i2 + blockIdx.x * 64;
-  const int r0 = blockIdx.y * 64;
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < nb; k0 += 32) {
-    for (int e = threadIdx.x; e < 32 * 64; e += 256) {
-      const int k = e / 64, x = e % 64;
-      const bool kin = k0 + k < nb;
-      se[k][x] = (kin && r0 + x < m) ? errT[static_cast<size_t>(k0 + k) * m + r0 + x] : 0.0f;
-      su[k][x] = (kin && c0 + x < d) ? U[static_cast<size_t>(i1 + k0 + k) * d + c0 + x] : 0.0f;
+  const int ngroups = (nb + QUAD - 1) / QUAD;
+#pragma unroll 1
+  for (int g = 0; g < ngroups; ++g) {
+    const int q0 = QUAD * g;
+    if (a.group > 0 && (q0 % a.group) == 0) {
+      if (a.group == 16) fit_quad<4>(w, g, t, nb, a.g, s, z);
+      else if (a.group == 32) fit_quad<8>(w, g, t, nb, a.g, s, z);
+      else if (a.group == 64) fit_quad<16>(w, g, t, nb, a.g, s, z);
+      else fit_quad<WIN>(w, g, t, nb, a.g, s, z);
+      if (active && t == 0) {
+        const int gi = (i1 + q0) / a.group;
+        a.scales[static_cast<size_t>(gi) * a.m + r] = s;
+        a.zeros[static_cast<size_t>(gi) * a.m + r] = static_cast<int32_t>(z);
+      }
     }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float4 a4 = *reinterpret_cast<const float4*>(&se[k][ty * 4]);
-      const float4 b4 = *reinterpret_cast<const float4*>(&su[k][tx * 4]);
-      const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+    for (int o = 0; o < QUAD; ++o) {
+      const int q = q0 + o;
+      // the owner quantises its window's first slot
+      const float wq = w[0];
+      const float v = __fdiv_rn(wq, s);
+      const float code = fminf(fmaxf(rintf(v) + z, a.g.lowest), a.g.maxq);
+      const float what = s * (code - z);
+      const float e_own = (wq - what) * urinv[q < BLK ? q : 0];
+      const float e = __shfl_sync(0xffffffffu, e_own, qbase + o);
+      if (t == o && active && q < nb) {
+        a.codesT[static_cast<size_t>(i1 + q) * a.m + r] = static_cast<uint8_t>(code);
+        const __nv_bfloat16 eh = __float2bfloat16_rn(e);
+        a.ehi[static_cast<size_t>(q) * a.m + r] = eh;
+        a.elo[static_cast<size_t>(q) * a.m + r] = __float2bfloat16_rn(e - __bfloat162float(eh));
+        loss += 0.5 * static_cast<double>(e) * static_cast<double>(e);
+      }
+      const float* u = ulay + (q < BLK ? q : 0) * ROW_STRIDE + t * LANE_STRIDE;
+      if (o < QUAD - 1) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-    }
-    __syncthreads();
-  }
+        for (int i = 0; i < WIN; i += 4) {
+          const float4 u4 = *reinterpret_cast<const float4*>(u + i);
+          w[i] = fmaf(-e, u4.x, w[i]);
+          w[i + 1] = fmaf(-e, u4.y, w[i + 1]);
+          w[i + 2] = fmaf(-e, u4.z, w[i + 2]);
+          w[i + 3] = fmaf(-e, u4.w, w[i + 3]);
+        }
+      } else {
+        // last step of the group: slide the window by one slot
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int r = r0 + ty * 4 + u;
-    if (r >= m) continue;
-    float* wr = Wp + static_cast<size_t>(r) * d;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int c = c0 + tx * 4 + v;
-      if (c < d) wr[c] -= acc[u][v];
+        for (int i = 0; i < WIN; i += 4) {
+          const float4 u4 = *reinterpret_cast<const float4*>(u + i);
+          w[i] = fmaf(-e, u4.x, w[i + 1]);
+          w[i + 1] = fmaf(-e, u4.y, w[i + 2]);
+          w[i + 2] = fmaf(-e, u4.z, w[i + 3]);
+          if (i + 3 < WIN - 1) w[i + 3] = fmaf(-e, u4.w, w[i + 4 < WIN ? i + 4 : WIN - 1]);
+        }
+      }
     }
   }
+  // each lane accumulated the loss of the columns it owns
+  loss += __shfl_xor_sync(0xffffffffu, loss, 1);
+  loss += __shfl_xor_sync(0xffffffffu, loss, 2);
+  if (active && t == 0) a.loss_rows[r] += loss;
 }
 
 // ---------------------------------------------------------------- packing
@@ -408,7 +394,11 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                   static_cast<const float*>(q.W), d, q.perm, q.dead, q.Wp, q.loss_rows, q.st);
     }
 
-    const int loop_smem = (BLK * BLK + BLK) * static_cast<int>(sizeof(float));
+    GPTQ_LAUNCH(GPTQ_K_QUANT_SPLIT, s, ulayout_kernel, dim3((unsigned)ceil_div(d, BLK), BLK), 128,
+                0, q.U, d, q.Ublk);
+    launch_usplit(q.U, d, q.uhi, q.ulo, s);
+    const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, q.uhi, q.ulo, m, d);
+    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float));
     static bool loop_attr = false;
     if (!loop_attr) {
       GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel,
@@ -420,7 +410,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
       const int nb = (d - i1 < BLK) ? d - i1 : BLK;
       LoopArgs a;
       a.Wp = q.Wp;
-      a.U = q.U;
+      a.Ulay = q.Ublk;
       a.m = m;
       a.d = d;
       a.i1 = i1;
@@ -431,7 +421,8 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
       a.scales = q.scales;
       a.zeros = q.zeros;
       a.codesT = q.codesT;
-      a.errT = q.errT;
+      a.ehi = q.ehi;
+      a.elo = q.elo;
       a.loss_rows = q.loss_rows;
       if (!inblock_fit) {
         const bool start = (q.group == -1) ? (i1 == 0) : (i1 % q.group == 0);
@@ -443,13 +434,9 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
         }
         a.gi_outer = gi;
       }
-      GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, 128), 128,
+      GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, 128 / QUAD), 128,
                   loop_smem, a);
-      if (i1 + nb < d) {
-        dim3 grid((unsigned)ceil_div(d - i1 - nb, 64), (unsigned)ceil_div(m, 64));
-        GPTQ_LAUNCH(GPTQ_K_QUANT_LAZY, s, lazy_update_kernel, grid, 256, 0, q.Wp, q.U, q.errT, m,
-                    d, i1, nb);
-      }
+      if (i1 + nb < d) launch_lazy_tc(maps, q.Wp, m, d, i1, q.st, s);  // W[:, i2:] -= Err U
     }
     dim3 gq((unsigned)ceil_div(m, 128), static_cast<unsigned>(q.bits * d / 32));
     GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_kernel, gq, 128, 0, q.codesT, q.pos, m, d,
