@@ -23,10 +23,13 @@ int syrk_tc_token_granule();
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s);
 
+// floats of one 128-column block's solve layout (the loop's U layout, the factor's L)
+constexpr int kLoopUblkFloats = 128 * 160 + 128;
+
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, DevStatus* st, cudaStream_t s);
+                    float* lam, float* DI, float* LL, DevStatus* st, cudaStream_t s);
 
 // quantize.cu
 struct QuantArgs {
@@ -56,7 +59,14 @@ struct QuantArgs {
   DevStatus* st;
 };
 void launch_quantize(const QuantArgs& q, cudaStream_t s);
-constexpr int kLoopUblkFloats = 128 * 144 + 128;  // floats of one block's loop layout of U
+
+// gemm_tc.cu: C[i][j] = beta C[i][j] + alpha sum_{k<128} A[a_row0+i][a_k0+k]
+// B[b_row0+j][b_k0+k], float32-accurate (tf32 x3); maps from make_gemm_map.
+void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int ld);
+void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
+                        const CUtensorMap& mb, int b_row0, int b_k0, float* C, int ldc, int M,
+                        int N, float alpha, float beta, bool lower, DevStatus* st,
+                        cudaStream_t s);
 
 // lazy_tc.cu
 struct LazyMaps {

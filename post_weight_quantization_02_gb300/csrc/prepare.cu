@@ -12,7 +12,6 @@
 // Hr = J H_damp J directly, so both factorisations run on Hr and the last kernel
 // reverses the inverse into U.
 #include "common.cuh"
-#include "gemm_simt.cuh"
 #include "kernels.cuh"
 
 namespace gptq {
@@ -139,111 +138,188 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 
 // ---------------------------------------------------------------- blocked Cholesky
 
-// Factor the NB x NB diagonal block at (k, k) in place (lower).  One CTA of NB threads;
-// thread r holds row r in registers.  Right-looking with a rolling register window: at
-// step c the window holds the row's columns c .. NB-1 in w[0 ..], so the pivot column is
-// always w[0] and every register index is static; the update writes each compensated
-// column one slot down.  Per step: the pivot's owner publishes it, every later row
-// publishes l_rc, and all rows update.
-__global__ void __launch_bounds__(NB) chol_diag_kernel(float* __restrict__ A, int d, int k,
-                                                       DevStatus* st, int32_t info_base) {
-  __shared__ __align__(16) float col[NB + 4];
+// Layout of one factorised diagonal block for the quad triangular solves: for step t
+// (column t of L_kk) and lane u of a group of eight, 16 coefficients
+//   LL[t][u][i] = L_kk[c][t], c = 8(i + t/8 + (t%8 == 7)) + u, if t < c < nb, else 0,
+// (padded to 20), then the 128 reciprocals 1/L_kk[t][t].  Same shape as the column
+// loop's layout of U.
+constexpr int QL = 8, WL = NB / QL, LSTR = WL + 4, RSTR = QL * LSTR, RPT = 128 / QL;
+constexpr int kLLFloats = NB * RSTR + NB;
+static_assert(kLLFloats == kLoopUblkFloats, "workspace sizing of the solve layout");
+
+// Factor the NB x NB diagonal block at (k, k) in place (lower), then write its solve
+// layout LL.  One CTA of 512 threads: each row has a quad of lanes, lane u owning the
+// row's columns 4i+u in a sliding 32-register window (as in the column loop).  Per column
+// c: the diagonal's owner publishes the pivot; each row's owner of column c forms
+// l_rc = a_rc / sqrt(pivot) (sqrt(pivot) on the diagonal), writes it to A, and publishes
+// it at its window position; every later row then subtracts l_rc times the published
+// column from its own entries.
+__global__ void __launch_bounds__(512) chol_diag_kernel(float* __restrict__ A, int d, int k,
+                                                        float* __restrict__ LL, DevStatus* st,
+                                                        int32_t info_base) {
+  constexpr int QF = 4, WF = NB / QF;
+  __shared__ __align__(16) float col_s[QF][WF + 4];
   __shared__ float piv_s;
   if (st->code != 0) return;
   const int nb = min(NB, d - k);
-  const int r = threadIdx.x;
-  float w[NB];
-  const float* arow = A + static_cast<size_t>(k + (r < nb ? r : 0)) * d + k;
+  const int tid = threadIdx.x, lane = tid % 32, u = lane % QF, qb = lane & ~(QF - 1);
+  const int r = tid / QF;
+  float w[WF];
+  {
+    const float* arow = A + static_cast<size_t>(k + (r < nb ? r : 0)) * d + k;
 #pragma unroll
-  for (int j = 0; j < NB; j += 4) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nb && j < nb) v = *reinterpret_cast<const float4*>(arow + j);
-    w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+    for (int i = 0; i < WF; ++i) {
+      const int c = QF * i + u;
+      w[i] = (r < nb) ? (c <= r ? arow[c] : 0.0f) : (c == r ? 1.0f : 0.0f);
+    }
   }
-  float lrow_c = 0.0f;  // this row's finished entry of the current column
+  for (int e = tid; e < QF * (WF + 4); e += 512) (&col_s[0][0])[e] = 0.0f;
+  __syncthreads();
 #pragma unroll 1
-  for (int c = 0; c < nb; ++c) {
-    if (r == c) piv_s = w[0];
-    __syncthreads();
-    const float piv = piv_s;
-    if (!(piv > 0.0f) || !isfinite(piv)) {
-      if (r == 0) dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c));
-      return;
-    }
-    const float sq = sqrtf(piv);
-    if (r >= c) {
-      lrow_c = (r == c) ? sq : w[0] / sq;
-      if (r < nb) A[static_cast<size_t>(k + r) * d + k + c] = lrow_c;
-    }
-    // col[j'] = l_{c+1+j', c}
-    if (r > c) col[r - c - 1] = lrow_c;
-    __syncthreads();
-    if (r > c) {
+  for (int g = 0; g < WF; ++g) {
 #pragma unroll
-      for (int j = 0; j < NB - 1; j += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(col + j);
-        w[j] = fmaf(-lrow_c, l4.x, w[j + 1]);
-        if (j + 1 < NB - 1) w[j + 1] = fmaf(-lrow_c, l4.y, w[j + 2]);
-        if (j + 2 < NB - 1) w[j + 2] = fmaf(-lrow_c, l4.z, w[j + 3]);
-        if (j + 3 < NB - 1) w[j + 3] = fmaf(-lrow_c, l4.w, w[j + 4 < NB ? j + 4 : NB - 1]);
+    for (int o = 0; o < QF; ++o) {
+      const int c = QF * g + o;
+      if (r == c && u == o) piv_s = w[0];
+      __syncthreads();
+      const float piv = piv_s;
+      if (!(piv > 0.0f) || !isfinite(piv)) {
+        if (tid == 0) dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c));
+        return;
+      }
+      const float sq = sqrtf(piv);
+      const float own = (r == c) ? sq : w[0] / sq;
+      const float lrc = __shfl_sync(0xffffffffu, own, qb + o);
+      if (u == o && r >= c && r < nb && c < nb) A[static_cast<size_t>(k + r) * d + k + c] = lrc;
+      if (u == o && r > c) col_s[r % QF][r / QF - g - (o == QF - 1 ? 1 : 0)] = lrc;
+      __syncthreads();
+      if (r > c) {
+        const float* cl = col_s[u];
+        if (o < QF - 1) {
+#pragma unroll
+          for (int i = 0; i < WF; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(cl + i);
+            w[i] = fmaf(-lrc, l4.x, w[i]);
+            w[i + 1] = fmaf(-lrc, l4.y, w[i + 1]);
+            w[i + 2] = fmaf(-lrc, l4.z, w[i + 2]);
+            w[i + 3] = fmaf(-lrc, l4.w, w[i + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < WF; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(cl + i);
+            w[i] = fmaf(-lrc, l4.x, w[i + 1]);
+            w[i + 1] = fmaf(-lrc, l4.y, w[i + 2]);
+            w[i + 2] = fmaf(-lrc, l4.z, w[i + 3]);
+            if (i + 3 < WF - 1) w[i + 3] = fmaf(-lrc, l4.w, w[i + 4 < WF ? i + 4 : WF - 1]);
+          }
+        }
       }
     }
   }
+  __syncthreads();  // the factor's global writes are visible to the whole CTA
+  float* out = LL + static_cast<size_t>(k / NB) * kLLFloats;
+#pragma unroll 8
+  for (int e = tid; e < NB * RSTR; e += 512) {
+    const int t = e / RSTR, uu = (e % RSTR) / LSTR, i = e % LSTR;
+    const int c = QL * (i + t / QL + ((t % QL) == QL - 1 ? 1 : 0)) + uu;
+    out[e] = (i < WL && t < nb && c > t && c < nb) ? A[static_cast<size_t>(k + c) * d + k + t] : 0.0f;
+  }
+  for (int t = tid; t < NB; t += 512)
+    out[NB * RSTR + t] = (t < nb) ? 1.0f / A[static_cast<size_t>(k + t) * d + k + t] : 1.0f;
 }
 
-// Forward substitution L y = b for one right-hand side per thread, L = the NB x NB lower
-// factor at (k, k).  Used twice:
-//   panel (ident == 0): b = row r of A[k+NB:, k:k+NB]; y overwrites it, giving
-//                        L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T;
-//   inverse (ident == 1): b = e_c for c = threadIdx.x, one CTA per diagonal block
-//                        (blockIdx.x), y = column c of L_bb^-1 written to DI[b].
-// Right-looking with the same rolling register window as the factorisation; column t of
-// L below its diagonal is staged in shared memory as lt[t][j'] = L[t+1+j'][t].
-__global__ void __launch_bounds__(NB) trsv_rows_kernel(float* __restrict__ A, int d, int k,
-                                                       int ident, float* __restrict__ DI,
-                                                       const DevStatus* st) {
+// Forward substitution L_bb y = b, one right-hand side per group of QL = 8 lanes (lane u
+// owns unknowns 8i+u; a 16-register window slides as in the column loop).
+//   panel (ident == 0): b = row r of A[k+NB:, k:k+NB], y overwrites it, giving
+//                       L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T;
+//   inverse (ident == 1): b = e_c for 16 values of c per CTA (blockIdx.x = 8*block +
+//                       part), y = column c of L_bb^-1, written to DI[block].
+__global__ void __launch_bounds__(128) trsv_quad_kernel(float* __restrict__ A, int d, int k,
+                                                        int ident, const float* __restrict__ LLall,
+                                                        float* __restrict__ DI,
+                                                        const DevStatus* st) {
   extern __shared__ __align__(16) float smem_f[];
-  float(*lt)[NB] = reinterpret_cast<float(*)[NB]>(smem_f);
-  float* inv = smem_f + NB * NB;
+  float* ys = smem_f + kLLFloats;  // [NB][RPT] staged results
   if (st->code != 0) return;
-  const int kb = ident ? blockIdx.x * NB : k;
+  const int blk = ident ? blockIdx.x / QL : k / NB;
+  const int part = ident ? blockIdx.x % QL : 0;
+  const int kb = blk * NB;
   const int nb = min(NB, d - kb);
-  for (int e = threadIdx.x; e < NB * NB; e += NB) {
-    const int t = e / NB, j = e % NB;   // lt[t][j] = L[t+1+j][t]
-    lt[t][j] = (t < nb && t + 1 + j < nb) ? A[static_cast<size_t>(kb + t + 1 + j) * d + kb + t] : 0.0f;
+  {
+    const float4* src = reinterpret_cast<const float4*>(LLall + static_cast<size_t>(blk) * kLLFloats);
+    float4* dst = reinterpret_cast<float4*>(smem_f);
+    for (int e = threadIdx.x; e < kLLFloats / 4; e += 128) {
+      const uint32_t s_addr = static_cast<uint32_t>(__cvta_generic_to_shared(dst + e));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s_addr), "l"(src + e) : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   }
-  for (int t = threadIdx.x; t < NB; t += NB)
-    inv[t] = (t < nb) ? 1.0f / A[static_cast<size_t>(kb + t) * d + kb + t] : 1.0f;
   __syncthreads();
-  float w[NB];
-  float* yrow = nullptr;
+  const float* lay = smem_f;
+  const float* rinv = smem_f + NB * RSTR;
+  const int lane = threadIdx.x % 32, u = lane % QL, qbase = lane & ~(QL - 1);
+  const int rl = threadIdx.x / QL;  // 0..RPT-1
+  float w[WL];
+  int nrows;
+  size_t row0;
   if (ident) {
+    const int c = part * RPT + rl;
 #pragma unroll
-    for (int j = 0; j < NB; ++j) w[j] = (j == static_cast<int>(threadIdx.x)) ? 1.0f : 0.0f;
+    for (int i = 0; i < WL; ++i) w[i] = (QL * i + u == c) ? 1.0f : 0.0f;
+    nrows = RPT;
+    row0 = 0;
   } else {
-    const int r = k + NB + blockIdx.x * NB + threadIdx.x;
-    if (r >= d) return;
-    yrow = A + static_cast<size_t>(r) * d + k;
+    const int rbase = k + NB + blockIdx.x * RPT;
+    nrows = min(RPT, d - rbase);
+    row0 = static_cast<size_t>(rbase);
+    const float* arow = A + static_cast<size_t>(rbase + (rl < nrows ? rl : 0)) * d + k;
 #pragma unroll
-    for (int j = 0; j < NB; j += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(yrow + j);
-      w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+    for (int i = 0; i < WL; ++i) w[i] = (rl < nrows) ? arow[QL * i + u] : 0.0f;
+  }
+  const int ngroups = (nb + QL - 1) / QL;
+#pragma unroll 1
+  for (int g = 0; g < ngroups; ++g) {
+#pragma unroll
+    for (int o = 0; o < QL; ++o) {
+      const int t = QL * g + o;
+      const float y = __shfl_sync(0xffffffffu, w[0] * rinv[t], qbase + o);
+      if (u == o) ys[t * RPT + rl] = y;
+      const float* l = lay + t * RSTR + u * LSTR;
+      if (o < QL - 1) {
+#pragma unroll
+        for (int i = 0; i < WL; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(l + i);
+          w[i] = fmaf(-y, l4.x, w[i]);
+          w[i + 1] = fmaf(-y, l4.y, w[i + 1]);
+          w[i + 2] = fmaf(-y, l4.z, w[i + 2]);
+          w[i + 3] = fmaf(-y, l4.w, w[i + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < WL; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(l + i);
+          w[i] = fmaf(-y, l4.x, w[i + 1]);
+          w[i + 1] = fmaf(-y, l4.y, w[i + 2]);
+          w[i + 2] = fmaf(-y, l4.z, w[i + 3]);
+          if (i + 3 < WL - 1) w[i + 3] = fmaf(-y, l4.w, w[i + 4 < WL ? i + 4 : WL - 1]);
+        }
+      }
     }
   }
-  float* dcol = ident ? DI + static_cast<size_t>(blockIdx.x) * NB * NB + threadIdx.x : nullptr;
-#pragma unroll 1
-  for (int t = 0; t < NB; ++t) {
-    const float y = w[0] * inv[t];
-    if (ident) dcol[static_cast<size_t>(t) * NB] = y;
-    else yrow[t] = y;
-    const float* l = lt[t];
-#pragma unroll
-    for (int j = 0; j < NB - 1; j += 4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(l + j);
-      w[j] = fmaf(-y, l4.x, w[j + 1]);
-      if (j + 1 < NB - 1) w[j + 1] = fmaf(-y, l4.y, w[j + 2]);
-      if (j + 2 < NB - 1) w[j + 2] = fmaf(-y, l4.z, w[j + 3]);
-      if (j + 3 < NB - 1) w[j + 3] = fmaf(-y, l4.w, w[j + 4 < NB ? j + 4 : NB - 1]);
+  __syncthreads();
+  if (ident) {
+    // DI[blk][t][c] for the CTA's RPT columns c, all NB rows t (zeros above the diagonal
+    // come out of the substitution exactly); identity past a ragged end
+    float* dout = DI + static_cast<size_t>(blk) * NB * NB + part * RPT;
+    for (int e = threadIdx.x; e < NB * RPT; e += 128) {
+      const int t = e / RPT, j = e % RPT;
+      dout[static_cast<size_t>(t) * NB + j] = (t < nb) ? ys[e] : (t == part * RPT + j ? 1.0f : 0.0f);
+    }
+  } else {
+    for (int e = threadIdx.x; e < nrows * NB; e += 128) {
+      const int j = e / NB, t = e % NB;
+      if (t < nb) A[(row0 + j) * d + k + t] = ys[t * RPT + j];
     }
   }
 }
@@ -255,20 +331,27 @@ __global__ void identity_kernel(float* __restrict__ S, int d) {
   if (j < d) S[static_cast<size_t>(i) * d + j] = (i == j) ? 1.0f : 0.0f;
 }
 
-// U[i][j] = X[d-1-i][d-1-j] for j >= i, 0 below the diagonal.
-__global__ void reverse_kernel(const float* __restrict__ X, int d, float* __restrict__ U) {
-  const int i = blockIdx.y;
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
-  U[static_cast<size_t>(i) * d + j] =
-      (j >= i) ? X[static_cast<size_t>(d - 1 - i) * d + (d - 1 - j)] : 0.0f;
+// U[i][j] = X[d-1-i][d-1-j] = Y[d-1-j][d-1-i] for j >= i, 0 below the diagonal; 32x32
+// tiles transposed through shared memory.
+__global__ void reverse_transpose_kernel(const float* __restrict__ Y, int d, float* __restrict__ U) {
+  __shared__ float t[32][33];
+  const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+  for (int jj = threadIdx.y; jj < 32; jj += 8) {
+    const int j = j0 + jj, ii = threadIdx.x, i = i0 + ii;
+    t[jj][ii] = (i < d && j < d) ? Y[static_cast<size_t>(d - 1 - j) * d + (d - 1 - i)] : 0.0f;
+  }
+  __syncthreads();
+  for (int ii = threadIdx.y; ii < 32; ii += 8) {
+    const int i = i0 + ii, jj = threadIdx.x, j = j0 + jj;
+    if (i < d && j < d) U[static_cast<size_t>(i) * d + j] = (j >= i) ? t[jj][ii] : 0.0f;
+  }
 }
 
 }  // namespace
 
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, DevStatus* st, cudaStream_t s) {
+                    float* lam, float* DI, float* LL, DevStatus* st, cudaStream_t s) {
   GPTQ_LAUNCH(GPTQ_K_PREP_DIAG, s, prep_diag_kernel, 1, 1024, 0, H, d, damp, dead, diag_fixed,
               lam, st);
   GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 256), 256, 0,
@@ -287,49 +370,54 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
 
   // Cholesky of Hr (lower, in place), NB-wide panels.  A failing pivot at reversed
   // position a reports processing position d - a (1-based).
-  const int trsv_smem = (NB * NB + NB) * static_cast<int>(sizeof(float));
-  static bool trsv_attr = false;
-  if (!trsv_attr) {
-    GPTQ_CUDA(cudaFuncSetAttribute(trsv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int trsv_smem = (kLLFloats + NB * RPT) * static_cast<int>(sizeof(float));
+  static bool attrs = false;
+  if (!attrs) {
+    GPTQ_CUDA(cudaFuncSetAttribute(trsv_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    trsv_smem));
-    trsv_attr = true;
+    attrs = true;
   }
+  CUtensorMap mHr, mS, mDI;
+  make_gemm_map(&mHr, Hr, d, d, d);
+  make_gemm_map(&mS, S, d, d, d);
+  make_gemm_map(&mDI, DI, static_cast<int>(ceil_div(d, NB)) * NB, NB, NB);
   for (int k = 0; k < d; k += NB) {
-    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, s, chol_diag_kernel, 1, NB, 0, Hr, d, k, st, d);
+    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, s, chol_diag_kernel, 1, 512, 0, Hr, d, k, LL, st, d);
     const int rest = d - k - NB;
     if (rest <= 0) break;
-    GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, s, trsv_rows_kernel, (unsigned)ceil_div(rest, NB), NB, trsv_smem,
-                Hr, d, k, 0, DI, st);
-    GemmArgs upd{Hr + static_cast<size_t>(k + NB) * d + k + NB, d,
-                 Hr + static_cast<size_t>(k + NB) * d + k, d,
-                 Hr + static_cast<size_t>(k + NB) * d + k, d, rest, rest, NB, -1.0f, 1.0f};
-    launch_gemm_tile<true, true, true>(GPTQ_K_POTRF_UPDATE, upd, s);
+    GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, s, trsv_quad_kernel, (unsigned)ceil_div(rest, RPT), 128, trsv_smem,
+                Hr, d, k, 0, LL, DI, st);
+    // trailing update, lower tiles: Hr[k+NB+i][k+NB+j] -= L[k+NB+i, panel] . L[k+NB+j, panel]
+    launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
+                       Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest, rest, -1.0f, 1.0f,
+                       true, st, s);
   }
   // inverses of all diagonal blocks at once
-  GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, s, trsv_rows_kernel, (unsigned)ceil_div(d, NB), NB, trsv_smem, Hr,
-              d, 0, 1, DI, st);
+  GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, s, trsv_quad_kernel, (unsigned)(ceil_div(d, NB) * QL), 128, trsv_smem,
+              Hr, d, 0, 1, LL, DI, st);
 
-  // X = Hr^-1 (lower) into S: block rows in order, X[i] = DI[i] R[i], then the later rows'
-  // right-hand sides lose L[r, i] X[i].  Then U = J X J.
+  // The inverse X = L^-1 (L = the factor of Hr), kept transposed as Y = X^T in S so that
+  // both GEMM operands are K-major.  Block columns of Y in order: Y[:, blk i] = R DI[i]^T
+  // (R = Y's right-hand side, initially I), then every later block column loses
+  // Y[:, blk i] L[r, blk i]^T.  Finally U = J X J = (J Y J)^T.
   {
     dim3 grid((unsigned)ceil_div(d, 256), d);
     GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, identity_kernel, grid, 256, 0, S, d);
   }
   for (int i0 = 0; i0 < d; i0 += NB) {
     const int nbi = (d - i0 < NB) ? d - i0 : NB;
-    const float* DIi = DI + static_cast<size_t>(i0 / NB) * NB * NB;
-    GemmArgs rows{S + static_cast<size_t>(i0) * d, d, DIi, NB, S + static_cast<size_t>(i0) * d, d,
-                  nbi, i0 + nbi, nbi, 1.0f, 0.0f};
-    launch_gemm_tile<true, false, false>(GPTQ_K_TRTRI_DIAG, rows, s);
+    // Y[c][i0+t] = sum_k Y[c][i0+k] DI[i][t][k], rows c < i0 + nbi
+    launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, i0, mDI, i0, 0, S + i0, d, i0 + nbi, nbi, 1.0f,
+                       0.0f, false, st, s);
     const int rest = d - i0 - NB;
     if (rest <= 0) break;
-    GemmArgs upd{S + static_cast<size_t>(i0 + NB) * d, d, Hr + static_cast<size_t>(i0 + NB) * d + i0,
-                 d, S + static_cast<size_t>(i0) * d, d, rest, i0 + NB, NB, -1.0f, 1.0f};
-    launch_gemm_tile<true, false, false>(GPTQ_K_TRTRI_UPDATE, upd, s);
+    // Y[c][r] -= sum_k Y[c][i0+k] L[r][i0+k], c < i0 + NB <= r
+    launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, i0, mHr, i0 + NB, i0, S + i0 + NB, d, i0 + NB,
+                       rest, -1.0f, 1.0f, false, st, s);
   }
   {
-    dim3 grid((unsigned)ceil_div(d, 256), d);
-    GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_kernel, grid, 256, 0, S, d, U);
+    dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
+    GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_transpose_kernel, grid, dim3(32, 8), 0, S, d, U);
   }
 }
 

@@ -1,5 +1,5 @@
-// gptq_quantize_layer kernels: permuted working copy of W, group fit, the resident-block
-// column loop, the lazy trailing update (float32 FMA path), packing and the loss sum.
+// gptq_quantize_layer kernels: permuted working copy of W, group fit, the column loop,
+// packing and the loss sum (the lazy update's tensor-core kernel is in lazy_tc.cu).
 //
 // Method ("GPTQ Architecture, in depth", "The algorithm in code" and "Packing, tooling
 // and serving"; "Same Ruler, Smarter Placement: GPTQ", sections 1.5 and 1.8):
@@ -9,8 +9,10 @@
 //       e = (w_q - what) / U_qq; W[:, q+1:i2] -= e U[q, q+1:i2]; Err[:, q-i1] = e
 //     W[:, i2:] -= Err U[i1:i2, i2:]          (the lazy update)
 // Layouts in the workspace: Wp [m][d] float32 (processing order), codesT [d][m] uint8
-// (column-major codes, so that a step's codes are one coalesced row), ErrT [128][m]
-// float32, zeros [G][m] int32, loss_rows [m] float64, pos [d] int32 (inverse perm).
+// (column-major codes, so that a step's codes are one coalesced row), the block's errors
+// as bf16 halves ehi/elo [128][m] (e = hi + lo), U's bf16 halves [d][d], the loop's
+// per-block layout of U, zeros [G][m] int32, loss_rows [m] float64 and pos [d] int32
+// (the inverse permutation).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -79,6 +81,15 @@ struct Grid {
   float zfix;
 };
 
+// w / s as the reciprocal product with one residual correction: within one ulp of the
+// IEEE quotient (the two differ only where w / s sits on a rounding boundary of the
+// quotient itself, far inside the near-tie band the parity check allows).
+__device__ __forceinline__ float div_by_scale(float w, float s, float rs) {
+  const float v0 = w * rs;
+  const float r = fmaf(-v0, s, w);
+  return fmaf(r, rs, v0);
+}
+
 // Scale and zero of one row of a group from its min / max (or max |w|), float32.
 __device__ __forceinline__ void fit_from_range(const Grid& g, float mn, float mx, float amax,
                                                float& s, float& z) {
@@ -131,20 +142,20 @@ __device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
-// The column loop gives each output row a quad of four lanes; lane t of the quad owns the
-// block's columns c = 4i + t (i = 0..31).  Column q is quantised by its owner (lane q%4),
-// which broadcasts e to the quad; every lane then updates its own later columns.  Each
-// lane keeps a rolling window of 32 registers: during group g (steps 4g .. 4g+3) w[i] is
-// column 4(i+g)+t, and the last step of a group writes every compensated value one slot
-// down, so the window's first slot always holds the lane's next column and every register
-// index is static.  The U rows are laid out so that each (step, lane) reads 32
+// The column loop gives each output row a group of QUAD = 8 lanes; lane t owns the block's
+// columns c = 8i + t (i = 0..15).  Column q is quantised by its owner (lane q%8), which
+// broadcasts e to the group; every lane then updates its own later columns.  Each lane
+// keeps a rolling window of 16 registers: during window step g (columns 8g .. 8g+7) w[i]
+// is column 8(i+g)+t, and the last column of a step writes every compensated value one
+// slot down, so the window's first slot always holds the lane's next column and every
+// register index is static.  The U rows are laid out so that each (column, lane) reads 16
 // consecutive floats:
-//   Ulay[b][q][t][i] = U[i1+q][i1+c], c = 4(i + g + (q%4 == 3)) + t, if q < c < nb else 0
-// (i < 32, padded to 36 floats per lane), followed by the 128 reciprocals 1/U[i1+q][i1+q].
-constexpr int QUAD = 4;
-constexpr int WIN = BLK / QUAD;                     // 32 columns per lane
-constexpr int LANE_STRIDE = WIN + 4;                // padded: the quad's float4 reads hit
-                                                    // four different bank groups
+//   Ulay[b][q][t][i] = U[i1+q][i1+c], c = 8(i + g + (q%8 == 7)) + t, if q < c < nb else 0
+// (i < 16, padded to 20 floats per lane), followed by the 128 reciprocals 1/U[i1+q][i1+q].
+constexpr int QUAD = 8;
+constexpr int WIN = BLK / QUAD;                     // 16 columns per lane
+constexpr int LANE_STRIDE = WIN + 4;                // padded: the group's float4 reads hit
+                                                    // eight different bank groups
 constexpr int ROW_STRIDE = QUAD * LANE_STRIDE;      // floats per step q
 constexpr int kUlayFloats = BLK * ROW_STRIDE + BLK;
 static_assert(kUlayFloats == kLoopUblkFloats, "workspace sizing of the loop's U layout");
@@ -180,8 +191,8 @@ struct LoopArgs {
   double* loss_rows;   // [m]
 };
 
-// Group fit over the first NW window slots of each lane of the quad (warp-shuffle
-// min / max across the quad), masking columns past the block's end.
+// Group fit over the first NW window slots of each lane of the row's lane group
+// (warp-shuffle min / max across the group), masking columns past the block's end.
 template <int NW>
 __device__ __forceinline__ void fit_quad(const float (&w)[WIN], int g, int t, int nb,
                                          const Grid& gr, float& s, float& z) {
@@ -207,6 +218,12 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   const float* ulay = smem_f;
   const float* urinv = smem_f + BLK * ROW_STRIDE;
+  // the block's codes and bf16 error halves, staged so that the global writes are whole
+  // rows of 32 consecutive output rows
+  constexpr int RPC = 128 / QUAD;  // rows per CTA
+  uint8_t* codes_s = reinterpret_cast<uint8_t*>(smem_f + kUlayFloats);               // [128][32]
+  __nv_bfloat16* ehi_s = reinterpret_cast<__nv_bfloat16*>(codes_s + BLK * RPC);      // [128][32]
+  __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][32]
   const int i1 = a.i1, nb = a.nb;
   {
     const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
@@ -235,16 +252,22 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
     s = a.scales[static_cast<size_t>(a.gi_outer) * a.m + r];
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
   }
-  double loss = 0.0;
+  float rs = __frcp_rn(s);
+  const int rl = threadIdx.x / QUAD;  // row within the CTA
+  // a block's share of the loss (at most 16 terms per lane) is summed in float32 and
+  // added to the row's float64 total once per block; FP64 arithmetic inside the step
+  // chain would serialise on this part's low FP64 rate
+  float loss = 0.0f;
   const int ngroups = (nb + QUAD - 1) / QUAD;
 #pragma unroll 1
   for (int g = 0; g < ngroups; ++g) {
     const int q0 = QUAD * g;
     if (a.group > 0 && (q0 % a.group) == 0) {
-      if (a.group == 16) fit_quad<4>(w, g, t, nb, a.g, s, z);
-      else if (a.group == 32) fit_quad<8>(w, g, t, nb, a.g, s, z);
-      else if (a.group == 64) fit_quad<16>(w, g, t, nb, a.g, s, z);
+      if (a.group == 16) fit_quad<16 / QUAD>(w, g, t, nb, a.g, s, z);
+      else if (a.group == 32) fit_quad<32 / QUAD>(w, g, t, nb, a.g, s, z);
+      else if (a.group == 64) fit_quad<64 / QUAD>(w, g, t, nb, a.g, s, z);
       else fit_quad<WIN>(w, g, t, nb, a.g, s, z);
+      rs = __frcp_rn(s);
       if (active && t == 0) {
         const int gi = (i1 + q0) / a.group;
         a.scales[static_cast<size_t>(gi) * a.m + r] = s;
@@ -256,17 +279,17 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
       const int q = q0 + o;
       // the owner quantises its window's first slot
       const float wq = w[0];
-      const float v = __fdiv_rn(wq, s);
+      const float v = div_by_scale(wq, s, rs);
       const float code = fminf(fmaxf(rintf(v) + z, a.g.lowest), a.g.maxq);
       const float what = s * (code - z);
       const float e_own = (wq - what) * urinv[q < BLK ? q : 0];
       const float e = __shfl_sync(0xffffffffu, e_own, qbase + o);
-      if (t == o && active && q < nb) {
-        a.codesT[static_cast<size_t>(i1 + q) * a.m + r] = static_cast<uint8_t>(code);
+      if (t == o) {
         const __nv_bfloat16 eh = __float2bfloat16_rn(e);
-        a.ehi[static_cast<size_t>(q) * a.m + r] = eh;
-        a.elo[static_cast<size_t>(q) * a.m + r] = __float2bfloat16_rn(e - __bfloat162float(eh));
-        loss += 0.5 * static_cast<double>(e) * static_cast<double>(e);
+        codes_s[q * RPC + rl] = static_cast<uint8_t>(code);
+        ehi_s[q * RPC + rl] = eh;
+        elo_s[q * RPC + rl] = __float2bfloat16_rn(e - __bfloat162float(eh));
+        if (q < nb) loss = fmaf(0.5f * e, e, loss);
       }
       const float* u = ulay + (q < BLK ? q : 0) * ROW_STRIDE + t * LANE_STRIDE;
       if (o < QUAD - 1) {
@@ -292,9 +315,20 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
     }
   }
   // each lane accumulated the loss of the columns it owns
-  loss += __shfl_xor_sync(0xffffffffu, loss, 1);
-  loss += __shfl_xor_sync(0xffffffffu, loss, 2);
-  if (active && t == 0) a.loss_rows[r] += loss;
+#pragma unroll
+  for (int o = 1; o < QUAD; o <<= 1) loss += __shfl_xor_sync(0xffffffffu, loss, o);
+  if (active && t == 0) a.loss_rows[r] += static_cast<double>(loss);
+  __syncthreads();
+  const int r0 = blockIdx.x * RPC;
+  const int nrows = min(RPC, a.m - r0);
+  for (int e = threadIdx.x; e < nb * RPC; e += blockDim.x) {
+    const int q = e / RPC, j = e % RPC;
+    if (j < nrows) {
+      a.codesT[static_cast<size_t>(i1 + q) * a.m + r0 + j] = codes_s[e];
+      a.ehi[static_cast<size_t>(q) * a.m + r0 + j] = ehi_s[e];
+      a.elo[static_cast<size_t>(q) * a.m + r0 + j] = elo_s[e];
+    }
+  }
 }
 
 // ---------------------------------------------------------------- packing
@@ -398,7 +432,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
     const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, q.uhi, q.ulo, m, d);
-    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float));
+    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float)) + BLK * (128 / QUAD) * (1 + 2 + 2);
     static bool loop_attr = false;
     if (!loop_attr) {
       GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel,

@@ -47,16 +47,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up (returns false) when
-// another role of the CTA raised *abort, or after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, polling with the non-blocking
+// test_wait (a suspended try_wait was observed to wake late).  Gives up (returns false)
+// when another role of the CTA raised *abort, or after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 31) == 0) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((it & 255) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) return false;
     }
