@@ -264,6 +264,7 @@ gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
     float* lam = wc.take<float>(1);
     float* DI = wc.take<float>(static_cast<size_t>(ceil_div(d_in, 128)) * 128 * 128);
     float* LL = wc.take<float>(static_cast<size_t>(ceil_div(d_in, 128)) * kLoopUblkFloats);
+    std::lock_guard<std::mutex> lk(aux_mutex());  // the internal streams are shared
     begin_call(st, s);
     launch_prepare(H, d_in, damp, actorder ? 1 : 0, perm, dead, Hinv_chol, S, Hr, diag, lam, DI,
                    LL, st, s);

@@ -6,7 +6,9 @@
 #include <stdint.h>
 
 #include <cstdio>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/gptq.h"
 
@@ -103,5 +105,16 @@ const std::string& last_error();
 
 // Number of SMs of the current device.
 int sm_count();
+
+// Two library-internal streams of the current device (a: high priority, b: low priority)
+// and at least `nevents` timing-free events, created on first use and kept for the life
+// of the process.  Calls that use them hold aux_mutex() until their work has finished.
+struct AuxStreams {
+  cudaStream_t a = nullptr;
+  cudaStream_t b = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+AuxStreams& aux_streams(int nevents);
+std::mutex& aux_mutex();
 
 }  // namespace gptq

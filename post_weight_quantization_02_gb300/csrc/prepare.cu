@@ -148,93 +148,144 @@ constexpr int kLLFloats = NB * RSTR + NB;
 static_assert(kLLFloats == kLoopUblkFloats, "workspace sizing of the solve layout");
 
 // Factor the NB x NB diagonal block at (k, k) in place (lower), then write its solve
-// layout LL.  One CTA of 512 threads: each row has a quad of lanes, lane u owning the
-// row's columns 4i+u in a sliding 32-register window (as in the column loop).  Per column
-// c: the diagonal's owner publishes the pivot; each row's owner of column c forms
-// l_rc = a_rc / sqrt(pivot) (sqrt(pivot) on the diagonal), writes it to A, and publishes
-// it at its window position; every later row then subtracts l_rc times the published
-// column from its own entries.
+// layout LL.  One CTA of 512 threads, recursively by 32-column sub-panels c0:
+//   1. warp 0 factors the 32 x 32 diagonal sub-block in registers (lane = row; the pivot
+//      column is broadcast with shuffles);
+//   2. 96 threads solve the rows below it, x S^T = a, one row per thread in registers;
+//   3. the rest of the block takes L[r][j] -= sum_t L[r][c0+t] L[j][c0+t], one 4 x 4
+//      register tile per thread over the lower tiles, float4 shared-memory reads.
+constexpr int DSTR = NB + 4;  // row stride of the staged block (16-byte aligned rows)
 __global__ void __launch_bounds__(512) chol_diag_kernel(float* __restrict__ A, int d, int k,
                                                         float* __restrict__ LL, DevStatus* st,
                                                         int32_t info_base) {
-  constexpr int QF = 4, WF = NB / QF;
-  __shared__ __align__(16) float col_s[QF][WF + 4];
-  __shared__ float piv_s;
+  extern __shared__ __align__(16) float smem_f[];
+  float* L = smem_f;               // [NB][DSTR]
+  __shared__ float sinv[32];
+  __shared__ int bad;
   if (st->code != 0) return;
   const int nb = min(NB, d - k);
-  const int tid = threadIdx.x, lane = tid % 32, u = lane % QF, qb = lane & ~(QF - 1);
-  const int r = tid / QF;
-  float w[WF];
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   {
-    const float* arow = A + static_cast<size_t>(k + (r < nb ? r : 0)) * d + k;
+    float v[NB * NB / 512];
 #pragma unroll
-    for (int i = 0; i < WF; ++i) {
-      const int c = QF * i + u;
-      w[i] = (r < nb) ? (c <= r ? arow[c] : 0.0f) : (c == r ? 1.0f : 0.0f);
+    for (int p = 0; p < NB * NB / 512; ++p) {
+      const int e = tid + p * 512, r = e / NB, c = e % NB;
+      v[p] = (r < nb && c <= r) ? A[static_cast<size_t>(k + r) * d + k + c] : (r == c ? 1.0f : 0.0f);
+    }
+#pragma unroll
+    for (int p = 0; p < NB * NB / 512; ++p) {
+      const int e = tid + p * 512;
+      L[(e / NB) * DSTR + e % NB] = v[p];  // identity past a ragged end
     }
   }
-  for (int e = tid; e < QF * (WF + 4); e += 512) (&col_s[0][0])[e] = 0.0f;
+  if (tid == 0) bad = 0;
   __syncthreads();
+  for (int c0 = 0; c0 < NB; c0 += 32) {
+    // 1. the 32 x 32 diagonal sub-block
+    if (warp == 0) {
+      // rolling window: at step c, w[0] is this row's column c (static register indices)
+      float* lrow = L + (c0 + lane) * DSTR + c0;
+      float w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = (j <= lane) ? lrow[j] : 0.0f;
+      int badc = -1;
 #pragma unroll 1
-  for (int g = 0; g < WF; ++g) {
+      for (int c = 0; c < 32; ++c) {
+        const float piv = __shfl_sync(0xffffffffu, w[0], c);
+        if (badc < 0 && (!(piv > 0.0f) || !isfinite(piv))) badc = c;
+        const float l = sqrtf(piv);
+        const float il = 1.0f / l;
+        const float lc = (lane == c) ? l : ((lane > c) ? w[0] * il : 0.0f);
+        if (lane >= c) lrow[c] = lc;
+        if (lane == c) sinv[c] = il;
 #pragma unroll
-    for (int o = 0; o < QF; ++o) {
-      const int c = QF * g + o;
-      if (r == c && u == o) piv_s = w[0];
-      __syncthreads();
-      const float piv = piv_s;
-      if (!(piv > 0.0f) || !isfinite(piv)) {
-        if (tid == 0) dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c));
-        return;
-      }
-      const float sq = sqrtf(piv);
-      const float own = (r == c) ? sq : w[0] / sq;
-      const float lrc = __shfl_sync(0xffffffffu, own, qb + o);
-      if (u == o && r >= c && r < nb && c < nb) A[static_cast<size_t>(k + r) * d + k + c] = lrc;
-      if (u == o && r > c) col_s[r % QF][r / QF - g - (o == QF - 1 ? 1 : 0)] = lrc;
-      __syncthreads();
-      if (r > c) {
-        const float* cl = col_s[u];
-        if (o < QF - 1) {
-#pragma unroll
-          for (int i = 0; i < WF; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(cl + i);
-            w[i] = fmaf(-lrc, l4.x, w[i]);
-            w[i + 1] = fmaf(-lrc, l4.y, w[i + 1]);
-            w[i + 2] = fmaf(-lrc, l4.z, w[i + 2]);
-            w[i + 3] = fmaf(-lrc, l4.w, w[i + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < WF; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(cl + i);
-            w[i] = fmaf(-lrc, l4.x, w[i + 1]);
-            w[i + 1] = fmaf(-lrc, l4.y, w[i + 2]);
-            w[i + 2] = fmaf(-lrc, l4.z, w[i + 3]);
-            if (i + 3 < WF - 1) w[i + 3] = fmaf(-lrc, l4.w, w[i + 4 < WF ? i + 4 : WF - 1]);
-          }
+        for (int j = 0; j < 31; ++j) {
+          const float lx = __shfl_sync(0xffffffffu, lc, (c + 1 + j) & 31);
+          w[j] = fmaf(-lc, lx, w[j + 1]);
         }
       }
+      if (lane == 0 && badc >= 0 && c0 + badc < nb) {
+        bad = 1;
+        dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c0 + badc));
+      }
     }
+    __syncthreads();
+    if (bad) return;
+    // 2. rows below the sub-block: x_c = (a_c - sum_{t<c} x_t S[c][t]) / S[c][c]
+    if (tid < NB - c0 - 32) {
+      float* xrow = L + (c0 + 32 + tid) * DSTR + c0;
+      float x[32];
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(xrow + j);
+        x[j] = v.x; x[j + 1] = v.y; x[j + 2] = v.z; x[j + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float* srow = L + (c0 + c) * DSTR + c0;
+        float acc = x[c];
+#pragma unroll
+        for (int t = 0; t < c; ++t) acc = fmaf(-x[t], srow[t], acc);
+        x[c] = acc * sinv[c];
+      }
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(xrow + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+    }
+    __syncthreads();
+    // 3. the rest of the block, lower 4 x 4 tiles
+    const int m2 = NB - c0 - 32;
+    const int T = m2 / 4;
+    for (int tile = tid; tile < T * (T + 1) / 2; tile += 512) {
+      int ti = 0, rem = tile;
+      while (rem > ti) { rem -= ti + 1; ++ti; }
+      const int tj = rem;
+      const int r0 = c0 + 32 + 4 * ti, j0 = c0 + 32 + 4 * tj;
+      float acc[4][4] = {};
+#pragma unroll
+      for (int t = 0; t < 32; t += 4) {
+        float4 ra[4], rb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ra[u] = *reinterpret_cast<const float4*>(L + (r0 + u) * DSTR + c0 + t);
+          rb[u] = *reinterpret_cast<const float4*>(L + (j0 + u) * DSTR + c0 + t);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            acc[u][v] += ra[u].x * rb[v].x + ra[u].y * rb[v].y + ra[u].z * rb[v].z +
+                         ra[u].w * rb[v].w;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          if (j0 + v <= r0 + u) L[(r0 + u) * DSTR + j0 + v] -= acc[u][v];
+    }
+    __syncthreads();
   }
-  __syncthreads();  // the factor's global writes are visible to the whole CTA
+#pragma unroll 4
+  for (int e = tid; e < nb * nb; e += 512) {
+    const int r = e / nb, c = e % nb;
+    if (c <= r) A[static_cast<size_t>(k + r) * d + k + c] = L[r * DSTR + c];
+  }
   float* out = LL + static_cast<size_t>(k / NB) * kLLFloats;
-#pragma unroll 8
+#pragma unroll 4
   for (int e = tid; e < NB * RSTR; e += 512) {
     const int t = e / RSTR, uu = (e % RSTR) / LSTR, i = e % LSTR;
     const int c = QL * (i + t / QL + ((t % QL) == QL - 1 ? 1 : 0)) + uu;
-    out[e] = (i < WL && t < nb && c > t && c < nb) ? A[static_cast<size_t>(k + c) * d + k + t] : 0.0f;
+    out[e] = (i < WL && t < nb && c > t && c < nb) ? L[c * DSTR + t] : 0.0f;
   }
-  for (int t = tid; t < NB; t += 512)
-    out[NB * RSTR + t] = (t < nb) ? 1.0f / A[static_cast<size_t>(k + t) * d + k + t] : 1.0f;
+  for (int t = tid; t < NB; t += 512) out[NB * RSTR + t] = (t < nb) ? 1.0f / L[t * DSTR + t] : 1.0f;
 }
 
 // Forward substitution L_bb y = b, one right-hand side per group of QL = 8 lanes (lane u
 // owns unknowns 8i+u; a 16-register window slides as in the column loop).
 //   panel (ident == 0): b = row r of A[k+NB:, k:k+NB], y overwrites it, giving
 //                       L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T;
-//   inverse (ident == 1): b = e_c for 16 values of c per CTA (blockIdx.x = 8*block +
-//                       part), y = column c of L_bb^-1, written to DI[block].
+//   inverse (ident == 1): b = e_c for 16 values of c per CTA (blockIdx.x = 8*(block -
+//                       k/NB) + part), y = column c of L_bb^-1, written to DI[block].
 __global__ void __launch_bounds__(128) trsv_quad_kernel(float* __restrict__ A, int d, int k,
                                                         int ident, const float* __restrict__ LLall,
                                                         float* __restrict__ DI,
@@ -242,7 +293,7 @@ __global__ void __launch_bounds__(128) trsv_quad_kernel(float* __restrict__ A, i
   extern __shared__ __align__(16) float smem_f[];
   float* ys = smem_f + kLLFloats;  // [NB][RPT] staged results
   if (st->code != 0) return;
-  const int blk = ident ? blockIdx.x / QL : k / NB;
+  const int blk = ident ? k / NB + blockIdx.x / QL : k / NB;
   const int part = ident ? blockIdx.x % QL : 0;
   const int kb = blk * NB;
   const int nb = min(NB, d - kb);
@@ -368,11 +419,22 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_LAUNCH(GPTQ_K_PREP_GATHER, s, prep_gather_kernel, d, 256, row_smem, S, d, perm, dead, lam,
               Hr);
 
-  // Cholesky of Hr (lower, in place), NB-wide panels.  A failing pivot at reversed
-  // position a reports processing position d - a (1-based).
+  // Cholesky of Hr (lower, in place) by NB-wide panels on stream A, and the inverse of
+  // the factor on stream B: block column k of the inverse needs only L's first k+1 block
+  // columns, so it runs as soon as panel k is final, overlapping the (latency-bound)
+  // factorisation of the next panels.  A failing pivot at reversed position a reports
+  // processing position d - a (1-based).
+  //
+  // The inverse X = L^-1 is kept transposed as Y = X^T in S so that both GEMM operands
+  // are K-major: block column i of Y is Y[:, i] = R DI[i]^T (R = the accumulated right-
+  // hand side, initially I), after which every later block column loses
+  // Y[:, i] L[r, i]^T.  Finally U = J X J = (J Y J)^T.
   const int trsv_smem = (kLLFloats + NB * RPT) * static_cast<int>(sizeof(float));
+  const int diag_smem = NB * DSTR * static_cast<int>(sizeof(float));
   static bool attrs = false;
   if (!attrs) {
+    GPTQ_CUDA(cudaFuncSetAttribute(chol_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   diag_smem));
     GPTQ_CUDA(cudaFuncSetAttribute(trsv_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    trsv_smem));
     attrs = true;
@@ -381,40 +443,49 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   make_gemm_map(&mHr, Hr, d, d, d);
   make_gemm_map(&mS, S, d, d, d);
   make_gemm_map(&mDI, DI, static_cast<int>(ceil_div(d, NB)) * NB, NB, NB);
-  for (int k = 0; k < d; k += NB) {
-    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, s, chol_diag_kernel, 1, 512, 0, Hr, d, k, LL, st, d);
-    const int rest = d - k - NB;
-    if (rest <= 0) break;
-    GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, s, trsv_quad_kernel, (unsigned)ceil_div(rest, RPT), 128, trsv_smem,
-                Hr, d, k, 0, LL, DI, st);
-    // trailing update, lower tiles: Hr[k+NB+i][k+NB+j] -= L[k+NB+i, panel] . L[k+NB+j, panel]
-    launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
-                       Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest, rest, -1.0f, 1.0f,
-                       true, st, s);
-  }
-  // inverses of all diagonal blocks at once
-  GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, s, trsv_quad_kernel, (unsigned)(ceil_div(d, NB) * QL), 128, trsv_smem,
-              Hr, d, 0, 1, LL, DI, st);
-
-  // The inverse X = L^-1 (L = the factor of Hr), kept transposed as Y = X^T in S so that
-  // both GEMM operands are K-major.  Block columns of Y in order: Y[:, blk i] = R DI[i]^T
-  // (R = Y's right-hand side, initially I), then every later block column loses
-  // Y[:, blk i] L[r, blk i]^T.  Finally U = J X J = (J Y J)^T.
   {
     dim3 grid((unsigned)ceil_div(d, 256), d);
     GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, identity_kernel, grid, 256, 0, S, d);
   }
-  for (int i0 = 0; i0 < d; i0 += NB) {
-    const int nbi = (d - i0 < NB) ? d - i0 : NB;
-    // Y[c][i0+t] = sum_k Y[c][i0+k] DI[i][t][k], rows c < i0 + nbi
-    launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, i0, mDI, i0, 0, S + i0, d, i0 + nbi, nbi, 1.0f,
-                       0.0f, false, st, s);
-    const int rest = d - i0 - NB;
-    if (rest <= 0) break;
-    // Y[c][r] -= sum_k Y[c][i0+k] L[r][i0+k], c < i0 + NB <= r
-    launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, i0, mHr, i0 + NB, i0, S + i0 + NB, d, i0 + NB,
-                       rest, -1.0f, 1.0f, false, st, s);
+  const int nblk = static_cast<int>(ceil_div(d, NB));
+  AuxStreams& aux = aux_streams(nblk + 2);
+  cudaStream_t sa = aux.a, sb = aux.b;
+  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk], s));
+  GPTQ_CUDA(cudaStreamWaitEvent(sa, aux.ev[nblk], 0));
+  GPTQ_CUDA(cudaStreamWaitEvent(sb, aux.ev[nblk], 0));
+  for (int k = 0; k < d; k += NB) {
+    const int kb = k / NB;
+    const int rest = d - k - NB;
+    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, sa, chol_diag_kernel, 1, 512, diag_smem, Hr, d, k, LL, st, d);
+    if (rest > 0) {
+      GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, sa, trsv_quad_kernel, (unsigned)ceil_div(rest, RPT), 128,
+                  trsv_smem, Hr, d, k, 0, LL, DI, st);
+    }
+    GPTQ_CUDA(cudaEventRecord(aux.ev[kb], sa));
+    if (rest > 0) {
+      // trailing update, lower tiles: Hr[k+NB+i][k+NB+j] -= L[k+NB+i, panel] . L[k+NB+j, panel]
+      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
+                         Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest, rest, -1.0f,
+                         1.0f, true, st, sa);
+    }
+    // inverse, block column kb, on stream B once panel kb is final
+    GPTQ_CUDA(cudaStreamWaitEvent(sb, aux.ev[kb], 0));
+    const int nbi = (d - k < NB) ? d - k : NB;
+    GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, sb, trsv_quad_kernel, (unsigned)QL, 128, trsv_smem, Hr, d, k, 1,
+                LL, DI, st);
+    // Y[c][k+t] = sum_j Y[c][k+j] DI[kb][t][j], rows c < k + nbi
+    launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, k, mDI, k, 0, S + k, d, k + nbi, nbi, 1.0f, 0.0f,
+                       false, st, sb);
+    if (rest > 0) {
+      // Y[c][r] -= sum_j Y[c][k+j] L[r][k+j], c < k + NB <= r
+      launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, k, mHr, k + NB, k, S + k + NB, d, k + NB,
+                         rest, -1.0f, 1.0f, false, st, sb);
+    }
   }
+  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk + 1], sb));
+  GPTQ_CUDA(cudaStreamWaitEvent(s, aux.ev[nblk + 1], 0));
+  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk], sa));
+  GPTQ_CUDA(cudaStreamWaitEvent(s, aux.ev[nblk], 0));
   {
     dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
     GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_transpose_kernel, grid, dim3(32, 8), 0, S, d, U);

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <map>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -138,6 +139,33 @@ int sm_count() {
     cached_dev = dev;
   }
   return cached;
+}
+
+AuxStreams& aux_streams(int nevents) {
+  static std::map<int, AuxStreams> per_dev;
+  int dev = 0;
+  cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  AuxStreams& a = per_dev[dev];
+  if (a.a == nullptr) {
+    int least = 0, greatest = 0;
+    cuda_check(cudaDeviceGetStreamPriorityRange(&least, &greatest),
+               "cudaDeviceGetStreamPriorityRange");
+    cuda_check(cudaStreamCreateWithPriority(&a.a, cudaStreamNonBlocking, greatest),
+               "cudaStreamCreateWithPriority");
+    cuda_check(cudaStreamCreateWithPriority(&a.b, cudaStreamNonBlocking, least),
+               "cudaStreamCreateWithPriority");
+  }
+  while (static_cast<int>(a.ev.size()) < nevents) {
+    cudaEvent_t e;
+    cuda_check(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreateWithFlags");
+    a.ev.push_back(e);
+  }
+  return a;
+}
+
+std::mutex& aux_mutex() {
+  static std::mutex m;
+  return m;
 }
 
 void make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
