@@ -43,23 +43,27 @@ def unpack_zeros(qzeros: np.ndarray, bits: int, m: int) -> np.ndarray:
     return O.unpack_bitstream(qzeros, bits, m)
 
 
-def check_quantize(W, U, perm, dead, bits, group, sym, gpu, rows=None, check_loss=True):
+def check_quantize(W, U, perm, dead, bits, group, sym, gpu, rows=None, check_loss=True,
+                   w_rows_only=False):
     """Replay the oracle on (W, U, perm) with the GPU's codes as near-tie hints and check
     every element.  ``gpu`` holds numpy copies of qweight, scales, qzeros, g_idx, loss.
+    With ``w_rows_only`` W holds just the sampled ``rows`` (large layers).
     Returns a report dict."""
+    m = gpu["scales"].shape[1]
+    sel = np.arange(m) if rows is None else np.asarray(rows)
+    if rows is not None and not w_rows_only:
+        W = np.asarray(W)[sel]
     W = np.asarray(W, dtype=np.float64)
-    m, d = W.shape
-    codes_gpu = unpack_codes(gpu["qweight"], bits, d)
+    d = W.shape[1]
+    codes_sel = unpack_codes(gpu["qweight"][:, sel], bits, d)   # only the checked rows
     zeros_gpu = unpack_zeros(gpu["qzeros"], bits, m)
     scales_gpu = gpu["scales"]
     perm_np = np.arange(d) if perm is None else np.asarray(perm, dtype=np.int64)
-    sel = np.arange(m) if rows is None else np.asarray(rows)
-    hint = dict(codes=codes_gpu[sel][:, perm_np], zeros=zeros_gpu[:, sel])
+    hint = dict(codes=codes_sel[:, perm_np], zeros=zeros_gpu[:, sel])
     ref = O.gptq_quantize_layer(W, U, perm_np, dead, bits, group, sym, blocksize=128,
-                                rows=None if rows is None else sel, hint=hint, tie_eps=TIE_EPS,
-                                pack=False)
-    n_codes = codes_gpu[sel].size
-    mismatch = int(np.count_nonzero(ref["codes"] != codes_gpu[sel]))
+                                hint=hint, tie_eps=TIE_EPS, pack=False)
+    n_codes = codes_sel.size
+    mismatch = int(np.count_nonzero(ref["codes"] != codes_sel))
     zero_mismatch = int(np.count_nonzero(ref["zeros"] != zeros_gpu[:, sel]))
     ties = ref["stats"].get("codes", 0) + ref["stats"].get("zeros", 0)
     srel = float(np.max(np.abs(ref["scales"].astype(np.float64) - scales_gpu[:, sel])

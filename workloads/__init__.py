@@ -9,6 +9,8 @@ from .synthetic import (  # noqa: F401
     CONFIGS,
     LayerConfig,
     channel_multipliers,
+    make_permutation,
+    make_upper_factor,
     make_weight,
     make_tokens,
     make_tokens_chunk,

@@ -187,3 +187,25 @@ def token_chunks(cfg: LayerConfig, device="cpu") -> Iterator[torch.Tensor]:
 def make_tokens(cfg: LayerConfig, device="cpu") -> torch.Tensor:
     """The whole calibration stream ``[n_tokens, d_in]`` (only for streams that fit)."""
     return torch.cat(list(token_chunks(cfg, device)), dim=0).contiguous()
+
+
+def make_upper_factor(d: int, seed: int, device="cpu", offdiag: float = 0.5) -> torch.Tensor:
+    """A random upper-triangular float32 ``[d, d]`` with a positive diagonal.
+
+    Any such matrix is the inverse Cholesky factor of some positive-definite Hessian, so
+    it is a valid, cheap-to-draw input for the column loop at sizes where the factor of
+    a real Hessian is out of the CPU oracle's reach.  Diagonal: exp(0.3 N(0,1)); above
+    it: row's diagonal x N(0,1) x offdiag / sqrt(d).
+    """
+    g = _gen(seed * 1000 + 7, device)
+    diag = torch.exp(0.3 * torch.randn(d, generator=g, device=device))
+    U = torch.randn(d, d, generator=g, device=device) * (offdiag / d ** 0.5)
+    U = torch.triu(U, diagonal=1) * diag[:, None]
+    U.diagonal().copy_(diag)
+    return U.float().contiguous()
+
+
+def make_permutation(d: int, seed: int, device="cpu") -> torch.Tensor:
+    """A random permutation of ``range(d)`` (int32)."""
+    g = _gen(seed * 1000 + 8, device)
+    return torch.randperm(d, generator=g, device=device).to(torch.int32)
