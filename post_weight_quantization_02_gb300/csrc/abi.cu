@@ -139,7 +139,6 @@ size_t prepare_ws_bytes(int d) {
   w.add<float>(d);                           // fixed diagonal
   w.add<float>(1);                           // lambda
   w.add<float>(static_cast<size_t>(ceil_div(d, 128)) * 128 * 128);  // diagonal-block inverses
-  w.add<float>(static_cast<size_t>(ceil_div(d, 128)) * kLoopUblkFloats);  // solve layouts
   return w.bytes;
 }
 
@@ -148,8 +147,8 @@ size_t quantize_ws_bytes(int m, int d, int G) {
   w.add<DevStatus>(1);
   w.add<float>(static_cast<size_t>(m) * d);    // Wp
   w.add<uint8_t>(static_cast<size_t>(m) * d);  // codesT
-  w.add<uint16_t>(static_cast<size_t>(128) * m);  // errors, bf16 hi
-  w.add<uint16_t>(static_cast<size_t>(128) * m);  // errors, bf16 lo
+  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 hi
+  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 lo
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 hi
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 lo
   w.add<int32_t>(static_cast<size_t>(G) * m);  // zeros
@@ -263,11 +262,10 @@ gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
     float* diag = wc.take<float>(d_in);
     float* lam = wc.take<float>(1);
     float* DI = wc.take<float>(static_cast<size_t>(ceil_div(d_in, 128)) * 128 * 128);
-    float* LL = wc.take<float>(static_cast<size_t>(ceil_div(d_in, 128)) * kLoopUblkFloats);
     std::lock_guard<std::mutex> lk(aux_mutex());  // the internal streams are shared
     begin_call(st, s);
     launch_prepare(H, d_in, damp, actorder ? 1 : 0, perm, dead, Hinv_chol, S, Hr, diag, lam, DI,
-                   LL, st, s);
+                   st, s);
     DevStatus h = finish_call(st, s);
     if (h.code == GPTQ_ERR_NOT_PD) pivot = h.info;
     raise_device_status(h, "gptq_prepare");
@@ -316,8 +314,8 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
     q.st = wc.take<DevStatus>(1);
     q.Wp = wc.take<float>(static_cast<size_t>(d_out) * d_in);
     q.codesT = wc.take<uint8_t>(static_cast<size_t>(d_out) * d_in);
-    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(128) * d_out);
-    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(128) * d_out);
+    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
+    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
     q.uhi = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.ulo = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.zeros = wc.take<int32_t>(static_cast<size_t>(G) * d_out);

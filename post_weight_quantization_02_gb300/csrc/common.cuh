@@ -106,12 +106,13 @@ const std::string& last_error();
 // Number of SMs of the current device.
 int sm_count();
 
-// Two library-internal streams of the current device (a: high priority, b: low priority)
-// and at least `nevents` timing-free events, created on first use and kept for the life
+// Three library-internal streams of the current device (a: highest priority, c: middle,
+// b: lowest) and at least `nevents` timing-free events, created on first use and kept for the life
 // of the process.  Calls that use them hold aux_mutex() until their work has finished.
 struct AuxStreams {
   cudaStream_t a = nullptr;
   cudaStream_t b = nullptr;
+  cudaStream_t c = nullptr;
   std::vector<cudaEvent_t> ev;
 };
 AuxStreams& aux_streams(int nevents);

@@ -1,5 +1,5 @@
 // Float32-accurate tensor-core GEMM for the factorisation updates:
-//   C[i][j] = beta C[i][j] + alpha sum_{k<128} A[i][k] B[j][k]
+//   C[i][j] = beta C[i][j] + alpha sum_{k<128} A[i][k] B[j][k],   beta in {0, 1},
 // with both operands K-major (rows of 128 consecutive k), read through tensor maps that
 // cover whole matrices: the launch passes each operand's row and column offset.
 //
@@ -7,10 +7,19 @@
 // tensor core reads the same bits as x) and lo = x - hi; the products hi*hi + hi*lo +
 // lo*hi are accumulated in float32 TMEM with tcgen05.mma kind::tf32 (the dropped lo*lo is
 // ~2^-21 relative).  TMA lands each K-quarter (32) of the fp32 tiles in shared memory
-// with 128-byte swizzle; the CTA's threads then write the lo parts elementwise into twin
-// buffers (same swizzled layout) before one thread issues the MMAs.  One CTA per
-// 128 x 128 output tile, 64 KB of shared memory, so three CTAs share an SM and overlap
-// their load / convert / MMA phases.
+// with 128-byte swizzle, two quarters in flight (double-buffered), so the next quarter's
+// load overlaps this quarter's split and MMAs; the CTA's threads write the lo parts
+// elementwise into twin buffers (same swizzled layout) before one thread issues the MMAs.
+//
+// Epilogue: each warp moves 32-row x 32-column boxes of alpha D from TMEM through a
+// swizzled shared buffer to C with one TMA bulk copy each: a store (beta = 0) or a
+// reduce-add performed by the memory system (beta = 1), so the SM never reads C.  The C
+// map spans exactly the M x N result, so partial tiles are clipped by the TMA unit; in
+// `lower` mode the entries of a diagonal tile above its diagonal are sent as zeros (C
+// unchanged).
+//
+// One CTA of 256 threads per 128 x 128 output tile, 96 KB of shared memory, two CTAs
+// per SM.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -22,9 +31,13 @@ namespace gptq {
 namespace {
 
 constexpr int TM = 128, TN = 128, TK = 128, KQ = 32;  // K-quarter per phase
+constexpr int THREADS = 256;
 constexpr int A_BYTES = TM * KQ * 4;                   // 16 KB
 constexpr int B_BYTES = TN * KQ * 4;                   // 16 KB
-constexpr int SMEM_BYTES = 2 * A_BYTES + 2 * B_BYTES + 1024 + 128;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// hi: two stages of (A, B) quarters; lo: one (A, B) quarter
+constexpr int SMEM_BYTES = 3 * STAGE_BYTES + 1024 + 128;
+constexpr int BOXB = 32 * 32 * 4;                      // one epilogue box: 32 x 32 float32
 
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((b_mn ? 1u : 0u) << 16) |
@@ -32,33 +45,48 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn) {
 }
 
 struct TcGemmArgs {
-  float* C;
-  int ldc;
   int a_row0, a_k0;  // operand offsets inside the tensor maps
   int b_row0, b_k0;
   int M, N;
-  float alpha, beta;
-  int lower;     // only tiles with row tile >= column tile; only entries j <= i written
-  int n_tiles;   // column tiles (non-lower enumeration)
+  float alpha;
+  int accumulate;  // beta = 1: reduce-add into C; beta = 0: store
+  int lower;       // only tiles with row tile >= column tile; only entries j <= i change
+  int n_tiles;     // column tiles (non-lower enumeration)
   DevStatus* st;
 };
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// TMA of K-quarter ph of the A and B tiles into stage ph % 2
+__device__ __forceinline__ void load_quarter(uint8_t* smem, uint64_t* bar_load,
+                                             const CUtensorMap* tma, const CUtensorMap* tmb,
+                                             const TcGemmArgs& g, int i0, int j0, int ph) {
+  uint8_t* a_hi = smem + (ph & 1) * STAGE_BYTES;
+  uint64_t* bar = bar_load + (ph & 1);
+  tc::mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES);
+  tc::tma_load_2d(a_hi, tma, bar, g.a_k0 + ph * KQ, g.a_row0 + i0);
+  tc::tma_load_2d(a_hi + A_BYTES, tmb, bar, g.b_k0 + ph * KQ, g.b_row0 + j0);
 }
 
-__global__ void __launch_bounds__(128) gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tma,
-                                                          const __grid_constant__ CUtensorMap tmb,
-                                                          const TcGemmArgs g) {
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(tc::smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tma,
+                                                              const __grid_constant__ CUtensorMap tmb,
+                                                              const __grid_constant__ CUtensorMap tmc,
+                                                              const TcGemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* a_hi = smem;
-  uint8_t* a_lo = smem + A_BYTES;
-  uint8_t* b_hi = smem + 2 * A_BYTES;
-  uint8_t* b_lo = b_hi + B_BYTES;
-  uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + 2 * A_BYTES + 2 * B_BYTES);
-  uint64_t* bar_mma = bar_load + 1;
+  // stage q: A hi at q * STAGE_BYTES, B hi right after it; the lo pair after both stages
+  uint8_t* a_lo = smem + 2 * STAGE_BYTES;
+  uint8_t* b_lo = a_lo + A_BYTES;
+  uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + 3 * STAGE_BYTES);  // [2]
+  uint64_t* bar_mma = bar_load + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -77,6 +105,7 @@ __global__ void __launch_bounds__(128) gemm_tf32x3_kernel(const __grid_constant_
 
   if (tid == 0) {
     tc::mbar_init(bar_load, 1);
+    tc::mbar_init(bar_load + 1, 1);
     tc::mbar_init(bar_mma, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -92,36 +121,37 @@ __global__ void __launch_bounds__(128) gemm_tf32x3_kernel(const __grid_constant_
   constexpr uint32_t IDESC = idesc_tf32(TM, TN, false);
   bool ok = true;
 
+  if (tid == 0) {
+    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 0);
+    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
+  }
   for (int ph = 0; ph < TK / KQ && ok; ++ph) {
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(bar_load, A_BYTES + B_BYTES);
-      tc::tma_load_2d(a_hi, &tma, bar_load, g.a_k0 + ph * KQ, g.a_row0 + i0);
-      tc::tma_load_2d(b_hi, &tmb, bar_load, g.b_k0 + ph * KQ, g.b_row0 + j0);
-    }
-    if (!tc::mbar_wait(bar_load, ph & 1, abort_flag)) { ok = false; break; }
+    uint8_t* a_hi = smem + (ph & 1) * STAGE_BYTES;
+    uint8_t* b_hi = a_hi + A_BYTES;
+    if (!tc::mbar_wait(bar_load + (ph & 1), (ph >> 1) & 1, abort_flag)) { ok = false; break; }
     // lo = x - trunc_tf32(x), elementwise in the same swizzled layout
     {
       const float4* src_a = reinterpret_cast<const float4*>(a_hi);
       float4* dst_a = reinterpret_cast<float4*>(a_lo);
       const float4* src_b = reinterpret_cast<const float4*>(b_hi);
       float4* dst_b = reinterpret_cast<float4*>(b_lo);
-#pragma unroll 4
-      for (int e = tid; e < A_BYTES / 16; e += 128) {
+#pragma unroll
+      for (int e = tid; e < A_BYTES / 16; e += THREADS) {
         float4 x = src_a[e];
+        float4 y = src_b[e];
         x.x -= __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
         x.y -= __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
         x.z -= __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
         x.w -= __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
-        dst_a[e] = x;
-        float4 y = src_b[e];
         y.x -= __uint_as_float(__float_as_uint(y.x) & 0xFFFFE000u);
         y.y -= __uint_as_float(__float_as_uint(y.y) & 0xFFFFE000u);
         y.z -= __uint_as_float(__float_as_uint(y.z) & 0xFFFFE000u);
         y.w -= __uint_as_float(__float_as_uint(y.w) & 0xFFFFE000u);
+        dst_a[e] = x;
         dst_b[e] = y;
       }
     }
-    fence_proxy_async();
+    tc::fence_proxy_async_shared();
     tc::fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -156,52 +186,42 @@ __global__ void __launch_bounds__(128) gemm_tf32x3_kernel(const __grid_constant_
     }
     if (!tc::mbar_wait(bar_mma, ph & 1, abort_flag)) { ok = false; break; }
     tc::fence_after();
+    // both buffers of this stage are free again: fetch the quarter after next into it
+    if (tid == 0 && ph + 2 < TK / KQ) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
   }
 
   if (ok) {
-    // epilogue, in two 64-column halves staged through the (now free) operand buffers:
-    // warp w moves TMEM lanes 32w..32w+31 (tile rows) into shared memory, then the CTA
-    // reads and writes C as coalesced float4 rows
-    float* stage = reinterpret_cast<float*>(smem);   // [128][68]
-    constexpr int SROW = 68;
-    for (int half = 0; half < 2; ++half) {
+    // warp w: TMEM lanes (tile rows) 32 (w % 4) .., columns 64 (w / 4) .. + 64, as two
+    // 32 x 32 boxes, each staged in its own 4 KB buffer (the operand buffers are free)
+    const int rq = warp % 4, ch = warp / 4;
+    const int row = i0 + 32 * rq + lane;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + half * 64 + c * 32, r);
-        tc::tmem_ld_wait();
-        float* srow = stage + (32 * warp + lane) * SROW + c * 32;
+    for (int c = 0; c < 2; ++c) {
+      const int colt = 64 * ch + 32 * c;  // column inside the tile
+      uint8_t* box = smem + (warp * 2 + c) * BOXB;
+      uint32_t r[32];
+      tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * rq) << 16) + colt, r);
+      tc::tmem_ld_wait();
+      uint8_t* srow = box + lane * 128;  // 128-byte swizzle: chunk j at (j ^ (lane % 8))
 #pragma unroll
-        for (int k = 0; k < 32; k += 4)
-          *reinterpret_cast<float4*>(srow + k) =
-              make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]),
-                          __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+      for (int j = 0; j < 8; ++j) {
+        const int col = j0 + colt + 4 * j;
+        float4 v;
+        v.x = (!g.lower || col <= row) ? g.alpha * __uint_as_float(r[4 * j]) : 0.0f;
+        v.y = (!g.lower || col + 1 <= row) ? g.alpha * __uint_as_float(r[4 * j + 1]) : 0.0f;
+        v.z = (!g.lower || col + 2 <= row) ? g.alpha * __uint_as_float(r[4 * j + 2]) : 0.0f;
+        v.w = (!g.lower || col + 3 <= row) ? g.alpha * __uint_as_float(r[4 * j + 3]) : 0.0f;
+        *reinterpret_cast<float4*>(srow + ((j ^ (lane & 7)) << 4)) = v;
       }
-      __syncthreads();
-      for (int e = tid; e < TM * 16; e += 128) {
-        const int rr = e / 16, c4 = (e % 16) * 4;
-        const int row = i0 + rr, col = j0 + half * 64 + c4;
-        if (row >= g.M || col >= g.N) continue;
-        if (g.lower && col > row) continue;
-        const float4 v = *reinterpret_cast<const float4*>(stage + rr * SROW + c4);
-        float4* cp = reinterpret_cast<float4*>(g.C + static_cast<size_t>(row) * g.ldc + col);
-        float4 o = (g.beta != 0.0f) ? *cp : make_float4(0.f, 0.f, 0.f, 0.f);
-        // a lower tile's diagonal keeps the entries above it as they were
-        const bool w1 = !g.lower || col + 1 <= row, w2 = !g.lower || col + 2 <= row,
-                   w3 = !g.lower || col + 3 <= row;
-        o.x = fmaf(g.alpha, v.x, o.x);
-        if (w1) o.y = fmaf(g.alpha, v.y, o.y);
-        if (w2) o.z = fmaf(g.alpha, v.z, o.z);
-        if (w3) o.w = fmaf(g.alpha, v.w, o.w);
-        if (g.beta == 0.0f) {
-          if (!w1) o.y = cp->y;
-          if (!w2) o.z = cp->z;
-          if (!w3) o.w = cp->w;
-        }
-        *cp = o;
+      tc::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0 && i0 + 32 * rq < g.M && j0 + colt < g.N) {
+        if (g.accumulate) tc::tma_reduce_add_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
+        else tma_store_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
+        tc::bulk_commit_group();
       }
-      __syncthreads();
     }
+    if (lane == 0) tc::bulk_wait_group0();
   } else {
     *abort_flag = 1;
     if (lane == 0) {
@@ -234,15 +254,21 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         int N, float alpha, float beta, bool lower, DevStatus* st,
                         cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
+  if ((beta != 0.0f && beta != 1.0f) || (lower && beta != 1.0f)) {
+    fail(GPTQ_ERR_INVALID_ARG, "launch_gemm_tf32x3: beta must be 0 or 1 (1 in lower mode)");
+  }
   static bool attr = false;
   if (!attr) {
     GPTQ_CUDA(cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    SMEM_BYTES));
     attr = true;
   }
+  // the M x N result, in boxes of 32 x 32 (128-byte rows, swizzled like the staging)
+  CUtensorMap mc;
+  make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
+               static_cast<uint64_t>(M), static_cast<uint64_t>(ldc) * 4, 32, 32,
+               CU_TENSOR_MAP_SWIZZLE_128B);
   TcGemmArgs g;
-  g.C = C;
-  g.ldc = ldc;
   g.a_row0 = a_row0;
   g.a_k0 = a_k0;
   g.b_row0 = b_row0;
@@ -250,14 +276,14 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.M = M;
   g.N = N;
   g.alpha = alpha;
-  g.beta = beta;
+  g.accumulate = (beta != 0.0f) ? 1 : 0;
   g.lower = lower ? 1 : 0;
   const int tm = static_cast<int>(ceil_div(M, TM)), tn = static_cast<int>(ceil_div(N, TN));
   g.n_tiles = tn;
   g.st = st;
   const unsigned grid = lower ? static_cast<unsigned>(tm * (tm + 1) / 2)
                               : static_cast<unsigned>(tm * tn);
-  GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, 128, SMEM_BYTES, ma, mb, g);
+  GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
 }
 
 }  // namespace gptq

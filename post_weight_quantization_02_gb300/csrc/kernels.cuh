@@ -29,7 +29,7 @@ constexpr int kLoopUblkFloats = 128 * 160 + 128;
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, float* LL, DevStatus* st, cudaStream_t s);
+                    float* lam, float* DI, DevStatus* st, cudaStream_t s);
 
 // quantize.cu
 struct QuantArgs {
@@ -69,13 +69,20 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         cudaStream_t s);
 
 // lazy_tc.cu
+// ErrT rows kept for the deferred update: one 512-column superblock of the loop
+constexpr int kErrRows = 512;
+
 struct LazyMaps {
-  CUtensorMap ehi, elo, uhi, ulo;
+  CUtensorMap ehi, elo, uhi, ulo, w;
+  int m, d;
 };
-LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo,
-                        const __nv_bfloat16* uhi, const __nv_bfloat16* ulo, int m, int d);
+// ErrT hi/lo [erows][m], U hi/lo [d][d] (bf16), W [m][d] (float32)
+LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int erows,
+                        const __nv_bfloat16* uhi, const __nv_bfloat16* ulo, float* W, int m,
+                        int d);
 void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s);
-void launch_lazy_tc(const LazyMaps& mp, float* W, int m, int d, int i1, DevStatus* st,
-                    cudaStream_t s);
+// W[:, c_begin:c_end] -= ErrT[e_row0 : e_row0 + k]^T U[u_row0 : u_row0 + k, c_begin:c_end]
+void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
+                    DevStatus* st, cudaStream_t s);
 
 }  // namespace gptq

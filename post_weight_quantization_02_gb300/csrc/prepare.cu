@@ -138,70 +138,104 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 
 // ---------------------------------------------------------------- blocked Cholesky
 
-// Layout of one factorised diagonal block for the quad triangular solves: for step t
-// (column t of L_kk) and lane u of a group of eight, 16 coefficients
-//   LL[t][u][i] = L_kk[c][t], c = 8(i + t/8 + (t%8 == 7)) + u, if t < c < nb, else 0,
-// (padded to 20), then the 128 reciprocals 1/L_kk[t][t].  Same shape as the column
-// loop's layout of U.
-constexpr int QL = 8, WL = NB / QL, LSTR = WL + 4, RSTR = QL * LSTR, RPT = 128 / QL;
-constexpr int kLLFloats = NB * RSTR + NB;
-static_assert(kLLFloats == kLoopUblkFloats, "workspace sizing of the solve layout");
+// ------------------------------------------------------ diagonal block: factor, inverse
 
-// Factor the NB x NB diagonal block at (k, k) in place (lower), then write its solve
-// layout LL.  One CTA of 512 threads, recursively by 32-column sub-panels c0:
-//   1. warp 0 factors the 32 x 32 diagonal sub-block in registers (lane = row; the pivot
-//      column is broadcast with shuffles);
-//   2. 96 threads solve the rows below it, x S^T = a, one row per thread in registers;
+// One CTA of 512 threads factors the NB x NB diagonal block at (k, k) of A (lower) and
+// writes the inverse of its factor, V = L_kk^-1, densely to DI[k/NB] (row-major, exact
+// zeros above the diagonal, identity past a ragged end).  The factor itself stays in
+// shared memory: the panel below it is solved against V by a GEMM, and the inverse of
+// the whole factor is assembled from the V blocks.
+//
+// Factor, recursively by 32-column sub-panels c0:
+//   1. warp 0 factors the 32 x 32 diagonal sub-block, lane = row, columns in registers.
+//      Column c: l_cc = sqrt(p), l_rc = a_rc / l_cc, via one reciprocal square root of the
+//      pivot p; the column is published through shared memory (ST[c][r] = l_rc,
+//      ST[c][c] = 1/l_cc) and every row subtracts l_rc l_jc from its entries j > c.  The
+//      next pivot only needs row c+1's own l_{c+1,c}, so it is formed first and the
+//      broadcast stays off the pivot chain.
+//   2. the rows below solve x S^T = a right-looking, one row per thread (x_c = acc_c /
+//      l_cc, then acc_j -= x_c l_jc for j > c).
 //   3. the rest of the block takes L[r][j] -= sum_t L[r][c0+t] L[j][c0+t], one 4 x 4
-//      register tile per thread over the lower tiles, float4 shared-memory reads.
-constexpr int DSTR = NB + 4;  // row stride of the staged block (16-byte aligned rows)
-__global__ void __launch_bounds__(512) chol_diag_kernel(float* __restrict__ A, int d, int k,
-                                                        float* __restrict__ LL, DevStatus* st,
-                                                        int32_t info_base) {
+//      register tile per thread over the lower tiles.
+// Inverse, by 32 x 32 blocks (block indices): V_ii = L_ii^-1 by forward substitution,
+// lane = column, four warps at once; then, by distance i - j = 1, 2, 3,
+//   V_ij = -V_ii sum_{t=j}^{i-1} L_it V_tj.
+// Shared memory (95 KB, so the CTA fits beside a GEMM CTA on one SM): the staged block
+// L, whose six upper 32 x 32 blocks are free and hold the published sub-panel columns
+// (ST, four blocks) and later the inverse's partial products (TB, three blocks); the V_ii
+// overwrite the diagonal blocks of L once their columns are published; the six V_ij
+// below the diagonal have their own array.
+constexpr int DSTR = NB + 4;   // row stride of the staged block (16-byte rows)
+constexpr int SB = 32;         // sub-panel width
+constexpr int NSB = NB / SB;
+constexpr int VSTR = SB + 4;   // row stride of an off-diagonal V block
+constexpr int kDiagSmemFloats = NB * DSTR + (NSB * (NSB - 1) / 2) * SB * VSTR;
+
+// the free upper block that holds sub-panel s's columns (s = 0..3), then TB[s] (s < 3)
+__device__ __forceinline__ float* upper_slot(float* L, int s) {
+  const int bi = s < 3 ? 0 : 1, bj = s < 3 ? s + 1 : 2;
+  return L + (SB * bi) * DSTR + SB * bj;
+}
+__device__ __forceinline__ int voff_index(int i, int j) { return i * (i - 1) / 2 + j; }
+
+__global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restrict__ A, int d,
+                                                            int k, float* __restrict__ DI,
+                                                            DevStatus* st, int32_t info_base) {
   extern __shared__ __align__(16) float smem_f[];
-  float* L = smem_f;               // [NB][DSTR]
-  __shared__ float sinv[32];
+  float* L = smem_f;             // [NB][DSTR]
+  float* Voff = L + NB * DSTR;   // [6][SB][VSTR]
   __shared__ int bad;
   if (st->code != 0) return;
-  const int nb = min(NB, d - k);
+  const int nb = min(NB, d - k);  // a multiple of 8
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  {
-    float v[NB * NB / 512];
 #pragma unroll
-    for (int p = 0; p < NB * NB / 512; ++p) {
-      const int e = tid + p * 512, r = e / NB, c = e % NB;
-      v[p] = (r < nb && c <= r) ? A[static_cast<size_t>(k + r) * d + k + c] : (r == c ? 1.0f : 0.0f);
+  for (int p = 0; p < NB * NB / 4 / 512; ++p) {
+    const int e4 = tid + p * 512, r = e4 / (NB / 4), c = (e4 % (NB / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nb && c < nb) {
+      v = *reinterpret_cast<const float4*>(A + static_cast<size_t>(k + r) * d + k + c);
+      if (c + 1 > r) v.y = 0.0f;
+      if (c + 2 > r) v.z = 0.0f;
+      if (c + 3 > r) v.w = 0.0f;
+      if (c > r) v.x = 0.0f;
+    } else if (r >= nb && r >= c && r < c + 4) {  // identity past a ragged end
+      (&v.x)[r - c] = 1.0f;
     }
-#pragma unroll
-    for (int p = 0; p < NB * NB / 512; ++p) {
-      const int e = tid + p * 512;
-      L[(e / NB) * DSTR + e % NB] = v[p];  // identity past a ragged end
-    }
+    *reinterpret_cast<float4*>(L + r * DSTR + c) = v;
   }
   if (tid == 0) bad = 0;
   __syncthreads();
-  for (int c0 = 0; c0 < NB; c0 += 32) {
+
+  for (int s = 0; s < NSB; ++s) {
+    const int c0 = s * SB;
+    float* STs = upper_slot(L, s);  // STs[c * DSTR + j] = l_{c0+j, c0+c} (j > c), 1/l_cc (j = c)
     // 1. the 32 x 32 diagonal sub-block
     if (warp == 0) {
-      // rolling window: at step c, w[0] is this row's column c (static register indices)
       float* lrow = L + (c0 + lane) * DSTR + c0;
-      float w[32];
+      float w[SB];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = (j <= lane) ? lrow[j] : 0.0f;
+      for (int j = 0; j < SB; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(lrow + j);
+        w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+      }
       int badc = -1;
-#pragma unroll 1
-      for (int c = 0; c < 32; ++c) {
-        const float piv = __shfl_sync(0xffffffffu, w[0], c);
-        if (badc < 0 && (!(piv > 0.0f) || !isfinite(piv))) badc = c;
-        const float l = sqrtf(piv);
-        const float il = 1.0f / l;
-        const float lc = (lane == c) ? l : ((lane > c) ? w[0] * il : 0.0f);
-        if (lane >= c) lrow[c] = lc;
-        if (lane == c) sinv[c] = il;
+      float piv = __shfl_sync(0xffffffffu, w[0], 0);
 #pragma unroll
-        for (int j = 0; j < 31; ++j) {
-          const float lx = __shfl_sync(0xffffffffu, lc, (c + 1 + j) & 31);
-          w[j] = fmaf(-lc, lx, w[j + 1]);
+      for (int c = 0; c < SB; ++c) {
+        if (badc < 0 && (!(piv > 0.0f) || !isfinite(piv))) badc = c;
+        const float il = rsqrtf(piv);
+        const float lc = (lane == c) ? piv * il : w[c] * il;
+        if (lane >= c) lrow[c] = lc;
+        STs[c * DSTR + lane] = (lane > c) ? lc : ((lane == c) ? il : 0.0f);
+        if (c + 1 < SB) piv = __shfl_sync(0xffffffffu, fmaf(-lc, lc, w[c + 1]), c + 1);
+        __syncwarp();
+#pragma unroll
+        for (int j4 = ((c + 1) / 4) * 4; j4 < SB; j4 += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(STs + c * DSTR + j4);
+          if (j4 > c) w[j4] = fmaf(-lc, v.x, w[j4]);
+          if (j4 + 1 > c) w[j4 + 1] = fmaf(-lc, v.y, w[j4 + 1]);
+          if (j4 + 2 > c) w[j4 + 2] = fmaf(-lc, v.z, w[j4 + 2]);
+          if (j4 + 3 > c) w[j4 + 3] = fmaf(-lc, v.w, w[j4 + 3]);
         }
       }
       if (lane == 0 && badc >= 0 && c0 + badc < nb) {
@@ -211,39 +245,45 @@ __global__ void __launch_bounds__(512) chol_diag_kernel(float* __restrict__ A, i
     }
     __syncthreads();
     if (bad) return;
-    // 2. rows below the sub-block: x_c = (a_c - sum_{t<c} x_t S[c][t]) / S[c][c]
-    if (tid < NB - c0 - 32) {
-      float* xrow = L + (c0 + 32 + tid) * DSTR + c0;
-      float x[32];
+    const int m2 = NB - c0 - SB;
+    // 2. rows below the sub-block
+    if (tid < m2) {
+      float* xrow = L + (c0 + SB + tid) * DSTR + c0;
+      float x[SB];
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
+      for (int j = 0; j < SB; j += 4) {
         const float4 v = *reinterpret_cast<const float4*>(xrow + j);
         x[j] = v.x; x[j + 1] = v.y; x[j + 2] = v.z; x[j + 3] = v.w;
       }
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float* srow = L + (c0 + c) * DSTR + c0;
-        float acc = x[c];
+      for (int c = 0; c < SB; ++c) {
+        const float* srow = STs + c * DSTR;
+        const float xc = x[c] * srow[c];
+        x[c] = xc;
 #pragma unroll
-        for (int t = 0; t < c; ++t) acc = fmaf(-x[t], srow[t], acc);
-        x[c] = acc * sinv[c];
+        for (int j4 = ((c + 1) / 4) * 4; j4 < SB; j4 += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(srow + j4);
+          if (j4 > c) x[j4] = fmaf(-xc, v.x, x[j4]);
+          if (j4 + 1 > c) x[j4 + 1] = fmaf(-xc, v.y, x[j4 + 1]);
+          if (j4 + 2 > c) x[j4 + 2] = fmaf(-xc, v.z, x[j4 + 2]);
+          if (j4 + 3 > c) x[j4 + 3] = fmaf(-xc, v.w, x[j4 + 3]);
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
+      for (int j = 0; j < SB; j += 4)
         *reinterpret_cast<float4*>(xrow + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
     }
     __syncthreads();
     // 3. the rest of the block, lower 4 x 4 tiles
-    const int m2 = NB - c0 - 32;
     const int T = m2 / 4;
     for (int tile = tid; tile < T * (T + 1) / 2; tile += 512) {
       int ti = 0, rem = tile;
       while (rem > ti) { rem -= ti + 1; ++ti; }
       const int tj = rem;
-      const int r0 = c0 + 32 + 4 * ti, j0 = c0 + 32 + 4 * tj;
+      const int r0 = c0 + SB + 4 * ti, j0 = c0 + SB + 4 * tj;
       float acc[4][4] = {};
 #pragma unroll
-      for (int t = 0; t < 32; t += 4) {
+      for (int t = 0; t < SB; t += 4) {
         float4 ra[4], rb[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -265,113 +305,91 @@ __global__ void __launch_bounds__(512) chol_diag_kernel(float* __restrict__ A, i
     }
     __syncthreads();
   }
-#pragma unroll 4
-  for (int e = tid; e < nb * nb; e += 512) {
-    const int r = e / nb, c = e % nb;
-    if (c <= r) A[static_cast<size_t>(k + r) * d + k + c] = L[r * DSTR + c];
-  }
-  float* out = LL + static_cast<size_t>(k / NB) * kLLFloats;
-#pragma unroll 4
-  for (int e = tid; e < NB * RSTR; e += 512) {
-    const int t = e / RSTR, uu = (e % RSTR) / LSTR, i = e % LSTR;
-    const int c = QL * (i + t / QL + ((t % QL) == QL - 1 ? 1 : 0)) + uu;
-    out[e] = (i < WL && t < nb && c > t && c < nb) ? L[c * DSTR + t] : 0.0f;
-  }
-  for (int t = tid; t < NB; t += 512) out[NB * RSTR + t] = (t < nb) ? 1.0f / L[t * DSTR + t] : 1.0f;
-}
 
-// Forward substitution L_bb y = b, one right-hand side per group of QL = 8 lanes (lane u
-// owns unknowns 8i+u; a 16-register window slides as in the column loop).
-//   panel (ident == 0): b = row r of A[k+NB:, k:k+NB], y overwrites it, giving
-//                       L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T;
-//   inverse (ident == 1): b = e_c for 16 values of c per CTA (blockIdx.x = 8*(block -
-//                       k/NB) + part), y = column c of L_bb^-1, written to DI[block].
-__global__ void __launch_bounds__(128) trsv_quad_kernel(float* __restrict__ A, int d, int k,
-                                                        int ident, const float* __restrict__ LLall,
-                                                        float* __restrict__ DI,
-                                                        const DevStatus* st) {
-  extern __shared__ __align__(16) float smem_f[];
-  float* ys = smem_f + kLLFloats;  // [NB][RPT] staged results
-  if (st->code != 0) return;
-  const int blk = ident ? k / NB + blockIdx.x / QL : k / NB;
-  const int part = ident ? blockIdx.x % QL : 0;
-  const int kb = blk * NB;
-  const int nb = min(NB, d - kb);
-  {
-    const float4* src = reinterpret_cast<const float4*>(LLall + static_cast<size_t>(blk) * kLLFloats);
-    float4* dst = reinterpret_cast<float4*>(smem_f);
-    for (int e = threadIdx.x; e < kLLFloats / 4; e += 128) {
-      const uint32_t s_addr = static_cast<uint32_t>(__cvta_generic_to_shared(dst + e));
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s_addr), "l"(src + e) : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-  }
-  __syncthreads();
-  const float* lay = smem_f;
-  const float* rinv = smem_f + NB * RSTR;
-  const int lane = threadIdx.x % 32, u = lane % QL, qbase = lane & ~(QL - 1);
-  const int rl = threadIdx.x / QL;  // 0..RPT-1
-  float w[WL];
-  int nrows;
-  size_t row0;
-  if (ident) {
-    const int c = part * RPT + rl;
+  // inverse: diagonal blocks, warp w = block w, lane = column; V_ww replaces L_ww
+  if (warp < NSB) {
+    const float* STw = upper_slot(L, warp);
+    float y[SB];
 #pragma unroll
-    for (int i = 0; i < WL; ++i) w[i] = (QL * i + u == c) ? 1.0f : 0.0f;
-    nrows = RPT;
-    row0 = 0;
-  } else {
-    const int rbase = k + NB + blockIdx.x * RPT;
-    nrows = min(RPT, d - rbase);
-    row0 = static_cast<size_t>(rbase);
-    const float* arow = A + static_cast<size_t>(rbase + (rl < nrows ? rl : 0)) * d + k;
+    for (int t = 0; t < SB; ++t) y[t] = (t == lane) ? 1.0f : 0.0f;
 #pragma unroll
-    for (int i = 0; i < WL; ++i) w[i] = (rl < nrows) ? arow[QL * i + u] : 0.0f;
-  }
-  const int ngroups = (nb + QL - 1) / QL;
-#pragma unroll 1
-  for (int g = 0; g < ngroups; ++g) {
+    for (int t = 0; t < SB; ++t) {
+      const float* srow = STw + t * DSTR;
+      const float yt = y[t] * srow[t];
+      y[t] = yt;
 #pragma unroll
-    for (int o = 0; o < QL; ++o) {
-      const int t = QL * g + o;
-      const float y = __shfl_sync(0xffffffffu, w[0] * rinv[t], qbase + o);
-      if (u == o) ys[t * RPT + rl] = y;
-      const float* l = lay + t * RSTR + u * LSTR;
-      if (o < QL - 1) {
-#pragma unroll
-        for (int i = 0; i < WL; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(l + i);
-          w[i] = fmaf(-y, l4.x, w[i]);
-          w[i + 1] = fmaf(-y, l4.y, w[i + 1]);
-          w[i + 2] = fmaf(-y, l4.z, w[i + 2]);
-          w[i + 3] = fmaf(-y, l4.w, w[i + 3]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < WL; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(l + i);
-          w[i] = fmaf(-y, l4.x, w[i + 1]);
-          w[i + 1] = fmaf(-y, l4.y, w[i + 2]);
-          w[i + 2] = fmaf(-y, l4.z, w[i + 3]);
-          if (i + 3 < WL - 1) w[i + 3] = fmaf(-y, l4.w, w[i + 4 < WL ? i + 4 : WL - 1]);
-        }
+      for (int j4 = ((t + 1) / 4) * 4; j4 < SB; j4 += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(srow + j4);
+        if (j4 > t) y[j4] = fmaf(-yt, v.x, y[j4]);
+        if (j4 + 1 > t) y[j4 + 1] = fmaf(-yt, v.y, y[j4 + 1]);
+        if (j4 + 2 > t) y[j4 + 2] = fmaf(-yt, v.z, y[j4 + 2]);
+        if (j4 + 3 > t) y[j4 + 3] = fmaf(-yt, v.w, y[j4 + 3]);
       }
     }
+    float* vcol = L + (SB * warp) * DSTR + SB * warp + lane;
+#pragma unroll
+    for (int t = 0; t < SB; ++t) vcol[t * DSTR] = y[t];
   }
   __syncthreads();
-  if (ident) {
-    // DI[blk][t][c] for the CTA's RPT columns c, all NB rows t (zeros above the diagonal
-    // come out of the substitution exactly); identity past a ragged end
-    float* dout = DI + static_cast<size_t>(blk) * NB * NB + part * RPT;
-    for (int e = threadIdx.x; e < NB * RPT; e += 128) {
-      const int t = e / RPT, j = e % RPT;
-      dout[static_cast<size_t>(t) * NB + j] = (t < nb) ? ys[e] : (t == part * RPT + j ? 1.0f : 0.0f);
+  // off-diagonal blocks by distance; item = (block, row, 4 columns)
+  for (int dl = 1; dl < NSB; ++dl) {
+    const int items = (NSB - dl) * SB * (SB / 4);
+    for (int item = tid; item < items; item += 512) {
+      const int b = item / (SB * SB / 4), rr = (item % (SB * SB / 4)) / (SB / 4);
+      const int c4 = (item % (SB / 4)) * 4, i = dl + b, j = i - dl;
+      const float* lrow = L + (SB * i + rr) * DSTR;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int tb = j; tb < i; ++tb) {  // V_tb,j: the diagonal block of L, or Voff
+        const float* vb = (tb == j) ? L + (SB * j) * DSTR + SB * j + c4
+                                    : Voff + voff_index(tb, j) * SB * VSTR + c4;
+        const int vs = (tb == j) ? DSTR : VSTR;
+        const float* lt = lrow + SB * tb;
+#pragma unroll 8
+        for (int t = 0; t < SB; ++t) {
+          const float l = lt[t];
+          const float4 v = *reinterpret_cast<const float4*>(vb + t * vs);
+          acc.x = fmaf(l, v.x, acc.x);
+          acc.y = fmaf(l, v.y, acc.y);
+          acc.z = fmaf(l, v.z, acc.z);
+          acc.w = fmaf(l, v.w, acc.w);
+        }
+      }
+      *reinterpret_cast<float4*>(upper_slot(L, b) + rr * DSTR + c4) = acc;
     }
-  } else {
-    for (int e = threadIdx.x; e < nrows * NB; e += 128) {
-      const int j = e / NB, t = e % NB;
-      if (t < nb) A[(row0 + j) * d + k + t] = ys[t * RPT + j];
+    __syncthreads();
+    for (int item = tid; item < items; item += 512) {
+      const int b = item / (SB * SB / 4), rr = (item % (SB * SB / 4)) / (SB / 4);
+      const int c4 = (item % (SB / 4)) * 4, i = dl + b, j = i - dl;
+      const float* vrow = L + (SB * i + rr) * DSTR + SB * i;  // row rr of V_ii (lower)
+      const float* tb = upper_slot(L, b) + c4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int t = 0; t <= rr; ++t) {
+        const float a = vrow[t];
+        const float4 v = *reinterpret_cast<const float4*>(tb + t * DSTR);
+        acc.x = fmaf(a, v.x, acc.x);
+        acc.y = fmaf(a, v.y, acc.y);
+        acc.z = fmaf(a, v.z, acc.z);
+        acc.w = fmaf(a, v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(Voff + voff_index(i, j) * SB * VSTR + rr * VSTR + c4) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
+    __syncthreads();
+  }
+  float* dout = DI + static_cast<size_t>(k / NB) * NB * NB;
+#pragma unroll
+  for (int p = 0; p < NB * NB / 4 / 512; ++p) {
+    const int e4 = tid + p * 512, r = e4 / (NB / 4), c = (e4 % (NB / 4)) * 4;
+    const int bi = r / SB, bj = c / SB;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bi == bj) {
+      v = *reinterpret_cast<const float4*>(L + r * DSTR + c);
+    } else if (bi > bj) {
+      v = *reinterpret_cast<const float4*>(Voff + voff_index(bi, bj) * SB * VSTR +
+                                           (r % SB) * VSTR + c % SB);
+    }
+    *reinterpret_cast<float4*>(dout + r * NB + c) = v;
   }
 }
 
@@ -402,7 +420,7 @@ __global__ void reverse_transpose_kernel(const float* __restrict__ Y, int d, flo
 
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, float* LL, DevStatus* st, cudaStream_t s) {
+                    float* lam, float* DI, DevStatus* st, cudaStream_t s) {
   GPTQ_LAUNCH(GPTQ_K_PREP_DIAG, s, prep_diag_kernel, 1, 1024, 0, H, d, damp, dead, diag_fixed,
               lam, st);
   GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 256), 256, 0,
@@ -419,24 +437,27 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_LAUNCH(GPTQ_K_PREP_GATHER, s, prep_gather_kernel, d, 256, row_smem, S, d, perm, dead, lam,
               Hr);
 
-  // Cholesky of Hr (lower, in place) by NB-wide panels on stream A, and the inverse of
-  // the factor on stream B: block column k of the inverse needs only L's first k+1 block
-  // columns, so it runs as soon as panel k is final, overlapping the (latency-bound)
-  // factorisation of the next panels.  A failing pivot at reversed position a reports
-  // processing position d - a (1-based).
+  // Cholesky of Hr (lower, in place) by NB-wide panels, right-looking with one panel of
+  // look-ahead.  Stream A carries the critical chain: factor and invert the diagonal
+  // block, solve the panel below it, apply the panel's update to the next block column
+  // only (the near update).  Stream C applies the rest of the panel's update (the far
+  // update, block columns >= kb + 2) behind it.  Ordering: block column kb is final
+  // once the near update of kb - 1 (stream A, in order) and the far update of kb - 2 have
+  // run; the near update of kb writes block column kb + 1, which the far update of
+  // kb - 1 also writes, so it waits for that one.  A failing pivot at reversed position
+  // a reports processing position d - a (1-based).
   //
-  // The inverse X = L^-1 is kept transposed as Y = X^T in S so that both GEMM operands
-  // are K-major: block column i of Y is Y[:, i] = R DI[i]^T (R = the accumulated right-
-  // hand side, initially I), after which every later block column loses
-  // Y[:, i] L[r, i]^T.  Finally U = J X J = (J Y J)^T.
-  const int trsv_smem = (kLLFloats + NB * RPT) * static_cast<int>(sizeof(float));
-  const int diag_smem = NB * DSTR * static_cast<int>(sizeof(float));
+  // Stream B inverts the factor meanwhile: block column kb of the inverse needs only L's
+  // first kb + 1 block columns, so it runs as soon as panel kb is final.  The inverse
+  // X = L^-1 is kept transposed as Y = X^T in S so that both GEMM operands are K-major:
+  // block column i of Y is Y[:, i] = R DI[i]^T (R = the accumulated right-hand side,
+  // initially I), after which every later block column loses Y[:, i] L[r, i]^T.
+  // Finally U = J X J = (J Y J)^T.
+  const int diag_smem = kDiagSmemFloats * static_cast<int>(sizeof(float));
   static bool attrs = false;
   if (!attrs) {
-    GPTQ_CUDA(cudaFuncSetAttribute(chol_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   diag_smem));
-    GPTQ_CUDA(cudaFuncSetAttribute(trsv_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   trsv_smem));
+    GPTQ_CUDA(cudaFuncSetAttribute(chol_inv_diag_kernel,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, diag_smem));
     attrs = true;
   }
   CUtensorMap mHr, mS, mDI;
@@ -448,31 +469,49 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
     GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, identity_kernel, grid, 256, 0, S, d);
   }
   const int nblk = static_cast<int>(ceil_div(d, NB));
-  AuxStreams& aux = aux_streams(nblk + 2);
-  cudaStream_t sa = aux.a, sb = aux.b;
-  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk], s));
-  GPTQ_CUDA(cudaStreamWaitEvent(sa, aux.ev[nblk], 0));
-  GPTQ_CUDA(cudaStreamWaitEvent(sb, aux.ev[nblk], 0));
-  for (int k = 0; k < d; k += NB) {
-    const int kb = k / NB;
+  AuxStreams& aux = aux_streams(2 * nblk + 3);
+  cudaStream_t sa = aux.a, sb = aux.b, sc = aux.c;
+  cudaEvent_t* ev_panel = aux.ev.data();         // [nblk] panel kb factored and solved
+  cudaEvent_t* ev_far = aux.ev.data() + nblk;    // [nblk] far update of panel kb applied
+  cudaEvent_t ev_fork = aux.ev[2 * nblk], ev_b = aux.ev[2 * nblk + 1], ev_c = aux.ev[2 * nblk + 2];
+  GPTQ_CUDA(cudaEventRecord(ev_fork, s));
+  GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_fork, 0));
+  GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_fork, 0));
+  GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_fork, 0));
+  for (int kb = 0; kb < nblk; ++kb) {
+    const int k = kb * NB;
     const int rest = d - k - NB;
-    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, sa, chol_diag_kernel, 1, 512, diag_smem, Hr, d, k, LL, st, d);
+    if (kb >= 2) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 2], 0));
+    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, sa, chol_inv_diag_kernel, 1, 512, diag_smem, Hr, d, k, DI,
+                st, d);
     if (rest > 0) {
-      GPTQ_LAUNCH(GPTQ_K_POTRF_TRSM, sa, trsv_quad_kernel, (unsigned)ceil_div(rest, RPT), 128,
-                  trsv_smem, Hr, d, k, 0, LL, DI, st);
+      // the panel below, in place: L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T (rows r >= k + NB;
+      // each CTA owns whole rows, loaded before it writes them)
+      launch_gemm_tf32x3(GPTQ_K_POTRF_TRSM, mHr, k + NB, k, mDI, k, 0,
+                         Hr + static_cast<size_t>(k + NB) * d + k, d, rest, NB, 1.0f, 0.0f,
+                         false, st, sa);
     }
-    GPTQ_CUDA(cudaEventRecord(aux.ev[kb], sa));
+    GPTQ_CUDA(cudaEventRecord(ev_panel[kb], sa));
     if (rest > 0) {
-      // trailing update, lower tiles: Hr[k+NB+i][k+NB+j] -= L[k+NB+i, panel] . L[k+NB+j, panel]
+      // near update, block column kb + 1: Hr[r][k+NB+j] -= L[r, panel] . L[k+NB+j, panel]
+      // (whole tiles; the entries it changes above the diagonal are never read)
+      if (kb >= 1) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 1], 0));
       launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
-                         Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest, rest, -1.0f,
-                         1.0f, true, st, sa);
+                         Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest,
+                         rest < NB ? rest : NB, -1.0f, 1.0f, false, st, sa);
+    }
+    if (rest > NB) {
+      // far update, lower tiles of block columns >= kb + 2, on stream C
+      const int far = rest - NB;
+      GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_panel[kb], 0));
+      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + 2 * NB, k, mHr, k + 2 * NB, k,
+                         Hr + static_cast<size_t>(k + 2 * NB) * d + k + 2 * NB, d, far, far,
+                         -1.0f, 1.0f, true, st, sc);
+      GPTQ_CUDA(cudaEventRecord(ev_far[kb], sc));
     }
     // inverse, block column kb, on stream B once panel kb is final
-    GPTQ_CUDA(cudaStreamWaitEvent(sb, aux.ev[kb], 0));
+    GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_panel[kb], 0));
     const int nbi = (d - k < NB) ? d - k : NB;
-    GPTQ_LAUNCH(GPTQ_K_TRTRI_DIAG, sb, trsv_quad_kernel, (unsigned)QL, 128, trsv_smem, Hr, d, k, 1,
-                LL, DI, st);
     // Y[c][k+t] = sum_j Y[c][k+j] DI[kb][t][j], rows c < k + nbi
     launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, k, mDI, k, 0, S + k, d, k + nbi, nbi, 1.0f, 0.0f,
                        false, st, sb);
@@ -482,10 +521,12 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
                          rest, -1.0f, 1.0f, false, st, sb);
     }
   }
-  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk + 1], sb));
-  GPTQ_CUDA(cudaStreamWaitEvent(s, aux.ev[nblk + 1], 0));
-  GPTQ_CUDA(cudaEventRecord(aux.ev[nblk], sa));
-  GPTQ_CUDA(cudaStreamWaitEvent(s, aux.ev[nblk], 0));
+  GPTQ_CUDA(cudaEventRecord(ev_b, sb));
+  GPTQ_CUDA(cudaStreamWaitEvent(s, ev_b, 0));
+  GPTQ_CUDA(cudaEventRecord(ev_c, sc));
+  GPTQ_CUDA(cudaStreamWaitEvent(s, ev_c, 0));
+  GPTQ_CUDA(cudaEventRecord(ev_fork, sa));
+  GPTQ_CUDA(cudaStreamWaitEvent(s, ev_fork, 0));
   {
     dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
     GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_transpose_kernel, grid, dim3(32, 8), 0, S, d, U);

@@ -8,9 +8,12 @@
 //       code = clamp(round(w_q / s) + z, lowest, maxq); what = s (code - z);
 //       e = (w_q - what) / U_qq; W[:, q+1:i2] -= e U[q, q+1:i2]; Err[:, q-i1] = e
 //     W[:, i2:] -= Err U[i1:i2, i2:]          (the lazy update)
-// Layouts in the workspace: Wp [m][d] float32 (processing order), codesT [d][m] uint8
-// (column-major codes, so that a step's codes are one coalesced row), the block's errors
-// as bf16 halves ehi/elo [128][m] (e = hi + lo), U's bf16 halves [d][d], the loop's
+// The lazy update is deferred in two levels (same product, fewer passes over W): after a
+// block only the rest of its 512-column superblock, after the superblock every later
+// column.  Layouts in the workspace: Wp [m][d] float32 (processing order), codesT [d][m]
+// uint8 (column-major codes, so that a step's codes are one coalesced row), the
+// superblock's errors as bf16 halves ehi/elo [512][m] (e = hi + lo), U's bf16 halves
+// [d][d], the loop's
 // per-block layout of U, zeros [G][m] int32, loss_rows [m] float64 and pos [d] int32
 // (the inverse permutation).
 #include <cuda_bf16.h>
@@ -186,7 +189,7 @@ struct LoopArgs {
   float* scales;       // [G][m]
   int32_t* zeros;      // [G][m]
   uint8_t* codesT;     // [d][m]
-  __nv_bfloat16* ehi;  // [128][m]: e = hi + lo, both bf16
+  __nv_bfloat16* ehi;  // [128][m] rows of the superblock's [512][m]: e = hi + lo, bf16
   __nv_bfloat16* elo;
   double* loss_rows;   // [m]
 };
@@ -431,7 +434,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
     GPTQ_LAUNCH(GPTQ_K_QUANT_SPLIT, s, ulayout_kernel, dim3((unsigned)ceil_div(d, BLK), BLK), 128,
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
-    const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, q.uhi, q.ulo, m, d);
+    const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, kErrRows, q.uhi, q.ulo, q.Wp, m, d);
     const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float)) + BLK * (128 / QUAD) * (1 + 2 + 2);
     static bool loop_attr = false;
     if (!loop_attr) {
@@ -440,37 +443,49 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
       loop_attr = true;
     }
     const bool inblock_fit = (q.group > 0 && q.group <= BLK);
-    for (int i1 = 0; i1 < d; i1 += BLK) {
-      const int nb = (d - i1 < BLK) ? d - i1 : BLK;
-      LoopArgs a;
-      a.Wp = q.Wp;
-      a.Ulay = q.Ublk;
-      a.m = m;
-      a.d = d;
-      a.i1 = i1;
-      a.nb = nb;
-      a.group = inblock_fit ? q.group : 0;
-      a.gi_outer = 0;
-      a.g = g;
-      a.scales = q.scales;
-      a.zeros = q.zeros;
-      a.codesT = q.codesT;
-      a.ehi = q.ehi;
-      a.elo = q.elo;
-      a.loss_rows = q.loss_rows;
-      if (!inblock_fit) {
-        const bool start = (q.group == -1) ? (i1 == 0) : (i1 % q.group == 0);
-        const int gi = (q.group == -1) ? 0 : i1 / q.group;
-        if (start) {
-          const int len = (q.group == -1) ? d : ((d - i1 < q.group) ? d - i1 : q.group);
-          GPTQ_LAUNCH(GPTQ_K_QUANT_FIT, s, fit_kernel, (unsigned)ceil_div(m, 8), 256, 0, q.Wp, m,
-                      d, i1, len, g, gi, q.scales, q.zeros);
+    // Deferred updates in two levels: superblocks of kErrRows columns, unless a group that
+    // starts inside a superblock would reach past its end (its fit must see every earlier
+    // block's update), in which case every block is its own superblock.
+    const bool groups_nest = q.group == -1 || q.group <= BLK || kErrRows % q.group == 0 ||
+                             q.group % kErrRows == 0;
+    const int sb_cols = groups_nest ? kErrRows : BLK;
+    for (int s0 = 0; s0 < d; s0 += sb_cols) {
+      const int s1 = (d - s0 < sb_cols) ? d : s0 + sb_cols;
+      for (int i1 = s0; i1 < s1; i1 += BLK) {
+        const int nb = (d - i1 < BLK) ? d - i1 : BLK;
+        LoopArgs a;
+        a.Wp = q.Wp;
+        a.Ulay = q.Ublk;
+        a.m = m;
+        a.d = d;
+        a.i1 = i1;
+        a.nb = nb;
+        a.group = inblock_fit ? q.group : 0;
+        a.gi_outer = 0;
+        a.g = g;
+        a.scales = q.scales;
+        a.zeros = q.zeros;
+        a.codesT = q.codesT;
+        a.ehi = q.ehi + static_cast<size_t>(i1 - s0) * m;
+        a.elo = q.elo + static_cast<size_t>(i1 - s0) * m;
+        a.loss_rows = q.loss_rows;
+        if (!inblock_fit) {
+          const bool start = (q.group == -1) ? (i1 == 0) : (i1 % q.group == 0);
+          const int gi = (q.group == -1) ? 0 : i1 / q.group;
+          if (start) {
+            const int len = (q.group == -1) ? d : ((d - i1 < q.group) ? d - i1 : q.group);
+            GPTQ_LAUNCH(GPTQ_K_QUANT_FIT, s, fit_kernel, (unsigned)ceil_div(m, 8), 256, 0, q.Wp,
+                        m, d, i1, len, g, gi, q.scales, q.zeros);
+          }
+          a.gi_outer = gi;
         }
-        a.gi_outer = gi;
+        GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, 128 / QUAD),
+                    128, loop_smem, a);
+        // near: the rest of the superblock, W[:, i2:s1] -= Err_block U[i1:i2, i2:s1]
+        if (i1 + nb < s1) launch_lazy_tc(maps, i1 - s0, i1, nb, i1 + nb, s1, q.st, s);
       }
-      GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, 128 / QUAD), 128,
-                  loop_smem, a);
-      if (i1 + nb < d) launch_lazy_tc(maps, q.Wp, m, d, i1, q.st, s);  // W[:, i2:] -= Err U
+      // far: every later column, W[:, s1:] -= Err_superblock U[s0:s1, s1:]
+      if (s1 < d) launch_lazy_tc(maps, 0, s0, s1 - s0, s1, d, q.st, s);
     }
     dim3 gq((unsigned)ceil_div(m, 128), static_cast<unsigned>(q.bits * d / 32));
     GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_kernel, gq, 128, 0, q.codesT, q.pos, m, d,

@@ -154,6 +154,8 @@ AuxStreams& aux_streams(int nevents) {
                "cudaStreamCreateWithPriority");
     cuda_check(cudaStreamCreateWithPriority(&a.b, cudaStreamNonBlocking, least),
                "cudaStreamCreateWithPriority");
+    cuda_check(cudaStreamCreateWithPriority(&a.c, cudaStreamNonBlocking, (least + greatest) / 2),
+               "cudaStreamCreateWithPriority");
   }
   while (static_cast<int>(a.ev.size()) < nevents) {
     cudaEvent_t e;
