@@ -23,8 +23,8 @@ int syrk_tc_token_granule();
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s);
 
-// floats of one 128-column block's solve layout (the loop's U layout, the factor's L)
-constexpr int kLoopUblkFloats = 128 * 160 + 128;
+// floats of one 128-column block's layout of U for the column loop
+constexpr int kLoopUblkFloats = 128 * 144 + 128;
 
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,

@@ -146,44 +146,160 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // shared memory: the panel below it is solved against V by a GEMM, and the inverse of
 // the whole factor is assembled from the V blocks.
 //
-// Factor, recursively by 32-column sub-panels c0:
-//   1. warp 0 factors the 32 x 32 diagonal sub-block, lane = row, columns in registers.
-//      Column c: l_cc = sqrt(p), l_rc = a_rc / l_cc, via one reciprocal square root of the
-//      pivot p; the column is published through shared memory (ST[c][r] = l_rc,
-//      ST[c][c] = 1/l_cc) and every row subtracts l_rc l_jc from its entries j > c.  The
-//      next pivot only needs row c+1's own l_{c+1,c}, so it is formed first and the
-//      broadcast stays off the pivot chain.
-//   2. the rows below solve x S^T = a right-looking, one row per thread (x_c = acc_c /
-//      l_cc, then acc_j -= x_c l_jc for j > c).
-//   3. the rest of the block takes L[r][j] -= sum_t L[r][c0+t] L[j][c0+t], one 4 x 4
-//      register tile per thread over the lower tiles.
-// Inverse, by 32 x 32 blocks (block indices): V_ii = L_ii^-1 by forward substitution,
-// lane = column, four warps at once; then, by distance i - j = 1, 2, 3,
-//   V_ij = -V_ii sum_{t=j}^{i-1} L_it V_tj.
-// Shared memory (95 KB, so the CTA fits beside a GEMM CTA on one SM): the staged block
-// L, whose six upper 32 x 32 blocks are free and hold the published sub-panel columns
-// (ST, four blocks) and later the inverse's partial products (TB, three blocks); the V_ii
-// overwrite the diagonal blocks of L once their columns are published; the six V_ij
-// below the diagonal have their own array.
-constexpr int DSTR = NB + 4;   // row stride of the staged block (16-byte rows)
-constexpr int SB = 32;         // sub-panel width
+// Factor, right-looking by 32-column sub-panels s (columns c0 = 32 s ..):
+//   P1. warp 0 factors the 32 x 32 diagonal sub-block, lane = row, columns in registers.
+//       Column c: l_cc = sqrt(p), l_rc = a_rc / l_cc, through one reciprocal square root
+//       of the pivot p; the column is published in shared memory (ST[c][r] = l_rc,
+//       ST[c][c] = 1/l_cc) and every row subtracts l_rc l_jc from its entries j > c.  The
+//       next pivot only needs row c+1's own l_{c+1,c}, so it is formed first and the
+//       broadcast stays off the pivot chain; the pivots are checked after the column loop.
+//   P2. the rows below solve x S^T = a right-looking, one row per thread (x_c = acc_c /
+//       l_cc, then acc_j -= x_c l_jc for j > c), and also store the solved panel
+//       transposed (XT).
+//   P3. the rank-32 update of the rest of the block, L[r][j] -= sum_t L[r][c0+t] L[j][c0+t]
+//       (j <= r): one warp per 32 rows x 16 columns, lane = row; each lane holds its own
+//       panel row in registers and the 16 columns' panel values are read from XT with
+//       warp-wide broadcast loads.  With one sub-panel of look-ahead: the next sub-panel's
+//       columns first (P3a), the columns after it (P3b) while warp 0 runs the next P1.
+// Inverse, by 32 x 32 blocks (block indices), interleaved with the factor: V_ss = L_ss^-1
+// (forward substitution, lane = column, on a spare warp next to P2) replaces L_ss, and
+// then the row block V_sj = -V_ss sum_{t=j}^{s-1} L_st V_tj (j < s) on spare warps next
+// to P3a, each warp forming 32 x 16 of the sum in registers (own L row times broadcast V
+// rows) and applying V_ss through a private buffer.
+// Shared memory (about 120 KB, so the CTA fits beside one GEMM CTA on an SM): the staged
+// block L, whose free upper 32 x 32 blocks hold the published columns; the six V_ij
+// below the diagonal; XT; six private 32 x 16 buffers.
+constexpr int DSTR = NB + 4;       // row stride of the staged block (16-byte rows)
+constexpr int SB = 32;             // sub-panel width
 constexpr int NSB = NB / SB;
-constexpr int VSTR = SB + 4;   // row stride of an off-diagonal V block
-constexpr int kDiagSmemFloats = NB * DSTR + (NSB * (NSB - 1) / 2) * SB * VSTR;
+constexpr int VSTR = SB + 4;       // row stride of an off-diagonal V block
+constexpr int XSTR = NB - SB + 4;  // row stride of XT (up to 96 rows below a sub-panel)
+constexpr int TBSTR = 16 + 4;      // row stride of a private 32 x 16 buffer
+constexpr int NTB = 6;             // private buffers (inverse tasks of one step)
+constexpr int kNVoff = NSB * (NSB - 1) / 2;
+constexpr int kDiagSmemFloats = NB * DSTR + kNVoff * SB * VSTR + SB * XSTR + NTB * SB * TBSTR;
 
-// the free upper block that holds sub-panel s's columns (s = 0..3), then TB[s] (s < 3)
-__device__ __forceinline__ float* upper_slot(float* L, int s) {
+// the free upper block that holds sub-panel s's published columns
+__device__ __forceinline__ float* st_slot(float* L, int s) {
   const int bi = s < 3 ? 0 : 1, bj = s < 3 ? s + 1 : 2;
   return L + (SB * bi) * DSTR + SB * bj;
 }
 __device__ __forceinline__ int voff_index(int i, int j) { return i * (i - 1) / 2 + j; }
 
+// P3 task: rows r0 + lane, columns j0 .. j0 + 15 (entries j <= r) lose
+// sum_t L[r][c0 + t] XT[t][j - (c0 + SB)].
+__device__ __forceinline__ void rank32_task(float* L, const float* XT, int c0, int r0, int j0,
+                                            int lane) {
+  const int r = r0 + lane;
+  float xr[SB];
+  {
+    const float* xrow = L + r * DSTR + c0;
+#pragma unroll
+    for (int t = 0; t < SB; t += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(xrow + t);
+      xr[t] = v.x; xr[t + 1] = v.y; xr[t + 2] = v.z; xr[t + 3] = v.w;
+    }
+  }
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+  const float* xt = XT + (j0 - c0 - SB);
+#pragma unroll
+  for (int t = 0; t < SB; ++t) {
+#pragma unroll
+    for (int q = 0; q < 16; q += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(xt + t * XSTR + q);
+      acc[q] = fmaf(xr[t], v.x, acc[q]);
+      acc[q + 1] = fmaf(xr[t], v.y, acc[q + 1]);
+      acc[q + 2] = fmaf(xr[t], v.z, acc[q + 2]);
+      acc[q + 3] = fmaf(xr[t], v.w, acc[q + 3]);
+    }
+  }
+  float* lrow = L + r * DSTR + j0;
+#pragma unroll
+  for (int q = 0; q < 16; q += 4) {
+    float4 v = *reinterpret_cast<float4*>(lrow + q);
+    if (j0 + q <= r) v.x -= acc[q];
+    if (j0 + q + 1 <= r) v.y -= acc[q + 1];
+    if (j0 + q + 2 <= r) v.z -= acc[q + 2];
+    if (j0 + q + 3 <= r) v.w -= acc[q + 3];
+    *reinterpret_cast<float4*>(lrow + q) = v;
+  }
+}
+
+// Inverse task: V_sj[:, 16h .. 16h + 15] = -V_ss sum_{t=j}^{s-1} L_st V_tj[:, same], one
+// warp, lane = row; Tw is the warp's private 32 x 16 buffer.
+__device__ __forceinline__ void inv_task(float* L, float* Voff, float* Tw, int s, int j, int h,
+                                         int lane) {
+  const int r = SB * s + lane;
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+  for (int tb = j; tb < s; ++tb) {
+    const float* vb = (tb == j) ? L + (SB * j) * DSTR + SB * j + 16 * h
+                                : Voff + voff_index(tb, j) * SB * VSTR + 16 * h;
+    const int vs = (tb == j) ? DSTR : VSTR;
+    float lv[SB];
+    const float* lrow = L + r * DSTR + SB * tb;
+#pragma unroll
+    for (int t = 0; t < SB; t += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(lrow + t);
+      lv[t] = v.x; lv[t + 1] = v.y; lv[t + 2] = v.z; lv[t + 3] = v.w;
+    }
+#pragma unroll
+    for (int t = 0; t < SB; ++t) {
+#pragma unroll
+      for (int q = 0; q < 16; q += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(vb + t * vs + q);
+        acc[q] = fmaf(lv[t], v.x, acc[q]);
+        acc[q + 1] = fmaf(lv[t], v.y, acc[q + 1]);
+        acc[q + 2] = fmaf(lv[t], v.z, acc[q + 2]);
+        acc[q + 3] = fmaf(lv[t], v.w, acc[q + 3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 16; q += 4)
+    *reinterpret_cast<float4*>(Tw + lane * TBSTR + q) =
+        make_float4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+  __syncwarp();
+  float vrow[SB];
+  {
+    const float* vss = L + r * DSTR + SB * s;  // row `lane` of V_ss (zeros above the diagonal)
+#pragma unroll
+    for (int t = 0; t < SB; t += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(vss + t);
+      vrow[t] = v.x; vrow[t + 1] = v.y; vrow[t + 2] = v.z; vrow[t + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+#pragma unroll
+  for (int t = 0; t < SB; ++t) {
+#pragma unroll
+    for (int q = 0; q < 16; q += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(Tw + t * TBSTR + q);
+      acc[q] = fmaf(vrow[t], v.x, acc[q]);
+      acc[q + 1] = fmaf(vrow[t], v.y, acc[q + 1]);
+      acc[q + 2] = fmaf(vrow[t], v.z, acc[q + 2]);
+      acc[q + 3] = fmaf(vrow[t], v.w, acc[q + 3]);
+    }
+  }
+  float* out = Voff + voff_index(s, j) * SB * VSTR + lane * VSTR + 16 * h;
+#pragma unroll
+  for (int q = 0; q < 16; q += 4)
+    *reinterpret_cast<float4*>(out + q) = make_float4(-acc[q], -acc[q + 1], -acc[q + 2], -acc[q + 3]);
+  __syncwarp();  // the buffer may be reused by the warp's next task
+}
+
 __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restrict__ A, int d,
                                                             int k, float* __restrict__ DI,
                                                             DevStatus* st, int32_t info_base) {
   extern __shared__ __align__(16) float smem_f[];
-  float* L = smem_f;             // [NB][DSTR]
-  float* Voff = L + NB * DSTR;   // [6][SB][VSTR]
+  float* L = smem_f;                  // [NB][DSTR]
+  float* Voff = L + NB * DSTR;        // [6][SB][VSTR]
+  float* XT = Voff + kNVoff * SB * VSTR;  // [SB][XSTR]
+  float* Tbuf = XT + SB * XSTR;       // [NTB][SB][TBSTR]
   __shared__ int bad;
   if (st->code != 0) return;
   const int nb = min(NB, d - k);  // a multiple of 8
@@ -208,24 +324,23 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
 
   for (int s = 0; s < NSB; ++s) {
     const int c0 = s * SB;
-    float* STs = upper_slot(L, s);  // STs[c * DSTR + j] = l_{c0+j, c0+c} (j > c), 1/l_cc (j = c)
-    // 1. the 32 x 32 diagonal sub-block
+    float* STs = st_slot(L, s);  // STs[c * DSTR + j] = l_{c0+j, c0+c} (j > c), 1/l_cc (j = c)
+    // [A] P1(s) on warp 0; P3b of sub-panel s - 1 on the other warps
     if (warp == 0) {
-      float* lrow = L + (c0 + lane) * DSTR + c0;
+      const float* lrow = L + (c0 + lane) * DSTR + c0;
       float w[SB];
 #pragma unroll
       for (int j = 0; j < SB; j += 4) {
         const float4 v = *reinterpret_cast<const float4*>(lrow + j);
         w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
       }
-      int badc = -1;
+      float il_own = 1.0f;
       float piv = __shfl_sync(0xffffffffu, w[0], 0);
 #pragma unroll
       for (int c = 0; c < SB; ++c) {
-        if (badc < 0 && (!(piv > 0.0f) || !isfinite(piv))) badc = c;
         const float il = rsqrtf(piv);
         const float lc = (lane == c) ? piv * il : w[c] * il;
-        if (lane >= c) lrow[c] = lc;
+        if (lane == c) il_own = il;
         STs[c * DSTR + lane] = (lane > c) ? lc : ((lane == c) ? il : 0.0f);
         if (c + 1 < SB) piv = __shfl_sync(0xffffffffu, fmaf(-lc, lc, w[c + 1]), c + 1);
         __syncwarp();
@@ -238,15 +353,27 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
           if (j4 + 3 > c) w[j4 + 3] = fmaf(-lc, v.w, w[j4 + 3]);
         }
       }
-      if (lane == 0 && badc >= 0 && c0 + badc < nb) {
+      // a pivot that is not positive and finite gives a reciprocal root that is not either
+      const unsigned badmask =
+          __ballot_sync(0xffffffffu, !(il_own > 0.0f && il_own < INFINITY) && c0 + lane < nb);
+      if (lane == 0 && badmask != 0u) {
         bad = 1;
-        dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c0 + badc));
+        dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c0 + __ffs(badmask) - 1));
+      }
+    } else if (s >= 1 && s <= 2) {
+      // P3b of sub-panel s - 1: rows and columns >= c0 + SB (its XT is still in place)
+      const int ntask = (s == 1) ? 6 : 2;
+      for (int task = warp - 1; task < ntask; task += 15) {
+        int g = 0;
+        while ((g + 1) * (g + 2) <= task) ++g;
+        const int h = task - g * (g + 1);
+        rank32_task(L, XT, c0 - SB, c0 + SB + SB * g, c0 + SB + 16 * h, lane);
       }
     }
     __syncthreads();
     if (bad) return;
+    // [B] P2(s) on the threads of the rows below; V_ss on warp 15
     const int m2 = NB - c0 - SB;
-    // 2. rows below the sub-block
     if (tid < m2) {
       float* xrow = L + (c0 + SB + tid) * DSTR + c0;
       float x[SB];
@@ -272,111 +399,46 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
 #pragma unroll
       for (int j = 0; j < SB; j += 4)
         *reinterpret_cast<float4*>(xrow + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+#pragma unroll
+      for (int t = 0; t < SB; ++t) XT[t * XSTR + tid] = x[t];
+    }
+    if (warp == 15) {
+      float y[SB];
+#pragma unroll
+      for (int t = 0; t < SB; ++t) y[t] = (t == lane) ? 1.0f : 0.0f;
+#pragma unroll
+      for (int t = 0; t < SB; ++t) {
+        const float* srow = STs + t * DSTR;
+        const float yt = y[t] * srow[t];
+        y[t] = yt;
+#pragma unroll
+        for (int j4 = ((t + 1) / 4) * 4; j4 < SB; j4 += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(srow + j4);
+          if (j4 > t) y[j4] = fmaf(-yt, v.x, y[j4]);
+          if (j4 + 1 > t) y[j4 + 1] = fmaf(-yt, v.y, y[j4 + 1]);
+          if (j4 + 2 > t) y[j4 + 2] = fmaf(-yt, v.z, y[j4 + 2]);
+          if (j4 + 3 > t) y[j4 + 3] = fmaf(-yt, v.w, y[j4 + 3]);
+        }
+      }
+      float* vcol = L + c0 * DSTR + c0 + lane;  // V_ss replaces L_ss
+#pragma unroll
+      for (int t = 0; t < SB; ++t) vcol[t * DSTR] = y[t];
     }
     __syncthreads();
-    // 3. the rest of the block, lower 4 x 4 tiles
-    const int T = m2 / 4;
-    for (int tile = tid; tile < T * (T + 1) / 2; tile += 512) {
-      int ti = 0, rem = tile;
-      while (rem > ti) { rem -= ti + 1; ++ti; }
-      const int tj = rem;
-      const int r0 = c0 + SB + 4 * ti, j0 = c0 + SB + 4 * tj;
-      float acc[4][4] = {};
-#pragma unroll
-      for (int t = 0; t < SB; t += 4) {
-        float4 ra[4], rb[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ra[u] = *reinterpret_cast<const float4*>(L + (r0 + u) * DSTR + c0 + t);
-          rb[u] = *reinterpret_cast<const float4*>(L + (j0 + u) * DSTR + c0 + t);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            acc[u][v] += ra[u].x * rb[v].x + ra[u].y * rb[v].y + ra[u].z * rb[v].z +
-                         ra[u].w * rb[v].w;
+    // [C] P3a(s): columns c0 + SB .. c0 + 2 SB, rows below; row block s of V
+    const int n3a = (s < NSB - 1) ? 2 * (NSB - 1 - s) : 0;
+    const int ntasks = n3a + 2 * s;
+    for (int task = warp; task < ntasks; task += 16) {
+      if (task < n3a) {
+        rank32_task(L, XT, c0, c0 + SB + SB * (task / 2), c0 + SB + 16 * (task % 2), lane);
+      } else {
+        const int it = task - n3a;
+        inv_task(L, Voff, Tbuf + (warp % NTB) * SB * TBSTR, s, it / 2, it % 2, lane);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          if (j0 + v <= r0 + u) L[(r0 + u) * DSTR + j0 + v] -= acc[u][v];
     }
     __syncthreads();
   }
 
-  // inverse: diagonal blocks, warp w = block w, lane = column; V_ww replaces L_ww
-  if (warp < NSB) {
-    const float* STw = upper_slot(L, warp);
-    float y[SB];
-#pragma unroll
-    for (int t = 0; t < SB; ++t) y[t] = (t == lane) ? 1.0f : 0.0f;
-#pragma unroll
-    for (int t = 0; t < SB; ++t) {
-      const float* srow = STw + t * DSTR;
-      const float yt = y[t] * srow[t];
-      y[t] = yt;
-#pragma unroll
-      for (int j4 = ((t + 1) / 4) * 4; j4 < SB; j4 += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(srow + j4);
-        if (j4 > t) y[j4] = fmaf(-yt, v.x, y[j4]);
-        if (j4 + 1 > t) y[j4 + 1] = fmaf(-yt, v.y, y[j4 + 1]);
-        if (j4 + 2 > t) y[j4 + 2] = fmaf(-yt, v.z, y[j4 + 2]);
-        if (j4 + 3 > t) y[j4 + 3] = fmaf(-yt, v.w, y[j4 + 3]);
-      }
-    }
-    float* vcol = L + (SB * warp) * DSTR + SB * warp + lane;
-#pragma unroll
-    for (int t = 0; t < SB; ++t) vcol[t * DSTR] = y[t];
-  }
-  __syncthreads();
-  // off-diagonal blocks by distance; item = (block, row, 4 columns)
-  for (int dl = 1; dl < NSB; ++dl) {
-    const int items = (NSB - dl) * SB * (SB / 4);
-    for (int item = tid; item < items; item += 512) {
-      const int b = item / (SB * SB / 4), rr = (item % (SB * SB / 4)) / (SB / 4);
-      const int c4 = (item % (SB / 4)) * 4, i = dl + b, j = i - dl;
-      const float* lrow = L + (SB * i + rr) * DSTR;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int tb = j; tb < i; ++tb) {  // V_tb,j: the diagonal block of L, or Voff
-        const float* vb = (tb == j) ? L + (SB * j) * DSTR + SB * j + c4
-                                    : Voff + voff_index(tb, j) * SB * VSTR + c4;
-        const int vs = (tb == j) ? DSTR : VSTR;
-        const float* lt = lrow + SB * tb;
-#pragma unroll 8
-        for (int t = 0; t < SB; ++t) {
-          const float l = lt[t];
-          const float4 v = *reinterpret_cast<const float4*>(vb + t * vs);
-          acc.x = fmaf(l, v.x, acc.x);
-          acc.y = fmaf(l, v.y, acc.y);
-          acc.z = fmaf(l, v.z, acc.z);
-          acc.w = fmaf(l, v.w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(upper_slot(L, b) + rr * DSTR + c4) = acc;
-    }
-    __syncthreads();
-    for (int item = tid; item < items; item += 512) {
-      const int b = item / (SB * SB / 4), rr = (item % (SB * SB / 4)) / (SB / 4);
-      const int c4 = (item % (SB / 4)) * 4, i = dl + b, j = i - dl;
-      const float* vrow = L + (SB * i + rr) * DSTR + SB * i;  // row rr of V_ii (lower)
-      const float* tb = upper_slot(L, b) + c4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int t = 0; t <= rr; ++t) {
-        const float a = vrow[t];
-        const float4 v = *reinterpret_cast<const float4*>(tb + t * DSTR);
-        acc.x = fmaf(a, v.x, acc.x);
-        acc.y = fmaf(a, v.y, acc.y);
-        acc.z = fmaf(a, v.z, acc.z);
-        acc.w = fmaf(a, v.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(Voff + voff_index(i, j) * SB * VSTR + rr * VSTR + c4) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
-  }
   float* dout = DI + static_cast<size_t>(k / NB) * NB * NB;
 #pragma unroll
   for (int p = 0; p < NB * NB / 4 / 512; ++p) {

@@ -145,22 +145,24 @@ __device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
-// The column loop gives each output row a group of QUAD = 8 lanes; lane t owns the block's
-// columns c = 8i + t (i = 0..15).  Column q is quantised by its owner (lane q%8), which
-// broadcasts e to the group; every lane then updates its own later columns.  Each lane
-// keeps a rolling window of 16 registers: during window step g (columns 8g .. 8g+7) w[i]
-// is column 8(i+g)+t, and the last column of a step writes every compensated value one
-// slot down, so the window's first slot always holds the lane's next column and every
-// register index is static.  The U rows are laid out so that each (column, lane) reads 16
-// consecutive floats:
-//   Ulay[b][q][t][i] = U[i1+q][i1+c], c = 8(i + g + (q%8 == 7)) + t, if q < c < nb else 0
-// (i < 16, padded to 20 floats per lane), followed by the 128 reciprocals 1/U[i1+q][i1+q].
-constexpr int QUAD = 8;
-constexpr int WIN = BLK / QUAD;                     // 16 columns per lane
-constexpr int LANE_STRIDE = WIN + 4;                // padded: the group's float4 reads hit
-                                                    // eight different bank groups
-constexpr int ROW_STRIDE = QUAD * LANE_STRIDE;      // floats per step q
-constexpr int kUlayFloats = BLK * ROW_STRIDE + BLK;
+// The column loop gives each output row LPR = 4 lanes; lane t holds the block's columns
+// 32t .. 32t+31 in registers for the whole block.  Sub-block b (columns 32b ..) is
+// quantised by lane b, column after column: the owner rounds its column, broadcasts the
+// error e to the row's lanes, and every lane subtracts e U[q][c] from its columns (U is
+// laid out with zeros at c <= q, so the same 32 FMAs serve the owner, the lanes after it
+// and, as no-ops, the lanes before it).  The owner forms its next column's value from its
+// own e before the broadcast returns, which keeps the shuffle off the column chain.  The
+// U rows are read with loads that four lane positions share across the warp:
+//   Ulay[b][q][t][j] = U[i1+q][i1+32t+j] if q < 32t+j < nb else 0
+// (j < 32, padded to 36 floats per lane position so the four positions hit different
+// banks), followed by the 128 reciprocals 1/U[i1+q][i1+q].
+constexpr int LPR = 4;                         // lanes per row
+constexpr int LW = BLK / LPR;                  // 32 columns per lane
+constexpr int LSTR = LW + 4;                   // padded lane stride
+constexpr int UROW = LPR * LSTR;               // floats per row q of the layout
+constexpr int kUlayFloats = BLK * UROW + BLK;
+constexpr int LOOP_THREADS = 64;
+constexpr int RPC = LOOP_THREADS / LPR;        // rows per CTA
 static_assert(kUlayFloats == kLoopUblkFloats, "workspace sizing of the loop's U layout");
 
 __global__ void ulayout_kernel(const float* __restrict__ U, int d, float* __restrict__ Ulay) {
@@ -169,13 +171,12 @@ __global__ void ulayout_kernel(const float* __restrict__ U, int d, float* __rest
   const int nb = min(BLK, d - i1);
   float* out = Ulay + static_cast<size_t>(b) * kUlayFloats;
   const float* urow = U + static_cast<size_t>(i1 + (q < nb ? q : 0)) * d + i1;
-  const int g = q / QUAD + ((q % QUAD) == QUAD - 1 ? 1 : 0);
-  for (int e = threadIdx.x; e < ROW_STRIDE; e += blockDim.x) {
-    const int t = e / LANE_STRIDE, i = e % LANE_STRIDE;
-    const int c = QUAD * (i + g) + t;
-    out[q * ROW_STRIDE + e] = (i < WIN && q < nb && c > q && c < nb) ? urow[c] : 0.0f;
+  for (int e = threadIdx.x; e < UROW; e += blockDim.x) {
+    const int t = e / LSTR, j = e % LSTR;
+    const int c = LW * t + j;
+    out[q * UROW + e] = (j < LW && q < nb && c > q && c < nb) ? urow[c] : 0.0f;
   }
-  if (threadIdx.x == 0) out[BLK * ROW_STRIDE + q] = (q < nb) ? 1.0f / urow[q] : 1.0f;
+  if (threadIdx.x == 0) out[BLK * UROW + q] = (q < nb) ? 1.0f / urow[q] : 1.0f;
 }
 
 struct LoopArgs {
@@ -194,60 +195,128 @@ struct LoopArgs {
   double* loss_rows;   // [m]
 };
 
-// Group fit over the first NW window slots of each lane of the row's lane group
-// (warp-shuffle min / max across the group), masking columns past the block's end.
-template <int NW>
-__device__ __forceinline__ void fit_quad(const float (&w)[WIN], int g, int t, int nb,
-                                         const Grid& gr, float& s, float& z) {
+// Group fit at column j of the lane's window: over w[j .. j+15] (group 16) or the whole
+// window, combined across the lanes of the group (2 for 64, 4 for 128), masking columns
+// past the block's end.
+template <int J>
+__device__ __forceinline__ void fit_lanes(const float (&w)[LW], int group, int t, int nb,
+                                          const Grid& gr, float& s, float& z) {
   float mn = INFINITY, mx = -INFINITY, am = 0.0f;
+  const int lo = (group == 16) ? J : 0, hi = (group == 16) ? J + 16 : LW;
 #pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    if (QUAD * (i + g) + t < nb) {
+  for (int i = 0; i < LW; ++i) {
+    if (i >= lo && i < hi && LW * t + i < nb) {
       mn = fminf(mn, w[i]);
       mx = fmaxf(mx, w[i]);
       am = fmaxf(am, fabsf(w[i]));
     }
   }
-#pragma unroll
-  for (int o = 1; o < QUAD; o <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if (group >= 64) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  }
+  if (group >= 128) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
   }
   fit_from_range(gr, mn, mx, am, s, z);
 }
 
-__global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
+// One column q = 32 b + J of sub-block b: fit at a group start, round the owner's value
+// wq, broadcast e, update every lane's window.  The owner's code and error stay in
+// registers (code_r[J], e_r[J]) until the sub-block ends, so a column is one branch-free
+// stretch of code that the compiler can overlap with the next column's rounding.
+// Returns the owner's next column value.
+template <int J>
+__device__ __forceinline__ float loop_column(float (&w)[LW], float (&code_r)[LW],
+                                             float (&e_r)[LW], float wq, int b, int t, int gb,
+                                             bool active, int r, const LoopArgs& a,
+                                             const float* __restrict__ ulay,
+                                             const float* __restrict__ urinv, float& s,
+                                             float& z, float& rs, float& loss) {
+  const int q = LW * b + J;
+  // groups of 16 .. 128 start only at window positions 0 and 16
+  if constexpr (J == 0 || J == 16) {
+    if (a.group > 0 && (q % a.group) == 0) {
+      fit_lanes<J>(w, a.group, t, a.nb, a.g, s, z);
+      rs = __frcp_rn(s);
+      wq = w[J];  // the fit saw the settled window
+      if (active && t == b) {
+        const int gi = (a.i1 + q) / a.group;
+        a.scales[static_cast<size_t>(gi) * a.m + r] = s;
+        a.zeros[static_cast<size_t>(gi) * a.m + r] = static_cast<int32_t>(z);
+      }
+    }
+  }
+  const float v = div_by_scale(wq, s, rs);
+  const float code = fminf(fmaxf(rintf(v) + z, a.g.lowest), a.g.maxq);
+  const float what = s * (code - z);
+  const float e_own = (wq - what) * urinv[q];
+  const float* u = ulay + q * UROW + t * LSTR;
+  // the owner's next column from its own error (the broadcast update below computes the
+  // same value with the same fma)
+  float wnext = 0.0f;
+  if constexpr (J + 1 < LW) wnext = fmaf(-e_own, u[J + 1], w[J + 1]);
+  const float e = __shfl_sync(0xffffffffu, e_own, gb + b);
+  code_r[J] = code;
+  e_r[J] = e;
+  loss = fmaf((t == b && q < a.nb) ? 0.5f * e : 0.0f, e, loss);
+#pragma unroll
+  for (int i = 0; i < LW; i += 4) {
+    const float4 u4 = *reinterpret_cast<const float4*>(u + i);
+    w[i] = fmaf(-e, u4.x, w[i]);
+    w[i + 1] = fmaf(-e, u4.y, w[i + 1]);
+    w[i + 2] = fmaf(-e, u4.z, w[i + 2]);
+    w[i + 3] = fmaf(-e, u4.w, w[i + 3]);
+  }
+  return wnext;
+}
+
+template <int J>
+__device__ __forceinline__ void loop_columns(float (&w)[LW], float (&code_r)[LW],
+                                             float (&e_r)[LW], float& wq, int b, int t, int gb,
+                                             bool active, int r, const LoopArgs& a,
+                                             const float* __restrict__ ulay,
+                                             const float* __restrict__ urinv, float& s,
+                                             float& z, float& rs, float& loss) {
+  wq = loop_column<J>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs, loss);
+  if constexpr (J + 1 < LW)
+    loop_columns<J + 1>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs,
+                        loss);
+}
+
+__global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   const float* ulay = smem_f;
-  const float* urinv = smem_f + BLK * ROW_STRIDE;
+  const float* urinv = smem_f + BLK * UROW;
   // the block's codes and bf16 error halves, staged so that the global writes are whole
-  // rows of 32 consecutive output rows
-  constexpr int RPC = 128 / QUAD;  // rows per CTA
-  uint8_t* codes_s = reinterpret_cast<uint8_t*>(smem_f + kUlayFloats);               // [128][32]
-  __nv_bfloat16* ehi_s = reinterpret_cast<__nv_bfloat16*>(codes_s + BLK * RPC);      // [128][32]
-  __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][32]
+  // rows of RPC consecutive output rows
+  uint8_t* codes_s = reinterpret_cast<uint8_t*>(smem_f + kUlayFloats);               // [128][RPC]
+  __nv_bfloat16* ehi_s = reinterpret_cast<__nv_bfloat16*>(codes_s + BLK * RPC);      // [128][RPC]
+  __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][RPC]
   const int i1 = a.i1, nb = a.nb;
   {
     const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
     float4* dst = reinterpret_cast<float4*>(smem_f);
     for (int e = threadIdx.x; e < kUlayFloats / 4; e += blockDim.x) cp_async16(dst + e, src + e);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  __syncthreads();
-
   const int lane = threadIdx.x % 32;
-  const int t = lane % QUAD;
-  const int qbase = lane & ~(QUAD - 1);
-  const int r = blockIdx.x * (blockDim.x / QUAD) + threadIdx.x / QUAD;
+  const int t = lane % LPR;
+  const int gb = lane & ~(LPR - 1);
+  const int rl = threadIdx.x / LPR;  // row within the CTA
+  const int r = blockIdx.x * RPC + rl;
   const bool active = r < a.m;
-  float w[WIN];
+  float w[LW];
   {
-    const float* wrow = a.Wp + static_cast<size_t>(active ? r : 0) * a.d + i1;
+    const float* wrow = a.Wp + static_cast<size_t>(active ? r : 0) * a.d + i1 + LW * t;
 #pragma unroll
-    for (int i = 0; i < WIN; ++i) {
-      const int c = QUAD * i + t;
-      w[i] = (active && c < nb) ? wrow[c] : 0.0f;
+    for (int j = 0; j < LW; j += 4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active && LW * t + j < nb) v = *reinterpret_cast<const float4*>(wrow + j);
+      w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
     }
   }
   float s = 1.0f, z = 0.0f;
@@ -256,70 +325,33 @@ __global__ void __launch_bounds__(128) column_loop_kernel(const LoopArgs a) {
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
   }
   float rs = __frcp_rn(s);
-  const int rl = threadIdx.x / QUAD;  // row within the CTA
-  // a block's share of the loss (at most 16 terms per lane) is summed in float32 and
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  // a block's share of the loss (at most 32 terms per lane) is summed in float32 and
   // added to the row's float64 total once per block; FP64 arithmetic inside the step
   // chain would serialise on this part's low FP64 rate
   float loss = 0.0f;
-  const int ngroups = (nb + QUAD - 1) / QUAD;
 #pragma unroll 1
-  for (int g = 0; g < ngroups; ++g) {
-    const int q0 = QUAD * g;
-    if (a.group > 0 && (q0 % a.group) == 0) {
-      if (a.group == 16) fit_quad<16 / QUAD>(w, g, t, nb, a.g, s, z);
-      else if (a.group == 32) fit_quad<32 / QUAD>(w, g, t, nb, a.g, s, z);
-      else if (a.group == 64) fit_quad<64 / QUAD>(w, g, t, nb, a.g, s, z);
-      else fit_quad<WIN>(w, g, t, nb, a.g, s, z);
-      rs = __frcp_rn(s);
-      if (active && t == 0) {
-        const int gi = (i1 + q0) / a.group;
-        a.scales[static_cast<size_t>(gi) * a.m + r] = s;
-        a.zeros[static_cast<size_t>(gi) * a.m + r] = static_cast<int32_t>(z);
-      }
-    }
+  for (int b = 0; b < LPR; ++b) {
+    if (LW * b >= nb) break;
+    // the owner's first column, settled by every earlier column's update
+    float wq = w[0];
+    float code_r[LW], e_r[LW];
+    loop_columns<0>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs, loss);
+    if (t == b) {
 #pragma unroll
-    for (int o = 0; o < QUAD; ++o) {
-      const int q = q0 + o;
-      // the owner quantises its window's first slot
-      const float wq = w[0];
-      const float v = div_by_scale(wq, s, rs);
-      const float code = fminf(fmaxf(rintf(v) + z, a.g.lowest), a.g.maxq);
-      const float what = s * (code - z);
-      const float e_own = (wq - what) * urinv[q < BLK ? q : 0];
-      const float e = __shfl_sync(0xffffffffu, e_own, qbase + o);
-      if (t == o) {
-        const __nv_bfloat16 eh = __float2bfloat16_rn(e);
-        codes_s[q * RPC + rl] = static_cast<uint8_t>(code);
+      for (int j = 0; j < LW; ++j) {
+        const int q = LW * b + j;
+        const __nv_bfloat16 eh = __float2bfloat16_rn(e_r[j]);
+        codes_s[q * RPC + rl] = static_cast<uint8_t>(code_r[j]);
         ehi_s[q * RPC + rl] = eh;
-        elo_s[q * RPC + rl] = __float2bfloat16_rn(e - __bfloat162float(eh));
-        if (q < nb) loss = fmaf(0.5f * e, e, loss);
-      }
-      const float* u = ulay + (q < BLK ? q : 0) * ROW_STRIDE + t * LANE_STRIDE;
-      if (o < QUAD - 1) {
-#pragma unroll
-        for (int i = 0; i < WIN; i += 4) {
-          const float4 u4 = *reinterpret_cast<const float4*>(u + i);
-          w[i] = fmaf(-e, u4.x, w[i]);
-          w[i + 1] = fmaf(-e, u4.y, w[i + 1]);
-          w[i + 2] = fmaf(-e, u4.z, w[i + 2]);
-          w[i + 3] = fmaf(-e, u4.w, w[i + 3]);
-        }
-      } else {
-        // last step of the group: slide the window by one slot
-#pragma unroll
-        for (int i = 0; i < WIN; i += 4) {
-          const float4 u4 = *reinterpret_cast<const float4*>(u + i);
-          w[i] = fmaf(-e, u4.x, w[i + 1]);
-          w[i + 1] = fmaf(-e, u4.y, w[i + 2]);
-          w[i + 2] = fmaf(-e, u4.z, w[i + 3]);
-          if (i + 3 < WIN - 1) w[i + 3] = fmaf(-e, u4.w, w[i + 4 < WIN ? i + 4 : WIN - 1]);
-        }
+        elo_s[q * RPC + rl] = __float2bfloat16_rn(e_r[j] - __bfloat162float(eh));
       }
     }
   }
   // each lane accumulated the loss of the columns it owns
-#pragma unroll
-  for (int o = 1; o < QUAD; o <<= 1) loss += __shfl_xor_sync(0xffffffffu, loss, o);
+  loss += __shfl_xor_sync(0xffffffffu, loss, 1);
+  loss += __shfl_xor_sync(0xffffffffu, loss, 2);
   if (active && t == 0) a.loss_rows[r] += static_cast<double>(loss);
   __syncthreads();
   const int r0 = blockIdx.x * RPC;
@@ -435,7 +467,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
     const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, kErrRows, q.uhi, q.ulo, q.Wp, m, d);
-    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float)) + BLK * (128 / QUAD) * (1 + 2 + 2);
+    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float)) + BLK * RPC * (1 + 2 + 2);
     static bool loop_attr = false;
     if (!loop_attr) {
       GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel,
@@ -479,8 +511,8 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
           }
           a.gi_outer = gi;
         }
-        GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, 128 / QUAD),
-                    128, loop_smem, a);
+        GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, RPC),
+                    LOOP_THREADS, loop_smem, a);
         // near: the rest of the superblock, W[:, i2:s1] -= Err_block U[i1:i2, i2:s1]
         if (i1 + nb < s1) launch_lazy_tc(maps, i1 - s0, i1, nb, i1 + nb, s1, q.st, s);
       }
