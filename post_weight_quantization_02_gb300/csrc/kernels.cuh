@@ -23,8 +23,11 @@ int syrk_tc_token_granule();
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s);
 
-// floats of one 128-column block's layout of U for the column loop
-constexpr int kLoopUblkFloats = 128 * 144 + 128;
+// lanes of the column loop per output row, and the floats of one 128-column block's
+// layout of U for it (per row q of the block: kLoopLanesPerRow runs of 128 /
+// kLoopLanesPerRow floats, each padded by 4; then 128 reciprocals)
+constexpr int kLoopLanesPerRow = 4;
+constexpr int kLoopUblkFloats = 128 * kLoopLanesPerRow * (128 / kLoopLanesPerRow + 4) + 128;
 
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,

@@ -145,19 +145,20 @@ __device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
-// The column loop gives each output row LPR = 4 lanes; lane t holds the block's columns
-// 32t .. 32t+31 in registers for the whole block.  Sub-block b (columns 32b ..) is
-// quantised by lane b, column after column: the owner rounds its column, broadcasts the
-// error e to the row's lanes, and every lane subtracts e U[q][c] from its columns (U is
-// laid out with zeros at c <= q, so the same 32 FMAs serve the owner, the lanes after it
-// and, as no-ops, the lanes before it).  The owner forms its next column's value from its
-// own e before the broadcast returns, which keeps the shuffle off the column chain.  The
-// U rows are read with loads that four lane positions share across the warp:
-//   Ulay[b][q][t][j] = U[i1+q][i1+32t+j] if q < 32t+j < nb else 0
-// (j < 32, padded to 36 floats per lane position so the four positions hit different
-// banks), followed by the 128 reciprocals 1/U[i1+q][i1+q].
-constexpr int LPR = 4;                         // lanes per row
-constexpr int LW = BLK / LPR;                  // 32 columns per lane
+// The column loop gives each output row LPR lanes; lane t holds the block's LW = 128 / LPR
+// columns LW t .. LW t + LW - 1 in registers for the whole block.  Sub-block b (columns
+// LW b ..) is quantised by lane b, column after column: the owner rounds its column,
+// broadcasts the error e to the row's lanes, and every lane subtracts e U[q][c] from its
+// columns (U is laid out with zeros at c <= q, so the same LW FMAs serve the owner, the
+// lanes after it and, as no-ops, the lanes before it).  The owner forms its next column's
+// value from its own e before the broadcast returns, which keeps the shuffle off the
+// column chain.  The U rows are read with loads that the LPR lane positions share across
+// the warp:
+//   Ulay[b][q][t][j] = U[i1+q][i1+LW t+j] if q < LW t+j < nb else 0
+// (j < LW, padded by 4 floats per lane position so the positions hit different banks),
+// followed by the 128 reciprocals 1/U[i1+q][i1+q].
+constexpr int LPR = kLoopLanesPerRow;          // lanes per row
+constexpr int LW = BLK / LPR;                  // columns per lane
 constexpr int LSTR = LW + 4;                   // padded lane stride
 constexpr int UROW = LPR * LSTR;               // floats per row q of the layout
 constexpr int kUlayFloats = BLK * UROW + BLK;
@@ -195,14 +196,14 @@ struct LoopArgs {
   double* loss_rows;   // [m]
 };
 
-// Group fit at column j of the lane's window: over w[j .. j+15] (group 16) or the whole
-// window, combined across the lanes of the group (2 for 64, 4 for 128), masking columns
-// past the block's end.
+// Group fit at column J of the lane's window: over w[J .. J+group) when a group is
+// narrower than the window, else over the whole window combined across the group's
+// group / LW lanes (xor shuffles), masking columns past the block's end.
 template <int J>
 __device__ __forceinline__ void fit_lanes(const float (&w)[LW], int group, int t, int nb,
                                           const Grid& gr, float& s, float& z) {
   float mn = INFINITY, mx = -INFINITY, am = 0.0f;
-  const int lo = (group == 16) ? J : 0, hi = (group == 16) ? J + 16 : LW;
+  const int lo = (group < LW) ? J : 0, hi = (group < LW) ? J + group : LW;
 #pragma unroll
   for (int i = 0; i < LW; ++i) {
     if (i >= lo && i < hi && LW * t + i < nb) {
@@ -211,20 +212,18 @@ __device__ __forceinline__ void fit_lanes(const float (&w)[LW], int group, int t
       am = fmaxf(am, fabsf(w[i]));
     }
   }
-  if (group >= 64) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-  }
-  if (group >= 128) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+#pragma unroll
+  for (int o = 1; o < LPR; o <<= 1) {
+    if (o * LW < group) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    }
   }
   fit_from_range(gr, mn, mx, am, s, z);
 }
 
-// One column q = 32 b + J of sub-block b: fit at a group start, round the owner's value
+// One column q = LW b + J of sub-block b: fit at a group start, round the owner's value
 // wq, broadcast e, update every lane's window.  The owner's code and error stay in
 // registers (code_r[J], e_r[J]) until the sub-block ends, so a column is one branch-free
 // stretch of code that the compiler can overlap with the next column's rounding.
@@ -237,8 +236,8 @@ __device__ __forceinline__ float loop_column(float (&w)[LW], float (&code_r)[LW]
                                              const float* __restrict__ urinv, float& s,
                                              float& z, float& rs, float& loss) {
   const int q = LW * b + J;
-  // groups of 16 .. 128 start only at window positions 0 and 16
-  if constexpr (J == 0 || J == 16) {
+  // groups (16 .. 128 columns) start only at window positions that are multiples of 16
+  if constexpr (J % 16 == 0) {
     if (a.group > 0 && (q % a.group) == 0) {
       fit_lanes<J>(w, a.group, t, a.nb, a.g, s, z);
       rs = __frcp_rn(s);
