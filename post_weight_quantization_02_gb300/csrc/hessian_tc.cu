@@ -5,21 +5,31 @@
 // Placement: GPTQ", section 1.4) for bf16 X, with float32 accumulation in TMEM.  Only
 // tiles that touch the upper 128-tile triangle are computed.
 //
-// Persistent, warp-specialised kernel, one CTA per SM:
-//   warp 0      TMA producer: X tiles [64 tokens x 128 | 256 columns] into a 4-stage ring
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, both operands
-//               MN-major (the column index of X is contiguous in memory)
-//   warps 2..9  epilogue: drain finished TMEM accumulators into float32 registers, then
-//               store the unit's tile of P[s]
-// A unit is (row tile I of 128, column tile J of 256, token split s).  The tensor core's
-// float32 accumulation does not round to nearest, so its error grows with the length of
-// an accumulation chain; each chain therefore covers only a few stages (512 tokens) and
-// is then added, with round-to-nearest float32 adds in a fixed order, into the epilogue
-// warps' registers.  Two 256-column TMEM accumulators alternate between chains, so the
-// MMAs of one chain overlap the drain of the previous one.
+// Persistent, warp-specialised kernel, one CTA per SM, the CTAs in pairs (clusters of
+// two) that run paired-SM MMAs: a unit is one 256 x 256 tile of H (row tiles 2p, 2p+1 of
+// 128, column tile J of 256) for one token split s.  The even CTA's TMEM holds rows
+// 256p .. + 127, the odd CTA's the next 128; each CTA's shared memory holds its own 128
+// rows' operand and half of the 256-column operand, so an SM reads 32 KB of operands per
+// 64-token stage (48 KB for a one-SM 128 x 256 tile), which keeps the tensor core fed.
+//   warp 0      TMA producer (both CTAs): X tiles [64 tokens x 128 | 128 columns] into a
+//               6-stage ring; completion is counted on the even CTA's barrier
+//   warp 1      TMEM owner (both CTAs, paired allocation); in the even CTA also the MMA
+//               issuer: tcgen05.mma.cta_group::2 256x256x16, both operands MN-major (the
+//               column index of X is contiguous in memory)
+//   warps 2..9  epilogue (both CTAs): drain finished TMEM accumulators into float32
+//               registers, then store the CTA's 128 x 256 part of the unit's tile of P[s]
+//   warp 10     in the even CTA: waits for two stages' data (and, at a chain start, for
+//               the accumulator) and releases warp 1 through a named barrier.  The issuing
+//               warp never waits on an mbarrier: such a wait holds it until its
+//               outstanding MMAs have read their operands, which empties the tensor pipe.
+//               Two stages (8 MMAs) per hand-off keep the pipe fed across it.
+// A stage is refilled when the pair's MMAs have consumed it (the commit arrives on both
+// CTAs' barriers).  The tensor core's float32 accumulation does not round to nearest, so
+// its error grows with the length of an accumulation chain; each chain therefore covers
+// only a few stages (512 tokens) and is then added, with round-to-nearest float32 adds in
+// a fixed order, into the epilogue warps' registers.  Two 256-column TMEM accumulators
+// alternate between chains, so the MMAs of one chain overlap the drain of the previous one.
 #include <cuda_bf16.h>
-
-#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -29,19 +39,21 @@ namespace gptq {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // tokens per stage
-constexpr int NSTAGE = 4;
+constexpr int BM = 128;  // rows of H per CTA
+constexpr int BN = 256;  // columns of H per unit (128 in each CTA's shared memory)
+constexpr int BK = 64;   // tokens per stage
+constexpr int NSTAGE = 6;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * BK * 2;  // one TMA box: 64 columns x 64 tokens
 constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024 + 256;
-constexpr int CHAIN_DEFAULT = 8;    // stages per TMEM accumulation chain (512 tokens)
+constexpr int CHAIN = 8;            // stages per TMEM accumulation chain (512 tokens), even
 constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, 128 columns each
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, true, true);
+constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
+constexpr int WAITER_WARP = 2 + EPI_WARPS;
+constexpr uint32_t kHandoffBarrier = 1;  // named barrier of warps 1 and WAITER_WARP
+constexpr uint32_t IDESC = tc::idesc_bf16_f32(2 * BM, BN, true, true);  // paired: M = 256
 
 struct SyrkArgs {
   int d;
@@ -49,24 +61,26 @@ struct SyrkArgs {
   int64_t tok_per_split;
   int n_i;       // row tiles of 128
   int n_j;       // column tiles of 256
-  int n_tiles;   // tiles intersecting the upper 128-tile triangle
+  int n_pairs;   // row-tile pairs of the tiles intersecting the upper 128-tile triangle
   int splits;
-  int chain;     // stages per accumulation chain
   float* P;      // [splits][d][d]
   DevStatus* st;
 };
 
-__device__ __forceinline__ void decode_tile(int tile, int n_i, int n_j, int& I, int& J) {
-  int rem = tile;
+// pair p of column tile J: row tiles 2p and 2p + 1 (the second may lie past the last row
+// tile when a column tile has an odd count; its CTA then multiplies zeros and stores
+// nothing)
+__device__ __forceinline__ void decode_pair(int pair, int n_i, int n_j, int& P, int& J) {
+  int rem = pair;
   for (J = 0; J < n_j; ++J) {
-    int cnt = min(2 * J + 2, n_i);
-    if (rem < cnt) { I = rem; return; }
+    const int cnt = (min(2 * J + 2, n_i) + 1) / 2;
+    if (rem < cnt) { P = rem; return; }
     rem -= cnt;
   }
-  I = 0;
+  P = 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     syrk_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SyrkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -80,27 +94,30 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int64_t n_units = static_cast<int64_t>(a.n_tiles) * a.splits;
+  const int crank = static_cast<int>(tc::cluster_ctarank());
+  const int64_t n_units = static_cast<int64_t>(a.n_pairs) * a.splits;
+  const int64_t unit0 = blockIdx.x / 2, unit_step = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&full[s], 1);   // the even CTA's: both CTAs' bytes
+      tc::mbar_init(&empty[s], 1);  // the pair's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
-      tc::mbar_init(&accempty[b], EPI_WARPS);
+      tc::mbar_init(&accempty[b], 2 * EPI_WARPS);  // the even CTA's: both CTAs' epilogues
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmap);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 512);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(tmem_slot, 512);
+    tc::tmem_relinquish_pair();
   }
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // both CTAs' barriers exist before either multicasts into them
   tc::fence_after();
   const uint32_t tmem_base = *tmem_slot;
   bool ok = true;
@@ -109,10 +126,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- producer
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int s = static_cast<int>(u / a.n_tiles);
-      int I, J;
-      decode_tile(static_cast<int>(u % a.n_tiles), a.n_i, a.n_j, I, J);
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
+      const int s = static_cast<int>(u / a.n_pairs);
+      int pp, J;
+      decode_pair(static_cast<int>(u % a.n_pairs), a.n_i, a.n_j, pp, J);
+      const int I = 2 * pp + crank;
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
@@ -120,69 +138,87 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
-        tc::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        // both CTAs' 32 KB land on the even CTA's barrier
+        const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
+        if (crank == 0) tc::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
         const int tok = static_cast<int>(t0 + static_cast<int64_t>(kb) * BK);
-        tc::tma_load_2d(sa, &tmap, &full[stage], I * BM, tok);
-        tc::tma_load_2d(sa + BOX_BYTES, &tmap, &full[stage], I * BM + 64, tok);
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-          tc::tma_load_2d(sb + h * BOX_BYTES, &tmap, &full[stage], J * BN + 64 * h, tok);
+        tc::tma_load_2d_pair(sa, &tmap, bar, I * BM, tok);
+        tc::tma_load_2d_pair(sa + BOX_BYTES, &tmap, bar, I * BM + 64, tok);
+        tc::tma_load_2d_pair(sb, &tmap, bar, J * BN + 128 * crank, tok);
+        tc::tma_load_2d_pair(sb + BOX_BYTES, &tmap, bar, J * BN + 128 * crank + 64, tok);
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (crank == 0 && (warp == 1 || warp == WAITER_WARP)) {
+    // ---------------------------------------------------------------- MMA issuer and its
+    // waiter (even CTA): both walk the same stages, two per hand-off; the waiter's lane 0
+    // waits, then both warps meet at the named barrier, which also carries a failed wait
+    const bool waiter = (warp == WAITER_WARP);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t accphase = 0;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int s = static_cast<int>(u / a.n_tiles);
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
+      const int s = static_cast<int>(u / a.n_pairs);
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int kc = kb % a.chain;
-        if (kc == 0) {
-          if (!tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag)) { ok = false; break; }
-          tc::fence_after();
+      for (int kb = 0; kb < nk; kb += 2) {
+        const int nst = (kb + 1 < nk) ? 2 : 1;
+        bool bad = false;
+        if (waiter && lane == 0) {
+          if ((kb % CHAIN) == 0) bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag);
+          if (!bad) bad = !tc::mbar_wait(&full[stage], phase, abort_flag);
+          if (!bad && nst == 2) {
+            const int s2 = (stage + 1 == NSTAGE) ? 0 : stage + 1;
+            bad = !tc::mbar_wait(&full[s2], (stage + 1 == NSTAGE) ? (phase ^ 1u) : phase,
+                                 abort_flag);
+          }
         }
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t abase = tc::smem_u32(smem + stage * STAGE_BYTES);
-        const uint32_t bbase = abase + A_BYTES;
+        if (tc::handoff_or(kHandoffBarrier, 64, bad)) { ok = false; break; }
+        for (int q = 0; q < nst; ++q) {
+          const int kq = kb + q;
+          const int kc = kq % CHAIN;
+          if (!waiter && lane == 0) {
+            tc::fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            const uint32_t abase = tc::smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t bbase = abase + A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // 16 tokens = two 8-row core groups of 1024 B; 64-column atoms are one TMA box
-          // (8192 B) apart.
-          const uint64_t ad = tc::smem_desc(abase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
-          const uint64_t bd = tc::smem_desc(bbase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
-          tc::mma_f16(d_tmem, ad, bd, IDESC, (kc | kk) != 0 ? 1u : 0u);
-        }
-        tc::mma_commit(&empty[stage]);
-        if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
-        if (kc == a.chain - 1 || kb == nk - 1) {
-          tc::mma_commit(&accfull[acc]);
-          acc ^= 1;
-          if (acc == 0) accphase ^= 1u;
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // 16 tokens = two 8-row core groups of 1024 B; 64-column atoms are one TMA
+              // box (8192 B) apart.
+              const uint64_t ad = tc::smem_desc(abase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
+              const uint64_t bd = tc::smem_desc(bbase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
+              tc::mma_f16_pair(d_tmem, ad, bd, IDESC, (kc | kk) != 0 ? 1u : 0u);
+            }
+            tc::mma_commit_pair(&empty[stage], static_cast<uint16_t>(0x3));
+            if (kc == CHAIN - 1 || kq == nk - 1)
+              tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3));
+          }
+          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+          if (kc == CHAIN - 1 || kq == nk - 1) {
+            acc ^= 1;
+            if (acc == 0) accphase ^= 1u;
+          }
         }
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp % 4;            // TMEM lane quarter this warp may access
     const int half = (warp - 2) / 4;   // which 128 of the 256 columns
     int acc = 0;
     uint32_t accphase = 0;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int s = static_cast<int>(u / a.n_tiles);
-      int I, J;
-      decode_tile(static_cast<int>(u % a.n_tiles), a.n_i, a.n_j, I, J);
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
+      const int s = static_cast<int>(u / a.n_pairs);
+      int pp, J;
+      decode_pair(static_cast<int>(u % a.n_pairs), a.n_i, a.n_j, pp, J);
+      const int I = 2 * pp + crank;
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
-      const int nchain = (nk + a.chain - 1) / a.chain;
+      const int nchain = (nk + CHAIN - 1) / CHAIN;
       float sum[128];
 #pragma unroll
       for (int k = 0; k < 128; ++k) sum[k] = 0.0f;
@@ -202,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&accempty[acc]), 0));
         acc ^= 1;
         if (acc == 0) accphase ^= 1u;
       }
@@ -234,20 +270,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
-    tc::tmem_dealloc(tmem_base, 512);
+    tc::tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
 }  // namespace
 
+// CTAs' tiles per token split (pairs of row tiles, the odd tile of a column padded)
 int syrk_tc_tiles(int d) {
   const int n_i = (d + BM - 1) / BM, n_j = (d + BN - 1) / BN;
   int n = 0;
-  for (int J = 0; J < n_j; ++J) n += (2 * J + 2 < n_i) ? 2 * J + 2 : n_i;
+  for (int J = 0; J < n_j; ++J) n += 2 * ((((2 * J + 2 < n_i) ? 2 * J + 2 : n_i) + 1) / 2);
   return n;
 }
 
@@ -271,17 +309,28 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.tok_per_split = tok_per_split;
   a.n_i = (d + BM - 1) / BM;
   a.n_j = (d + BN - 1) / BN;
-  a.n_tiles = syrk_tc_tiles(d);
+  a.n_pairs = syrk_tc_tiles(d) / 2;
   a.splits = splits;
-  a.chain = CHAIN_DEFAULT;
-  if (const char* e = std::getenv("GPTQ_SYRK_CHAIN")) {  // tuning knob: stages per chain
-    const int c = std::atoi(e);
-    if (c >= 1 && c <= 1024) a.chain = c;
-  }
   a.P = P;
   a.st = st;
-  const int64_t units = static_cast<int64_t>(a.n_tiles) * splits;
-  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  // one cluster of two CTAs per pair unit, no more clusters than can be resident at once
+  // (a cluster needs two SMs of one GPC, so that may be fewer than half the SMs)
+  static int resident = 0;
+  if (resident <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    resident = n < sm_count() / 2 ? n : sm_count() / 2;
+  }
+  const int64_t units = static_cast<int64_t>(a.n_pairs) * splits;
+  const int64_t clusters = resident;
+  const int grid = 2 * static_cast<int>(units < clusters ? units : clusters);
   GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel, grid, THREADS, SMEM_BYTES, tmap, a);
 }
 

@@ -16,6 +16,9 @@
 //   warp 0      TMA: ErrT hi/lo [64 k x 128 rows] and U hi/lo [64 k x 256 columns] per
 //               chunk, both MN-major, 96 KB per stage
 //   warp 1      TMEM owner and MMA issuer: 4 k-steps x 3 tcgen05.mma 128x256x16 per chunk
+//   warp 10     waits for each chunk's data (and, per tile, for the accumulator) and
+//               releases warp 1 through a named barrier, so that the issuing warp never
+//               waits on an mbarrier (which would drain the tensor pipe each chunk)
 //   warps 2..9  epilogue: TMEM -> registers -> -D into a swizzled shared box -> TMA
 //               reduce-add into W.  The memory system applies W += (-D) (one rounding,
 //               as a float32 subtraction); the SM never reads W.
@@ -40,7 +43,9 @@ constexpr int NSTAGE = 2;
 constexpr int EPI_WARPS = 8;
 constexpr int STG_BYTES = 32 * 32 * 4;           // per epilogue warp: 32 rows x 32 columns
 constexpr int SMEM_BYTES = NSTAGE * STAGE + EPI_WARPS * STG_BYTES + 1024 + 256;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
+constexpr int WAITER_WARP = 2 + EPI_WARPS;
+constexpr uint32_t kHandoffBarrier = 1;  // named barrier of warps 1 and WAITER_WARP
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, true, true);
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 
@@ -126,41 +131,49 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == WAITER_WARP) {
+    // ------------------------------------------------------------ MMA issuer and its
+    // waiter: both walk the same chunks; the waiter's lane 0 waits, then both warps meet
+    // at the named barrier, which also carries a failed wait
+    const bool waiter = (warp == WAITER_WARP);
     uint32_t it = 0;
     int acc = 0;
     uint32_t accphase = 0;
     const uint32_t sbase = tc::smem_u32(smem);
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      if (!tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag)) { ok = false; break; }
-      tc::fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kc = 0; kc < a.nk; ++kc, ++it) {
         const int s = static_cast<int>(it % NSTAGE);
         const uint32_t ph = (it / NSTAGE) & 1u;
-        if (!tc::mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t base = sbase + static_cast<uint32_t>(s * STAGE);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t ko = static_cast<uint32_t>(kk * 2048);  // 16 k-rows of 128 B
-          const uint64_t ahi = tc::smem_desc(base + a_off(0, 0) + ko, BOX, 1024, tc::kSwizzle128B);
-          const uint64_t alo = tc::smem_desc(base + a_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
-          const uint64_t bhi = tc::smem_desc(base + b_off(0, 0) + ko, BOX, 1024, tc::kSwizzle128B);
-          const uint64_t blo = tc::smem_desc(base + b_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
-          tc::mma_f16(d_tmem, ahi, bhi, IDESC, (kc | kk) != 0 ? 1u : 0u);
-          tc::mma_f16(d_tmem, ahi, blo, IDESC, 1u);
-          tc::mma_f16(d_tmem, alo, bhi, IDESC, 1u);
+        bool bad = false;
+        if (waiter && lane == 0) {
+          if (kc == 0) bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag);
+          if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag);
         }
-        tc::mma_commit(&empty[s]);
+        if (tc::handoff_or(kHandoffBarrier, 64, bad)) { ok = false; break; }
+        if (!waiter && lane == 0) {
+          tc::fence_after();
+          const uint32_t base = sbase + static_cast<uint32_t>(s * STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t ko = static_cast<uint32_t>(kk * 2048);  // 16 k-rows of 128 B
+            const uint64_t ahi = tc::smem_desc(base + a_off(0, 0) + ko, BOX, 1024, tc::kSwizzle128B);
+            const uint64_t alo = tc::smem_desc(base + a_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
+            const uint64_t bhi = tc::smem_desc(base + b_off(0, 0) + ko, BOX, 1024, tc::kSwizzle128B);
+            const uint64_t blo = tc::smem_desc(base + b_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
+            tc::mma_f16(d_tmem, ahi, bhi, IDESC, (kc | kk) != 0 ? 1u : 0u);
+            tc::mma_f16(d_tmem, ahi, blo, IDESC, 1u);
+            tc::mma_f16(d_tmem, alo, bhi, IDESC, 1u);
+          }
+          tc::mma_commit(&empty[s]);
+          if (kc == a.nk - 1) tc::mma_commit(&accfull[acc]);
+        }
       }
       if (!ok) break;
-      tc::mma_commit(&accfull[acc]);
       acc ^= 1;
       if (acc == 0) accphase ^= 1u;
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int q = warp % 4;             // TMEM lane quarter = tile rows 32q..32q+31
     const int half = (warp - 2) / 4;    // tile columns half*128 ..
