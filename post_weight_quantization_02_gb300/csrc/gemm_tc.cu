@@ -103,12 +103,15 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   const int i0 = bi * TM, j0 = bj * TN;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
-  if (tid == 0) {
+  if (tid == 32) {
+    // barriers first, then the first two K-quarters in flight while warp 0 allocates TMEM
     tc::mbar_init(bar_load, 1);
     tc::mbar_init(bar_load + 1, 1);
     tc::mbar_init(bar_mma, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
+    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 0);
+    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
   }
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, 128);
@@ -121,10 +124,6 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   constexpr uint32_t IDESC = idesc_tf32(TM, TN, false);
   bool ok = true;
 
-  if (tid == 0) {
-    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 0);
-    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
-  }
   for (int ph = 0; ph < TK / KQ && ok; ++ph) {
     uint8_t* a_hi = smem + (ph & 1) * STAGE_BYTES;
     uint8_t* b_hi = a_hi + A_BYTES;
@@ -187,7 +186,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     if (!tc::mbar_wait(bar_mma, ph & 1, abort_flag)) { ok = false; break; }
     tc::fence_after();
     // both buffers of this stage are free again: fetch the quarter after next into it
-    if (tid == 0 && ph + 2 < TK / KQ) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
+    if (tid == 32 && ph + 2 < TK / KQ) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
   }
 
   if (ok) {
@@ -221,7 +220,9 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
         tc::bulk_commit_group();
       }
     }
-    if (lane == 0) tc::bulk_wait_group0();
+    // the boxes have been read out of shared memory; the memory system completes the
+    // stores / reduce-adds before the grid is finished
+    if (lane == 0) tc::bulk_wait_group_read0();
   } else {
     *abort_flag = 1;
     if (lane == 0) {
