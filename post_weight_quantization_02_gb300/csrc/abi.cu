@@ -147,8 +147,8 @@ size_t quantize_ws_bytes(int m, int d, int G) {
   w.add<DevStatus>(1);
   w.add<float>(static_cast<size_t>(m) * d);    // Wp
   w.add<uint8_t>(static_cast<size_t>(m) * d);  // codesT
-  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 hi
-  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 lo
+  w.add<uint16_t>(static_cast<size_t>(2 * kErrRows) * m);  // errors, bf16 hi
+  w.add<uint16_t>(static_cast<size_t>(2 * kErrRows) * m);  // errors, bf16 lo
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 hi
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 lo
   w.add<int32_t>(static_cast<size_t>(G) * m);  // zeros
@@ -314,8 +314,8 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
     q.st = wc.take<DevStatus>(1);
     q.Wp = wc.take<float>(static_cast<size_t>(d_out) * d_in);
     q.codesT = wc.take<uint8_t>(static_cast<size_t>(d_out) * d_in);
-    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
-    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
+    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(2 * kErrRows) * d_out);
+    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(2 * kErrRows) * d_out);
     q.uhi = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.ulo = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.zeros = wc.take<int32_t>(static_cast<size_t>(G) * d_out);
@@ -338,6 +338,7 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
     q.qzeros = qzeros;
     q.g_idx = g_idx;
     q.loss = loss;
+    std::lock_guard<std::mutex> lk(aux_mutex());  // the internal streams are shared
     begin_call(q.st, s);
     launch_quantize(q, s);
     raise_device_status(finish_call(q.st, s), "gptq_quantize_layer");

@@ -72,7 +72,8 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         cudaStream_t s);
 
 // lazy_tc.cu
-// ErrT rows kept for the deferred update: one 512-column superblock of the loop
+// ErrT rows kept for the deferred update: one 512-column superblock of the loop (the
+// workspace holds two, alternating between superblocks)
 constexpr int kErrRows = 512;
 
 struct LazyMaps {
@@ -84,8 +85,11 @@ LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int 
                         const __nv_bfloat16* uhi, const __nv_bfloat16* ulo, float* W, int m,
                         int d);
 void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s);
-// W[:, c_begin:c_end] -= ErrT[e_row0 : e_row0 + k]^T U[u_row0 : u_row0 + k, c_begin:c_end]
+// W[:, c_begin:c_end] -= ErrT[e_row0 : e_row0 + k]^T U[u_row0 : u_row0 + k, c_begin:c_end];
+// max_ctas > 0 caps the persistent grid (to leave SMs to concurrent work)
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
-                    DevStatus* st, cudaStream_t s);
+                    DevStatus* st, cudaStream_t s, int max_ctas);
+// CTAs of a far update's tail, which runs beside the column loop
+constexpr int kTailCtas = 24;
 
 }  // namespace gptq

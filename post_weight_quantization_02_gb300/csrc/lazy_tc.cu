@@ -284,7 +284,7 @@ LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int 
 }
 
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
-                    DevStatus* st, cudaStream_t s) {
+                    DevStatus* st, cudaStream_t s, int max_ctas) {
   if (k <= 0 || c_end <= c_begin || mp.m <= 0) return;
   static bool attr = false;
   if (!attr) {
@@ -304,7 +304,8 @@ void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_beg
   a.n_nt = static_cast<int>(ceil_div(c_end - c_begin, BN));
   a.st = st;
   const int units = a.n_mt * a.n_nt;
-  const int grid = units < sm_count() ? units : sm_count();
+  int grid = units < sm_count() ? units : sm_count();
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   GPTQ_LAUNCH(GPTQ_K_QUANT_LAZY, s, lazy_tc_kernel, grid, THREADS, SMEM_BYTES, mp.ehi, mp.elo,
               mp.uhi, mp.ulo, mp.w, a);
 }
