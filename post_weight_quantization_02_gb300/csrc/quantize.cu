@@ -162,8 +162,9 @@ constexpr int LW = BLK / LPR;                  // columns per lane
 constexpr int LSTR = LW + 4;                   // padded lane stride
 constexpr int UROW = LPR * LSTR;               // floats per row q of the layout
 constexpr int kUlayFloats = BLK * UROW + BLK;
-constexpr int LOOP_THREADS = 64;
+constexpr int LOOP_THREADS = 128;
 constexpr int RPC = LOOP_THREADS / LPR;        // rows per CTA
+static_assert(RPC % 16 == 0, "the loop's write-out stores 16 output rows per 16 bytes");
 static_assert(kUlayFloats == kLoopUblkFloats, "workspace sizing of the loop's U layout");
 
 __global__ void ulayout_kernel(const float* __restrict__ U, int d, float* __restrict__ Ulay) {
@@ -324,6 +325,8 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
   }
   float rs = __frcp_rn(s);
+  // the row's loss total so far, read now so that the read is off the block's tail
+  const double loss_prev = (active && t == 0) ? a.loss_rows[r] : 0.0;
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   // a block's share of the loss (at most 32 terms per lane) is summed in float32 and
@@ -351,16 +354,33 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   // each lane accumulated the loss of the columns it owns
   loss += __shfl_xor_sync(0xffffffffu, loss, 1);
   loss += __shfl_xor_sync(0xffffffffu, loss, 2);
-  if (active && t == 0) a.loss_rows[r] += static_cast<double>(loss);
+  if (active && t == 0) a.loss_rows[r] = loss_prev + static_cast<double>(loss);
   __syncthreads();
   const int r0 = blockIdx.x * RPC;
   const int nrows = min(RPC, a.m - r0);
-  for (int e = threadIdx.x; e < nb * RPC; e += blockDim.x) {
-    const int q = e / RPC, j = e % RPC;
-    if (j < nrows) {
-      a.codesT[static_cast<size_t>(i1 + q) * a.m + r0 + j] = codes_s[e];
-      a.ehi[static_cast<size_t>(q) * a.m + r0 + j] = ehi_s[e];
-      a.elo[static_cast<size_t>(q) * a.m + r0 + j] = elo_s[e];
+  if (nrows == RPC && a.m % 16 == 0) {
+    // whole rows of RPC outputs, 16 bytes per store (every row start is 16-byte aligned)
+    constexpr int CV = RPC / 16, EV = RPC / 8;
+    for (int e = threadIdx.x; e < nb * CV; e += blockDim.x) {
+      const int q = e / CV, v = e % CV;
+      reinterpret_cast<uint4*>(a.codesT + static_cast<size_t>(i1 + q) * a.m + r0)[v] =
+          reinterpret_cast<const uint4*>(codes_s + q * RPC)[v];
+    }
+    for (int e = threadIdx.x; e < nb * EV; e += blockDim.x) {
+      const int q = e / EV, v = e % EV;
+      reinterpret_cast<uint4*>(a.ehi + static_cast<size_t>(q) * a.m + r0)[v] =
+          reinterpret_cast<const uint4*>(ehi_s + q * RPC)[v];
+      reinterpret_cast<uint4*>(a.elo + static_cast<size_t>(q) * a.m + r0)[v] =
+          reinterpret_cast<const uint4*>(elo_s + q * RPC)[v];
+    }
+  } else {
+    for (int e = threadIdx.x; e < nb * RPC; e += blockDim.x) {
+      const int q = e / RPC, j = e % RPC;
+      if (j < nrows) {
+        a.codesT[static_cast<size_t>(i1 + q) * a.m + r0 + j] = codes_s[e];
+        a.ehi[static_cast<size_t>(q) * a.m + r0 + j] = ehi_s[e];
+        a.elo[static_cast<size_t>(q) * a.m + r0 + j] = elo_s[e];
+      }
     }
   }
 }
