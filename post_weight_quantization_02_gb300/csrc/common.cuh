@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/gptq.h"
@@ -101,6 +102,43 @@ const std::string& last_error();
     kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);                   \
     ::gptq::cuda_check(cudaGetLastError(), #kernel);                              \
     ::gptq::trace_end((kind), (stream));                                          \
+  } while (0)
+
+// Programmatic dependent launch.  A kernel launched with GPTQ_LAUNCH_PDL may start while
+// the kernel before it in the stream is still running: it must call griddep_wait() before
+// it reads or writes global memory that earlier work in the stream touches (the wait
+// returns once the earlier grid has completed and its writes are visible; for a kernel
+// launched without the attribute it returns at once).  griddep_launch_dependents() lets
+// the next such kernel start as soon as every CTA of this one has issued it.
+#ifdef __CUDACC__
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+template <typename... P, typename... A>
+void launch_pdl(const char* name, void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                cudaStream_t s, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cuda_check(cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...), name);
+}
+
+#define GPTQ_LAUNCH_PDL(kind, stream, kernel, grid, block, smem, ...)                    \
+  do {                                                                                  \
+    ::gptq::trace_begin((kind), (stream));                                              \
+    ::gptq::launch_pdl(#kernel, kernel, dim3(grid), dim3(block), (smem), (stream),      \
+                       __VA_ARGS__);                                                    \
+    ::gptq::trace_end((kind), (stream));                                                \
   } while (0)
 
 // Number of SMs of the current device.

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   }
   const int i0 = bi * TM, j0 = bj * TN;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  griddep_launch_dependents();
 
   if (tid == 32) {
     // barriers first, then the first two K-quarters in flight while warp 0 allocates TMEM
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     tc::mbar_init(bar_mma, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
+    griddep_wait();
     load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 0);
     load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
   }
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     tc::tmem_alloc(tmem_slot, 128);
     tc::tmem_relinquish();
   }
+  // no thread touches global memory before the previous kernel in the stream is done
+  griddep_wait();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -253,7 +257,7 @@ void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int 
 void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         const CUtensorMap& mb, int b_row0, int b_k0, float* C, int ldc, int M,
                         int N, float alpha, float beta, bool lower, DevStatus* st,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool pdl) {
   if (M <= 0 || N <= 0) return;
   if ((beta != 0.0f && beta != 1.0f) || (lower && beta != 1.0f)) {
     fail(GPTQ_ERR_INVALID_ARG, "launch_gemm_tf32x3: beta must be 0 or 1 (1 in lower mode)");
@@ -284,7 +288,11 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.st = st;
   const unsigned grid = lower ? static_cast<unsigned>(tm * (tm + 1) / 2)
                               : static_cast<unsigned>(tm * tn);
-  GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+  if (pdl) {
+    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+  } else {
+    GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+  }
 }
 
 }  // namespace gptq

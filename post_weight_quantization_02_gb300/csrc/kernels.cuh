@@ -64,12 +64,13 @@ struct QuantArgs {
 void launch_quantize(const QuantArgs& q, cudaStream_t s);
 
 // gemm_tc.cu: C[i][j] = beta C[i][j] + alpha sum_{k<128} A[a_row0+i][a_k0+k]
-// B[b_row0+j][b_k0+k], float32-accurate (tf32 x3); maps from make_gemm_map.
+// B[b_row0+j][b_k0+k], float32-accurate (tf32 x3); maps from make_gemm_map.  pdl: launched
+// as a programmatic dependent of the kernel before it in the stream.
 void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int ld);
 void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         const CUtensorMap& mb, int b_row0, int b_k0, float* C, int ldc, int M,
                         int N, float alpha, float beta, bool lower, DevStatus* st,
-                        cudaStream_t s);
+                        cudaStream_t s, bool pdl);
 
 // lazy_tc.cu
 // ErrT rows kept for the deferred update: one 512-column superblock of the loop (the

@@ -11,6 +11,8 @@
 // one triangular inverse (2d^3/3 flops instead of 4d^3/3).  The gather writes
 // Hr = J H_damp J directly, so both factorisations run on Hr and the last kernel
 // reverses the inverse into U.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -166,9 +168,9 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 // then the row block V_sj = -V_ss sum_{t=j}^{s-1} L_st V_tj (j < s) on spare warps next
 // to P3a, each warp forming 32 x 16 of the sum in registers (own L row times broadcast V
 // rows) and applying V_ss through a private buffer.
-// Shared memory (about 120 KB, so the CTA fits beside one GEMM CTA on an SM): the staged
-// block L, whose free upper 32 x 32 blocks hold the published columns; the six V_ij
-// below the diagonal; XT; six private 32 x 16 buffers.
+// Shared memory (about 120 KB; the launch asks for a whole SM's worth so that the CTA runs
+// alone on its SM): the staged block L, whose free upper 32 x 32 blocks hold the
+// published columns; the six V_ij below the diagonal; XT; six private 32 x 16 buffers.
 constexpr int DSTR = NB + 4;       // row stride of the staged block (16-byte rows)
 constexpr int SB = 32;             // sub-panel width
 constexpr int NSB = NB / SB;
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
   float* XT = Voff + kNVoff * SB * VSTR;  // [SB][XSTR]
   float* Tbuf = XT + SB * XSTR;       // [NTB][SB][TBSTR]
   __shared__ int bad;
+  griddep_launch_dependents();
+  griddep_wait();
   if (st->code != 0) return;
   const int nb = min(NB, d - k);  // a multiple of 8
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -515,7 +519,13 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   // block column i of Y is Y[:, i] = R DI[i]^T (R = the accumulated right-hand side,
   // initially I), after which every later block column loses Y[:, i] L[r, i]^T.
   // Finally U = J X J = (J Y J)^T.
-  const int diag_smem = kDiagSmemFloats * static_cast<int>(sizeof(float));
+  // The diagonal block's CTA asks for all of an SM's shared memory, so that no GEMM CTA
+  // of the other streams shares its SM: its chain of dependent steps runs about 15 %
+  // slower beside one.
+  int dev = 0, smem_optin = 0;
+  GPTQ_CUDA(cudaGetDevice(&dev));
+  GPTQ_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  const int diag_smem = std::max(kDiagSmemFloats * static_cast<int>(sizeof(float)), smem_optin);
   static bool attrs = false;
   if (!attrs) {
     GPTQ_CUDA(cudaFuncSetAttribute(chol_inv_diag_kernel,
@@ -543,32 +553,39 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   for (int kb = 0; kb < nblk; ++kb) {
     const int k = kb * NB;
     const int rest = d - k - NB;
-    if (kb >= 2) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 2], 0));
-    GPTQ_LAUNCH(GPTQ_K_POTRF_PANEL, sa, chol_inv_diag_kernel, 1, 512, diag_smem, Hr, d, k, DI,
-                st, d);
+    // block column kb is complete once the near update of panel kb - 1 is: that update
+    // waited for the far update of panel kb - 2, the last one that touches block column kb
+    // the factor's critical chain (diagonal block, panel solve, near update) runs on
+    // stream A as programmatic dependents, each launched during the kernel before it
+    GPTQ_LAUNCH_PDL(GPTQ_K_POTRF_PANEL, sa, chol_inv_diag_kernel, 1, 512, diag_smem, Hr, d, k,
+                    DI, st, d);
     if (rest > 0) {
       // the panel below, in place: L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T (rows r >= k + NB;
       // each CTA owns whole rows, loaded before it writes them)
       launch_gemm_tf32x3(GPTQ_K_POTRF_TRSM, mHr, k + NB, k, mDI, k, 0,
                          Hr + static_cast<size_t>(k + NB) * d + k, d, rest, NB, 1.0f, 0.0f,
-                         false, st, sa);
+                         false, st, sa, true);
     }
-    GPTQ_CUDA(cudaEventRecord(ev_panel[kb], sa));
     if (rest > 0) {
       // near update, block column kb + 1: Hr[r][k+NB+j] -= L[r, panel] . L[k+NB+j, panel]
-      // (whole tiles; the entries it changes above the diagonal are never read)
+      // (whole tiles; the entries it changes above the diagonal are never read).  It adds
+      // into block column kb + 1 after the far update of panel kb - 1 has, so that every
+      // entry receives its updates in panel order.
       if (kb >= 1) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 1], 0));
       launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
                          Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest,
-                         rest < NB ? rest : NB, -1.0f, 1.0f, false, st, sa);
+                         rest < NB ? rest : NB, -1.0f, 1.0f, false, st, sa, true);
     }
+    // panel kb is final (recorded after the near update, which keeps this stream's
+    // kernel-to-kernel steps free of other stream operations where it can)
+    GPTQ_CUDA(cudaEventRecord(ev_panel[kb], sa));
     if (rest > NB) {
       // far update, lower tiles of block columns >= kb + 2, on stream C
       const int far = rest - NB;
       GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_panel[kb], 0));
       launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + 2 * NB, k, mHr, k + 2 * NB, k,
                          Hr + static_cast<size_t>(k + 2 * NB) * d + k + 2 * NB, d, far, far,
-                         -1.0f, 1.0f, true, st, sc);
+                         -1.0f, 1.0f, true, st, sc, false);
       GPTQ_CUDA(cudaEventRecord(ev_far[kb], sc));
     }
     // inverse, block column kb, on stream B once panel kb is final
@@ -576,11 +593,11 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
     const int nbi = (d - k < NB) ? d - k : NB;
     // Y[c][k+t] = sum_j Y[c][k+j] DI[kb][t][j], rows c < k + nbi
     launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, k, mDI, k, 0, S + k, d, k + nbi, nbi, 1.0f, 0.0f,
-                       false, st, sb);
+                       false, st, sb, false);
     if (rest > 0) {
       // Y[c][r] -= sum_j Y[c][k+j] L[r][k+j], c < k + NB <= r
       launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, k, mHr, k + NB, k, S + k + NB, d, k + NB,
-                         rest, -1.0f, 1.0f, false, st, sb);
+                         rest, -1.0f, 1.0f, false, st, sb, false);
     }
   }
   GPTQ_CUDA(cudaEventRecord(ev_b, sb));
