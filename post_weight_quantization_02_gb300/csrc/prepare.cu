@@ -305,15 +305,25 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
   __shared__ int bad;
   griddep_launch_dependents();
   griddep_wait();
-  if (st->code != 0) return;
   const int nb = min(NB, d - k);  // a multiple of 8
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  // every load of the block in flight at once, with the status word
+  constexpr int NLD = NB * NB / 4 / 512;
+  float4 vin[NLD];
 #pragma unroll
-  for (int p = 0; p < NB * NB / 4 / 512; ++p) {
+  for (int p = 0; p < NLD; ++p) {
+    const int e4 = tid + p * 512, r = e4 / (NB / 4), c = (e4 % (NB / 4)) * 4;
+    vin[p] = (r < nb && c < nb && c <= r)
+                 ? *reinterpret_cast<const float4*>(A + static_cast<size_t>(k + r) * d + k + c)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (st->code != 0) return;
+#pragma unroll
+  for (int p = 0; p < NLD; ++p) {
     const int e4 = tid + p * 512, r = e4 / (NB / 4), c = (e4 % (NB / 4)) * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r < nb && c < nb) {
-      v = *reinterpret_cast<const float4*>(A + static_cast<size_t>(k + r) * d + k + c);
+      v = vin[p];
       if (c + 1 > r) v.y = 0.0f;
       if (c + 2 > r) v.z = 0.0f;
       if (c + 3 > r) v.w = 0.0f;
@@ -522,10 +532,14 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   // The diagonal block's CTA asks for all of an SM's shared memory, so that no GEMM CTA
   // of the other streams shares its SM: its chain of dependent steps runs about 15 %
   // slower beside one.
+  // (the block's limit covers its static shared memory too)
   int dev = 0, smem_optin = 0;
   GPTQ_CUDA(cudaGetDevice(&dev));
   GPTQ_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-  const int diag_smem = std::max(kDiagSmemFloats * static_cast<int>(sizeof(float)), smem_optin);
+  cudaFuncAttributes diag_attr;
+  GPTQ_CUDA(cudaFuncGetAttributes(&diag_attr, chol_inv_diag_kernel));
+  const int diag_smem = std::max(kDiagSmemFloats * static_cast<int>(sizeof(float)),
+                                 smem_optin - static_cast<int>(diag_attr.sharedSizeBytes));
   static bool attrs = false;
   if (!attrs) {
     GPTQ_CUDA(cudaFuncSetAttribute(chol_inv_diag_kernel,
