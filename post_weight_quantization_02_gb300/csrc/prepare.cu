@@ -54,30 +54,26 @@ __global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict
 // ---------------------------------------------------------------- act-order ranking
 
 // rank[j] = #{k : diag[k] > diag[j] or (diag[k] == diag[j] and k < j)}; perm[rank] = j.
-// This is the stable descending order of "GPTQ > ActOrder" with ties by index.
+// This is the stable descending order of "GPTQ > ActOrder" with ties by index.  One warp
+// per j: the lanes count over interleaved k (coalesced reads of diag, which stays in L1)
+// and the warp sums the counts.
 __global__ void __launch_bounds__(256) prep_rank_kernel(const float* __restrict__ diag, int d,
                                                         int actorder, int32_t* __restrict__ perm) {
-  __shared__ float tile[2048];
-  const int j = blockIdx.x * 256 + threadIdx.x;
-  const float dj = (j < d) ? diag[j] : 0.0f;
-  int rank = 0;
+  const int j = blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (j >= d) return;
   if (!actorder) {
-    if (j < d) perm[j] = j;
+    if (lane == 0) perm[j] = j;
     return;
   }
-  for (int k0 = 0; k0 < d; k0 += 2048) {
-    const int n = min(2048, d - k0);
-    __syncthreads();
-    for (int t = threadIdx.x; t < n; t += 256) tile[t] = diag[k0 + t];
-    __syncthreads();
-    if (j < d) {
-      for (int t = 0; t < n; ++t) {
-        const float dk = tile[t];
-        rank += (dk > dj) || (dk == dj && k0 + t < j);
-      }
-    }
+  const float dj = diag[j];
+  unsigned cnt = 0;
+  for (int k = lane; k < d; k += 32) {
+    const float dk = diag[k];
+    cnt += (dk > dj) || (dk == dj && k < j);
   }
-  if (j < d) perm[rank] = j;
+  const unsigned rank = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0) perm[rank] = j;
 }
 
 // ---------------------------------------------------------------- symmetric copy
@@ -481,9 +477,11 @@ __global__ void identity_kernel(float* __restrict__ S, int d) {
 __global__ void reverse_transpose_kernel(const float* __restrict__ Y, int d, float* __restrict__ U) {
   __shared__ float t[32][33];
   const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+  const bool below = j0 + 31 < i0;  // a tile of zeros: nothing to read
   for (int jj = threadIdx.y; jj < 32; jj += 8) {
     const int j = j0 + jj, ii = threadIdx.x, i = i0 + ii;
-    t[jj][ii] = (i < d && j < d) ? Y[static_cast<size_t>(d - 1 - j) * d + (d - 1 - i)] : 0.0f;
+    t[jj][ii] = (!below && i < d && j < d) ? Y[static_cast<size_t>(d - 1 - j) * d + (d - 1 - i)]
+                                           : 0.0f;
   }
   __syncthreads();
   for (int ii = threadIdx.y; ii < 32; ii += 8) {
@@ -499,7 +497,7 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
                     float* lam, float* DI, DevStatus* st, cudaStream_t s) {
   GPTQ_LAUNCH(GPTQ_K_PREP_DIAG, s, prep_diag_kernel, 1, 1024, 0, H, d, damp, dead, diag_fixed,
               lam, st);
-  GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 256), 256, 0,
+  GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 8), 256, 0,
               diag_fixed, d, actorder, perm);
   const unsigned t32 = (unsigned)ceil_div(d, 32);
   GPTQ_LAUNCH(GPTQ_K_PREP_MIRROR, s, prep_mirror_kernel, dim3(t32, t32), 256, 0, H, d, S, st);
@@ -550,10 +548,6 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   make_gemm_map(&mHr, Hr, d, d, d);
   make_gemm_map(&mS, S, d, d, d);
   make_gemm_map(&mDI, DI, static_cast<int>(ceil_div(d, NB)) * NB, NB, NB);
-  {
-    dim3 grid((unsigned)ceil_div(d, 256), d);
-    GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, s, identity_kernel, grid, 256, 0, S, d);
-  }
   const int nblk = static_cast<int>(ceil_div(d, NB));
   AuxStreams& aux = aux_streams(2 * nblk + 3);
   cudaStream_t sa = aux.a, sb = aux.b, sc = aux.c;
@@ -564,6 +558,11 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_fork, 0));
   GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_fork, 0));
   GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_fork, 0));
+  {
+    // S = I on stream B, where the inverse needs it first (the gather has read S)
+    dim3 grid((unsigned)ceil_div(d, 256), d);
+    GPTQ_LAUNCH(GPTQ_K_TRTRI_UPDATE, sb, identity_kernel, grid, 256, 0, S, d);
+  }
   for (int kb = 0; kb < nblk; ++kb) {
     const int k = kb * NB;
     const int rest = d - k - NB;
