@@ -33,14 +33,26 @@ __global__ void __launch_bounds__(1024) prep_diag_kernel(const float* __restrict
                                                          DevStatus* st) {
   __shared__ double part[1024];
   double s = 0.0;
-  for (int j = threadIdx.x; j < d; j += 1024) {
-    float h = H[static_cast<size_t>(j) * d + j];
-    if (!isfinite(h)) dev_fail(st, GPTQ_ERR_NONFINITE, j + 1);
-    uint8_t is_dead = (h == 0.0f) ? 1 : 0;
-    float f = is_dead ? 1.0f : h;
-    dead[j] = is_dead;
-    diag_fixed[j] = f;
-    s += static_cast<double>(f);
+  // four strided loads in flight per thread; the sum keeps the order j, j + 1024, ...
+  for (int j0 = threadIdx.x; j0 < d; j0 += 4 * 1024) {
+    float hv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q * 1024;
+      hv[q] = (j < d) ? H[static_cast<size_t>(j) * d + j] : 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q * 1024;
+      if (j >= d) break;
+      const float h = hv[q];
+      if (!isfinite(h)) dev_fail(st, GPTQ_ERR_NONFINITE, j + 1);
+      const uint8_t is_dead = (h == 0.0f) ? 1 : 0;
+      const float f = is_dead ? 1.0f : h;
+      dead[j] = is_dead;
+      diag_fixed[j] = f;
+      s += static_cast<double>(f);
+    }
   }
   part[threadIdx.x] = s;
   __syncthreads();
@@ -79,33 +91,43 @@ __global__ void __launch_bounds__(256) prep_rank_kernel(const float* __restrict_
 // ---------------------------------------------------------------- symmetric copy
 
 // S[i][j] = H[min(i,j)][max(i,j)] (strict upper triangle of H is authoritative).
-// 32x32 tiles, 32x8 threads; the lower half is read through a shared-memory transpose.
+// 32x32 tiles, 256 threads; each thread moves one 16-byte piece of a row in and one out,
+// and the lower half is read through a shared-memory transpose (row stride 33: the
+// scalar stores and the transposed reads both hit 32 different banks).
 __global__ void __launch_bounds__(256) prep_mirror_kernel(const float* __restrict__ H, int d,
                                                           float* __restrict__ S, DevStatus* st) {
   __shared__ float t[32][33];
   const int bi = blockIdx.y, bj = blockIdx.x;
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  const int r = threadIdx.x / 8, c = (threadIdx.x % 8) * 4;
   // read the source tile (bi', bj') = upper one of (bi, bj) / (bj, bi)
   const int si = min(bi, bj), sj = max(bi, bj);
-  for (int r = ty; r < 32; r += 8) {
-    const int i = si * 32 + r, j = sj * 32 + tx;
-    float v = 0.0f;
-    if (i < d && j < d) {
-      v = H[static_cast<size_t>(i) * d + j];
-      if (i <= j && !isfinite(v)) dev_fail(st, GPTQ_ERR_NONFINITE, 0);
+  {
+    const int i = si * 32 + r, j = sj * 32 + c;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < d && j < d) {  // d is a multiple of 8: a row piece is whole or absent
+      v = *reinterpret_cast<const float4*>(H + static_cast<size_t>(i) * d + j);
+      const bool upper = i <= j + 3;  // some of the piece is on or above the diagonal
+      if (upper && !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w))) {
+        // only entries on or above the diagonal are authoritative
+        const float e[4] = {v.x, v.y, v.z, v.w};
+        for (int q = 0; q < 4; ++q)
+          if (i <= j + q && !isfinite(e[q])) dev_fail(st, GPTQ_ERR_NONFINITE, 0);
+      }
     }
-    t[r][tx] = v;
+    t[r][c] = v.x; t[r][c + 1] = v.y; t[r][c + 2] = v.z; t[r][c + 3] = v.w;
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int i = bi * 32 + r, j = bj * 32 + tx;
-    if (i >= d || j >= d) continue;
-    float v;
-    if (bi < bj) v = t[r][tx];
-    else if (bi > bj) v = t[tx][r];
-    else v = (r <= tx) ? t[r][tx] : t[tx][r];
-    S[static_cast<size_t>(i) * d + j] = v;
+  const int i = bi * 32 + r, j = bj * 32 + c;
+  if (i >= d || j >= d) return;
+  float e[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int cc = c + q;
+    if (bi < bj) e[q] = t[r][cc];
+    else if (bi > bj) e[q] = t[cc][r];
+    else e[q] = (r <= cc) ? t[r][cc] : t[cc][r];
   }
+  *reinterpret_cast<float4*>(S + static_cast<size_t>(i) * d + j) = make_float4(e[0], e[1], e[2], e[3]);
 }
 
 // ---------------------------------------------------------------- reversed gather
