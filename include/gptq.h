@@ -111,6 +111,39 @@ gptq_status gptq_hessian_accumulate_noalloc(float* H, int64_t* nseen, const void
                                             void* stream);
 
 /*
+ * gptq_hessian_accumulate_async -- gptq_hessian_accumulate without the synchronisation.
+ * An interface addition (the pages' hook is a synchronous PyTorch call): it lets a
+ * caller overlap the host-to-device copy of the next batch with this batch's kernels.
+ *
+ * Same arguments, arithmetic and argument checks as gptq_hessian_accumulate ("GPTQ
+ * Architecture, in depth", HessianHook; "Same Ruler, Smarter Placement: GPTQ" section
+ * 1.4).  It enqueues the batch's kernels on `stream` and returns without waiting: *nseen
+ * is updated at once, H when the work completes.  X must stay valid and unmodified until
+ * then (order its reuse after the work with an event on `stream`).  Device-side failures
+ * (TIMEOUT, CUDA faults of the kernels) are not returned here: they collect in the status
+ * word at the start of `ws`, which a call with *nseen == 0 clears, and
+ * gptq_hessian_status reports and clears them.  All calls on one `ws` must be issued on
+ * one stream (they share its token-split partials).
+ * Errors returned directly: INVALID_ARG, UNSUPPORTED, WORKSPACE (nothing enqueued), CUDA
+ * (a launch failed).
+ */
+gptq_status gptq_hessian_accumulate_async(float* H, int64_t* nseen, const void* X,
+                                          int xdtype, int64_t ntok, int32_t d_in, void* ws,
+                                          size_t ws_bytes, void* stream);
+
+/*
+ * gptq_hessian_status -- synchronise `stream` and return the status collected by the
+ * gptq_hessian_accumulate_async calls on `ws` since the last call with *nseen == 0 (the
+ * first failure, as GPTQ_OK or the error code with gptq_last_error() describing it); the
+ * status word is cleared afterwards.
+ *
+ * ws, ws_bytes  the same workspace the async calls used (device, 256-byte aligned).
+ * Errors: INVALID_ARG (null, unaligned or too small ws), CUDA, TIMEOUT, and whatever the
+ *         kernels recorded.
+ */
+gptq_status gptq_hessian_status(void* ws, size_t ws_bytes, void* stream);
+
+/*
  * gptq_prepare -- everything GPTQ does to H before the column loop.
  *
  * Defined by "GPTQ Architecture, in depth", "The algorithm in code" and "Groups,

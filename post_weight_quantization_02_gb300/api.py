@@ -70,6 +70,16 @@ class LayerEngine:
         X = X.reshape(-1, self.d_in)
         self.nseen = G.gptq_hessian_accumulate(self.H, self.nseen, X, self.ws_h, stream)
 
+    def add_batch_async(self, X: torch.Tensor, stream=None) -> None:
+        """The Hessian hook for one batch, enqueued without waiting (X must stay valid
+        until the stream reaches the work); hessian_status() reports device failures."""
+        X = X.reshape(-1, self.d_in)
+        self.nseen = G.gptq_hessian_accumulate_async(self.H, self.nseen, X, self.ws_h, stream)
+
+    def hessian_status(self, stream=None) -> None:
+        """Wait for the enqueued Hessian steps and raise the first device-side failure."""
+        G.gptq_hessian_status(self.ws_h, stream)
+
     def prepare(self, stream=None) -> int:
         return G.gptq_prepare(self.H, self.damp, self.actorder, self.perm, self.dead,
                               self.Hinv_chol, self.ws_p, stream)
@@ -95,8 +105,9 @@ def quantize_layer_from_host(engine: LayerEngine, W_host: torch.Tensor,
     """End to end from (pinned) host memory.
 
     Token chunks are copied host-to-device on a side stream, double buffered, while the
-    Hessian kernels of the previous chunk run; the weights follow; the packed outputs are
-    copied back into ``out`` (pinned host tensors) when given.
+    Hessian kernels of the previous chunk run (enqueued without waiting, so the host
+    issues the next copy at once); the weights follow; the packed outputs are copied back
+    into ``out`` (pinned host tensors) when given.
     """
     dev = engine.device
     compute = torch.cuda.current_stream(dev)
@@ -114,12 +125,13 @@ def quantize_layer_from_host(engine: LayerEngine, W_host: torch.Tensor,
             bufs[b].copy_(xh, non_blocking=True)
             ready[b].record(copy)
         compute.wait_event(ready[b])
-        engine.add_batch(bufs[b], compute)
+        engine.add_batch_async(bufs[b], compute)
         done[b].record(compute)
     with torch.cuda.stream(copy):
         Wd = W_host.to(dev, non_blocking=True)
         wready = torch.cuda.Event()
         wready.record(copy)
+    engine.hessian_status(compute)
     engine.prepare(compute)
     compute.wait_event(wready)
     res = engine.quantize_weights(Wd, compute)

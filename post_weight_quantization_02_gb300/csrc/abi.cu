@@ -164,6 +164,50 @@ bool group_supported(int group) {
   return group == -1 || group == 16 || group == 32 || group == 64 || (group > 0 && group % 128 == 0);
 }
 
+// The Hessian step behind gptq_hessian_accumulate (sync) and its enqueue-only form.
+void hessian_step(float* H, int64_t* nseen, const void* X, int xdtype, int64_t ntok,
+                  int32_t d_in, void* ws, size_t ws_bytes, void* stream, bool sync) {
+  require(H != nullptr && nseen != nullptr && ws != nullptr, GPTQ_ERR_INVALID_ARG,
+          "gptq_hessian_accumulate: null H, nseen or ws");
+  require(d_in > 0 && ntok >= 0 && *nseen >= 0, GPTQ_ERR_INVALID_ARG,
+          "gptq_hessian_accumulate: need d_in > 0, ntok >= 0, *nseen >= 0");
+  require(xdtype == GPTQ_F32 || xdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
+          "gptq_hessian_accumulate: xdtype must be GPTQ_F32 or GPTQ_BF16");
+  require(d_in % 8 == 0, GPTQ_ERR_UNSUPPORTED, "gptq_hessian_accumulate: d_in must be a multiple of 8");
+  require(ntok == 0 || X != nullptr, GPTQ_ERR_INVALID_ARG, "gptq_hessian_accumulate: null X");
+  require(aligned(H, 16) && aligned(X, 16) && aligned(ws, 256), GPTQ_ERR_INVALID_ARG,
+          "gptq_hessian_accumulate: H and X must be 16-byte aligned, ws 256-byte aligned");
+  require(ntok < (int64_t(1) << 31), GPTQ_ERR_UNSUPPORTED,
+          "gptq_hessian_accumulate: at most 2^31 - 1 tokens per call");
+  const int64_t one = hessian_ws_bytes(d_in, 1);
+  require(ws_bytes >= static_cast<size_t>(one), GPTQ_ERR_WORKSPACE,
+          "gptq_hessian_accumulate: workspace smaller than d_in*d_in*4 + 256 bytes");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsCarver wc(ws, ws_bytes);
+  DevStatus* st = wc.take<DevStatus>(1);
+  // the enqueue-only form clears the status word at a layer's first batch and lets it
+  // collect failures until gptq_hessian_status reads it
+  if (!sync && *nseen == 0) begin_call(st, s);
+  if (ntok == 0) return;
+  const bool tc = use_tensor_cores(xdtype);
+  const size_t per = static_cast<size_t>(d_in) * d_in * sizeof(float);
+  const int64_t cap = static_cast<int64_t>((ws_bytes - 256) / per);
+  SplitPlan p = plan_splits(ntok, d_in, tc, cap, sm_count());
+  float* P = wc.take<float>(static_cast<size_t>(p.splits) * d_in * d_in);
+
+  const int64_t n_old = *nseen;
+  const double n_new = static_cast<double>(n_old) + static_cast<double>(ntok);
+  const float alpha = static_cast<float>(2.0 / n_new);
+  const float beta = static_cast<float>(static_cast<double>(n_old) / n_new);
+
+  if (sync) begin_call(st, s);
+  if (tc) launch_syrk_tc(X, ntok, d_in, p.splits, p.tok_per_split, P, st, s);
+  else launch_syrk_simt(X, xdtype == GPTQ_BF16, ntok, d_in, p.splits, p.tok_per_split, P, s);
+  launch_syrk_reduce(H, P, d_in, p.splits, alpha, beta, n_old == 0, s);
+  if (sync) raise_device_status(finish_call(st, s), "gptq_hessian_accumulate");
+  *nseen = n_old + ntok;
+}
+
 }  // namespace
 }  // namespace gptq
 
@@ -196,44 +240,26 @@ size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, in
 gptq_status gptq_hessian_accumulate(float* H, int64_t* nseen, const void* X, int xdtype,
                                     int64_t ntok, int32_t d_in, void* ws, size_t ws_bytes,
                                     void* stream) {
-  return guarded([&] {
-    require(H != nullptr && nseen != nullptr && ws != nullptr, GPTQ_ERR_INVALID_ARG,
-            "gptq_hessian_accumulate: null H, nseen or ws");
-    require(d_in > 0 && ntok >= 0 && *nseen >= 0, GPTQ_ERR_INVALID_ARG,
-            "gptq_hessian_accumulate: need d_in > 0, ntok >= 0, *nseen >= 0");
-    require(xdtype == GPTQ_F32 || xdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
-            "gptq_hessian_accumulate: xdtype must be GPTQ_F32 or GPTQ_BF16");
-    require(d_in % 8 == 0, GPTQ_ERR_UNSUPPORTED, "gptq_hessian_accumulate: d_in must be a multiple of 8");
-    require(ntok == 0 || X != nullptr, GPTQ_ERR_INVALID_ARG, "gptq_hessian_accumulate: null X");
-    require(aligned(H, 16) && aligned(X, 16) && aligned(ws, 256), GPTQ_ERR_INVALID_ARG,
-            "gptq_hessian_accumulate: H and X must be 16-byte aligned, ws 256-byte aligned");
-    require(ntok < (int64_t(1) << 31), GPTQ_ERR_UNSUPPORTED,
-            "gptq_hessian_accumulate: at most 2^31 - 1 tokens per call");
-    const int64_t one = hessian_ws_bytes(d_in, 1);
-    require(ws_bytes >= static_cast<size_t>(one), GPTQ_ERR_WORKSPACE,
-            "gptq_hessian_accumulate: workspace smaller than d_in*d_in*4 + 256 bytes");
-    if (ntok == 0) return;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool tc = use_tensor_cores(xdtype);
-    const size_t per = static_cast<size_t>(d_in) * d_in * sizeof(float);
-    const int64_t cap = static_cast<int64_t>((ws_bytes - 256) / per);
-    SplitPlan p = plan_splits(ntok, d_in, tc, cap, sm_count());
+  return guarded([&] { hessian_step(H, nseen, X, xdtype, ntok, d_in, ws, ws_bytes, stream, true); });
+}
 
+gptq_status gptq_hessian_accumulate_async(float* H, int64_t* nseen, const void* X, int xdtype,
+                                          int64_t ntok, int32_t d_in, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  return guarded([&] { hessian_step(H, nseen, X, xdtype, ntok, d_in, ws, ws_bytes, stream, false); });
+}
+
+gptq_status gptq_hessian_status(void* ws, size_t ws_bytes, void* stream) {
+  return guarded([&] {
+    require(ws != nullptr && aligned(ws, 256) && ws_bytes >= sizeof(DevStatus),
+            GPTQ_ERR_INVALID_ARG, "gptq_hessian_status: null, unaligned or too small ws");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsCarver wc(ws, ws_bytes);
     DevStatus* st = wc.take<DevStatus>(1);
-    float* P = wc.take<float>(static_cast<size_t>(p.splits) * d_in * d_in);
-
-    const int64_t n_old = *nseen;
-    const double n_new = static_cast<double>(n_old) + static_cast<double>(ntok);
-    const float alpha = static_cast<float>(2.0 / n_new);
-    const float beta = static_cast<float>(static_cast<double>(n_old) / n_new);
-
-    begin_call(st, s);
-    if (tc) launch_syrk_tc(X, ntok, d_in, p.splits, p.tok_per_split, P, st, s);
-    else launch_syrk_simt(X, xdtype == GPTQ_BF16, ntok, d_in, p.splits, p.tok_per_split, P, s);
-    launch_syrk_reduce(H, P, d_in, p.splits, alpha, beta, n_old == 0, s);
-    raise_device_status(finish_call(st, s), "gptq_hessian_accumulate");
-    *nseen = n_old + ntok;
+    const DevStatus h = finish_call(st, s);
+    GPTQ_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+    GPTQ_CUDA(cudaStreamSynchronize(s));
+    raise_device_status(h, "gptq_hessian_accumulate_async");
   });
 }
 

@@ -20,7 +20,8 @@ __all__ = [
     "GPTQ_ERR_NONFINITE", "GPTQ_ERR_CUDA", "GPTQ_ERR_TIMEOUT", "GPTQ_ERR_WORKSPACE",
     "GPTQ_F32", "GPTQ_BF16", "GPTQ_OP_HESSIAN", "GPTQ_OP_PREPARE", "GPTQ_OP_QUANTIZE",
     "GptqError", "GptqLibraryError", "lib", "library_path",
-    "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_prepare", "gptq_quantize_layer",
+    "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
+    "gptq_hessian_status", "gptq_prepare", "gptq_quantize_layer",
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_read", "gptq_profile_reset", "gptq_kernel_name",
     "gptq_launch_count", "KERNEL_KINDS", "workspace",
@@ -53,6 +54,9 @@ _SIGS = {
                                            _vp, _sz, _vp]),
     "gptq_hessian_accumulate_noalloc": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int,
                                                    _i64, _i32, _vp]),
+    "gptq_hessian_accumulate_async": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int, _i64,
+                                                 _i32, _vp, _sz, _vp]),
+    "gptq_hessian_status": (_c.c_int, [_vp, _sz, _vp]),
     "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
                                 _vp, _sz, _vp]),
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
@@ -154,6 +158,26 @@ def gptq_hessian_accumulate(H: torch.Tensor, nseen: int, X: torch.Tensor,
                                          _dtype_code(X), X.shape[0], d, _ptr(ws), ws.numel(),
                                          _stream(stream)))
     return int(n.value)
+
+
+def gptq_hessian_accumulate_async(H: torch.Tensor, nseen: int, X: torch.Tensor,
+                                  ws: torch.Tensor, stream=None) -> int:
+    """Enqueue one hook step without waiting; returns the new n.  Device-side failures
+    are reported by gptq_hessian_status on the same workspace."""
+    d = H.shape[0]
+    if X.dim() != 2 or X.shape[1] != d:
+        raise ValueError("X must be [ntok, d_in]")
+    n = ctypes.c_int64(int(nseen))
+    _check(lib().gptq_hessian_accumulate_async(_ptr(H), ctypes.byref(n),
+                                               _ptr(X) if X.numel() else None, _dtype_code(X),
+                                               X.shape[0], d, _ptr(ws), ws.numel(),
+                                               _stream(stream)))
+    return int(n.value)
+
+
+def gptq_hessian_status(ws: torch.Tensor, stream=None) -> None:
+    """Synchronise the stream; raise the first failure of the async Hessian steps on ws."""
+    _check(lib().gptq_hessian_status(_ptr(ws), ws.numel(), _stream(stream)))
 
 
 def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tensor,

@@ -53,6 +53,31 @@ def test_hessian_streaming_chunks(lib, cuda_device):
     assert rel_fro(H[mask], ref[mask]) <= H_REL_FRO
 
 
+def test_hessian_async_matches_sync(lib, cuda_device):
+    """The enqueue-only form runs the same kernels in the same order: H is bit-identical
+    to the synchronous calls' (and to the oracle within tolerance), the status is OK."""
+    d = 384
+    g = torch.Generator().manual_seed(11)
+    X = (torch.randn(5000, d, generator=g) * 2.0).bfloat16().to(cuda_device)
+    parts = [X[:1800], X[1800:1801], X[1801:4000], X[4000:]]
+    ws = lib.workspace(lib.gptq_workspace_size(lib.GPTQ_OP_HESSIAN, 4000, 0, d), cuda_device)
+    H_sync = torch.full((d, d), float("nan"), dtype=torch.float32, device=cuda_device)
+    H_async = torch.full((d, d), float("nan"), dtype=torch.float32, device=cuda_device)
+    n = 0
+    for p in parts:
+        n = lib.gptq_hessian_accumulate(H_sync, n, p, ws)
+    na = 0
+    for p in parts:
+        na = lib.gptq_hessian_accumulate_async(H_async, na, p, ws)
+    lib.gptq_hessian_status(ws)
+    assert n == na == 5000
+    mask = upper_tile_mask(d)
+    Hs, Ha = to_np(H_sync), to_np(H_async)
+    assert np.array_equal(Hs[mask], Ha[mask])
+    ref, _ = O.hessian_streaming([p.float().cpu().numpy() for p in parts])
+    assert rel_fro(Ha[mask], ref[mask]) <= H_REL_FRO
+
+
 def test_hessian_fp32_layer_256(lib, cuda_device):
     """The 256x256 layer's float32 calibration stream (2048 tokens)."""
     cfg = CONFIGS["layer_256x256"]
