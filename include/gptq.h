@@ -229,8 +229,11 @@ int gptq_abi_version(void);
  * launches with CUDA events on the call's stream and accumulate the device time per
  * kernel kind; gptq_profile_read(kind, &ms, &launches) returns the totals and
  * gptq_profile_reset() clears them.  Kinds are the gptq_kernel_kind values; the name of
- * a kind is gptq_kernel_name(kind).  gptq_launch_count() counts every kernel launched by
- * the library since load (profiling or not).
+ * a kind is gptq_kernel_name(kind).  gptq_profile_select(kinds) limits the tracing to the
+ * kinds whose bit (1 << kind) is set (all of them after load): the events between
+ * consecutive kernels cost time and keep dependent launches apart, so a caller that
+ * times whole calls traces only the kinds it needs.  gptq_launch_count() counts every
+ * kernel launched by the library since load (profiling or not).
  */
 typedef enum {
   GPTQ_K_SYRK_TC = 0, GPTQ_K_SYRK_SIMT, GPTQ_K_SYRK_REDUCE,
@@ -243,6 +246,7 @@ typedef enum {
 } gptq_kernel_kind;
 
 void gptq_profile_enable(int on);
+void gptq_profile_select(uint32_t kinds);
 int gptq_profile_read(int kind, double* ms_total, int64_t* launches);
 void gptq_profile_reset(void);
 const char* gptq_kernel_name(int kind);

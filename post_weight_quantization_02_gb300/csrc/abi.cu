@@ -390,6 +390,7 @@ const char* gptq_status_string(int status) {
 int gptq_abi_version(void) { return 1; }
 
 void gptq_profile_enable(int on) { profile_enable(on != 0); }
+void gptq_profile_select(uint32_t kinds) { profile_select(kinds); }
 int gptq_profile_read(int kind, double* ms_total, int64_t* launches) {
   return profile_read(kind, ms_total, launches) ? 0 : -1;
 }

@@ -91,6 +91,7 @@ void trace_end(int kind, cudaStream_t s);
 void trace_flush();    // after the call's stream is synchronised
 void trace_discard();  // on failure: drop this thread's pending events
 void profile_enable(bool on);
+void profile_select(uint32_t mask);
 void profile_reset();
 bool profile_read(int kind, double* ms, int64_t* n);
 int64_t launch_count();

@@ -49,6 +49,7 @@ struct Pending {
 
 std::mutex g_mu;
 std::atomic<bool> g_enabled{false};
+std::atomic<uint32_t> g_mask{0xffffffffu};  // kinds that are traced while enabled
 std::atomic<int64_t> g_launches{0};
 double g_ms[GPTQ_K_COUNT] = {};
 int64_t g_count[GPTQ_K_COUNT] = {};
@@ -68,17 +69,21 @@ cudaEvent_t pool_get() {
 
 }  // namespace
 
+static bool traced(int kind) {
+  return g_enabled.load(std::memory_order_relaxed) && kind >= 0 && kind < 32 &&
+         ((g_mask.load(std::memory_order_relaxed) >> kind) & 1u) != 0;
+}
+
 void trace_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (!g_enabled.load(std::memory_order_relaxed)) return;
+  if (!traced(kind)) return;
   Pending p{kind, pool_get(), nullptr};
   cuda_check(cudaEventRecord(p.start, s), "cudaEventRecord");
   t_pending.push_back(p);
 }
 
 void trace_end(int kind, cudaStream_t s) {
-  (void)kind;
-  if (!g_enabled.load(std::memory_order_relaxed) || t_pending.empty()) return;
+  if (!traced(kind) || t_pending.empty()) return;
   Pending& p = t_pending.back();
   if (p.stop != nullptr) return;
   p.stop = pool_get();
@@ -111,6 +116,7 @@ void trace_discard() {
 }
 
 void profile_enable(bool on) { g_enabled.store(on); }
+void profile_select(uint32_t mask) { g_mask.store(mask); }
 void profile_reset() {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int k = 0; k < GPTQ_K_COUNT; ++k) {

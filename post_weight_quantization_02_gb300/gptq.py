@@ -23,8 +23,9 @@ __all__ = [
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
     "gptq_hessian_status", "gptq_prepare", "gptq_quantize_layer",
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
-    "gptq_profile_enable", "gptq_profile_read", "gptq_profile_reset", "gptq_kernel_name",
-    "gptq_launch_count", "KERNEL_KINDS", "workspace",
+    "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
+    "gptq_kernel_name",
+    "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "workspace",
 ]
 
 GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 3
@@ -32,6 +33,7 @@ GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 
 GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE = 0, 1, 2
 KERNEL_KINDS = 20
+GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
 
 
 class GptqLibraryError(RuntimeError):
@@ -66,6 +68,7 @@ _SIGS = {
     "gptq_status_string": (_c.c_char_p, [_c.c_int]),
     "gptq_abi_version": (_c.c_int, []),
     "gptq_profile_enable": (None, [_c.c_int]),
+    "gptq_profile_select": (None, [_c.c_uint32]),
     "gptq_profile_read": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_double), _c.POINTER(_i64)]),
     "gptq_profile_reset": (None, []),
     "gptq_kernel_name": (_c.c_char_p, [_c.c_int]),
@@ -214,6 +217,12 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional
 
 def gptq_profile_enable(on: bool) -> None:
     lib().gptq_profile_enable(int(bool(on)))
+
+
+def gptq_profile_select(kinds) -> None:
+    """Trace only the given kernel kinds (an iterable of kinds, or None for all)."""
+    mask = 0xFFFFFFFF if kinds is None else sum(1 << int(k) for k in kinds)
+    lib().gptq_profile_select(mask)
 
 
 def gptq_profile_reset() -> None:
