@@ -20,7 +20,8 @@
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
  *   call enqueues its kernels on `stream`, then synchronises `stream` and returns the
  *   status of the work it enqueued (device-side failures such as a non-positive-definite
- *   matrix are reported this way).
+ *   matrix are reported this way); gptq_hessian_accumulate_async is the one call that
+ *   returns without synchronising (gptq_hessian_status reports its device-side status).
  * - Matrices are row-major.  Indices and sizes are 32-bit unless stated.
  * - On any status other than GPTQ_OK, gptq_last_error() (thread-local) describes it.
  *   Invalid arguments are detected before anything is enqueued; outputs are then
