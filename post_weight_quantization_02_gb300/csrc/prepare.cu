@@ -183,9 +183,10 @@ __global__ void __launch_bounds__(256) prep_gather_kernel(const float* __restric
 //       columns first (P3a), the columns after it (P3b) while warp 0 runs the next P1.
 // Inverse, by 32 x 32 blocks (block indices), interleaved with the factor: V_ss = L_ss^-1
 // (forward substitution, lane = column, on a spare warp next to P2) replaces L_ss, and
-// then the row block V_sj = -V_ss sum_{t=j}^{s-1} L_st V_tj (j < s) on spare warps next
-// to P3a, each warp forming 32 x 16 of the sum in registers (own L row times broadcast V
-// rows) and applying V_ss through a private buffer.
+// then the row block V_sj = -V_ss sum_{t=j}^{s-1} L_st V_tj (j < s): each warp forms
+// 32 x 16 of the sum in registers (own L row times broadcast V rows) on the spare warps
+// beside P1(s), when every input is final, and leaves it in a private buffer; beside
+// P2(s), V_sj = L_ss^-1 (-sum) is solved by forward substitution like V_ss itself.
 // Shared memory (about 120 KB; the launch asks for a whole SM's worth so that the CTA runs
 // alone on its SM): the staged block L, whose free upper 32 x 32 blocks hold the
 // published columns; the six V_ij below the diagonal; XT; six private 32 x 16 buffers.
@@ -247,10 +248,13 @@ __device__ __forceinline__ void rank32_task(float* L, const float* XT, int c0, i
   }
 }
 
-// Inverse task: V_sj[:, 16h .. 16h + 15] = -V_ss sum_{t=j}^{s-1} L_st V_tj[:, same], one
-// warp, lane = row; Tw is the warp's private 32 x 16 buffer.
-__device__ __forceinline__ void inv_task(float* L, float* Voff, float* Tw, int s, int j, int h,
-                                         int lane) {
+// Inverse row block s, first half (one warp, lane = row):
+//   T_j[:, 16h .. 16h + 15] = sum_{t=j}^{s-1} L_st V_tj[:, same]
+// (all of it final once sub-panel s - 1 is done, so it runs beside P1(s)), into the
+// private buffer Tw of slot 2 j + h.  The second half, V_sj = L_ss^-1 (-T_j), is a
+// forward substitution beside P2(s).
+__device__ __forceinline__ void inv_sum_task(const float* L, const float* Voff, float* Tw, int s,
+                                             int j, int h, int lane) {
   const int r = SB * s + lane;
   float acc[16];
 #pragma unroll
@@ -282,34 +286,6 @@ __device__ __forceinline__ void inv_task(float* L, float* Voff, float* Tw, int s
   for (int q = 0; q < 16; q += 4)
     *reinterpret_cast<float4*>(Tw + lane * TBSTR + q) =
         make_float4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
-  __syncwarp();
-  float vrow[SB];
-  {
-    const float* vss = L + r * DSTR + SB * s;  // row `lane` of V_ss (zeros above the diagonal)
-#pragma unroll
-    for (int t = 0; t < SB; t += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(vss + t);
-      vrow[t] = v.x; vrow[t + 1] = v.y; vrow[t + 2] = v.z; vrow[t + 3] = v.w;
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
-#pragma unroll
-  for (int t = 0; t < SB; ++t) {
-#pragma unroll
-    for (int q = 0; q < 16; q += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(Tw + t * TBSTR + q);
-      acc[q] = fmaf(vrow[t], v.x, acc[q]);
-      acc[q + 1] = fmaf(vrow[t], v.y, acc[q + 1]);
-      acc[q + 2] = fmaf(vrow[t], v.z, acc[q + 2]);
-      acc[q + 3] = fmaf(vrow[t], v.w, acc[q + 3]);
-    }
-  }
-  float* out = Voff + voff_index(s, j) * SB * VSTR + lane * VSTR + 16 * h;
-#pragma unroll
-  for (int q = 0; q < 16; q += 4)
-    *reinterpret_cast<float4*>(out + q) = make_float4(-acc[q], -acc[q + 1], -acc[q + 2], -acc[q + 3]);
-  __syncwarp();  // the buffer may be reused by the warp's next task
 }
 
 __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restrict__ A, int d,
@@ -392,19 +368,25 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
         bad = 1;
         dev_fail(st, GPTQ_ERR_NOT_PD, info_base - (k + c0 + __ffs(badmask) - 1));
       }
-    } else if (s >= 1 && s <= 2) {
-      // P3b of sub-panel s - 1: rows and columns >= c0 + SB (its XT is still in place)
-      const int ntask = (s == 1) ? 6 : 2;
-      for (int task = warp - 1; task < ntask; task += 15) {
-        int g = 0;
-        while ((g + 1) * (g + 2) <= task) ++g;
-        const int h = task - g * (g + 1);
-        rank32_task(L, XT, c0 - SB, c0 + SB + SB * g, c0 + SB + 16 * h, lane);
+    } else {
+      // P3b of sub-panel s - 1 (rows and columns >= c0 + SB; its XT is still in place),
+      // then the sums of the inverse's row block s, on warps 1 .. 15
+      const int np3b = (s == 1) ? 6 : (s == 2) ? 2 : 0;
+      for (int task = warp - 1; task < np3b + 2 * s; task += 15) {
+        if (task < np3b) {
+          int g = 0;
+          while ((g + 1) * (g + 2) <= task) ++g;
+          const int h = task - g * (g + 1);
+          rank32_task(L, XT, c0 - SB, c0 + SB + SB * g, c0 + SB + 16 * h, lane);
+        } else {
+          const int it = task - np3b;  // slot 2 j + h
+          inv_sum_task(L, Voff, Tbuf + it * SB * TBSTR, s, it / 2, it % 2, lane);
+        }
       }
     }
     __syncthreads();
     if (bad) return;
-    // [B] P2(s) on the threads of the rows below; V_ss on warp 15
+    // [B] P2(s) on the threads of the rows below; V_ss and row block s of V beside it
     const int m2 = NB - c0 - SB;
     if (tid < m2) {
       float* xrow = L + (c0 + SB + tid) * DSTR + c0;
@@ -434,10 +416,17 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
 #pragma unroll
       for (int t = 0; t < SB; ++t) XT[t * XSTR + tid] = x[t];
     }
-    if (warp == 15) {
+    // V_ss (warp 15) and the row block V_sj = L_ss^-1 (-T_j), j < s (one warp per j, on
+    // the warps after P2's), by forward substitution with lane = column
+    const int wv = m2 / SB;  // first warp after P2's
+    const bool vss = (warp == 15);
+    const bool vsj = (warp >= wv && warp < wv + s);
+    if (vss || vsj) {
+      const int j = warp - wv;
+      const float* tcol = Tbuf + (2 * j + lane / 16) * SB * TBSTR + lane % 16;
       float y[SB];
 #pragma unroll
-      for (int t = 0; t < SB; ++t) y[t] = (t == lane) ? 1.0f : 0.0f;
+      for (int t = 0; t < SB; ++t) y[t] = vss ? ((t == lane) ? 1.0f : 0.0f) : -tcol[t * TBSTR];
 #pragma unroll
       for (int t = 0; t < SB; ++t) {
         const float* srow = STs + t * DSTR;
@@ -452,22 +441,17 @@ __global__ void __launch_bounds__(512) chol_inv_diag_kernel(const float* __restr
           if (j4 + 3 > t) y[j4 + 3] = fmaf(-yt, v.w, y[j4 + 3]);
         }
       }
-      float* vcol = L + c0 * DSTR + c0 + lane;  // V_ss replaces L_ss
+      // V_ss replaces L_ss; V_sj goes to its off-diagonal block
+      float* vcol = vss ? L + c0 * DSTR + c0 + lane : Voff + voff_index(s, j) * SB * VSTR + lane;
+      const int vstride = vss ? DSTR : VSTR;
 #pragma unroll
-      for (int t = 0; t < SB; ++t) vcol[t * DSTR] = y[t];
+      for (int t = 0; t < SB; ++t) vcol[t * vstride] = y[t];
     }
     __syncthreads();
-    // [C] P3a(s): columns c0 + SB .. c0 + 2 SB, rows below; row block s of V
+    // [C] P3a(s): columns c0 + SB .. c0 + 2 SB, rows below
     const int n3a = (s < NSB - 1) ? 2 * (NSB - 1 - s) : 0;
-    const int ntasks = n3a + 2 * s;
-    for (int task = warp; task < ntasks; task += 16) {
-      if (task < n3a) {
-        rank32_task(L, XT, c0, c0 + SB + SB * (task / 2), c0 + SB + 16 * (task % 2), lane);
-      } else {
-        const int it = task - n3a;
-        inv_task(L, Voff, Tbuf + (warp % NTB) * SB * TBSTR, s, it / 2, it % 2, lane);
-      }
-    }
+    for (int task = warp; task < n3a; task += 16)
+      rank32_task(L, XT, c0, c0 + SB + SB * (task / 2), c0 + SB + 16 * (task % 2), lane);
     __syncthreads();
   }
 
