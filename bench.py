@@ -267,6 +267,9 @@ def run_ours(args, world, rank, local):
         roofline = {"bound": "tensor", "kernel": "syrk_tc", "achieved": round(achieved, 1),
                     "peak": bf16, "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
                     "peak_source": f"{peak_src} bf16 dense burst",
+                    # the measured power-capped figure (a GEMM run back to back), for context
+                    "peak_sustained": bf16_sus,
+                    "frac_of_sustained": round(achieved / bf16_sus, 4),
                     "algorithmic_flops_per_launch": flops,
                     "traffic": ncu_traffic("post_weight_quantization_02_gb300/csrc/hessian_tc.cu",
                                            args.config)}
