@@ -30,6 +30,11 @@ Readings where the pages are silent or disagree (all restated in the design doc):
   [-(2^(b-1)-1), 2^(b-1)-1], stored with the offset 2^(b-1) (the 4x4 example's
   max|w|/7 at 4 bits).
 * ``group = -1`` is one group spanning the whole row, fitted before the first column.
+* Static groups ("GPTQ Architecture, in depth", "Groups, act-order and other knobs": groups
+  fixed in the original order before permuting): group G is original columns
+  [G*g, (G+1)*g); its scale and zero are fitted once, before the loop, on W after the dead
+  fix (no permutation, no compensation yet); processed column q uses the group of
+  original column perm[q]; g_idx[c] = c // g.
 * Act-order ties are broken by ascending original index (a stable sort).
 * Wherever a float decides an integer (a code, a zero point), the decision is taken in
   float32, the precision of the page's code (``.float()``); the weights themselves evolve
@@ -56,7 +61,8 @@ __all__ = [
     "grid", "fit_group", "round_to_grid",
     "gptq_sweep", "gptq_sweep_obs",
     "gptq_prepare", "gptq_quantize_layer", "gptq_layer",
-    "group_index", "pack_bitstream", "unpack_bitstream", "checkpoint_bytes",
+    "group_index", "static_group_fit", "pack_bitstream", "unpack_bitstream",
+    "checkpoint_bytes",
     "quadratic_loss", "rtn_quantize",
 ]
 
@@ -269,8 +275,8 @@ def _group_span(q: int, group: int, d: int) -> Optional[Tuple[int, int]]:
 
 def gptq_sweep(Wp, U, bits: int = 4, group: int = 128, sym: bool = False,
                blocksize: int = 128, hint: Optional[dict] = None,
-               tie_eps: float = 1e-3, column_quantizer: Optional[Callable] = None
-               ) -> Dict[str, np.ndarray]:
+               tie_eps: float = 1e-3, column_quantizer: Optional[Callable] = None,
+               static: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """The blocked fixed-order column loop with lazy batch updates.
 
     "GPTQ Architecture, in depth", "The algorithm in code" (the gptq loop) and
@@ -289,6 +295,9 @@ def gptq_sweep(Wp, U, bits: int = 4, group: int = 128, sym: bool = False,
     ``column_quantizer(q, w_col) -> (codes, what)``, if given, replaces the per-row group
     grid (the 4x4 worked example of "Same Ruler", section 1.11, uses one symmetric scale
     per column); scales and zeros are then not recorded.
+    ``static`` (``scales`` ``[G, m]``, ``zeros`` ``[G, m]``, ``gcol`` ``[d]``), if given,
+    fixes the grids before the loop: column q uses group ``gcol[q]`` and nothing is fitted
+    inside the loop (static groups).
 
     Returns codes ``[m, d]`` (processing order), scales ``[G, m]`` float32, zeros
     ``[G, m]``, loss_rows ``[m]`` (sum of e^2/2), Q ``[m, d]`` (dequantised, processing
@@ -312,6 +321,11 @@ def gptq_sweep(Wp, U, bits: int = 4, group: int = 128, sym: bool = False,
         for q in range(i1, i2):
             if column_quantizer is not None:
                 c, what = column_quantizer(q, W[:, q].copy())
+            elif static is not None:
+                gi = int(static["gcol"][q])
+                s, z = static["scales"][gi], static["zeros"][gi]
+                hc = None if hint is None else hint["codes"][:, q]
+                c, what = round_to_grid(W[:, q], s, z, bits, sym, hc, tie_eps, stats)
             else:
                 span = _group_span(q, group, d)
                 if span is not None:
@@ -329,6 +343,9 @@ def gptq_sweep(Wp, U, bits: int = 4, group: int = 128, sym: bool = False,
             loss += 0.5 * e * e
         if i2 < d:
             W[:, i2:] -= Err @ U[i1:i2, i2:]
+    if static is not None:
+        scales = np.asarray(static["scales"], dtype=F32).copy()
+        zeros = np.asarray(static["zeros"], dtype=np.int64).copy()
     return dict(codes=codes, scales=scales, zeros=zeros, loss_rows=loss, Q=Q, stats=stats)
 
 
@@ -377,19 +394,43 @@ def gptq_sweep_obs(Wp, Hd, bits: int = 4, group: int = 128, sym: bool = False,
 # Output format
 # --------------------------------------------------------------------------------------
 
-def group_index(perm: np.ndarray, group: int) -> np.ndarray:
+def group_index(perm: np.ndarray, group: int, static: bool = False) -> np.ndarray:
     """g_idx[c] = (position of original column c in the processing order) // g.
 
     "GPTQ Architecture, in depth", "Groups, act-order and other knobs": with act-order
     the groups follow the permuted order, so each original column records its group.
+    With static groups the groups stay in the original order: g_idx[c] = c // g.
     ``group = -1`` puts every column in group 0.
     """
     perm = np.asarray(perm, dtype=np.int64)
+    if static and group != -1:
+        return (np.arange(perm.size) // group).astype(np.int32)
     pos = np.empty_like(perm)
     pos[perm] = np.arange(perm.size)
     if group == -1:
         return np.zeros(perm.size, dtype=np.int32)
     return (pos // group).astype(np.int32)
+
+
+def static_group_fit(W0, group: int, bits: int, sym: bool, hint_zeros=None,
+                     tie_eps: float = 1e-3, stats: Optional[dict] = None
+                     ) -> Tuple[np.ndarray, np.ndarray]:
+    """Scales and zeros ``[G, m]`` of the static groups: group G is the original columns
+    [G*g, (G+1)*g) of ``W0`` (weights after the dead fix, original order, before any
+    compensation), fitted once ("GPTQ Architecture, in depth", "Groups, act-order and
+    other knobs": groups fixed in the original order before permuting)."""
+    W0 = np.asarray(W0, dtype=F64)
+    m, d = W0.shape
+    if group == -1:
+        spans = [(0, d)]
+    else:
+        spans = [(c, min(c + group, d)) for c in range(0, d, group)]
+    scales = np.zeros((len(spans), m), dtype=F32)
+    zeros = np.zeros((len(spans), m), dtype=np.int64)
+    for gi, (a, b) in enumerate(spans):
+        hz = None if hint_zeros is None else hint_zeros[gi]
+        scales[gi], zeros[gi] = fit_group(W0[:, a:b], bits, sym, hz, tie_eps, stats)
+    return scales, zeros
 
 
 def pack_bitstream(values: np.ndarray, bits: int) -> np.ndarray:
@@ -455,7 +496,8 @@ def gptq_prepare(H, damp: float = 0.01, actorder: bool = True) -> Dict[str, np.n
 def gptq_quantize_layer(W, U, perm=None, dead=None, bits: int = 4, group: int = 128,
                         sym: bool = False, blocksize: int = 128,
                         rows: Optional[np.ndarray] = None, hint: Optional[dict] = None,
-                        tie_eps: float = 1e-3, pack: bool = True) -> Dict[str, np.ndarray]:
+                        tie_eps: float = 1e-3, pack: bool = True,
+                        static_groups: bool = False) -> Dict[str, np.ndarray]:
     """Quantise W given U and perm, and produce the packed checkpoint tensors.
 
     W ``[m, d]`` in original column order.  ``rows`` restricts the work to a subset of
@@ -463,7 +505,9 @@ def gptq_quantize_layer(W, U, perm=None, dead=None, bits: int = 4, group: int = 
     algorithm on one page").  Codes come back in original column order (the un-permute,
     ``Q[:, argsort(perm)]``).  With ``pack`` (needs all rows): qweight
     ``[bits*d/32, m]`` packed along d, qzeros ``[G, bits*m/32]`` packed along m (only
-    when both lengths fill whole words).  g_idx is always produced.
+    when both lengths fill whole words).  g_idx is always produced.  ``static_groups``
+    fits the groups in the original column order before the loop (``static_group_fit``);
+    scales and zeros then come in original group order.
     """
     W = np.array(W, dtype=F64, copy=True)
     m, d = W.shape
@@ -472,14 +516,25 @@ def gptq_quantize_layer(W, U, perm=None, dead=None, bits: int = 4, group: int = 
     if dead is not None:
         W[:, np.asarray(dead, dtype=bool)] = 0.0
     perm = np.arange(d, dtype=np.int64) if perm is None else np.asarray(perm, np.int64)
-    res = gptq_sweep(W[:, perm], U, bits, group, sym, blocksize, hint, tie_eps)
+    static = None
+    if static_groups:
+        st_stats: dict = {}
+        sc, ze = static_group_fit(W, group, bits, sym,
+                                  None if hint is None else hint["zeros"], tie_eps, st_stats)
+        gcol = np.zeros(d, dtype=np.int64) if group == -1 else perm // group
+        static = dict(scales=sc, zeros=ze, gcol=gcol)
+    res = gptq_sweep(W[:, perm], U, bits, group, sym, blocksize, hint, tie_eps,
+                     static=static)
+    if static_groups and st_stats:
+        for k, v in st_stats.items():
+            res["stats"][k] = res["stats"].get(k, 0) + v
     codes = np.empty_like(res["codes"])
     codes[:, perm] = res["codes"]
     out = dict(res)
     out["codes_proc"] = res["codes"]
     out["codes"] = codes
     out["loss"] = float(np.sum(res["loss_rows"]))
-    out["g_idx"] = group_index(perm, group)
+    out["g_idx"] = group_index(perm, group, static_groups)
     if pack and rows is None and (d * bits) % 32 == 0 and (m * bits) % 32 == 0:
         out["qweight"] = pack_bitstream(codes, bits).T.copy()
         out["qzeros"] = pack_bitstream(res["zeros"], bits)
@@ -488,11 +543,11 @@ def gptq_quantize_layer(W, U, perm=None, dead=None, bits: int = 4, group: int = 
 
 def gptq_layer(W, H, bits: int = 4, group: int = 128, sym: bool = False,
                actorder: bool = True, damp: float = 0.01, blocksize: int = 128,
-               rows=None) -> Dict[str, np.ndarray]:
+               rows=None, static_groups: bool = False) -> Dict[str, np.ndarray]:
     """The whole per-layer method: prepare, then the column loop and packing."""
     prep = gptq_prepare(H, damp, actorder)
     out = gptq_quantize_layer(W, prep["U"], prep["perm"], prep["dead"], bits, group, sym,
-                              blocksize, rows)
+                              blocksize, rows, static_groups=static_groups)
     out.update(perm=prep["perm"], dead=prep["dead"], lam=prep["lam"], U=prep["U"],
                Hd=prep["Hd"])
     return out
@@ -517,11 +572,16 @@ def rtn_quantize(Wp, bits: int = 4, group: int = 128, sym: bool = False
     rounding to nearest breaks at 4 bits")."""
     W = np.asarray(Wp, dtype=F64)
     m, d = W.shape
+    G = 1 if group == -1 else -(-d // group)
     Q = np.zeros_like(W)
     codes = np.zeros((m, d), dtype=np.int64)
+    scales = np.zeros((G, m), dtype=F32)
+    zeros = np.zeros((G, m), dtype=np.int64)
     for q in range(d):
         span = _group_span(q, group, d)
         if span is not None:
             s, z = fit_group(W[:, span[0]:span[1]], bits, sym)
+            gi = 0 if group == -1 else q // group
+            scales[gi], zeros[gi] = s, z
         codes[:, q], Q[:, q] = round_to_grid(W[:, q], s, z, bits, sym)
-    return dict(codes=codes, Q=Q)
+    return dict(codes=codes, Q=Q, scales=scales, zeros=zeros)

@@ -45,6 +45,12 @@ MUTATIONS = {
     "round_floor": ("own = np.clip(np.rint(v) + z, lowest, maxq)",
                     "own = np.clip(np.floor(v) + z, lowest, maxq)"),
     "dead_not_zeroed": ("W[:, dead] = 0.0", "pass"),
+    "static_group_of_processing_position": (
+        "gcol = np.zeros(d, dtype=np.int64) if group == -1 else perm // group",
+        "gcol = np.zeros(d, dtype=np.int64) if group == -1 else np.arange(d) // group"),
+    "static_fit_on_permuted": ("sc, ze = static_group_fit(W, group, bits, sym,",
+                               "sc, ze = static_group_fit(W[:, perm], group, bits, sym,"),
+    "static_g_idx_permuted": ("if static and group != -1:", "if False:"),
 }
 
 

@@ -376,12 +376,65 @@ def pin_format_roundtrip(O):
         assert np.array_equal(codes, r["codes"])
 
 
+def pin_static_groups(O):
+    """Static groups ("GPTQ Architecture, in depth", "Groups, act-order and other knobs":
+    groups fixed in the original order before permuting).
+
+    * With a diagonal H the factor U is diagonal, so no error reaches a later column and
+      GPTQ with grids fixed before the loop is round-to-nearest on those grids: the codes
+      in original column order equal RTN on the original order (act-order on, so a
+      column read through the wrong group would show), and differ from dynamic groups.
+    * With one group per row the fit sees every column of the row before any update in
+      both modes, so static equals dynamic exactly.
+    * With a general H the static scales and zeros are the RTN fit of the original,
+      uncompensated weights; g_idx[c] = c // g; blocking does not change the result.
+    """
+    rng = np.random.default_rng(41)
+    m, d, g = 5, 32, 8
+    for bits, sym in [(4, False), (3, True)]:
+        W = rng.standard_normal((m, d)) * 0.02 * np.exp(rng.standard_normal(d))
+        H = np.diag(np.exp(rng.standard_normal(d)))
+        st = O.gptq_layer(W, H, bits, g, sym, actorder=True, static_groups=True)
+        assert not np.array_equal(st["perm"], np.arange(d))
+        rtn = O.rtn_quantize(W, bits, g, sym)
+        assert np.array_equal(st["codes"], rtn["codes"])
+        assert np.array_equal(st["scales"], rtn["scales"])
+        assert np.array_equal(st["zeros"], rtn["zeros"])
+        dyn = O.gptq_layer(W, H, bits, g, sym, actorder=True)
+        assert not np.array_equal(dyn["codes"], st["codes"])
+    for bits, sym in [(4, False), (3, True)]:
+        W, H, _ = _small_layer(rng, 6, 24)
+        a = O.gptq_layer(W, H, bits, -1, sym, actorder=True, static_groups=True)
+        b = O.gptq_layer(W, H, bits, -1, sym, actorder=True)
+        assert np.array_equal(a["codes"], b["codes"])
+        assert np.array_equal(a["scales"], b["scales"]) and np.array_equal(a["zeros"], b["zeros"])
+        assert a["loss"] == b["loss"]
+        assert np.array_equal(a["g_idx"], b["g_idx"])
+    W, H, _ = _small_layer(rng, 6, 48)
+    H[7, :] = 0.0
+    H[:, 7] = 0.0                                   # a dead channel
+    st = O.gptq_layer(W, H, 4, g, False, actorder=True, static_groups=True)
+    W0 = W.copy()
+    W0[:, 7] = 0.0
+    rtn = O.rtn_quantize(W0, 4, g, False)
+    assert np.array_equal(st["scales"], rtn["scales"]) and np.array_equal(st["zeros"], rtn["zeros"])
+    assert np.array_equal(st["g_idx"], np.arange(48) // g)
+    prep = O.gptq_prepare(H, 0.01, True)
+    ref = O.gptq_quantize_layer(W, prep["U"], prep["perm"], prep["dead"], 4, g, False,
+                                blocksize=10 ** 9, static_groups=True)
+    for B in (1, 8, 16):
+        r = O.gptq_quantize_layer(W, prep["U"], prep["perm"], prep["dead"], 4, g, False,
+                                  blocksize=B, static_groups=True)
+        assert np.array_equal(r["codes"], ref["codes"]), B
+        assert np.allclose(r["loss_rows"], ref["loss_rows"], rtol=1e-10)
+
+
 PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
         pin_cholesky_2x2, pin_cholesky_general, pin_obs_equals_cholesky,
         pin_blocked_equals_unblocked, pin_loss_identity, pin_brute_force_optimum,
         pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
         pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
-        pin_format_roundtrip]
+        pin_format_roundtrip, pin_static_groups]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
