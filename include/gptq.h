@@ -202,7 +202,7 @@ gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
  *            packed along d_in as a little-endian bit stream (code k of output row r at
  *            bits [bits*k, bits*k+bits) of column r's stream).
  * scales     device float32 [G, d_out], out; G = ceil(d_in/group) (1 when group=-1),
- *            groups in processing order.
+ *            groups in processing order (original order with static groups, below).
  * qzeros     device int32 [G, bits*d_out/32], out: zero points packed along d_out.
  * g_idx      device int32 [d_in], out: g_idx[c] = (position of c in perm) / group.
  * loss       device float64 scalar, out: sum over rows and columns of e^2 / 2, the OBS
@@ -215,6 +215,28 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
                                 int32_t* qweight, float* scales, int32_t* qzeros,
                                 int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * gptq_quantize_layer_ex -- gptq_quantize_layer with option flags (the same arguments,
+ * plus `flags` after `blocksize`; flags = 0 is gptq_quantize_layer).
+ *
+ * GPTQ_QUANT_STATIC_GROUPS: static groups ("GPTQ Architecture, in depth", "Groups,
+ * act-order and other knobs": groups fixed in the original order before permuting, so
+ * that a serving kernel reads its scales contiguously).  Group G is the original columns
+ * [G*group, (G+1)*group); its (s, z) per row are fitted once, before the column loop, on
+ * W after the dead fix (no permutation, no compensation yet), with the same formulas as
+ * above; processed column q then rounds on the grid of group perm[q] / group.  scales
+ * and qzeros come in original group order and g_idx[c] = c / group.  With group = -1 it
+ * is the same as flags = 0.
+ * Errors: as gptq_quantize_layer; INVALID_ARG for an unknown flag.
+ */
+#define GPTQ_QUANT_STATIC_GROUPS 1
+gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_chol,
+                                   const int32_t* perm, const uint8_t* dead, int32_t d_out,
+                                   int32_t d_in, int bits, int group, int sym, int blocksize,
+                                   int flags, int32_t* qweight, float* scales, int32_t* qzeros,
+                                   int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* gptq_last_error(void);

@@ -39,11 +39,12 @@ class LayerEngine:
     def __init__(self, d_out: int, d_in: int, bits: int = 4, group: int = 128,
                  sym: bool = False, actorder: bool = True, damp: float = 0.01,
                  blocksize: int = 128, max_chunk_tokens: int = 16384,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, static_groups: bool = False):
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         self.d_out, self.d_in = int(d_out), int(d_in)
         self.bits, self.group, self.sym = int(bits), int(group), bool(sym)
         self.actorder, self.damp, self.blocksize = bool(actorder), float(damp), int(blocksize)
+        self.static_groups = bool(static_groups)
         dev, d, m = self.device, self.d_in, self.d_out
         ngroups = 1 if group == -1 else -(-d // group)
         self.H = torch.empty(d, d, dtype=torch.float32, device=dev)
@@ -87,7 +88,8 @@ class LayerEngine:
     def quantize_weights(self, W: torch.Tensor, stream=None) -> QuantizedLayer:
         G.gptq_quantize_layer(W, self.Hinv_chol, self.perm, self.dead, self.bits, self.group,
                               self.sym, self.blocksize, self.qweight, self.scales, self.qzeros,
-                              self.g_idx, self.loss, self.ws_q, stream)
+                              self.g_idx, self.loss, self.ws_q, stream,
+                              static_groups=self.static_groups)
         return QuantizedLayer(self.qweight, self.scales, self.qzeros, self.g_idx, self.perm,
                               self.loss)
 

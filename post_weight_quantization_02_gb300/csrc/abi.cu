@@ -300,13 +300,15 @@ gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
   return st_code;
 }
 
-gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_chol,
-                                const int32_t* perm, const uint8_t* dead, int32_t d_out,
-                                int32_t d_in, int bits, int group, int sym, int blocksize,
-                                int32_t* qweight, float* scales, int32_t* qzeros,
-                                int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
-                                void* stream) {
+gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_chol,
+                                   const int32_t* perm, const uint8_t* dead, int32_t d_out,
+                                   int32_t d_in, int bits, int group, int sym, int blocksize,
+                                   int flags, int32_t* qweight, float* scales, int32_t* qzeros,
+                                   int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
+                                   void* stream) {
   return guarded([&] {
+    require((flags & ~GPTQ_QUANT_STATIC_GROUPS) == 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer: unknown flags");
     require(d_in > 0 && d_out >= 0, GPTQ_ERR_INVALID_ARG,
             "gptq_quantize_layer: need d_in > 0 and d_out >= 0");
     require(Hinv_chol != nullptr && g_idx != nullptr && loss != nullptr && ws != nullptr,
@@ -357,6 +359,7 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
     q.d = d_in;
     q.bits = bits;
     q.group = group;
+    q.static_groups = (flags & GPTQ_QUANT_STATIC_GROUPS) != 0;
     q.sym = sym;
     q.G = G;
     q.qweight = qweight;
@@ -369,6 +372,17 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
     launch_quantize(q, s);
     raise_device_status(finish_call(q.st, s), "gptq_quantize_layer");
   });
+}
+
+gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_chol,
+                                const int32_t* perm, const uint8_t* dead, int32_t d_out,
+                                int32_t d_in, int bits, int group, int sym, int blocksize,
+                                int32_t* qweight, float* scales, int32_t* qzeros,
+                                int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
+                                void* stream) {
+  return gptq_quantize_layer_ex(W, wdtype, Hinv_chol, perm, dead, d_out, d_in, bits, group, sym,
+                                blocksize, 0, qweight, scales, qzeros, g_idx, loss, ws,
+                                ws_bytes, stream);
 }
 
 const char* gptq_last_error(void) { return last_error().c_str(); }

@@ -42,6 +42,7 @@ struct QuantArgs {
   const int32_t* perm;  // may be null
   const uint8_t* dead;  // may be null
   int m, d, bits, group, sym, G;
+  bool static_groups;   // groups fixed in the original column order before the loop
   // workspace
   float* Wp;
   uint8_t* codesT;

@@ -64,14 +64,15 @@ __global__ void __launch_bounds__(256) gather_w_kernel(const T* __restrict__ W, 
   if (threadIdx.x == 0) loss_rows[r] = 0.0;
 }
 
-// pos[perm[k]] = k; g_idx[c] = pos[c] / group (0 for group == -1).
-__global__ void gidx_kernel(const int32_t* __restrict__ perm, int d, int group,
+// pos[perm[k]] = k; g_idx[c] = pos[c] / group (0 for group == -1), or c / group with
+// static groups (fixed in the original order).
+__global__ void gidx_kernel(const int32_t* __restrict__ perm, int d, int group, int static_groups,
                             int32_t* __restrict__ pos, int32_t* __restrict__ g_idx) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= d) return;
   const int c = perm ? perm[k] : k;
   pos[c] = k;
-  g_idx[c] = (group == -1) ? 0 : k / group;
+  g_idx[c] = (group == -1) ? 0 : (static_groups ? c : k) / group;
 }
 
 // ---------------------------------------------------------------- group fit
@@ -137,6 +138,46 @@ __global__ void __launch_bounds__(256) fit_kernel(const float* __restrict__ Wp, 
   }
 }
 
+// Static groups ("GPTQ Architecture, in depth", "Groups, act-order and other knobs":
+// groups fixed in the original order before permuting): scale and zero of every row and
+// original group [gi*group, (gi+1)*group) from W after the dead fix, before the loop.
+// One warp per row (warp-shuffle min / max).
+template <typename T>
+__global__ void __launch_bounds__(256) static_fit_kernel(const T* __restrict__ W,
+                                                         const uint8_t* __restrict__ dead,
+                                                         int m, int d, int group, Grid g,
+                                                         float* __restrict__ scales,
+                                                         int32_t* __restrict__ zeros) {
+  const int r = blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= m) return;
+  const T* row = W + static_cast<size_t>(r) * d;
+  const int G = (d + group - 1) / group;
+  for (int gi = 0; gi < G; ++gi) {
+    const int c1 = min(d, (gi + 1) * group);
+    float mn = INFINITY, mx = -INFINITY, am = 0.0f;
+    for (int c = gi * group + lane; c < c1; c += 32) {
+      float v = ldf(row + c);
+      if (dead != nullptr && dead[c]) v = 0.0f;
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+      am = fmaxf(am, fabsf(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    }
+    if (lane == 0) {
+      float sc, z;
+      fit_from_range(g, mn, mx, am, sc, z);
+      scales[static_cast<size_t>(gi) * m + r] = sc;
+      zeros[static_cast<size_t>(gi) * m + r] = static_cast<int32_t>(z);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- the column loop
 
 // 16-byte asynchronous global -> shared copy.
@@ -188,6 +229,8 @@ struct LoopArgs {
   int i1, nb;          // block start and width (nb <= 128)
   int group;           // in-kernel fit width (16, 32, 64 or 128), or 0: fitted outside
   int gi_outer;        // group index of the outside fit (group -1 or wide groups)
+  int static_group;    // static groups: the group width (column q uses perm[q] / it), else 0
+  const int32_t* perm; // processing order (static groups), may be null
   Grid g;
   float* scales;       // [G][m]
   int32_t* zeros;      // [G][m]
@@ -229,16 +272,23 @@ __device__ __forceinline__ void fit_lanes(const float (&w)[LW], int group, int t
 // registers (code_r[J], e_r[J]) until the sub-block ends, so a column is one branch-free
 // stretch of code that the compiler can overlap with the next column's rounding.
 // Returns the owner's next column value.
-template <int J>
+template <bool STATIC, int J>
 __device__ __forceinline__ float loop_column(float (&w)[LW], float (&code_r)[LW],
                                              float (&e_r)[LW], float wq, int b, int t, int gb,
                                              bool active, int r, const LoopArgs& a,
                                              const float* __restrict__ ulay,
-                                             const float* __restrict__ urinv, float& s,
+                                             const float* __restrict__ urinv,
+                                             const float* __restrict__ szr, float& s,
                                              float& z, float& rs, float& loss) {
   const int q = LW * b + J;
-  // groups (16 .. 128 columns) start only at window positions that are multiples of 16
-  if constexpr (J % 16 == 0) {
+  if constexpr (STATIC) {
+    // static groups: this column's grid was fitted before the loop (scale, zero, 1/scale
+    // of the row's group, staged per column)
+    s = szr[q * RPC];
+    z = szr[(BLK + q) * RPC];
+    rs = szr[(2 * BLK + q) * RPC];
+  } else if constexpr (J % 16 == 0) {
+    // groups (16 .. 128 columns) start only at window positions that are multiples of 16
     if (a.group > 0 && (q % a.group) == 0) {
       fit_lanes<J>(w, a.group, t, a.nb, a.g, s, z);
       rs = __frcp_rn(s);
@@ -274,19 +324,27 @@ __device__ __forceinline__ float loop_column(float (&w)[LW], float (&code_r)[LW]
   return wnext;
 }
 
-template <int J>
+template <bool STATIC, int J>
 __device__ __forceinline__ void loop_columns(float (&w)[LW], float (&code_r)[LW],
                                              float (&e_r)[LW], float& wq, int b, int t, int gb,
                                              bool active, int r, const LoopArgs& a,
                                              const float* __restrict__ ulay,
-                                             const float* __restrict__ urinv, float& s,
+                                             const float* __restrict__ urinv,
+                                             const float* __restrict__ szr, float& s,
                                              float& z, float& rs, float& loss) {
-  wq = loop_column<J>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs, loss);
+  wq = loop_column<STATIC, J>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, szr, s,
+                              z, rs, loss);
   if constexpr (J + 1 < LW)
-    loop_columns<J + 1>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs,
-                        loss);
+    loop_columns<STATIC, J + 1>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, szr,
+                                s, z, rs, loss);
 }
 
+// Shared memory of the loop: the U layout, the staging of codes and bf16 error halves,
+// and with static groups the per-column scale, zero and reciprocal of each row.
+constexpr int kLoopSmemDynamic = kUlayFloats * 4 + BLK * RPC * (1 + 2 + 2);
+constexpr int kLoopSmemStatic = kLoopSmemDynamic + 3 * BLK * RPC * 4;
+
+template <bool STATIC>
 __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArgs a) {
   extern __shared__ __align__(16) float smem_f[];
   const float* ulay = smem_f;
@@ -296,6 +354,7 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   uint8_t* codes_s = reinterpret_cast<uint8_t*>(smem_f + kUlayFloats);               // [128][RPC]
   __nv_bfloat16* ehi_s = reinterpret_cast<__nv_bfloat16*>(codes_s + BLK * RPC);      // [128][RPC]
   __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][RPC]
+  float* sz_s = reinterpret_cast<float*>(elo_s + BLK * RPC);  // static groups: [3][128][RPC]
   const int i1 = a.i1, nb = a.nb;
   {
     const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
@@ -320,7 +379,23 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
     }
   }
   float s = 1.0f, z = 0.0f;
-  if (a.group == 0 && active) {
+  if constexpr (STATIC) {
+    // each column's grid: the row's scale and zero of the original column's group
+    const int r0 = blockIdx.x * RPC;
+    for (int e = threadIdx.x; e < BLK * RPC; e += blockDim.x) {
+      const int q = e / RPC, j = e % RPC;
+      float sv = 1.0f, zv = 0.0f;
+      if (q < nb && r0 + j < a.m) {
+        const int c = a.perm ? a.perm[i1 + q] : i1 + q;
+        const size_t o = static_cast<size_t>(c / a.static_group) * a.m + r0 + j;
+        sv = a.scales[o];
+        zv = static_cast<float>(a.zeros[o]);
+      }
+      sz_s[e] = sv;
+      sz_s[BLK * RPC + e] = zv;
+      sz_s[2 * BLK * RPC + e] = __frcp_rn(sv);
+    }
+  } else if (a.group == 0 && active) {
     s = a.scales[static_cast<size_t>(a.gi_outer) * a.m + r];
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
   }
@@ -339,7 +414,8 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
     // the owner's first column, settled by every earlier column's update
     float wq = w[0];
     float code_r[LW], e_r[LW];
-    loop_columns<0>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, s, z, rs, loss);
+    loop_columns<STATIC, 0>(w, code_r, e_r, wq, b, t, gb, active, r, a, ulay, urinv, sz_s + rl,
+                            s, z, rs, loss);
     if (t == b) {
 #pragma unroll
       for (int j = 0; j < LW; ++j) {
@@ -456,8 +532,20 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
   g.lowest = q.sym ? 1.0f : 0.0f;
   g.zfix = static_cast<float>(1 << (q.bits - 1));
 
+  const bool stat = q.static_groups && q.group > 0;  // with group -1 both modes coincide
   GPTQ_LAUNCH(GPTQ_K_QUANT_GATHER, s, gidx_kernel, (unsigned)ceil_div(d, 256), 256, 0, q.perm,
-              d, q.group, q.pos, q.g_idx);
+              d, q.group, stat ? 1 : 0, q.pos, q.g_idx);
+  if (stat && m > 0) {
+    // every group's grid, fitted before the loop on W after the dead fix (original order)
+    if (q.w_bf16) {
+      GPTQ_LAUNCH(GPTQ_K_QUANT_FIT, s, static_fit_kernel<__nv_bfloat16>, (unsigned)ceil_div(m, 8),
+                  256, 0, static_cast<const __nv_bfloat16*>(q.W), q.dead, m, d, q.group, g,
+                  q.scales, q.zeros);
+    } else {
+      GPTQ_LAUNCH(GPTQ_K_QUANT_FIT, s, static_fit_kernel<float>, (unsigned)ceil_div(m, 8), 256, 0,
+                  static_cast<const float*>(q.W), q.dead, m, d, q.group, g, q.scales, q.zeros);
+    }
+  }
   if (m > 0) {
     const size_t row_smem = static_cast<size_t>(d) * sizeof(float);
     static size_t attr_f = 0, attr_b = 0;
@@ -486,19 +574,22 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
     const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, 2 * kErrRows, q.uhi, q.ulo, q.Wp, m, d);
-    const int loop_smem = kUlayFloats * static_cast<int>(sizeof(float)) + BLK * RPC * (1 + 2 + 2);
     static bool loop_attr = false;
     if (!loop_attr) {
-      GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, loop_smem));
+      GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kLoopSmemDynamic));
+      GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kLoopSmemStatic));
       loop_attr = true;
     }
-    const bool inblock_fit = (q.group > 0 && q.group <= BLK);
+    const bool inblock_fit = !stat && q.group > 0 && q.group <= BLK;
     // Deferred updates in two levels: superblocks of kErrRows columns, unless a group that
     // starts inside a superblock would reach past its end (its fit must see every earlier
     // block's update), in which case every block is its own superblock.
-    const bool groups_nest = q.group == -1 || q.group <= BLK || kErrRows % q.group == 0 ||
-                             q.group % kErrRows == 0;
+    const bool groups_nest = stat || q.group == -1 || q.group <= BLK ||
+                             kErrRows % q.group == 0 || q.group % kErrRows == 0;
     const int sb_cols = groups_nest ? kErrRows : BLK;
     // The far update of superblock S splits into a head, the next superblock's columns, on
     // the call's stream (the next superblock's loop needs it) and a tail, every column after
@@ -530,6 +621,8 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
         a.nb = nb;
         a.group = inblock_fit ? q.group : 0;
         a.gi_outer = 0;
+        a.static_group = stat ? q.group : 0;
+        a.perm = q.perm;
         a.g = g;
         a.scales = q.scales;
         a.zeros = q.zeros;
@@ -537,7 +630,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
         a.ehi = q.ehi + static_cast<size_t>(ebase + i1 - s0) * m;
         a.elo = q.elo + static_cast<size_t>(ebase + i1 - s0) * m;
         a.loss_rows = q.loss_rows;
-        if (!inblock_fit) {
+        if (!inblock_fit && !stat) {
           const bool start = (q.group == -1) ? (i1 == 0) : (i1 % q.group == 0);
           const int gi = (q.group == -1) ? 0 : i1 / q.group;
           if (start) {
@@ -547,8 +640,13 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
           }
           a.gi_outer = gi;
         }
-        GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel, (unsigned)ceil_div(m, RPC),
-                    LOOP_THREADS, loop_smem, a);
+        if (stat) {
+          GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel<true>, (unsigned)ceil_div(m, RPC),
+                      LOOP_THREADS, kLoopSmemStatic, a);
+        } else {
+          GPTQ_LAUNCH(GPTQ_K_QUANT_LOOP, s, column_loop_kernel<false>, (unsigned)ceil_div(m, RPC),
+                      LOOP_THREADS, kLoopSmemDynamic, a);
+        }
         // near: the rest of the superblock, W[:, i2:s1] -= Err_block U[i1:i2, i2:s1]
         if (i1 + nb < s1) launch_lazy_tc(maps, ebase + i1 - s0, i1, nb, i1 + nb, s1, q.st, s, 0);
       }

@@ -25,7 +25,8 @@ __all__ = [
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
     "gptq_kernel_name",
-    "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "workspace",
+    "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "GPTQ_QUANT_STATIC_GROUPS",
+    "workspace",
 ]
 
 GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 3
@@ -34,6 +35,7 @@ GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE = 0, 1, 2
 KERNEL_KINDS = 20
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
+GPTQ_QUANT_STATIC_GROUPS = 1
 
 
 class GptqLibraryError(RuntimeError):
@@ -64,6 +66,9 @@ _SIGS = {
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
                                        _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _sz, _vp]),
+    "gptq_quantize_layer_ex": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
+                                          _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp,
+                                          _vp, _vp, _vp, _vp, _sz, _vp]),
     "gptq_last_error": (_c.c_char_p, []),
     "gptq_status_string": (_c.c_char_p, [_c.c_int]),
     "gptq_abi_version": (_c.c_int, []),
@@ -205,14 +210,19 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional
                         dead: Optional[torch.Tensor], bits: int, group: int, sym: bool,
                         blocksize: int, qweight: torch.Tensor, scales: torch.Tensor,
                         qzeros: torch.Tensor, g_idx: torch.Tensor, loss: torch.Tensor,
-                        ws: Optional[torch.Tensor] = None, stream=None) -> None:
+                        ws: Optional[torch.Tensor] = None, stream=None,
+                        static_groups: bool = False) -> None:
+    """The column loop and packing; ``static_groups`` fits the groups in the original
+    column order before the loop (gptq_quantize_layer_ex, GPTQ_QUANT_STATIC_GROUPS)."""
     m, d = W.shape
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_QUANTIZE, 0, m, d, bits, group), W.device)
-    _check(lib().gptq_quantize_layer(_ptr(W), _dtype_code(W), _ptr(Hinv_chol), _ptr(perm),
-                                     _ptr(dead), m, d, bits, group, int(bool(sym)), blocksize,
-                                     _ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx),
-                                     _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)))
+    flags = GPTQ_QUANT_STATIC_GROUPS if static_groups else 0
+    _check(lib().gptq_quantize_layer_ex(_ptr(W), _dtype_code(W), _ptr(Hinv_chol), _ptr(perm),
+                                        _ptr(dead), m, d, bits, group, int(bool(sym)),
+                                        blocksize, flags, _ptr(qweight), _ptr(scales),
+                                        _ptr(qzeros), _ptr(g_idx), _ptr(loss), _ptr(ws),
+                                        ws.numel(), _stream(stream)))
 
 
 def gptq_profile_enable(on: bool) -> None:

@@ -44,7 +44,7 @@ def unpack_zeros(qzeros: np.ndarray, bits: int, m: int) -> np.ndarray:
 
 
 def check_quantize(W, U, perm, dead, bits, group, sym, gpu, rows=None, check_loss=True,
-                   w_rows_only=False):
+                   w_rows_only=False, static_groups=False):
     """Replay the oracle on (W, U, perm) with the GPU's codes as near-tie hints and check
     every element.  ``gpu`` holds numpy copies of qweight, scales, qzeros, g_idx, loss.
     With ``w_rows_only`` W holds just the sampled ``rows`` (large layers).
@@ -61,14 +61,15 @@ def check_quantize(W, U, perm, dead, bits, group, sym, gpu, rows=None, check_los
     perm_np = np.arange(d) if perm is None else np.asarray(perm, dtype=np.int64)
     hint = dict(codes=codes_sel[:, perm_np], zeros=zeros_gpu[:, sel])
     ref = O.gptq_quantize_layer(W, U, perm_np, dead, bits, group, sym, blocksize=128,
-                                hint=hint, tie_eps=TIE_EPS, pack=False)
+                                hint=hint, tie_eps=TIE_EPS, pack=False,
+                                static_groups=static_groups)
     n_codes = codes_sel.size
     mismatch = int(np.count_nonzero(ref["codes"] != codes_sel))
     zero_mismatch = int(np.count_nonzero(ref["zeros"] != zeros_gpu[:, sel]))
     ties = ref["stats"].get("codes", 0) + ref["stats"].get("zeros", 0)
     srel = float(np.max(np.abs(ref["scales"].astype(np.float64) - scales_gpu[:, sel])
                         / np.maximum(np.abs(ref["scales"].astype(np.float64)), 1e-30)))
-    gidx_ok = np.array_equal(O.group_index(perm_np, group), gpu["g_idx"])
+    gidx_ok = np.array_equal(O.group_index(perm_np, group, static_groups), gpu["g_idx"])
     rep = dict(mismatch=mismatch, zero_mismatch=zero_mismatch, near_ties=ties, n_codes=n_codes,
                scale_rel=srel, g_idx_ok=gidx_ok, loss_ref=ref["loss"], loss_gpu=float(gpu["loss"]))
     assert gidx_ok, "g_idx differs"
@@ -81,7 +82,8 @@ def check_quantize(W, U, perm, dead, bits, group, sym, gpu, rows=None, check_los
     return rep
 
 
-def gpu_quantize(lib_mod, Wt, U32, perm_t, dead_t, bits, group, sym, blocksize=128):
+def gpu_quantize(lib_mod, Wt, U32, perm_t, dead_t, bits, group, sym, blocksize=128,
+                 static_groups=False):
     """Run gptq_quantize_layer on device tensors; returns numpy copies of the outputs."""
     m, d = Wt.shape
     dev = Wt.device
@@ -95,6 +97,6 @@ def gpu_quantize(lib_mod, Wt, U32, perm_t, dead_t, bits, group, sym, blocksize=1
     )
     lib_mod.gptq_quantize_layer(Wt, U32, perm_t, dead_t, bits, group, sym, blocksize,
                                 out["qweight"], out["scales"], out["qzeros"], out["g_idx"],
-                                out["loss"])
+                                out["loss"], static_groups=static_groups)
     torch.cuda.synchronize()
     return {k: to_np(v) for k, v in out.items()}

@@ -54,6 +54,33 @@ def test_quantize_cases(lib, cuda_device, m, d, bits, group, sym, actorder):
     assert rep["n_codes"] == m * d
 
 
+STATIC_CASES = [
+    # (m, d, bits, group, sym): act-order on, static groups
+    (64, 384, 4, 128, False),
+    (96, 288, 3, 32, True),         # ragged last block
+    (64, 640, 4, 256, False),       # groups wider than a block, ragged
+    (128, 512, 2, 16, False),
+    (64, 256, 4, -1, False),        # one group per row: the dynamic mode
+]
+
+
+@pytest.mark.parametrize("m,d,bits,group,sym", STATIC_CASES)
+def test_quantize_static_groups(lib, cuda_device, m, d, bits, group, sym):
+    """Static groups (fixed in the original order before the loop) against the oracle."""
+    rng = np.random.default_rng(m * 5 + d + bits + 3)
+    W, U32, perm, dead = _inputs(rng, m, d, actorder=True, dead=(5,))
+    Wt = torch.from_numpy(W).to(cuda_device)
+    gpu = gpu_quantize(lib, Wt, torch.from_numpy(U32).to(cuda_device),
+                       torch.from_numpy(perm.astype(np.int32)).to(cuda_device),
+                       torch.from_numpy(dead.astype(np.uint8)).to(cuda_device),
+                       bits, group, sym, static_groups=True)
+    rep = check_quantize(W.astype(np.float64), U32.astype(np.float64), perm, dead, bits, group,
+                         sym, gpu, static_groups=True)
+    assert rep["n_codes"] == m * d
+    if group != -1:
+        assert np.array_equal(gpu["g_idx"], np.arange(d) // group)
+
+
 def test_quantize_bf16_weights(lib, cuda_device):
     rng = np.random.default_rng(11)
     W, U32, perm, dead = _inputs(rng, 64, 512)
