@@ -199,7 +199,8 @@ def run_ours(args, world, rank, local):
     X = torch.cat([make_tokens_chunk(cfg, i, dev, mult) for i in range(nch)])
     W = make_weight(cfg, dev)
     eng = LayerEngine(m, d, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
-                      cfg.blocksize, max_chunk_tokens=n, device=dev)
+                      cfg.blocksize, max_chunk_tokens=n, device=dev,
+                      static_groups=args.static_groups)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -303,7 +304,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": f"{cfg.name}: d_out={m} d_in={d}, {n} {str(cfg.x_dtype)[6:]} "
                                    f"calibration tokens, {cfg.bits}-bit "
                                    f"{'sym' if cfg.sym else 'asym'} group {cfg.group}, "
-                                   f"act-order {'on' if cfg.actorder else 'off'}, damp {cfg.damp}",
+                                   f"act-order {'on' if cfg.actorder else 'off'}, damp {cfg.damp}"
+                                   + (", static groups" if args.static_groups else ""),
                        "per_rank": "one independent layer replica per GPU",
                        "l2": "flushed between steps (256 MiB write, untimed); X > L2",
                        "step": "hessian_accumulate(all tokens) + prepare + quantize_layer",
@@ -335,7 +337,8 @@ def run_e2e(args, cfg, X, W, eng, dist, dev, world):
     out = QuantizedLayer(*(t.cpu().pin_memory() for t in
                            (eng.qweight, eng.scales, eng.qzeros, eng.g_idx, eng.perm, eng.loss)))
     e_eng = LayerEngine(m, d, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
-                        cfg.blocksize, max_chunk_tokens=chunk, device=dev)
+                        cfg.blocksize, max_chunk_tokens=chunk, device=dev,
+                        static_groups=args.static_groups)
     quantize_layer_from_host(e_eng, Wh, x_chunks, out)          # warm-up
     e_steps = max(1, min(args.steps, 5))
     barrier(dist, dev)
@@ -449,6 +452,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the calibration token count (small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--static-groups", action="store_true",
+                    help="groups fixed in the original column order before the loop")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()

@@ -186,6 +186,12 @@ __device__ __forceinline__ void cp_async16(float4* dst, const float4* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+
 // The column loop gives each output row LPR lanes; lane t holds the block's LW = 128 / LPR
 // columns LW t .. LW t + LW - 1 in registers for the whole block.  Sub-block b (columns
 // LW b ..) is quantised by lane b, column after column: the owner rounds its column,
@@ -342,7 +348,7 @@ __device__ __forceinline__ void loop_columns(float (&w)[LW], float (&code_r)[LW]
 // Shared memory of the loop: the U layout, the staging of codes and bf16 error halves,
 // and with static groups the per-column scale, zero and reciprocal of each row.
 constexpr int kLoopSmemDynamic = kUlayFloats * 4 + BLK * RPC * (1 + 2 + 2);
-constexpr int kLoopSmemStatic = kLoopSmemDynamic + 3 * BLK * RPC * 4;
+constexpr int kLoopSmemStatic = kLoopSmemDynamic + 3 * BLK * RPC * 4 + BLK * 4;
 
 template <bool STATIC>
 __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArgs a) {
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   uint8_t* codes_s = reinterpret_cast<uint8_t*>(smem_f + kUlayFloats);               // [128][RPC]
   __nv_bfloat16* ehi_s = reinterpret_cast<__nv_bfloat16*>(codes_s + BLK * RPC);      // [128][RPC]
   __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][RPC]
-  float* sz_s = reinterpret_cast<float*>(elo_s + BLK * RPC);  // static groups: [3][128][RPC]
+  float* sz_s = reinterpret_cast<float*>(elo_s + BLK * RPC);  // static: [3][128][RPC], [128]
   const int i1 = a.i1, nb = a.nb;
   {
     const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
@@ -380,21 +386,35 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   }
   float s = 1.0f, z = 0.0f;
   if constexpr (STATIC) {
-    // each column's grid: the row's scale and zero of the original column's group
-    const int r0 = blockIdx.x * RPC;
-    for (int e = threadIdx.x; e < BLK * RPC; e += blockDim.x) {
-      const int q = e / RPC, j = e % RPC;
-      float sv = 1.0f, zv = 0.0f;
-      if (q < nb && r0 + j < a.m) {
-        const int c = a.perm ? a.perm[i1 + q] : i1 + q;
-        const size_t o = static_cast<size_t>(c / a.static_group) * a.m + r0 + j;
-        sv = a.scales[o];
-        zv = static_cast<float>(a.zeros[o]);
-      }
-      sz_s[e] = sv;
-      sz_s[BLK * RPC + e] = zv;
-      sz_s[2 * BLK * RPC + e] = __frcp_rn(sv);
+    // each column's grid: the row's scale and zero of the original column's group.  The
+    // columns' groups go to shared memory first (one load per thread), then every
+    // thread gathers its row's scales and zeros with many loads in flight.
+    static_assert(LOOP_THREADS == BLK && RPC == 32, "static-group staging layout");
+    int* gcol_s = reinterpret_cast<int*>(sz_s + 3 * BLK * RPC);  // [128]
+    {
+      const int q = threadIdx.x;
+      gcol_s[q] = (q < nb) ? (a.perm ? a.perm[i1 + q] : i1 + q) / a.static_group : 0;
     }
+    __syncthreads();
+    const int r0 = blockIdx.x * RPC;
+    const int j = threadIdx.x % RPC;            // row within the CTA
+    const bool row_ok = r0 + j < a.m;
+    constexpr int QS = LOOP_THREADS / RPC;      // columns per pass
+    // asynchronous 4-byte copies (the zero's int32 bits for now), in flight with the U
+    // layout's; padding columns and rows take s = 1, z = 0
+    for (int q = threadIdx.x / RPC; q < BLK; q += QS) {
+      float* sd = sz_s + q * RPC + j;
+      float* zd = sz_s + (BLK + q) * RPC + j;
+      if (q < nb && row_ok) {
+        const size_t o = static_cast<size_t>(gcol_s[q]) * a.m + r0 + j;
+        cp_async4(sd, a.scales + o);
+        cp_async4(zd, reinterpret_cast<const float*>(a.zeros + o));
+      } else {
+        *sd = 1.0f;
+        *reinterpret_cast<int32_t*>(zd) = 0;
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   } else if (a.group == 0 && active) {
     s = a.scales[static_cast<size_t>(a.gi_outer) * a.m + r];
     z = static_cast<float>(a.zeros[static_cast<size_t>(a.gi_outer) * a.m + r]);
@@ -404,6 +424,15 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   const double loss_prev = (active && t == 0) ? a.loss_rows[r] : 0.0;
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
+  if constexpr (STATIC) {
+    // zeros to float and the scales' reciprocals, in place
+    for (int e = threadIdx.x; e < BLK * RPC; e += blockDim.x) {
+      const float sv = sz_s[e];
+      sz_s[BLK * RPC + e] = static_cast<float>(reinterpret_cast<const int32_t*>(sz_s)[BLK * RPC + e]);
+      sz_s[2 * BLK * RPC + e] = __frcp_rn(sv);
+    }
+    __syncthreads();
+  }
   // a block's share of the loss (at most 32 terms per lane) is summed in float32 and
   // added to the row's float64 total once per block; FP64 arithmetic inside the step
   // chain would serialise on this part's low FP64 rate

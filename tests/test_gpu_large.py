@@ -117,12 +117,14 @@ def test_prepare_down_proj_14336(lib, cuda_device):
     assert np.allclose(np.tril(U_np, -1), 0.0)
 
 
-@pytest.mark.parametrize("name,rows", [
-    ("down_proj_4096x14336", 64),     # symmetric, 4-bit, group 128
-    ("block_gateup_w3", 48),          # 3-bit, d_out = 28672
-    ("down_proj_8192x28672", 32),
+@pytest.mark.parametrize("name,rows,static", [
+    ("down_proj_4096x14336", 64, False),     # symmetric, 4-bit, group 128
+    ("block_gateup_w3", 48, False),          # 3-bit, d_out = 28672
+    ("down_proj_8192x28672", 32, False),
+    ("q_proj_4096x4096", 64, True),          # static groups
+    ("down_proj_4096x14336", 32, True),
 ])
-def test_quantize_large(lib, cuda_device, name, rows):
+def test_quantize_large(lib, cuda_device, name, rows, static):
     """The column loop and packing at full size with a drawn inverse Cholesky factor and
     permutation (any positive-diagonal upper-triangular U is the factor of some positive
     definite Hessian); sampled output rows are checked exactly against the oracle."""
@@ -131,12 +133,13 @@ def test_quantize_large(lib, cuda_device, name, rows):
     W = make_weight(cfg, dev)
     U = make_upper_factor(d, cfg.seed, dev)
     perm = make_permutation(d, cfg.seed, dev)
-    gpu = gpu_quantize(lib, W, U, perm, None, cfg.bits, cfg.group, cfg.sym)
+    gpu = gpu_quantize(lib, W, U, perm, None, cfg.bits, cfg.group, cfg.sym,
+                       static_groups=static)
     sel = np.sort(np.random.default_rng(cfg.seed).choice(m, rows, replace=False))
     Wsel = to_np(W[torch.from_numpy(sel).to(dev)])
     del W
     Un = to_np(U)
     del U
     rep = check_quantize(Wsel, Un, to_np(perm), None, cfg.bits, cfg.group, cfg.sym, gpu,
-                         rows=sel, check_loss=False, w_rows_only=True)
+                         rows=sel, check_loss=False, w_rows_only=True, static_groups=static)
     assert rep["n_codes"] == rows * d
