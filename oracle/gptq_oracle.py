@@ -62,7 +62,7 @@ __all__ = [
     "gptq_sweep", "gptq_sweep_obs",
     "gptq_prepare", "gptq_quantize_layer", "gptq_layer",
     "group_index", "static_group_fit", "pack_bitstream", "unpack_bitstream",
-    "checkpoint_bytes",
+    "checkpoint_bytes", "dequantize", "dequant_matmul",
     "quadratic_loss", "rtn_quantize",
 ]
 
@@ -460,6 +460,36 @@ def unpack_bitstream(words: np.ndarray, bits: int, L: int) -> np.ndarray:
     stream = ((words[..., :, None] >> np.arange(32)) & 1).reshape(*lead, nw * 32)
     stream = stream[..., :L * bits].reshape(*lead, L, bits)
     return (stream << np.arange(bits)).sum(axis=-1)
+
+
+def dequantize(qweight, scales, qzeros, g_idx, bits: int) -> np.ndarray:
+    """The weights a packed checkpoint stands for, ``[d_out, d_in]`` float64.
+
+    "GPTQ Architecture, in depth", "Packing, tooling and serving": a serving kernel
+    unpacks each code and dequantises it with its group's scale and zero point; the group
+    of original column c is g_idx[c]: w_hat[r, c] = s[g, r] * (code[r, c] - z[g, r]),
+    g = g_idx[c] (the page's Q = scale * (q - zero)).  ``qweight`` ``[bits*d/32, m]`` and
+    ``qzeros`` ``[G, bits*m/32]`` are little-endian bit streams as ``pack_bitstream``
+    writes them.
+    """
+    qweight = np.asarray(qweight)
+    m = qweight.shape[1]
+    d = qweight.shape[0] * 32 // bits
+    codes = unpack_bitstream(qweight.T, bits, d)                    # [m, d]
+    zeros = unpack_bitstream(np.asarray(qzeros), bits, m)           # [G, m]
+    g = np.asarray(g_idx, dtype=np.int64)
+    s = np.asarray(scales, dtype=F64)[g].T                          # [m, d]
+    z = zeros[g].T.astype(F64)
+    return s * (codes.astype(F64) - z)
+
+
+def dequant_matmul(x, qweight, scales, qzeros, g_idx, bits: int) -> np.ndarray:
+    """y = x W_hat^T, ``x`` ``[n, d_in]``: the product a W4A16-style serving kernel computes
+    from the packed checkpoint ("GPTQ Architecture, in depth", "Packing, tooling and
+    serving"; "Same Ruler, Smarter Placement: GPTQ", section 1.5: the layer output the
+    method preserves is W X)."""
+    W = dequantize(qweight, scales, qzeros, g_idx, bits)
+    return np.asarray(x, dtype=F64) @ W.T
 
 
 def checkpoint_bytes(d_out: int, d_in: int, group: int) -> int:

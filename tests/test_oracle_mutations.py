@@ -51,6 +51,9 @@ MUTATIONS = {
     "static_fit_on_permuted": ("sc, ze = static_group_fit(W, group, bits, sym,",
                                "sc, ze = static_group_fit(W[:, perm], group, bits, sym,"),
     "static_g_idx_permuted": ("if static and group != -1:", "if False:"),
+    "dequant_zero_dropped": ("return s * (codes.astype(F64) - z)", "return s * codes.astype(F64)"),
+    "dequant_scale_of_position": ("s = np.asarray(scales, dtype=F64)[g].T",
+                                  "s = np.asarray(scales, dtype=F64)[np.arange(g.size) * len(scales) // g.size].T"),
 }
 
 

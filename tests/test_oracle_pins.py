@@ -429,12 +429,37 @@ def pin_static_groups(O):
         assert np.allclose(r["loss_rows"], ref["loss_rows"], rtol=1e-10)
 
 
+def pin_dequantize(O):
+    """Unpacking the checkpoint reproduces the quantizer's own dequantised weights.
+
+    The column loop keeps what = s (code - z) for every weight (Q, processing order);
+    ``dequantize`` rebuilds it from qweight / scales / qzeros / g_idx alone, so the two
+    agree exactly (in original column order) for dynamic and static groups, every width
+    and act-order on; ``dequant_matmul`` is x times that matrix transposed.
+    """
+    rng = np.random.default_rng(43)
+    m, d = 32, 64
+    for bits, group, sym, static in [(4, 16, False, False), (3, 32, True, False),
+                                     (2, 16, False, True), (8, -1, False, False),
+                                     (4, 32, True, True)]:
+        W, H, _ = _small_layer(rng, m, d)
+        out = O.gptq_layer(W, H, bits, group, sym, actorder=True, static_groups=static)
+        Qo = np.empty_like(out["Q"])
+        Qo[:, out["perm"]] = out["Q"]
+        Wh = O.dequantize(out["qweight"], out["scales"], out["qzeros"], out["g_idx"], bits)
+        assert np.array_equal(Wh, Qo), (bits, group, sym, static)
+        x = rng.standard_normal((3, d))
+        y = O.dequant_matmul(x, out["qweight"], out["scales"], out["qzeros"], out["g_idx"],
+                             bits)
+        assert np.allclose(y, x @ Qo.T, rtol=1e-13, atol=0)
+
+
 PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
         pin_cholesky_2x2, pin_cholesky_general, pin_obs_equals_cholesky,
         pin_blocked_equals_unblocked, pin_loss_identity, pin_brute_force_optimum,
         pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
         pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
-        pin_format_roundtrip, pin_static_groups]
+        pin_format_roundtrip, pin_static_groups, pin_dequantize]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
