@@ -50,7 +50,9 @@ typedef enum {
 
 typedef enum { GPTQ_F32 = 0, GPTQ_BF16 = 1 } gptq_dtype;
 
-typedef enum { GPTQ_OP_HESSIAN = 0, GPTQ_OP_PREPARE = 1, GPTQ_OP_QUANTIZE = 2 } gptq_op;
+typedef enum {
+  GPTQ_OP_HESSIAN = 0, GPTQ_OP_PREPARE = 1, GPTQ_OP_QUANTIZE = 2, GPTQ_OP_DEQUANT_MATMUL = 3
+} gptq_op;
 
 /*
  * gptq_workspace_size -- bytes of workspace the call `op` wants for these sizes on the
@@ -238,6 +240,36 @@ gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_
                                    int32_t* g_idx, double* loss, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/*
+ * gptq_dequant_matmul -- y = x W_hat^T from the packed checkpoint, the product a W4A16-
+ * style serving kernel computes ("GPTQ Architecture, in depth", "Packing, tooling and
+ * serving": codes are unpacked and dequantised with their group's scale and zero point
+ * just before the multiply):
+ *   y[t, r] = sum_c x[t, c] * scales[g, r] * (code[r, c] - zero[g, r]),  g = g_idx[c].
+ * It reads exactly what gptq_quantize_layer(_ex) writes.
+ *
+ * x        device [n, d_in] row-major, `xdtype` (bfloat16 or float32).
+ * n        tokens, >= 0 (0: nothing is written).
+ * d_in     >= 32, multiple of 32;  d_out >= 0, multiple of 32.
+ * bits     2, 3, 4 or 8.
+ * qweight  device int32 [bits*d_in/32, d_out], scales device float32 [G, d_out], qzeros
+ *          device int32 [G, bits*d_out/32], g_idx device int32 [d_in] with values in
+ *          [0, G): the layout gptq_quantize_layer documents.
+ * G        number of groups (rows of scales).
+ * y        device float32 [n, d_out], out.
+ * ws       device workspace of gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, ...) bytes
+ *          (256-byte aligned; holds the status word).
+ * Accumulation is float32; the result does not depend on timing (the d_in slices are
+ * added in a fixed order).
+ * Errors: INVALID_ARG (arguments; a g_idx value outside [0, G), reported after the
+ *         kernel, which then read group 0 for it), UNSUPPORTED (bits, sizes), CUDA.
+ */
+gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_in,
+                                int32_t d_out, int bits, const int32_t* qweight,
+                                const float* scales, const int32_t* qzeros,
+                                const int32_t* g_idx, int32_t G, float* y, void* ws,
+                                size_t ws_bytes, void* stream);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* gptq_last_error(void);
 
@@ -264,7 +296,7 @@ typedef enum {
   GPTQ_K_POTRF_PANEL, GPTQ_K_POTRF_TRSM, GPTQ_K_POTRF_UPDATE,
   GPTQ_K_TRTRI_DIAG, GPTQ_K_TRTRI_UPDATE, GPTQ_K_PREP_REVERSE,
   GPTQ_K_QUANT_GATHER, GPTQ_K_QUANT_FIT, GPTQ_K_QUANT_LOOP, GPTQ_K_QUANT_LAZY,
-  GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT,
+  GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT, GPTQ_K_DEQUANT_MATMUL,
   GPTQ_K_COUNT
 } gptq_kernel_kind;
 

@@ -232,6 +232,8 @@ size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, in
     case GPTQ_OP_QUANTIZE:
       if (d_out < 0 || !group_supported(group)) return 0;
       return quantize_ws_bytes(d_out, d_in, groups_of(d_in, group));
+    case GPTQ_OP_DEQUANT_MATMUL:
+      return 256;  // the status word
     default:
       return 0;
   }
@@ -385,6 +387,37 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
                                 ws_bytes, stream);
 }
 
+gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_in,
+                                int32_t d_out, int bits, const int32_t* qweight,
+                                const float* scales, const int32_t* qzeros,
+                                const int32_t* g_idx, int32_t G, float* y, void* ws,
+                                size_t ws_bytes, void* stream) {
+  return guarded([&] {
+    require(n >= 0 && d_in > 0 && d_out >= 0 && G > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_dequant_matmul: need n >= 0, d_in > 0, d_out >= 0, G > 0");
+    require(xdtype == GPTQ_F32 || xdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
+            "gptq_dequant_matmul: xdtype must be GPTQ_F32 or GPTQ_BF16");
+    require(bits == 2 || bits == 3 || bits == 4 || bits == 8, GPTQ_ERR_UNSUPPORTED,
+            "gptq_dequant_matmul: bits must be 2, 3, 4 or 8");
+    require(d_in % 32 == 0 && d_out % 32 == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_dequant_matmul: d_in and d_out must be multiples of 32");
+    require(ws != nullptr && aligned(ws, 256) && ws_bytes >= sizeof(DevStatus),
+            GPTQ_ERR_INVALID_ARG, "gptq_dequant_matmul: null, unaligned or too small ws");
+    require(n == 0 || d_out == 0 ||
+                (x != nullptr && qweight != nullptr && scales != nullptr && qzeros != nullptr &&
+                 g_idx != nullptr && y != nullptr),
+            GPTQ_ERR_INVALID_ARG, "gptq_dequant_matmul: null input or output");
+    if (n == 0 || d_out == 0) return;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsCarver wc(ws, ws_bytes);
+    DevStatus* st = wc.take<DevStatus>(1);
+    begin_call(st, s);
+    launch_dequant_matmul(x, xdtype == GPTQ_BF16, n, d_in, d_out, bits, G, qweight, scales,
+                          qzeros, g_idx, y, st, s);
+    raise_device_status(finish_call(st, s), "gptq_dequant_matmul");
+  });
+}
+
 const char* gptq_last_error(void) { return last_error().c_str(); }
 
 const char* gptq_status_string(int status) {
@@ -415,7 +448,7 @@ const char* gptq_kernel_name(int kind) {
       "syrk_tc", "syrk_simt", "syrk_reduce", "prep_diag", "prep_rank", "prep_mirror",
       "prep_gather", "potrf_panel", "potrf_trsm", "potrf_update", "trtri_diag", "trtri_update",
       "prep_reverse", "quant_gather", "quant_fit", "quant_loop", "quant_lazy", "quant_pack",
-      "quant_loss", "quant_split"};
+      "quant_loss", "quant_split", "dequant_matmul"};
   if (kind < 0 || kind >= GPTQ_K_COUNT) return "";
   return names[kind];
 }

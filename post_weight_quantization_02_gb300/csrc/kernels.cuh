@@ -64,6 +64,11 @@ struct QuantArgs {
 };
 void launch_quantize(const QuantArgs& q, cudaStream_t s);
 
+// dequant_matmul.cu: y[n, m] = x[n, d] W_hat^T from the packed checkpoint
+void launch_dequant_matmul(const void* x, bool x_bf16, int64_t n, int d, int m, int bits, int G,
+                           const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                           const int32_t* g_idx, float* y, DevStatus* st, cudaStream_t s);
+
 // gemm_tc.cu: C[i][j] = beta C[i][j] + alpha sum_{k<128} A[a_row0+i][a_k0+k]
 // B[b_row0+j][b_k0+k], float32-accurate (tf32 x3); maps from make_gemm_map.  pdl: launched
 // as a programmatic dependent of the kernel before it in the stream.

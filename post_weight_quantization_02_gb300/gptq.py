@@ -19,6 +19,7 @@ __all__ = [
     "GPTQ_OK", "GPTQ_ERR_INVALID_ARG", "GPTQ_ERR_UNSUPPORTED", "GPTQ_ERR_NOT_PD",
     "GPTQ_ERR_NONFINITE", "GPTQ_ERR_CUDA", "GPTQ_ERR_TIMEOUT", "GPTQ_ERR_WORKSPACE",
     "GPTQ_F32", "GPTQ_BF16", "GPTQ_OP_HESSIAN", "GPTQ_OP_PREPARE", "GPTQ_OP_QUANTIZE",
+    "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul",
     "GptqError", "GptqLibraryError", "lib", "library_path",
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
     "gptq_hessian_status", "gptq_prepare", "gptq_quantize_layer",
@@ -32,8 +33,8 @@ __all__ = [
 GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 3
 GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 6, 7
 GPTQ_F32, GPTQ_BF16 = 0, 1
-GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE = 0, 1, 2
-KERNEL_KINDS = 20
+GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE, GPTQ_OP_DEQUANT_MATMUL = 0, 1, 2, 3
+KERNEL_KINDS = 21
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
 GPTQ_QUANT_STATIC_GROUPS = 1
 
@@ -69,6 +70,8 @@ _SIGS = {
     "gptq_quantize_layer_ex": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
                                           _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp,
                                           _vp, _vp, _vp, _vp, _sz, _vp]),
+    "gptq_dequant_matmul": (_c.c_int, [_vp, _c.c_int, _i64, _i32, _i32, _c.c_int, _vp, _vp,
+                                       _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
     "gptq_last_error": (_c.c_char_p, []),
     "gptq_status_string": (_c.c_char_p, [_c.c_int]),
     "gptq_abi_version": (_c.c_int, []),
@@ -223,6 +226,26 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional
                                         blocksize, flags, _ptr(qweight), _ptr(scales),
                                         _ptr(qzeros), _ptr(g_idx), _ptr(loss), _ptr(ws),
                                         ws.numel(), _stream(stream)))
+
+
+def gptq_dequant_matmul(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                        qzeros: torch.Tensor, g_idx: torch.Tensor, bits: int,
+                        y: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """y = x W_hat^T from the packed checkpoint (x [n, d_in] bf16 or fp32; y [n, d_out])."""
+    if x.dim() != 2:
+        raise ValueError("x must be [n, d_in]")
+    n, d = x.shape
+    m = qweight.shape[1]
+    if y is None:
+        y = torch.empty(n, m, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, 0, m, d, bits, -1), x.device)
+    _check(lib().gptq_dequant_matmul(_ptr(x) if x.numel() else None, _dtype_code(x), n, d, m,
+                                     bits, _ptr(qweight), _ptr(scales), _ptr(qzeros),
+                                     _ptr(g_idx), scales.shape[0], _ptr(y), _ptr(ws),
+                                     ws.numel(), _stream(stream)))
+    return y
 
 
 def gptq_profile_enable(on: bool) -> None:

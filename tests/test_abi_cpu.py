@@ -103,3 +103,35 @@ def test_prepare_and_hessian_argument_checks():
     assert lib.gptq_hessian_accumulate(None, ctypes.byref(n), P, 1, 10, 128, P, 1 << 30, None) \
         == G.GPTQ_ERR_INVALID_ARG
     assert n.value == 0
+
+
+def _call_dq(**kw):
+    a = dict(x=P, xt=1, n=4, d=256, m=64, bits=4, qw=P, sc=P, qz=P, gi=P, G=2, y=P, ws=P,
+             wsb=256)
+    a.update(kw)
+    return G.lib().gptq_dequant_matmul(a["x"], a["xt"], a["n"], a["d"], a["m"], a["bits"],
+                                       a["qw"], a["sc"], a["qz"], a["gi"], a["G"], a["y"],
+                                       a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=5), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(d=250), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(m=48), G.GPTQ_ERR_UNSUPPORTED),
+    (dict(xt=9), G.GPTQ_ERR_INVALID_ARG),
+    (dict(G=0), G.GPTQ_ERR_INVALID_ARG),
+    (dict(n=-1), G.GPTQ_ERR_INVALID_ARG),
+    (dict(ws=P + 4), G.GPTQ_ERR_INVALID_ARG),
+    (dict(wsb=8), G.GPTQ_ERR_INVALID_ARG),
+    (dict(y=None), G.GPTQ_ERR_INVALID_ARG),
+])
+def test_dequant_matmul_argument_checks(kw, status):
+    assert _call_dq(**kw) == status
+
+
+def test_quantize_flags_and_dequant_workspace():
+    assert G.gptq_workspace_size(G.GPTQ_OP_DEQUANT_MATMUL, 0, 64, 256, 4, -1) >= 256
+    # an unknown quantize flag is rejected before anything reaches CUDA
+    assert G.lib().gptq_quantize_layer_ex(P, 1, P, None, None, 64, 256, 4, 128, 0, 128, 2, P,
+                                          P, P, P, P, P, 1 << 30, None) == \
+        G.GPTQ_ERR_INVALID_ARG

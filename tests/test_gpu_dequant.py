@@ -1,0 +1,83 @@
+"""Parity of gptq_dequant_matmul (through the C ABI) with the float64 oracle: y = x W_hat^T
+from the packed checkpoint, for checkpoints the oracle and the GPU quantizer wrote."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as O
+from tests.parity import gpu_quantize, rel_fro, to_np
+from workloads import CONFIGS, make_permutation, make_upper_factor, make_weight
+
+pytestmark = pytest.mark.gpu
+
+# float32 products and sums over d_in terms against float64: the relative Frobenius error
+# is about sqrt(d_in) float32 epsilons on random data
+Y_REL_FRO = 1e-5
+
+
+def _oracle_checkpoint(rng, m, d, bits, group, sym, static):
+    X = rng.standard_normal((4 * d, d)) * np.exp(rng.standard_normal(d))
+    W = rng.standard_normal((m, d)) * 0.02
+    return O.gptq_layer(W, O.hessian(X), bits, group, sym, actorder=True, static_groups=static)
+
+
+def _dev(a, dev, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return t if dtype is None else t.to(dtype)
+
+
+@pytest.mark.parametrize("m,d,bits,group,sym,static,n,xdt", [
+    (96, 256, 4, 32, False, False, 1, torch.bfloat16),
+    (96, 256, 4, 32, False, False, 5, torch.bfloat16),
+    (64, 384, 3, 64, True, True, 16, torch.bfloat16),
+    (160, 512, 2, -1, False, False, 11, torch.float32),
+    (32, 1024, 8, 128, False, True, 8, torch.float32),
+])
+def test_dequant_matmul_small(lib, cuda_device, m, d, bits, group, sym, static, n, xdt):
+    rng = np.random.default_rng(m + d + bits + n)
+    ck = _oracle_checkpoint(rng, m, d, bits, group, sym, static)
+    x = _dev(rng.standard_normal((n, d)).astype(np.float32), cuda_device, xdt)
+    y = lib.gptq_dequant_matmul(x, _dev(ck["qweight"], cuda_device),
+                                _dev(ck["scales"], cuda_device), _dev(ck["qzeros"], cuda_device),
+                                _dev(ck["g_idx"], cuda_device), bits)
+    torch.cuda.synchronize()
+    ref = O.dequant_matmul(to_np(x).astype(np.float64), ck["qweight"], ck["scales"],
+                           ck["qzeros"], ck["g_idx"], bits)
+    assert y.shape == (n, m)
+    assert rel_fro(to_np(y), ref) <= Y_REL_FRO
+
+
+def test_dequant_matmul_bad_group_index(lib, cuda_device):
+    """A g_idx value outside the scales is reported (the kernel reads group 0 for it)."""
+    rng = np.random.default_rng(3)
+    ck = _oracle_checkpoint(rng, 64, 256, 4, 128, False, False)
+    gi = ck["g_idx"].copy()
+    gi[17] = 5                                            # G = 2
+    x = _dev(rng.standard_normal((2, 256)).astype(np.float32), cuda_device, torch.bfloat16)
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_dequant_matmul(x, _dev(ck["qweight"], cuda_device),
+                                _dev(ck["scales"], cuda_device),
+                                _dev(ck["qzeros"], cuda_device), _dev(gi, cuda_device), 4)
+    assert e.value.status == lib.GPTQ_ERR_INVALID_ARG
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("static", [False, True])
+def test_dequant_matmul_q_proj(lib, cuda_device, static):
+    """The q_proj checkpoint as the GPU quantizer writes it, 8 tokens, against the oracle."""
+    cfg = CONFIGS["q_proj_4096x4096"]
+    dev, m, d = cuda_device, cfg.d_out, cfg.d_in
+    W = make_weight(cfg, dev)
+    U = make_upper_factor(d, cfg.seed, dev)
+    perm = make_permutation(d, cfg.seed, dev)
+    ck = gpu_quantize(lib, W, U, perm, None, cfg.bits, cfg.group, cfg.sym, static_groups=static)
+    del W, U
+    rng = np.random.default_rng(7)
+    x = _dev(rng.standard_normal((8, d)).astype(np.float32), dev, torch.bfloat16)
+    y = lib.gptq_dequant_matmul(x, _dev(ck["qweight"], dev), _dev(ck["scales"], dev),
+                                _dev(ck["qzeros"], dev), _dev(ck["g_idx"], dev), cfg.bits)
+    torch.cuda.synchronize()
+    ref = O.dequant_matmul(to_np(x).astype(np.float64), ck["qweight"], ck["scales"],
+                           ck["qzeros"], ck["g_idx"], cfg.bits)
+    assert rel_fro(to_np(y), ref) <= Y_REL_FRO
