@@ -440,6 +440,90 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_dequant(args, world, rank, local):
+    """The packed checkpoint's consumer, y = x W_hat^T (gptq_dequant_matmul), on the layer
+    of ``--config`` quantized by the library: one JSON line per token count.  HBM-bound:
+    the algorithmic bytes are the packed weights, scales, zeros and g_idx plus x and y;
+    L2 is flushed before every launch (the checkpoint is smaller than L2)."""
+    import torch
+    from post_weight_quantization_02_gb300 import gptq as G
+    from workloads import CONFIGS, make_permutation, make_upper_factor, make_weight
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the engine has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    cfg = CONFIGS[args.config]
+    m, d, bits = cfg.d_out, cfg.d_in, cfg.bits
+    Gn = 1 if cfg.group == -1 else -(-d // cfg.group)
+    W = make_weight(cfg, dev)
+    U = make_upper_factor(d, cfg.seed, dev)
+    perm = make_permutation(d, cfg.seed, dev)
+    qw = torch.empty(bits * d // 32, m, dtype=torch.int32, device=dev)
+    sc = torch.empty(Gn, m, dtype=torch.float32, device=dev)
+    qz = torch.empty(Gn, bits * m // 32, dtype=torch.int32, device=dev)
+    gi = torch.empty(d, dtype=torch.int32, device=dev)
+    loss = torch.empty((), dtype=torch.float64, device=dev)
+    G.gptq_quantize_layer(W, U, perm, None, bits, cfg.group, cfg.sym, cfg.blocksize, qw, sc, qz,
+                          gi, loss, static_groups=args.static_groups)
+    del W, U
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ws = G.workspace(G.gptq_workspace_size(G.GPTQ_OP_DEQUANT_MATMUL, 0, m, d, bits, -1), dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm, _, _, peak_src = measured_peaks()
+    ckpt_bytes = (qw.numel() + qz.numel() + gi.numel()) * 4 + sc.numel() * 4
+    for n in (1, 8, 16):
+        x = torch.randn(n, d, device=dev).to(torch.bfloat16)
+        y = torch.empty(n, m, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            G.gptq_dequant_matmul(x, qw, sc, qz, gi, bits, y, ws)
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        # the kernel's own CUDA-event time (library tracing of this kind only) and the
+        # whole call's (status word cleared and read back, stream synchronised)
+        G.gptq_profile_reset()
+        G.gptq_profile_select([G.GPTQ_K_DEQUANT_MATMUL])
+        G.gptq_profile_enable(True)
+        with ClockSampler(dev.index) as clocks:
+            barrier(dist, dev)
+            for i in range(args.steps):
+                flush.fill_(float(i))          # cold L2 for every launch (not timed)
+                starts[i].record(stream)
+                G.gptq_dequant_matmul(x, qw, sc, qz, gi, bits, y, ws)
+                stops[i].record(stream)
+            torch.cuda.synchronize()
+            barrier(dist, dev)
+        G.gptq_profile_enable(False)
+        G.gptq_profile_select(None)
+        kt, kc = G.gptq_profile_read(G.GPTQ_K_DEQUANT_MATMUL)
+        us = max_over_ranks(dist, kt / max(kc, 1) * 1e3, dev)
+        call_us = max_over_ranks(dist, statistics.mean(a.elapsed_time(b) for a, b in
+                                                        zip(starts, stops)) * 1e3, dev)
+        nbytes = ckpt_bytes + x.numel() * 2 + y.numel() * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        if rank == 0:
+            print(json.dumps({
+                "metric": "dequant-matmul of the packed checkpoint (us per launch)",
+                "value": round(us, 3), "unit": "us", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16 x, int codes, f32 accumulate",
+                "data": "synthetic (the library's own checkpoint of a seeded layer)",
+                "config": {"workload": f"{cfg.name}: y[{n}, {m}] = x[{n}, {d}] W_hat^T, "
+                                       f"{bits}-bit group {cfg.group}"
+                                       + (" static groups" if args.static_groups else
+                                          " act-order groups"),
+                           "l2": "flushed before every launch",
+                           "call_us": round(call_us, 3)},
+                "clocks": clocks.summary(),
+                "roofline": {"bound": "hbm", "kernel": "dequant_matmul", "achieved": round(gbs, 1),
+                             "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                             "peak_source": f"{peak_src} HBM copy",
+                             "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+            }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,11 +538,15 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--static-groups", action="store_true",
                     help="groups fixed in the original column order before the loop")
+    ap.add_argument("--dequant-matmul", action="store_true",
+                    help="measure the packed checkpoint's consumer instead of the layer path")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.dequant_matmul:
+        run_dequant(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -7,12 +7,14 @@
 // the packing end to end.
 //
 // Design: one thread per output row; the row's packed words are read coalesced across
-// the CTA's 128 rows (qweight is [bits*d/32, m]), 32 codes at a time from `bits` words
-// with compile-time shifts; the scale and zero are reloaded only when the column's group
-// changes (once per group with static groups, often with act-order groups).  d_in is
-// split over the 8 CTAs of a cluster, and CTA 0 adds the 8 partial sums in rank order
-// from the others' shared memory, so the result does not depend on timing.  The kernel
-// is bound by the packed weight bytes (HBM) at decode batch sizes.
+// the CTA's 128 rows (qweight is [bits*d/32, m]), a 128-column chunk at a time with the
+// next chunk's loads in flight, and decoded with compile-time shifts.  A 32-column run
+// whose columns share one group (every run with static groups) uses one scale and zero;
+// other runs (act-order groups) look both up per column, without branches.  The CTA's
+// slice of x sits in shared memory column-major.  d_in is split over the 8 CTAs of a
+// cluster, and CTA 0 adds the 8 partial sums in rank order from the others' shared
+// memory, so the result does not depend on timing.  At decode batch sizes the kernel is
+// bound by the packed weight bytes (HBM).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -24,7 +26,7 @@ namespace {
 
 constexpr int DQ_ROWS = 128;  // output rows per CTA, one per thread
 constexpr int DQ_SPLIT = 8;   // CTAs of a cluster, each a slice of d_in
-constexpr int DQ_KC = 128;    // columns staged per pass
+constexpr int DQ_KC = 128;    // columns per chunk of packed words
 
 struct DqArgs {
   const void* x;
@@ -55,70 +57,116 @@ __device__ __forceinline__ uint32_t stream_bits(const uint32_t* __restrict__ wor
   return v & ((1u << BITS) - 1u);
 }
 
+// The same from a register array (b known at compile time once the caller is unrolled).
+template <int BITS, int N>
+__device__ __forceinline__ uint32_t reg_bits(const uint32_t (&words)[N], int b) {
+  const int w = b >> 5, sh = b & 31;
+  uint32_t v = words[w] >> sh;
+  if (sh + BITS > 32 && w + 1 < N) v |= words[w + 1] << (32 - sh);
+  return v & ((1u << BITS) - 1u);
+}
+
 __device__ __forceinline__ float ld_dsmem(uint32_t cluster_addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
   return v;
 }
 
+// Row r's zero point in group g (bits [BITS r, BITS r + BITS) of the group's stream).
+template <int BITS>
+__device__ __forceinline__ float zero_of(const uint32_t* __restrict__ qz, int zwords, int g,
+                                         int zbit) {
+  return static_cast<float>(stream_bits<BITS>(qz + static_cast<size_t>(g) * zwords, zbit));
+}
+
 template <int BITS, int NT>
-__global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS)
+__global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
     dequant_matmul_kernel(const DqArgs a) {
-  __shared__ __align__(16) float xs[NT][DQ_KC];
-  __shared__ int gs[DQ_KC];
+  // dynamic shared memory: x[t0 .. t0 + NT) over this CTA's slice of d_in, column-major
+  // (the NT values of a column together); the slice's group indices; per 32-column run,
+  // its group when every column of the run has the same one, else -1
+  extern __shared__ __align__(16) float dsm[];
+  float* xs = dsm;                                           // [kper][NT]
+  int* gs = reinterpret_cast<int*>(dsm + NT * a.kper);       // [kper]
+  int* guni = gs + a.kper;                                   // [kper / 32]
   __shared__ float part[NT][DQ_ROWS];
-  const int tid = threadIdx.x;
+  constexpr int CW = BITS * DQ_KC / 32;                      // packed words per chunk
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int r = blockIdx.x * DQ_ROWS + tid;
   const bool row_ok = r < a.m;
   const int rank = static_cast<int>(tc::cluster_ctarank());  // the slice of d_in
   const int k0 = rank * a.kper, k1 = min(a.d, k0 + a.kper);
+  const int kn_all = max(0, k1 - k0);                        // a multiple of 32
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.qweight);
   const uint32_t* qz = reinterpret_cast<const uint32_t*>(a.qzeros);
   const int zwords = BITS * a.m / 32;  // words of one group's zero stream
+  const int zbit = BITS * (row_ok ? r : 0);
+  for (int run = warp; run < kn_all / 32; run += DQ_ROWS / 32) {
+    int g = a.g_idx[k0 + 32 * run + lane];
+    if (g < 0 || g >= a.G) {  // a group index outside the scales: report, read group 0
+      dev_fail(a.st, GPTQ_ERR_INVALID_ARG, k0 + 32 * run + lane + 1);
+      g = 0;
+    }
+    gs[32 * run + lane] = g;
+    const bool same = __all_sync(0xffffffffu, g == __shfl_sync(0xffffffffu, g, 0));
+    if (lane == 0) guni[run] = same ? g : -1;
+  }
   for (int64_t t0 = 0; t0 < a.n; t0 += NT) {
+    for (int e = tid; e < NT * kn_all; e += DQ_ROWS) {
+      const int c = e / NT, t = e % NT;
+      xs[e] = (t0 + t < a.n) ? ld_x(a, t0 + t, k0 + c) : 0.0f;
+    }
+    __syncthreads();
     float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-    for (int kc = k0; kc < k1; kc += DQ_KC) {
-      const int kn = min(DQ_KC, k1 - kc);  // a multiple of 32
-      for (int e = tid; e < NT * DQ_KC; e += DQ_ROWS) {
-        const int t = e / DQ_KC, c = e % DQ_KC;
-        xs[t][c] = (t0 + t < a.n && c < kn) ? ld_x(a, t0 + t, kc + c) : 0.0f;
-      }
-      for (int c = tid; c < DQ_KC; c += DQ_ROWS) {
-        int g = (c < kn) ? a.g_idx[kc + c] : 0;
-        if (g < 0 || g >= a.G) {  // a group index outside the scales: report, read group 0
-          dev_fail(a.st, GPTQ_ERR_INVALID_ARG, kc + c + 1);
-          g = 0;
-        }
-        gs[c] = g;
-      }
-      __syncthreads();
-      if (row_ok) {
-        int gprev = -1;
-        float s = 0.0f, z = 0.0f;
-        for (int c0 = 0; c0 < kn; c0 += 32) {
-          uint32_t wds[BITS];  // the 32 codes of columns kc + c0 .. kc + c0 + 31
-          const int w0 = BITS * (kc + c0) / 32;
+    if (row_ok && kn_all > 0) {
+      // the packed words of one 128-column chunk, the next chunk's loads in flight while
+      // this one is decoded
+      uint32_t cur[CW], nxt[CW];
+      auto load_chunk = [&](uint32_t (&dst)[CW], int kc) {
+        const int nw = BITS * min(DQ_KC, k1 - kc) / 32;
+        const size_t w0 = static_cast<size_t>(BITS) * kc / 32;
 #pragma unroll
-          for (int i = 0; i < BITS; ++i) wds[i] = qw[static_cast<size_t>(w0 + i) * a.m + r];
+        for (int u = 0; u < CW; ++u) dst[u] = (u < nw) ? qw[(w0 + u) * a.m + r] : 0u;
+      };
+      load_chunk(cur, k0);
+      for (int kc = k0; kc < k1; kc += DQ_KC) {
+        if (kc + DQ_KC < k1) load_chunk(nxt, kc + DQ_KC);
+        const int kn = min(DQ_KC, k1 - kc);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float code = static_cast<float>(stream_bits<BITS>(wds, BITS * c));
-            const int g = gs[c0 + c];
-            if (g != gprev) {
-              s = a.scales[static_cast<size_t>(g) * a.m + r];
-              z = static_cast<float>(stream_bits<BITS>(qz + static_cast<size_t>(g) * zwords,
-                                                       BITS * r));
-              gprev = g;
+        for (int j = 0; j < DQ_KC / 32; ++j) {
+          if (32 * j >= kn) continue;
+          const int cb = kc - k0 + 32 * j;  // slice column of the run's first
+          const int g0 = guni[cb / 32];
+          if (g0 >= 0) {
+            // one group for the whole run
+            const float s = a.scales[static_cast<size_t>(g0) * a.m + r];
+            const float z = zero_of<BITS>(qz, zwords, g0, zbit);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float w = s * (static_cast<float>(reg_bits<BITS>(cur, BITS * (32 * j + c))) - z);
+              const float* xc = xs + (cb + c) * NT;
+#pragma unroll
+              for (int t = 0; t < NT; ++t) acc[t] = fmaf(xc[t], w, acc[t]);
             }
-            const float w = s * (code - z);
+          } else {
+            // each column's own group (act-order): independent lookups, no branch
 #pragma unroll
-            for (int t = 0; t < NT; ++t) acc[t] = fmaf(xs[t][c0 + c], w, acc[t]);
+            for (int c = 0; c < 32; ++c) {
+              const int g = gs[cb + c];
+              const float s = a.scales[static_cast<size_t>(g) * a.m + r];
+              const float z = zero_of<BITS>(qz, zwords, g, zbit);
+              const float w = s * (static_cast<float>(reg_bits<BITS>(cur, BITS * (32 * j + c))) - z);
+              const float* xc = xs + (cb + c) * NT;
+#pragma unroll
+              for (int t = 0; t < NT; ++t) acc[t] = fmaf(xc[t], w, acc[t]);
+            }
           }
         }
+#pragma unroll
+        for (int u = 0; u < CW; ++u) cur[u] = nxt[u];
       }
-      __syncthreads();
     }
     // the cluster's slices, added by CTA 0 in rank order
 #pragma unroll
@@ -135,18 +183,27 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS)
         a.y[(t0 + t) * a.m + r] = sum;
       }
     }
-    tc::cluster_sync();  // the partial sums stay readable until CTA 0 is done
+    tc::cluster_sync();  // the partial sums and x stay in place until CTA 0 is done
   }
+}
+
+template <int BITS, int NT>
+void launch_nt(const DqArgs& a, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.m, DQ_ROWS)), DQ_SPLIT);
+  const int smem = ((NT + 1) * a.kper + a.kper / 32) * static_cast<int>(sizeof(float));
+  static int attr = 0;  // the largest dynamic size set so far
+  if (smem > 48 * 1024 && smem > attr) {
+    GPTQ_CUDA(cudaFuncSetAttribute(dequant_matmul_kernel<BITS, NT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    attr = smem;
+  }
+  GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, NT>), grid, DQ_ROWS, smem, a);
 }
 
 template <int BITS>
 void launch_bits(const DqArgs& a, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>(ceil_div(a.m, DQ_ROWS)), DQ_SPLIT);
-  if (a.n == 1) {
-    GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, 1>), grid, DQ_ROWS, 0, a);
-  } else {
-    GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, 8>), grid, DQ_ROWS, 0, a);
-  }
+  if (a.n == 1) launch_nt<BITS, 1>(a, s);
+  else launch_nt<BITS, 8>(a, s);
 }
 
 }  // namespace

@@ -26,7 +26,8 @@ __all__ = [
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
     "gptq_kernel_name",
-    "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "GPTQ_QUANT_STATIC_GROUPS",
+    "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "GPTQ_K_DEQUANT_MATMUL",
+    "GPTQ_QUANT_STATIC_GROUPS",
     "workspace",
 ]
 
@@ -36,6 +37,7 @@ GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE, GPTQ_OP_DEQUANT_MATMUL = 0, 1, 2, 3
 KERNEL_KINDS = 21
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
+GPTQ_K_DEQUANT_MATMUL = 20
 GPTQ_QUANT_STATIC_GROUPS = 1
 
 
