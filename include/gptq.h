@@ -270,6 +270,22 @@ gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_
                                 const int32_t* g_idx, int32_t G, float* y, void* ws,
                                 size_t ws_bytes, void* stream);
 
+/*
+ * gptq_dequantize -- the dense weights the packed checkpoint stands for,
+ *   W_hat[r, c] = scales[g, r] * (code[r, c] - zero[g, r]),  g = g_idx[c]
+ * ("GPTQ Architecture, in depth", "Packing, tooling and serving"), e.g. to re-run a
+ * quantised block on many tokens with a dense matrix product.
+ *
+ * qweight, scales, qzeros, g_idx, G, bits, d_in, d_out: as gptq_dequant_matmul.
+ * W      device [d_out, d_in] row-major, out, `wdtype` (bfloat16 or float32).
+ * ws     device workspace of gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, ...) bytes.
+ * Errors: as gptq_dequant_matmul.
+ */
+gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                            const int32_t* g_idx, int32_t d_out, int32_t d_in, int bits,
+                            int32_t G, void* W, int wdtype, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* gptq_last_error(void);
 
@@ -297,6 +313,7 @@ typedef enum {
   GPTQ_K_TRTRI_DIAG, GPTQ_K_TRTRI_UPDATE, GPTQ_K_PREP_REVERSE,
   GPTQ_K_QUANT_GATHER, GPTQ_K_QUANT_FIT, GPTQ_K_QUANT_LOOP, GPTQ_K_QUANT_LAZY,
   GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT, GPTQ_K_DEQUANT_MATMUL,
+  GPTQ_K_DEQUANTIZE,
   GPTQ_K_COUNT
 } gptq_kernel_kind;
 

@@ -418,6 +418,35 @@ gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_
   });
 }
 
+gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                            const int32_t* g_idx, int32_t d_out, int32_t d_in, int bits,
+                            int32_t G, void* W, int wdtype, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return guarded([&] {
+    require(d_in > 0 && d_out >= 0 && G > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_dequantize: need d_in > 0, d_out >= 0, G > 0");
+    require(wdtype == GPTQ_F32 || wdtype == GPTQ_BF16, GPTQ_ERR_INVALID_ARG,
+            "gptq_dequantize: wdtype must be GPTQ_F32 or GPTQ_BF16");
+    require(bits == 2 || bits == 3 || bits == 4 || bits == 8, GPTQ_ERR_UNSUPPORTED,
+            "gptq_dequantize: bits must be 2, 3, 4 or 8");
+    require(d_in % 32 == 0 && d_out % 32 == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_dequantize: d_in and d_out must be multiples of 32");
+    require(ws != nullptr && aligned(ws, 256) && ws_bytes >= sizeof(DevStatus),
+            GPTQ_ERR_INVALID_ARG, "gptq_dequantize: null, unaligned or too small ws");
+    require(d_out == 0 || (qweight != nullptr && scales != nullptr && qzeros != nullptr &&
+                           g_idx != nullptr && W != nullptr),
+            GPTQ_ERR_INVALID_ARG, "gptq_dequantize: null input or output");
+    if (d_out == 0) return;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsCarver wc(ws, ws_bytes);
+    DevStatus* st = wc.take<DevStatus>(1);
+    begin_call(st, s);
+    launch_dequantize(qweight, scales, qzeros, g_idx, d_out, d_in, bits, G, W,
+                      wdtype == GPTQ_BF16, st, s);
+    raise_device_status(finish_call(st, s), "gptq_dequantize");
+  });
+}
+
 const char* gptq_last_error(void) { return last_error().c_str(); }
 
 const char* gptq_status_string(int status) {
@@ -448,7 +477,7 @@ const char* gptq_kernel_name(int kind) {
       "syrk_tc", "syrk_simt", "syrk_reduce", "prep_diag", "prep_rank", "prep_mirror",
       "prep_gather", "potrf_panel", "potrf_trsm", "potrf_update", "trtri_diag", "trtri_update",
       "prep_reverse", "quant_gather", "quant_fit", "quant_loop", "quant_lazy", "quant_pack",
-      "quant_loss", "quant_split", "dequant_matmul"};
+      "quant_loss", "quant_split", "dequant_matmul", "dequantize"};
   if (kind < 0 || kind >= GPTQ_K_COUNT) return "";
   return names[kind];
 }

@@ -206,7 +206,90 @@ void launch_bits(const DqArgs& a, cudaStream_t s) {
   else launch_nt<BITS, 8>(a, s);
 }
 
+// W_hat[r, c] = s[g, r] (code[r, c] - z[g, r]), g = g_idx[c], as bf16 or float32,
+// row-major.  A CTA takes 32 rows x 128 columns: the packed words are read across its
+// rows, decoded into a shared tile and written back along the rows.
+template <int BITS, typename T>
+__global__ void __launch_bounds__(256) dequantize_kernel(const int32_t* __restrict__ qweight,
+                                                         const float* __restrict__ scales,
+                                                         const int32_t* __restrict__ qzeros,
+                                                         const int32_t* __restrict__ g_idx,
+                                                         int m, int d, int G,
+                                                         T* __restrict__ W, DevStatus* st) {
+  __shared__ float tile[32][129];
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 128;
+  const uint32_t* qw = reinterpret_cast<const uint32_t*>(qweight);
+  const uint32_t* qz = reinterpret_cast<const uint32_t*>(qzeros);
+  const int zwords = BITS * m / 32;
+  {
+    // thread: row r0 + (tid % 32) (a warp reads 32 rows' words together), columns
+    // 16 run .. 16 run + 15 of the tile
+    const int rl = threadIdx.x % 32, run = threadIdx.x / 32;
+    const int r = r0 + rl;
+    const int cb = c0 + 16 * run;
+    if (r < m && cb < d) {
+      const int zbit = BITS * r;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = cb + c;
+        if (col >= d) break;
+        int g = g_idx[col];
+        if (g < 0 || g >= G) {
+          dev_fail(st, GPTQ_ERR_INVALID_ARG, col + 1);
+          g = 0;
+        }
+        const int bit = BITS * col;
+        const int w = bit >> 5, sh = bit & 31;
+        uint32_t v = qw[static_cast<size_t>(w) * m + r] >> sh;
+        if (sh + BITS > 32) v |= qw[static_cast<size_t>(w + 1) * m + r] << (32 - sh);
+        const float cv = static_cast<float>(v & ((1u << BITS) - 1u));
+        const float sv = scales[static_cast<size_t>(g) * m + r];
+        const float zv = zero_of<BITS>(qz, zwords, g, zbit);
+        tile[rl][16 * run + c] = sv * (cv - zv);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 32 * 128; e += 256) {
+    const int rl = e / 128, c = e % 128;
+    const int r = r0 + rl, col = c0 + c;
+    if (r < m && col < d) {
+      if constexpr (sizeof(T) == 2) {
+        W[static_cast<size_t>(r) * d + col] = __float2bfloat16_rn(tile[rl][c]);
+      } else {
+        W[static_cast<size_t>(r) * d + col] = tile[rl][c];
+      }
+    }
+  }
+}
+
+template <int BITS>
+void launch_dequantize_bits(const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                            const int32_t* g_idx, int m, int d, int G, void* W, bool w_bf16,
+                            DevStatus* st, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(d, 128)), static_cast<unsigned>(ceil_div(m, 32)));
+  if (w_bf16) {
+    GPTQ_LAUNCH(GPTQ_K_DEQUANTIZE, s, (dequantize_kernel<BITS, __nv_bfloat16>), grid, 256, 0,
+                qweight, scales, qzeros, g_idx, m, d, G, static_cast<__nv_bfloat16*>(W), st);
+  } else {
+    GPTQ_LAUNCH(GPTQ_K_DEQUANTIZE, s, (dequantize_kernel<BITS, float>), grid, 256, 0, qweight,
+                scales, qzeros, g_idx, m, d, G, static_cast<float*>(W), st);
+  }
+}
+
 }  // namespace
+
+void launch_dequantize(const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                       const int32_t* g_idx, int m, int d, int bits, int G, void* W, bool w_bf16,
+                       DevStatus* st, cudaStream_t s) {
+  if (m <= 0 || d <= 0) return;
+  switch (bits) {
+    case 2: launch_dequantize_bits<2>(qweight, scales, qzeros, g_idx, m, d, G, W, w_bf16, st, s); break;
+    case 3: launch_dequantize_bits<3>(qweight, scales, qzeros, g_idx, m, d, G, W, w_bf16, st, s); break;
+    case 4: launch_dequantize_bits<4>(qweight, scales, qzeros, g_idx, m, d, G, W, w_bf16, st, s); break;
+    default: launch_dequantize_bits<8>(qweight, scales, qzeros, g_idx, m, d, G, W, w_bf16, st, s); break;
+  }
+}
 
 void launch_dequant_matmul(const void* x, bool x_bf16, int64_t n, int d, int m, int bits, int G,
                            const int32_t* qweight, const float* scales, const int32_t* qzeros,

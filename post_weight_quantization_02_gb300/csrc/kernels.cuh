@@ -64,7 +64,10 @@ struct QuantArgs {
 };
 void launch_quantize(const QuantArgs& q, cudaStream_t s);
 
-// dequant_matmul.cu: y[n, m] = x[n, d] W_hat^T from the packed checkpoint
+// dequant_matmul.cu: y[n, m] = x[n, d] W_hat^T from the packed checkpoint, and W_hat
+void launch_dequantize(const int32_t* qweight, const float* scales, const int32_t* qzeros,
+                       const int32_t* g_idx, int m, int d, int bits, int G, void* W, bool w_bf16,
+                       DevStatus* st, cudaStream_t s);
 void launch_dequant_matmul(const void* x, bool x_bf16, int64_t n, int d, int m, int bits, int G,
                            const int32_t* qweight, const float* scales, const int32_t* qzeros,
                            const int32_t* g_idx, float* y, DevStatus* st, cudaStream_t s);

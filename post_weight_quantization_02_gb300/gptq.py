@@ -19,7 +19,7 @@ __all__ = [
     "GPTQ_OK", "GPTQ_ERR_INVALID_ARG", "GPTQ_ERR_UNSUPPORTED", "GPTQ_ERR_NOT_PD",
     "GPTQ_ERR_NONFINITE", "GPTQ_ERR_CUDA", "GPTQ_ERR_TIMEOUT", "GPTQ_ERR_WORKSPACE",
     "GPTQ_F32", "GPTQ_BF16", "GPTQ_OP_HESSIAN", "GPTQ_OP_PREPARE", "GPTQ_OP_QUANTIZE",
-    "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul",
+    "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul", "gptq_dequantize",
     "GptqError", "GptqLibraryError", "lib", "library_path",
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
     "gptq_hessian_status", "gptq_prepare", "gptq_quantize_layer",
@@ -35,7 +35,7 @@ GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 
 GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 6, 7
 GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE, GPTQ_OP_DEQUANT_MATMUL = 0, 1, 2, 3
-KERNEL_KINDS = 21
+KERNEL_KINDS = 22
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
 GPTQ_K_DEQUANT_MATMUL = 20
 GPTQ_QUANT_STATIC_GROUPS = 1
@@ -74,6 +74,8 @@ _SIGS = {
                                           _vp, _vp, _vp, _vp, _sz, _vp]),
     "gptq_dequant_matmul": (_c.c_int, [_vp, _c.c_int, _i64, _i32, _i32, _c.c_int, _vp, _vp,
                                        _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "gptq_dequantize": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _c.c_int, _i32, _vp,
+                                   _c.c_int, _vp, _sz, _vp]),
     "gptq_last_error": (_c.c_char_p, []),
     "gptq_status_string": (_c.c_char_p, [_c.c_int]),
     "gptq_abi_version": (_c.c_int, []),
@@ -248,6 +250,24 @@ def gptq_dequant_matmul(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
                                      _ptr(g_idx), scales.shape[0], _ptr(y), _ptr(ws),
                                      ws.numel(), _stream(stream)))
     return y
+
+
+def gptq_dequantize(qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor,
+                    g_idx: torch.Tensor, bits: int, dtype=torch.bfloat16,
+                    W: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """W_hat [d_out, d_in] (bf16 or fp32) from the packed checkpoint."""
+    m = qweight.shape[1]
+    d = qweight.shape[0] * 32 // bits
+    if W is None:
+        W = torch.empty(m, d, dtype=dtype, device=qweight.device)
+    if ws is None:
+        ws = workspace(gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, 0, m, d, bits, -1),
+                       qweight.device)
+    _check(lib().gptq_dequantize(_ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx), m, d,
+                                 bits, scales.shape[0], _ptr(W), _dtype_code(W), _ptr(ws),
+                                 ws.numel(), _stream(stream)))
+    return W
 
 
 def gptq_profile_enable(on: bool) -> None:

@@ -81,3 +81,20 @@ def test_dequant_matmul_q_proj(lib, cuda_device, static):
     ref = O.dequant_matmul(to_np(x).astype(np.float64), ck["qweight"], ck["scales"],
                            ck["qzeros"], ck["g_idx"], cfg.bits)
     assert rel_fro(to_np(y), ref) <= Y_REL_FRO
+
+
+@pytest.mark.parametrize("bits,group,static", [(4, 32, False), (3, 64, True), (8, -1, False)])
+def test_dequantize_dense(lib, cuda_device, bits, group, static):
+    """gptq_dequantize: W_hat = s (code - z) per original column's group.  One float32
+    multiply of a float32 scale by a small integer rounds like the oracle's float64 value
+    rounded to float32, so float32 output matches exactly; bf16 is that value rounded."""
+    rng = np.random.default_rng(bits + group)
+    m, d = 96, 256
+    ck = _oracle_checkpoint(rng, m, d, bits, group, False, static)
+    ref = O.dequantize(ck["qweight"], ck["scales"], ck["qzeros"], ck["g_idx"], bits)
+    args = [_dev(ck[k], cuda_device) for k in ("qweight", "scales", "qzeros", "g_idx")]
+    W32 = lib.gptq_dequantize(*args, bits, dtype=torch.float32)
+    Wbf = lib.gptq_dequantize(*args, bits, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(W32), ref.astype(np.float32))
+    assert torch.equal(Wbf, torch.from_numpy(ref.astype(np.float32)).to(cuda_device).bfloat16())
