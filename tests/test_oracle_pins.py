@@ -454,12 +454,39 @@ def pin_dequantize(O):
         assert np.allclose(y, x @ Qo.T, rtol=1e-13, atol=0)
 
 
+def pin_block_pipeline(O):
+    """The block oracle ("GPTQ Architecture, in depth", "The pipeline, block by block"):
+    zero weights make the block the identity (both residual branches vanish); with one
+    token the causal softmax has a single term, so attention returns v itself; rmsnorm
+    of a constant row is all ones; at 8 bits the quantised block stays close to the
+    original one; and a pipeline step feeds its re-forward output to the next block."""
+    from oracle import pipeline_oracle as P
+    rng = np.random.default_rng(47)
+    B, S, h, f, heads = 2, 8, 32, 64, 4
+    x = rng.standard_normal((B, S, h))
+    zero = {k: np.zeros((f if k in ("wg", "wu") else h, f if k == "wd" else h))
+            for k in ("wq", "wk", "wv", "wo", "wg", "wu", "wd")}
+    y, _ = P.block_forward(x, zero, heads)
+    assert np.array_equal(y, x)
+    q, k, v = (rng.standard_normal((B, 1, h)) for _ in range(3))
+    assert np.allclose(P.attention(q, k, v, heads), v, rtol=0, atol=1e-15)
+    assert np.allclose(P.rmsnorm(np.full((3, h), 2.5)), 1.0, rtol=1e-6)
+    W = {k: rng.standard_normal(zero[k].shape) * 0.05 for k in zero}
+    st = P.quantize_block(x, W, heads, bits=8, group=32)
+    y_ref, inputs = P.block_forward(x, W, heads)
+    assert np.linalg.norm(st["y"] - y_ref) <= 1e-2 * np.linalg.norm(y_ref)
+    assert set(st["H"]) == {"qkv", "o", "gateup", "down"}
+    assert np.allclose(st["H"]["qkv"], O.hessian(inputs["qkv"]))
+    steps = P.pipeline(x, [W, W], heads, bits=4, group=32)
+    assert np.array_equal(steps[1]["inputs"]["qkv"], P.rmsnorm(steps[0]["y"]).reshape(B * S, h))
+
+
 PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
         pin_cholesky_2x2, pin_cholesky_general, pin_obs_equals_cholesky,
         pin_blocked_equals_unblocked, pin_loss_identity, pin_brute_force_optimum,
         pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
         pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
-        pin_format_roundtrip, pin_static_groups, pin_dequantize]
+        pin_format_roundtrip, pin_static_groups, pin_dequantize, pin_block_pipeline]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
