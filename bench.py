@@ -524,6 +524,57 @@ def run_dequant(args, world, rank, local):
             }), flush=True)
 
 
+def run_pipeline(args, world, rank, local):
+    """The block-sequential pipeline on a Llama-shaped block (hidden 4096, MLP 14336, 32
+    heads, the 8B-class shapes of the survey's block configuration): Hessians of the four
+    input groups over every calibration token, prepare, all seven linears quantised, and
+    the re-forward with the dequantised weights.  One JSON line."""
+    import torch
+    from post_weight_quantization_02_gb300.pipeline import BlockQuantizer, make_block_weights
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the engine has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    hidden, inter, heads, seq = 4096, 14336, 32, 2048
+    tokens = args.tokens if args.tokens else 262144
+    B = max(1, tokens // seq)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    x = torch.randn(B, seq, hidden, generator=g).to(device=dev, dtype=torch.bfloat16)
+    W = make_block_weights(hidden, inter, 1, dev)
+    bq = BlockQuantizer(hidden, inter, heads, bits=4, group=128, static_groups=args.static_groups,
+                        seqs_per_chunk=8, max_chunk_tokens=8 * seq, device=dev)
+    for _ in range(max(1, args.warmup - 2)):
+        bq.quantize_block(x, W)
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    with ClockSampler(dev.index) as clocks:
+        barrier(dist, dev)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            bq.quantize_block(x, W)
+        torch.cuda.synchronize()
+        barrier(dist, dev)
+        ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / steps, dev)
+    weights = 4 * hidden * hidden + 3 * hidden * inter
+    if rank == 0:
+        print(json.dumps({
+            "metric": "block-sequential GPTQ, ms per Llama-shaped block (and weights/s)",
+            "value": round(ms, 3), "unit": "ms", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init block, seeded calibration tokens)",
+            "config": {"workload": f"block hidden {hidden}, MLP {inter}, {heads} heads, "
+                                   f"{B * seq} tokens ({B} x {seq}), 4-bit group 128, act-order"
+                                   + (", static groups" if args.static_groups else ""),
+                       "step": "forward (4 Hessian groups) + 4 prepares + 7 quantisations "
+                               "+ re-forward with the dequantised weights",
+                       "weights_per_s": round(weights / (ms * 1e-3), 1)},
+            "clocks": clocks.summary(),
+        }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -540,6 +591,8 @@ def main(argv=None):
                     help="groups fixed in the original column order before the loop")
     ap.add_argument("--dequant-matmul", action="store_true",
                     help="measure the packed checkpoint's consumer instead of the layer path")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="measure the block-sequential pipeline on a Llama-shaped block")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()
@@ -547,6 +600,8 @@ def main(argv=None):
         run_reference(args, world, rank)
     elif args.dequant_matmul:
         run_dequant(args, world, rank, local)
+    elif args.pipeline:
+        run_pipeline(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 
