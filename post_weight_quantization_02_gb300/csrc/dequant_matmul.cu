@@ -6,9 +6,10 @@
 // It reads the checkpoint exactly as gptq_quantize_layer writes it, so it also checks
 // the packing end to end.
 //
-// Design: one thread per output row; the row's packed words are read coalesced across
-// the CTA's 128 rows (qweight is [bits*d/32, m]), a 128-column chunk at a time with the
-// next chunk's loads in flight, and decoded with compile-time shifts.  A 32-column run
+// Design: two threads per output row, taking alternate 128-column chunks of the CTA's
+// slice; a chunk's packed words are read coalesced across the CTA's 128 rows (qweight is
+// [bits*d/32, m]), the thread's next chunk's loads in flight while one is decoded with
+// compile-time shifts.  A 32-column run
 // whose columns share one group (every run with static groups) uses one scale and zero;
 // other runs (act-order groups) look both up per column, without branches.  The CTA's
 // slice of x sits in shared memory column-major.  d_in is split over the 8 CTAs of a
@@ -24,7 +25,9 @@
 namespace gptq {
 namespace {
 
-constexpr int DQ_ROWS = 128;  // output rows per CTA, one per thread
+constexpr int DQ_ROWS = 128;  // output rows per CTA
+constexpr int DQ_HALVES = 2;  // threads per row, taking alternate chunks of the slice
+constexpr int DQ_THREADS = DQ_ROWS * DQ_HALVES;
 constexpr int DQ_SPLIT = 8;   // CTAs of a cluster, each a slice of d_in
 constexpr int DQ_KC = 128;    // columns per chunk of packed words
 
@@ -80,7 +83,7 @@ __device__ __forceinline__ float zero_of(const uint32_t* __restrict__ qz, int zw
 }
 
 template <int BITS, int NT>
-__global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
+__global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2)
     dequant_matmul_kernel(const DqArgs a) {
   // dynamic shared memory: x[t0 .. t0 + NT) over this CTA's slice of d_in, column-major
   // (the NT values of a column together); the slice's group indices; per 32-column run,
@@ -89,10 +92,11 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
   float* xs = dsm;                                           // [kper][NT]
   int* gs = reinterpret_cast<int*>(dsm + NT * a.kper);       // [kper]
   int* guni = gs + a.kper;                                   // [kper / 32]
-  __shared__ float part[NT][DQ_ROWS];
+  __shared__ float part[DQ_HALVES][NT][DQ_ROWS];
   constexpr int CW = BITS * DQ_KC / 32;                      // packed words per chunk
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int r = blockIdx.x * DQ_ROWS + tid;
+  const int rl = tid % DQ_ROWS, half = tid / DQ_ROWS;        // row within the CTA, chunk parity
+  const int r = blockIdx.x * DQ_ROWS + rl;
   const bool row_ok = r < a.m;
   const int rank = static_cast<int>(tc::cluster_ctarank());  // the slice of d_in
   const int k0 = rank * a.kper, k1 = min(a.d, k0 + a.kper);
@@ -101,7 +105,7 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
   const uint32_t* qz = reinterpret_cast<const uint32_t*>(a.qzeros);
   const int zwords = BITS * a.m / 32;  // words of one group's zero stream
   const int zbit = BITS * (row_ok ? r : 0);
-  for (int run = warp; run < kn_all / 32; run += DQ_ROWS / 32) {
+  for (int run = warp; run < kn_all / 32; run += DQ_THREADS / 32) {
     int g = a.g_idx[k0 + 32 * run + lane];
     if (g < 0 || g >= a.G) {  // a group index outside the scales: report, read group 0
       dev_fail(a.st, GPTQ_ERR_INVALID_ARG, k0 + 32 * run + lane + 1);
@@ -112,7 +116,7 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
     if (lane == 0) guni[run] = same ? g : -1;
   }
   for (int64_t t0 = 0; t0 < a.n; t0 += NT) {
-    for (int e = tid; e < NT * kn_all; e += DQ_ROWS) {
+    for (int e = tid; e < NT * kn_all; e += DQ_THREADS) {
       const int c = e / NT, t = e % NT;
       xs[e] = (t0 + t < a.n) ? ld_x(a, t0 + t, k0 + c) : 0.0f;
     }
@@ -120,9 +124,10 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
     float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-    if (row_ok && kn_all > 0) {
-      // the packed words of one 128-column chunk, the next chunk's loads in flight while
-      // this one is decoded
+    const int kfirst = k0 + half * DQ_KC;  // this thread's chunks: every other one
+    if (row_ok && kfirst < k1) {
+      // the packed words of one 128-column chunk, the thread's next chunk's loads in
+      // flight while this one is decoded
       uint32_t cur[CW], nxt[CW];
       auto load_chunk = [&](uint32_t (&dst)[CW], int kc) {
         const int nw = BITS * min(DQ_KC, k1 - kc) / 32;
@@ -130,9 +135,9 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
 #pragma unroll
         for (int u = 0; u < CW; ++u) dst[u] = (u < nw) ? qw[(w0 + u) * a.m + r] : 0u;
       };
-      load_chunk(cur, k0);
-      for (int kc = k0; kc < k1; kc += DQ_KC) {
-        if (kc + DQ_KC < k1) load_chunk(nxt, kc + DQ_KC);
+      load_chunk(cur, kfirst);
+      for (int kc = kfirst; kc < k1; kc += DQ_HALVES * DQ_KC) {
+        if (kc + DQ_HALVES * DQ_KC < k1) load_chunk(nxt, kc + DQ_HALVES * DQ_KC);
         const int kn = min(DQ_KC, k1 - kc);
 #pragma unroll
         for (int j = 0; j < DQ_KC / 32; ++j) {
@@ -168,18 +173,23 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_ROWS, 1)
         for (int u = 0; u < CW; ++u) cur[u] = nxt[u];
       }
     }
-    // the cluster's slices, added by CTA 0 in rank order
+    // the cluster's slices and each slice's two halves, added by CTA 0 in a fixed order
 #pragma unroll
-    for (int t = 0; t < NT; ++t) part[t][tid] = acc[t];
+    for (int t = 0; t < NT; ++t) part[half][t][rl] = acc[t];
     tc::cluster_sync();
-    if (rank == 0 && row_ok) {
+    if (rank == 0 && row_ok && half == 0) {
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         if (t0 + t >= a.n) break;
-        const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(&part[t][tid]));
         float sum = 0.0f;
 #pragma unroll
-        for (int j = 0; j < DQ_SPLIT; ++j) sum += ld_dsmem(tc::mapa_shared(sa, j));
+        for (int j = 0; j < DQ_SPLIT; ++j) {
+#pragma unroll
+          for (int h = 0; h < DQ_HALVES; ++h) {
+            const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(&part[h][t][rl]));
+            sum += ld_dsmem(tc::mapa_shared(sa, j));
+          }
+        }
         a.y[(t0 + t) * a.m + r] = sum;
       }
     }
@@ -197,7 +207,8 @@ void launch_nt(const DqArgs& a, cudaStream_t s) {
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     attr = smem;
   }
-  GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, NT>), grid, DQ_ROWS, smem, a);
+  GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, NT>), grid, DQ_THREADS, smem,
+              a);
 }
 
 template <int BITS>
