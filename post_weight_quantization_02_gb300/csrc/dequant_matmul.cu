@@ -11,7 +11,8 @@
 // [bits*d/32, m]), the thread's next chunk's loads in flight while one is decoded with
 // compile-time shifts.  A 32-column run
 // whose columns share one group (every run with static groups) uses one scale and zero;
-// other runs (act-order groups) look both up per column, without branches.  The CTA's
+// other runs (act-order groups) look both up per column, without branches; both read a
+// shared table of every group's scale and zero of the CTA's rows when it fits.  The CTA's
 // slice of x sits in shared memory column-major.  d_in is split over the 8 CTAs of a
 // cluster, and CTA 0 adds the 8 partial sums in rank order from the others' shared
 // memory, so the result does not depend on timing.  At decode batch sizes the kernel is
@@ -37,6 +38,7 @@ struct DqArgs {
   int64_t n;
   int d, m, G;
   int kper;  // columns per CTA of the cluster (a multiple of 32)
+  int table; // the CTA keeps every group's scale and zero of its rows in shared memory
   const int32_t* qweight;
   const float* scales;
   const int32_t* qzeros;
@@ -92,6 +94,8 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
   float* xs = dsm;                                           // [kper][NT]
   int* gs = reinterpret_cast<int*>(dsm + NT * a.kper);       // [kper]
   int* guni = gs + a.kper;                                   // [kper / 32]
+  float* stab = reinterpret_cast<float*>(guni + a.kper / 32);  // [G][DQ_ROWS] if a.table
+  float* ztab = stab + (a.table ? a.G * DQ_ROWS : 0);          // [G][DQ_ROWS]
   __shared__ float part[DQ_HALVES][NT][DQ_ROWS];
   constexpr int CW = BITS * DQ_KC / 32;                      // packed words per chunk
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -114,6 +118,15 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
     gs[32 * run + lane] = g;
     const bool same = __all_sync(0xffffffffu, g == __shfl_sync(0xffffffffu, g, 0));
     if (lane == 0) guni[run] = same ? g : -1;
+  }
+  if (a.table) {
+    // every group's scale and zero (as a float) of the CTA's rows
+    for (int e = tid; e < a.G * DQ_ROWS; e += DQ_THREADS) {
+      const int g = e / DQ_ROWS, row = blockIdx.x * DQ_ROWS + e % DQ_ROWS;
+      const bool ok = row < a.m;
+      stab[e] = ok ? a.scales[static_cast<size_t>(g) * a.m + row] : 0.0f;
+      ztab[e] = ok ? zero_of<BITS>(qz, zwords, g, BITS * row) : 0.0f;
+    }
   }
   for (int64_t t0 = 0; t0 < a.n; t0 += NT) {
     for (int e = tid; e < NT * kn_all; e += DQ_THREADS) {
@@ -146,8 +159,9 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
           const int g0 = guni[cb / 32];
           if (g0 >= 0) {
             // one group for the whole run
-            const float s = a.scales[static_cast<size_t>(g0) * a.m + r];
-            const float z = zero_of<BITS>(qz, zwords, g0, zbit);
+            const float s = a.table ? stab[g0 * DQ_ROWS + rl]
+                                    : a.scales[static_cast<size_t>(g0) * a.m + r];
+            const float z = a.table ? ztab[g0 * DQ_ROWS + rl] : zero_of<BITS>(qz, zwords, g0, zbit);
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const float w = s * (static_cast<float>(reg_bits<BITS>(cur, BITS * (32 * j + c))) - z);
@@ -160,8 +174,10 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const int g = gs[cb + c];
-              const float s = a.scales[static_cast<size_t>(g) * a.m + r];
-              const float z = zero_of<BITS>(qz, zwords, g, zbit);
+              const float s = a.table ? stab[g * DQ_ROWS + rl]
+                                      : a.scales[static_cast<size_t>(g) * a.m + r];
+              const float z = a.table ? ztab[g * DQ_ROWS + rl]
+                                      : zero_of<BITS>(qz, zwords, g, zbit);
               const float w = s * (static_cast<float>(reg_bits<BITS>(cur, BITS * (32 * j + c))) - z);
               const float* xc = xs + (cb + c) * NT;
 #pragma unroll
@@ -200,7 +216,12 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
 template <int BITS, int NT>
 void launch_nt(const DqArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(ceil_div(a.m, DQ_ROWS)), DQ_SPLIT);
-  const int smem = ((NT + 1) * a.kper + a.kper / 32) * static_cast<int>(sizeof(float));
+  const int base = ((NT + 1) * a.kper + a.kper / 32) * static_cast<int>(sizeof(float));
+  // the scale / zero table when it fits beside two CTAs' other shared memory on an SM
+  const int tab = 2 * a.G * DQ_ROWS * static_cast<int>(sizeof(float));
+  DqArgs b = a;
+  b.table = (base + tab <= 100 * 1024) ? 1 : 0;
+  const int smem = base + (b.table ? tab : 0);
   static int attr = 0;  // the largest dynamic size set so far
   if (smem > 48 * 1024 && smem > attr) {
     GPTQ_CUDA(cudaFuncSetAttribute(dequant_matmul_kernel<BITS, NT>,
@@ -208,7 +229,7 @@ void launch_nt(const DqArgs& a, cudaStream_t s) {
     attr = smem;
   }
   GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, NT>), grid, DQ_THREADS, smem,
-              a);
+              b);
 }
 
 template <int BITS>
@@ -314,6 +335,7 @@ void launch_dequant_matmul(const void* x, bool x_bf16, int64_t n, int d, int m, 
   a.m = m;
   a.G = G;
   a.kper = static_cast<int>(ceil_div(ceil_div(d, DQ_SPLIT), 32)) * 32;
+  a.table = 0;  // chosen per launch
   a.qweight = qweight;
   a.scales = scales;
   a.qzeros = qzeros;
