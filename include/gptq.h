@@ -254,7 +254,8 @@ gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_
  * bits     2, 3, 4 or 8.
  * qweight  device int32 [bits*d_in/32, d_out], scales device float32 [G, d_out], qzeros
  *          device int32 [G, bits*d_out/32], g_idx device int32 [d_in] with values in
- *          [0, G): the layout gptq_quantize_layer documents.
+ *          [0, G): the layout gptq_quantize_layer documents.  qweight and scales are
+ *          16-byte aligned (they are copied to shared memory 16 bytes at a time).
  * G        number of groups (rows of scales).
  * y        device float32 [n, d_out], out.
  * ws       device workspace of gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, ...) bytes

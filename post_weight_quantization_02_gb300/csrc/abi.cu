@@ -407,6 +407,8 @@ gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_
                 (x != nullptr && qweight != nullptr && scales != nullptr && qzeros != nullptr &&
                  g_idx != nullptr && y != nullptr),
             GPTQ_ERR_INVALID_ARG, "gptq_dequant_matmul: null input or output");
+    require(aligned(qweight, 16) && aligned(scales, 16), GPTQ_ERR_INVALID_ARG,
+            "gptq_dequant_matmul: qweight and scales must be 16-byte aligned");
     if (n == 0 || d_out == 0) return;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsCarver wc(ws, ws_bytes);

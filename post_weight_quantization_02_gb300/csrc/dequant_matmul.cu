@@ -7,21 +7,24 @@
 // the packing end to end.
 //
 // Design: two threads per output row, taking alternate 128-column chunks of the CTA's
-// slice.  Each thread copies its own row's packed words of a chunk (read coalesced across
-// the CTA's 128 rows: qweight is [bits*d/32, m]) into its own part of a shared-memory ring
-// with cp.async, two chunks in flight; the first two are requested before anything else,
-// so they land while the shared tables are filled.  Only the copying thread reads them, so
-// waiting on its own copy groups is all the ordering needed.  Decoding loops over 32-column
-// runs with the run's body unrolled: the whole kernel then fits the instruction cache,
-// which a fully unrolled chunk (tens of KB of code) does not.  No integer-to-float
-// conversion: the float whose exponent says 2^23 and whose low mantissa bits hold the code
-// is exactly 2^23 + code, so one OR and one subtraction of (2^23 + z) give code - z
-// exactly.  A run whose columns share one group (every run with static groups) sums
-// x (code - z) and applies the scale once; other runs (act-order groups) look up the scale
-// and zero per column, from a shared table of every group's (scale, 2^23 + zero) of the
-// CTA's rows when it fits.  The CTA's slice of x sits in shared memory column-major.  d_in
-// is split over the 8 CTAs of a cluster, and CTA 0 adds the 8 partial sums in rank order
-// from the others' shared memory, so the result does not depend on timing.
+// slice.  The packed words go through a shared-memory ring of two stages (a stage: the
+// CTA's 128 rows over 256 columns), copied with 16-byte cp.async (4 rows' words; a warp's
+// copies read one word of the 128 rows, coalesced: qweight is [bits*d/32, m]).  The
+// scales and packed zero words of every group of the CTA's rows are copied at the same
+// time, and the first two stages are requested before anything else, so decoding can
+// start as soon as stage 0 has landed while stage 1 streams in; after each stage a CTA
+// barrier makes the next one visible and frees its buffer for the stage after it.
+// Decoding loops over 32-column runs with the run's body unrolled: the whole kernel then
+// fits the instruction cache, which a fully unrolled chunk (tens of KB of code) does not.
+// No integer-to-float conversion: the float whose exponent says 2^23 and whose low
+// mantissa bits hold the code is exactly 2^23 + code, so one OR and one subtraction of
+// (2^23 + z) give code - z exactly.  A run whose columns share one group (every run with
+// static groups) sums x (code - z) and applies the scale once; runs that mix groups
+// (act-order) look up the scale and (2^23 + zero) per column from the shared table, built
+// only when such a run exists, or from global memory when the table does not fit.  The
+// CTA's slice of x sits in shared memory column-major.  d_in is split over the 8 CTAs of a
+// cluster, and CTA 0 adds the 8 partial sums in rank order from the others' shared memory,
+// so the result does not depend on timing.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -35,7 +38,10 @@ constexpr int DQ_ROWS = 128;  // output rows per CTA
 constexpr int DQ_HALVES = 2;  // threads per row, taking alternate chunks of the slice
 constexpr int DQ_THREADS = DQ_ROWS * DQ_HALVES;
 constexpr int DQ_SPLIT = 8;   // CTAs of a cluster, each a slice of d_in
-constexpr int DQ_KC = 128;    // columns per chunk of packed words
+constexpr int DQ_KC = 128;    // columns per thread's chunk of packed words
+constexpr int DQ_RING = 2;    // stages in the shared-memory ring (a third one only costs
+                              // occupancy: with x for eight tokens a wide layer's CTA no
+                              // longer fits twice on an SM)
 
 struct DqArgs {
   const void* x;
@@ -97,9 +103,13 @@ __device__ __forceinline__ float code_minus(uint32_t code, float zb) {
   return __uint_as_float(code | kTwo23Bits) - zb;
 }
 
-__device__ __forceinline__ void cp_async4(uint32_t* dst, const uint32_t* src) {
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -109,77 +119,121 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-constexpr int DQ_STAGES = 2;  // a thread's chunks in flight
+// Waits until at most `pending` (0 .. 2) of this thread's latest copy groups are in flight.
+__device__ __forceinline__ void cp_async_wait_upto(int pending) {
+  if (pending >= 2) cp_async_wait<2>();
+  else if (pending == 1) cp_async_wait<1>();
+  else cp_async_wait<0>();
+}
 
-// Shared memory bytes of the ring of packed words: DQ_STAGES chunks of every thread.
+// A stage is the CTA's 128 rows over DQ_HALVES * DQ_KC consecutive columns of its slice,
+// half h taking columns [DQ_KC h, DQ_KC h + DQ_KC); the ring holds DQ_RING of them.
+constexpr int DQ_STAGE_COLS = DQ_HALVES * DQ_KC;
+
 template <int BITS>
 constexpr int ring_bytes() {
-  return DQ_STAGES * (BITS * DQ_KC / 32) * DQ_THREADS * static_cast<int>(sizeof(uint32_t));
+  return DQ_RING * (BITS * DQ_KC / 32) * DQ_THREADS * static_cast<int>(sizeof(uint32_t));
+}
+
+// Shared memory bytes of the per-group table: the CTA's rows' scales and (2^23 + zero)
+// as floats, and the packed zero words they come from.
+template <int BITS>
+constexpr int table_bytes_per_group() {
+  return 2 * DQ_ROWS * static_cast<int>(sizeof(float)) +
+         (BITS * DQ_ROWS / 32) * static_cast<int>(sizeof(uint32_t));
 }
 
 template <int BITS, int NT>
 __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2)
     dequant_matmul_kernel(const DqArgs a) {
-  // dynamic shared memory: when a.table, (scale, 2^23 + zero) of every group of the
-  // slice's range and row of the CTA; the ring of packed words, [stage][word][thread], each thread reading only
-  // what it copied itself; x[t0 .. t0 + NT) over this CTA's slice of d_in, column-major
+  // dynamic shared memory: when a.table, for every group the scales of the CTA's rows,
+  // their (2^23 + zero) and the packed zero words; the ring of packed codes,
+  // [stage][word][half][row]; x[t0 .. t0 + NT) over this CTA's slice of d_in, column-major
   // (the NT values of a column together); the slice's group indices; per 32-column run,
   // its group when every column of the run has the same one, else -1
   extern __shared__ __align__(16) float dsm[];
-  constexpr int CW = BITS * DQ_KC / 32;                       // packed words per chunk
-  constexpr int S = DQ_HALVES * DQ_KC;                        // a thread's chunk stride
+  constexpr int CW = BITS * DQ_KC / 32;                       // packed words per row and chunk
+  constexpr int ZW = BITS * DQ_ROWS / 32;                     // zero words per group
   constexpr int WARPS = DQ_THREADS / 32;
-  float2* tab = reinterpret_cast<float2*>(dsm);               // [G][DQ_ROWS] if a.table
-  uint32_t* ring = reinterpret_cast<uint32_t*>(dsm + (a.table ? 2 * a.G * DQ_ROWS : 0));
-  float* xs = reinterpret_cast<float*>(ring + DQ_STAGES * CW * DQ_THREADS);  // [kper][NT]
+  const int tg = a.table ? a.G : 0;
+  float* stab = dsm;                                          // [tg][DQ_ROWS]
+  float* ztab = stab + tg * DQ_ROWS;                          // [tg][DQ_ROWS]
+  uint32_t* zraw = reinterpret_cast<uint32_t*>(ztab + tg * DQ_ROWS);  // [tg][ZW]
+  uint32_t* ring = zraw + tg * ZW;                            // [DQ_RING][CW][DQ_THREADS]
+  float* xs = reinterpret_cast<float*>(ring + DQ_RING * CW * DQ_THREADS);  // [kper][NT]
   int* gs = reinterpret_cast<int*>(xs + NT * a.kper);         // [kper]
   int* guni = gs + a.kper;                                    // [kper / 32]
   __shared__ float part[DQ_HALVES][NT][DQ_ROWS];
-  __shared__ int grange[2];  // the smallest and largest group of the slice
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int rl = tid % DQ_ROWS, half = tid / DQ_ROWS;         // row within the CTA, chunk parity
-  const int r = blockIdx.x * DQ_ROWS + rl;
-  const bool row_ok = r < a.m;
+  const int r0 = blockIdx.x * DQ_ROWS, r = r0 + rl;
+  const int rows = min(DQ_ROWS, a.m - r0);                    // a multiple of 32
+  const bool row_ok = rl < rows;
   const int rank = static_cast<int>(tc::cluster_ctarank());   // the slice of d_in
   const int k0 = rank * a.kper, k1 = min(a.d, k0 + a.kper);
   const int kn_all = max(0, k1 - k0);                         // a multiple of 32
+  const int nst = (kn_all + DQ_STAGE_COLS - 1) / DQ_STAGE_COLS;
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.qweight);
   const uint32_t* qz = reinterpret_cast<const uint32_t*>(a.qzeros);
   const int zwords = BITS * a.m / 32;  // words of one group's zero stream
   const int zbit = BITS * (row_ok ? r : 0);
-  const int kfirst = k0 + half * DQ_KC;  // this thread's chunks: every other one
-  const int nch = (row_ok && kfirst < k1) ? (k1 - kfirst + S - 1) / S : 0;
 
-  // chunk kc's words of this thread's row into ring stage `stage`, as one copy group
-  auto issue = [&](int stage, int kc) {
-    const int nw = BITS * min(DQ_KC, k1 - kc) / 32;
-    const size_t w0 = static_cast<size_t>(BITS) * kc / 32;
-    uint32_t* dst = ring + stage * CW * DQ_THREADS + tid;
+  // stage i of the slice into ring buffer i % DQ_RING: 16 bytes (4 rows' words) per
+  // copy, a warp's copies covering one word of 128 rows
+  auto issue_stage = [&](int i) {
+    constexpr int UNITS = DQ_HALVES * CW * (DQ_ROWS / 4);
+    const int buf = i % DQ_RING;
 #pragma unroll
-    for (int u = 0; u < CW; ++u)
-      if (u < nw) cp_async4(dst + u * DQ_THREADS, qw + (w0 + u) * a.m + r);
+    for (int e = tid; e < UNITS; e += DQ_THREADS) {
+      const int h = e / (CW * (DQ_ROWS / 4)), u = (e / (DQ_ROWS / 4)) % CW, q = e % (DQ_ROWS / 4);
+      const int kc = k0 + i * DQ_STAGE_COLS + h * DQ_KC;
+      if (kc < k1 && u < BITS * min(DQ_KC, k1 - kc) / 32 && 4 * q < rows)
+        cp_async16(ring + (buf * CW + u) * DQ_THREADS + h * DQ_ROWS + 4 * q,
+                   qw + (static_cast<size_t>(BITS) * kc / 32 + u) * a.m + r0 + 4 * q);
+    }
     cp_async_commit();
   };
-  auto issue_first = [&]() {
-    if (nch > 0) issue(0, kfirst);
-    if (nch > 1) issue(1, kfirst + S);
+  // the scales and packed zero words of every group for the CTA's rows
+  auto issue_table = [&]() {
+    for (int e = tid; e < tg * (DQ_ROWS / 4); e += DQ_THREADS) {
+      const int g = e / (DQ_ROWS / 4), q = e % (DQ_ROWS / 4);
+      if (4 * q < rows)
+        cp_async16(stab + g * DQ_ROWS + 4 * q, a.scales + static_cast<size_t>(g) * a.m + r0 + 4 * q);
+    }
+    for (int e = tid; e < tg * ZW; e += DQ_THREADS) {
+      const int g = e / ZW, i = e % ZW;
+      if (i < BITS * rows / 32)
+        cp_async4(zraw + e, qz + static_cast<size_t>(g) * zwords + BITS * r0 / 32 + i);
+    }
+    cp_async_commit();
   };
-  issue_first();  // in flight while the shared tables are filled
-  if (tid == 0) {
-    grange[0] = a.G;
-    grange[1] = -1;
-  }
-  __syncthreads();
-
-  // the slice's group indices, a warp per 32-column run, four runs' loads at a time
+  // x of tokens t0 .. t0 + NT over the slice, four values per thread at a time
+  auto x_load = [&](float (&v)[4], int e0, int64_t t0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * DQ_THREADS;
+      const int c = e / NT, t = e % NT;
+      v[u] = (e < NT * kn_all && t0 + t < a.n) ? ld_x(a, t0 + t, k0 + c) : 0.0f;
+    }
+  };
+  auto x_store = [&](const float (&v)[4], int e0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * DQ_THREADS;
+      if (e < NT * kn_all) xs[e] = v[u];
+    }
+  };
+  // the slice's group indices, a warp per 32-column run, four runs at a time
   const int nruns = kn_all / 32;
-  for (int run0 = warp; run0 < nruns; run0 += 4 * WARPS) {
-    int gv[4];
+  auto g_load = [&](int (&gv)[4], int run0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int run = run0 + u * WARPS;
       gv[u] = run < nruns ? a.g_idx[k0 + 32 * run + lane] : 0;
     }
+  };
+  bool mixed = false;  // a run of this warp's has columns of different groups
+  auto g_store = [&](const int (&gv)[4], int run0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int run = run0 + u * WARPS;  // the same for the whole warp
@@ -190,36 +244,45 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
         g = 0;
       }
       gs[32 * run + lane] = g;
-      const int lo = __reduce_min_sync(0xffffffffu, g), hi = __reduce_max_sync(0xffffffffu, g);
-      if (lane == 0) {
-        guni[run] = lo == hi ? g : -1;
-        atomicMin(&grange[0], lo);
-        atomicMax(&grange[1], hi);
-      }
+      const bool same = __all_sync(0xffffffffu, g == __shfl_sync(0xffffffffu, g, 0));
+      if (lane == 0) guni[run] = same ? g : -1;
+      mixed |= !same;
     }
+  };
+
+  // every copy the first pass needs is requested first; the loads of x and the group
+  // indices overlap them
+  issue_table();
+  for (int i = 0; i < min(nst, DQ_RING); ++i) issue_stage(i);
+  {
+    float v[4];
+    int gv[4];
+    x_load(v, tid, 0);
+    g_load(gv, warp);
+    x_store(v, tid);
+    g_store(gv, warp);
   }
-  __syncthreads();
-  const int glo = grange[0];  // the table holds groups glo .. grange[1]
-  if (a.table) {
-    // (with static groups a slice spans a few groups; with act-order groups, all)
-    const int total = max(0, grange[1] - glo + 1) * DQ_ROWS;
-    for (int e0 = tid; e0 < total; e0 += 16 * DQ_THREADS) {
-      float sv[16], zv[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int e = e0 + u * DQ_THREADS;
-        const int g = glo + e / DQ_ROWS, row = blockIdx.x * DQ_ROWS + e % DQ_ROWS;
-        const bool ok = e < total && row < a.m;
-        sv[u] = ok ? a.scales[static_cast<size_t>(g) * a.m + row] : 0.0f;
-        zv[u] = ok ? zero_of<BITS>(qz, zwords, g, BITS * row) : 0.0f;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int e = e0 + u * DQ_THREADS;
-        if (e < total) tab[e] = make_float2(sv[u], kTwo23 + zv[u]);
-      }
+  for (int e0 = tid + 4 * DQ_THREADS; e0 < NT * kn_all; e0 += 4 * DQ_THREADS) {
+    float v[4];
+    x_load(v, e0, 0);
+    x_store(v, e0);
+  }
+  for (int run0 = warp + 4 * WARPS; run0 < nruns; run0 += 4 * WARPS) {
+    int gv[4];
+    g_load(gv, run0);
+    g_store(gv, run0);
+  }
+  cp_async_wait_upto(min(nst, DQ_RING) - 1);  // the table and stage 0
+  // (scale, 2^23 + zero) per group and row for runs that mix groups; a run of one
+  // group reads its zero straight from the packed words
+  if (__syncthreads_or(mixed) && tg > 0) {
+    for (int e = tid; e < tg * DQ_ROWS; e += DQ_THREADS) {
+      const int g = e / DQ_ROWS, row = e % DQ_ROWS;
+      ztab[e] = kTwo23 + static_cast<float>(stream_bits<BITS>(zraw + g * ZW, BITS * row));
     }
+    __syncthreads();
   }
+
   // (scale, 2^23 + zero) of this thread's row in group g, from global memory
   auto scale_zero_g = [&](int g) -> float2 {
     return make_float2(a.scales[static_cast<size_t>(g) * a.m + r],
@@ -227,29 +290,27 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
   };
 
   for (int64_t t0 = 0; t0 < a.n; t0 += NT) {
-    for (int e0 = tid; e0 < NT * kn_all; e0 += 4 * DQ_THREADS) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * DQ_THREADS;
-        const int c = e / NT, t = e % NT;
-        v[u] = (e < NT * kn_all && t0 + t < a.n) ? ld_x(a, t0 + t, k0 + c) : 0.0f;
+    if (t0 > 0) {
+      // the next tokens: the first stages again (the ring is free: every thread has
+      // passed the cluster barrier after its decoding) and x
+      for (int i = 0; i < min(nst, DQ_RING); ++i) issue_stage(i);
+      for (int e0 = tid; e0 < NT * kn_all; e0 += 4 * DQ_THREADS) {
+        float v[4];
+        x_load(v, e0, t0);
+        x_store(v, e0);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * DQ_THREADS;
-        if (e < NT * kn_all) xs[e] = v[u];
-      }
+      cp_async_wait_upto(min(nst, DQ_RING) - 1);
+      __syncthreads();
     }
-    __syncthreads();
     float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-    // one chunk from ring stage `stage`: a loop over its 32-column runs, the run's body
-    // unrolled (a small body: the whole kernel stays in the instruction cache)
-    auto decode = [&](int stage, int kc) {
+    // this thread's chunk of a stage in ring buffer `buf`: a loop over its 32-column
+    // runs, the run's body unrolled (a small body: the whole kernel stays in the
+    // instruction cache)
+    auto decode = [&](int buf, int kc) {
       const int nrun = min(DQ_KC, k1 - kc) / 32;
-      const uint32_t* src = ring + stage * CW * DQ_THREADS + tid;
+      const uint32_t* src = ring + buf * CW * DQ_THREADS + tid;
 #pragma unroll 1
       for (int j = 0; j < nrun; ++j) {
         uint32_t w[BITS];  // the run's packed codes
@@ -260,7 +321,10 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
         const int g0 = guni[cb / 32];
         if (g0 >= 0) {
           // one group for the whole run: sum x (code - z), then scale once
-          const float2 sz = a.table ? tab[(g0 - glo) * DQ_ROWS + rl] : scale_zero_g(g0);
+          const float2 sz =
+              a.table ? make_float2(stab[g0 * DQ_ROWS + rl],
+                                    kTwo23 + static_cast<float>(stream_bits<BITS>(zraw + g0 * ZW, BITS * rl)))
+                      : scale_zero_g(g0);
           float racc[NT];
 #pragma unroll
           for (int t = 0; t < NT; ++t) racc[t] = 0.0f;
@@ -291,7 +355,8 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
             float2 sz[4];
             if (a.table) {
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc) sz[cc] = tab[(gg[cc] - glo) * DQ_ROWS + rl];
+              for (int cc = 0; cc < 4; ++cc)
+                sz[cc] = make_float2(stab[gg[cc] * DQ_ROWS + rl], ztab[gg[cc] * DQ_ROWS + rl]);
             } else {
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc) sz[cc] = scale_zero_g(gg[cc]);
@@ -307,14 +372,17 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
         }
       }
     };
-    // chunk i in stage i % 2; the stage is refilled with chunk i + 2 once decoded
-    for (int i = 0; i < nch; ++i) {
-      if (i + 1 < nch) cp_async_wait<1>();
-      else cp_async_wait<0>();
-      decode(i & 1, kfirst + i * S);
-      if (i + 2 < nch) issue(i & 1, kfirst + (i + 2) * S);
+    // stage i in buffer i % DQ_RING; once every thread is past stage i - 1 (the
+    // barrier), its buffer takes stage i + DQ_RING - 1, in flight with the stages between
+    for (int i = 0; i < nst; ++i) {
+      if (i > 0) {
+        cp_async_wait_upto(min(DQ_RING - 2, nst - 1 - i));
+        __syncthreads();
+        if (i + DQ_RING - 1 < nst) issue_stage(i + DQ_RING - 1);
+      }
+      const int kc = k0 + i * DQ_STAGE_COLS + half * DQ_KC;
+      if (row_ok && kc < k1) decode(i % DQ_RING, kc);
     }
-    if (t0 + NT < a.n) issue_first();  // the next tokens' pass, in flight during the sum
     // the cluster's slices and each slice's two halves, added by CTA 0 in a fixed order
 #pragma unroll
     for (int t = 0; t < NT; ++t) part[half][t][rl] = acc[t];
@@ -343,15 +411,26 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
   }
 }
 
+// Dynamic shared memory without the table, and the static partial sums, of one CTA.
+template <int BITS, int NT>
+int base_smem(int kper) {
+  return ring_bytes<BITS>() + ((NT + 1) * kper + kper / 32) * static_cast<int>(sizeof(float));
+}
+template <int NT>
+constexpr int static_smem() {
+  return DQ_HALVES * NT * DQ_ROWS * static_cast<int>(sizeof(float));
+}
+
 template <int BITS, int NT>
 void launch_nt(const DqArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(ceil_div(a.m, DQ_ROWS)), DQ_SPLIT);
-  const int base = ring_bytes<BITS>() +
-                   ((NT + 1) * a.kper + a.kper / 32) * static_cast<int>(sizeof(float));
-  // the (scale, 2^23 + zero) table when it fits beside two CTAs' other shared memory on an SM
-  const int tab = 2 * a.G * DQ_ROWS * static_cast<int>(sizeof(float));
+  const int base = base_smem<BITS, NT>(a.kper);
+  // the per-group table when two CTAs still fit on an SM (228 KB of shared memory, 1 KB
+  // of it reserved per CTA, and the static partial sums)
+  const int tab = a.G * table_bytes_per_group<BITS>();
+  const int two_per_sm = 228 * 1024 / 2 - 1024 - static_smem<NT>();
   DqArgs b = a;
-  b.table = (base + tab <= 100 * 1024) ? 1 : 0;
+  b.table = (base + tab <= two_per_sm) ? 1 : 0;
   const int smem = base + (b.table ? tab : 0);
   // the largest dynamic size allowed so far (the default allows 48 KB less the static
   // shared memory)
@@ -367,8 +446,12 @@ void launch_nt(const DqArgs& a, cudaStream_t s) {
 
 template <int BITS>
 void launch_bits(const DqArgs& a, cudaStream_t s) {
-  if (a.n == 1) launch_nt<BITS, 1>(a, s);
-  else launch_nt<BITS, 8>(a, s);
+  // eight tokens per pass unless their slice of x does not fit beside the ring (a CTA may
+  // have 227 KB of shared memory); then one token per pass
+  if (a.n > 1 && base_smem<BITS, 8>(a.kper) + static_smem<8>() <= 227 * 1024)
+    launch_nt<BITS, 8>(a, s);
+  else
+    launch_nt<BITS, 1>(a, s);
 }
 
 // W_hat[r, c] = s[g, r] (code[r, c] - z[g, r]), g = g_idx[c], as bf16 or float32,

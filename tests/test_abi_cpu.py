@@ -124,6 +124,8 @@ def _call_dq(**kw):
     (dict(ws=P + 4), G.GPTQ_ERR_INVALID_ARG),
     (dict(wsb=8), G.GPTQ_ERR_INVALID_ARG),
     (dict(y=None), G.GPTQ_ERR_INVALID_ARG),
+    (dict(qw=P + 4), G.GPTQ_ERR_INVALID_ARG),   # copied 16 bytes at a time
+    (dict(sc=P + 8), G.GPTQ_ERR_INVALID_ARG),
 ])
 def test_dequant_matmul_argument_checks(kw, status):
     assert _call_dq(**kw) == status

@@ -83,6 +83,27 @@ def test_dequant_matmul_q_proj(lib, cuda_device, static):
     assert rel_fro(to_np(y), ref) <= Y_REL_FRO
 
 
+@pytest.mark.parametrize("m,d,bits,group,n", [
+    (64, 32768, 8, 128, 16),   # eight tokens' x does not fit beside the ring: one per pass
+    (96, 28672, 4, 128, 3),    # the table (224 groups) does not fit: global lookups
+])
+def test_dequant_matmul_wide_random(lib, cuda_device, m, d, bits, group, n):
+    """Wide layers on a random valid checkpoint (any codes, positive scales, act-order
+    style g_idx), against the oracle's dequantise-then-multiply."""
+    rng = np.random.default_rng(d + bits)
+    G = d // group
+    qweight = rng.integers(-2**31, 2**31, size=(bits * d // 32, m), dtype=np.int64).astype(np.int32)
+    qzeros = rng.integers(-2**31, 2**31, size=(G, bits * m // 32), dtype=np.int64).astype(np.int32)
+    scales = (rng.random((G, m)) * 0.01 + 1e-3).astype(np.float32)
+    g_idx = (rng.permutation(d) // group).astype(np.int32)
+    x = _dev(rng.standard_normal((n, d)).astype(np.float32), cuda_device, torch.bfloat16)
+    y = lib.gptq_dequant_matmul(x, _dev(qweight, cuda_device), _dev(scales, cuda_device),
+                                _dev(qzeros, cuda_device), _dev(g_idx, cuda_device), bits)
+    torch.cuda.synchronize()
+    ref = O.dequant_matmul(to_np(x).astype(np.float64), qweight, scales, qzeros, g_idx, bits)
+    assert rel_fro(to_np(y), ref) <= Y_REL_FRO
+
+
 @pytest.mark.parametrize("bits,group,static", [(4, 32, False), (3, 64, True), (8, -1, False)])
 def test_dequantize_dense(lib, cuda_device, bits, group, static):
     """gptq_dequantize: W_hat = s (code - z) per original column's group.  One float32
