@@ -103,6 +103,25 @@ __device__ __forceinline__ float code_minus(uint32_t code, float zb) {
   return __uint_as_float(code | kTwo23Bits) - zb;
 }
 
+// Two floats in one 64-bit register pair, and the paired fused multiply-add of sm_100 and
+// later (one instruction for both lanes, each lane rounded as the scalar fmaf).  With
+// several tokens a pass pairs tokens 2p and 2p + 1 on the same weight.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
@@ -325,26 +344,50 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
               a.table ? make_float2(stab[g0 * DQ_ROWS + rl],
                                     kTwo23 + static_cast<float>(stream_bits<BITS>(zraw + g0 * ZW, BITS * rl)))
                       : scale_zero_g(g0);
-          float racc[NT];
+          if constexpr (NT == 1) {
+            // one token: scalar (paired lanes over columns measured no faster here)
+            float racc = 0.0f;
 #pragma unroll
-          for (int t = 0; t < NT; ++t) racc[t] = 0.0f;
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 xq = x4[c4];
+              const float xv[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            float xv[4 * NT];
+              for (int cc = 0; cc < 4; ++cc)
+                racc = fmaf(xv[cc], code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)), sz.y), racc);
+            }
+            acc[0] = fmaf(sz.x, racc, acc[0]);
+          } else {
+            // lanes: tokens 2p and 2p + 1
+            uint64_t r2[NT / 2];
 #pragma unroll
-            for (int q = 0; q < NT; ++q) *reinterpret_cast<float4*>(&xv[4 * q]) = x4[c4 * NT + q];
+            for (int p = 0; p < NT / 2; ++p) r2[p] = pack2(0.0f, 0.0f);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const float v = code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)), sz.y);
+            for (int c4 = 0; c4 < 8; ++c4) {
+              float xv[4 * NT];
 #pragma unroll
-              for (int t = 0; t < NT; ++t) racc[t] = fmaf(xv[cc * NT + t], v, racc[t]);
+              for (int q = 0; q < NT; ++q) *reinterpret_cast<float4*>(&xv[4 * q]) = x4[c4 * NT + q];
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const float v = code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)), sz.y);
+                const uint64_t v2 = pack2(v, v);
+#pragma unroll
+                for (int p = 0; p < NT / 2; ++p)
+                  r2[p] = fma2(pack2(xv[cc * NT + 2 * p], xv[cc * NT + 2 * p + 1]), v2, r2[p]);
+              }
+            }
+#pragma unroll
+            for (int p = 0; p < NT / 2; ++p) {
+              const float2 rr = unpack2(r2[p]);
+              acc[2 * p] = fmaf(sz.x, rr.x, acc[2 * p]);
+              acc[2 * p + 1] = fmaf(sz.x, rr.y, acc[2 * p + 1]);
             }
           }
-#pragma unroll
-          for (int t = 0; t < NT; ++t) acc[t] = fmaf(sz.x, racc[t], acc[t]);
         } else {
           // each column's own group (act-order)
           const int4* g4 = reinterpret_cast<const int4*>(gs + cb);
+          uint64_t r2[NT == 1 ? 1 : NT / 2];
+#pragma unroll
+          for (int p = 0; p < (NT == 1 ? 1 : NT / 2); ++p) r2[p] = pack2(0.0f, 0.0f);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             float xv[4 * NT];
@@ -361,12 +404,30 @@ __global__ void __cluster_dims__(1, DQ_SPLIT, 1) __launch_bounds__(DQ_THREADS, 2
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc) sz[cc] = scale_zero_g(gg[cc]);
             }
+            if constexpr (NT == 1) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const float v = sz[cc].x *
-                              code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)), sz[cc].y);
+              for (int cc = 0; cc < 4; ++cc)
+                acc[0] = fmaf(xv[cc], sz[cc].x * code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)),
+                                                            sz[cc].y),
+                              acc[0]);
+            } else {
 #pragma unroll
-              for (int t = 0; t < NT; ++t) acc[t] = fmaf(xv[cc * NT + t], v, acc[t]);
+              for (int cc = 0; cc < 4; ++cc) {
+                const float v = sz[cc].x *
+                                code_minus(reg_bits<BITS>(w, BITS * (4 * c4 + cc)), sz[cc].y);
+                const uint64_t v2 = pack2(v, v);
+#pragma unroll
+                for (int p = 0; p < NT / 2; ++p)
+                  r2[p] = fma2(pack2(xv[cc * NT + 2 * p], xv[cc * NT + 2 * p + 1]), v2, r2[p]);
+              }
+            }
+          }
+          if constexpr (NT > 1) {
+#pragma unroll
+            for (int p = 0; p < NT / 2; ++p) {
+              const float2 rr = unpack2(r2[p]);
+              acc[2 * p] += rr.x;
+              acc[2 * p + 1] += rr.y;
             }
           }
         }
