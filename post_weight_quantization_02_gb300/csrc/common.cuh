@@ -28,6 +28,14 @@ void set_last_error(const std::string& msg);
 
 #define GPTQ_CUDA(call) ::gptq::cuda_check((call), #call)
 
+// Lets kernel `func` take at least `bytes` of dynamic shared memory on the current device
+// (raised once per device and size; safe to call from several host threads).
+void ensure_dynamic_smem(const void* func, int bytes);
+template <typename F>
+void ensure_dynamic_smem(F* func, int bytes) {
+  ensure_dynamic_smem(reinterpret_cast<const void*>(func), bytes);
+}
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

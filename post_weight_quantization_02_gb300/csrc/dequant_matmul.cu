@@ -493,14 +493,8 @@ void launch_nt(const DqArgs& a, cudaStream_t s) {
   DqArgs b = a;
   b.table = (base + tab <= two_per_sm) ? 1 : 0;
   const int smem = base + (b.table ? tab : 0);
-  // the largest dynamic size allowed so far (the default allows 48 KB less the static
-  // shared memory)
-  static int attr = 0;
-  if (smem > attr) {
-    GPTQ_CUDA(cudaFuncSetAttribute(dequant_matmul_kernel<BITS, NT>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    attr = smem;
-  }
+  // (the default limit is 48 KB less the static shared memory)
+  ensure_dynamic_smem(dequant_matmul_kernel<BITS, NT>, smem);
   GPTQ_LAUNCH(GPTQ_K_DEQUANT_MATMUL, s, (dequant_matmul_kernel<BITS, NT>), grid, DQ_THREADS, smem,
               b);
 }

@@ -262,12 +262,7 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   if ((beta != 0.0f && beta != 1.0f) || (lower && beta != 1.0f)) {
     fail(GPTQ_ERR_INVALID_ARG, "launch_gemm_tf32x3: beta must be 0 or 1 (1 in lower mode)");
   }
-  static bool attr = false;
-  if (!attr) {
-    GPTQ_CUDA(cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SMEM_BYTES));
-    attr = true;
-  }
+  ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
   // the M x N result, in boxes of 32 x 32 (128-byte rows, swizzled like the staging)
   CUtensorMap mc;
   make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),

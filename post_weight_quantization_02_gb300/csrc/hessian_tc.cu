@@ -293,12 +293,7 @@ int syrk_tc_token_granule() { return BK; }
 
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA(cudaFuncSetAttribute(syrk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SMEM_BYTES));
-    attr_done = true;
-  }
+  ensure_dynamic_smem(syrk_tc_kernel, SMEM_BYTES);
   CUtensorMap tmap;
   make_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(d),
                static_cast<uint64_t>(ntok), static_cast<uint64_t>(d) * 2, 64, BK,

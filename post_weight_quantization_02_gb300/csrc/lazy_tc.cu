@@ -286,12 +286,7 @@ LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int 
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
                     DevStatus* st, cudaStream_t s, int max_ctas) {
   if (k <= 0 || c_end <= c_begin || mp.m <= 0) return;
-  static bool attr = false;
-  if (!attr) {
-    GPTQ_CUDA(cudaFuncSetAttribute(lazy_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SMEM_BYTES));
-    attr = true;
-  }
+  ensure_dynamic_smem(lazy_tc_kernel, SMEM_BYTES);
   LazyArgs a;
   a.m = mp.m;
   a.d = mp.d;

@@ -508,12 +508,7 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   const unsigned t32 = (unsigned)ceil_div(d, 32);
   GPTQ_LAUNCH(GPTQ_K_PREP_MIRROR, s, prep_mirror_kernel, dim3(t32, t32), 256, 0, H, d, S, st);
   const size_t row_smem = static_cast<size_t>(d) * sizeof(float);
-  static size_t attr_smem = 0;
-  if (row_smem > 48 * 1024 && row_smem > attr_smem) {
-    GPTQ_CUDA(cudaFuncSetAttribute(prep_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(row_smem)));
-    attr_smem = row_smem;
-  }
+  ensure_dynamic_smem(prep_gather_kernel, static_cast<int>(row_smem));
   GPTQ_LAUNCH(GPTQ_K_PREP_GATHER, s, prep_gather_kernel, d, 256, row_smem, S, d, perm, dead, lam,
               Hr);
 
@@ -544,12 +539,7 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_CUDA(cudaFuncGetAttributes(&diag_attr, chol_inv_diag_kernel));
   const int diag_smem = std::max(kDiagSmemFloats * static_cast<int>(sizeof(float)),
                                  smem_optin - static_cast<int>(diag_attr.sharedSizeBytes));
-  static bool attrs = false;
-  if (!attrs) {
-    GPTQ_CUDA(cudaFuncSetAttribute(chol_inv_diag_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, diag_smem));
-    attrs = true;
-  }
+  ensure_dynamic_smem(chol_inv_diag_kernel, diag_smem);
   CUtensorMap mHr, mS, mDI;
   make_gemm_map(&mHr, Hr, d, d, d);
   make_gemm_map(&mS, S, d, d, d);

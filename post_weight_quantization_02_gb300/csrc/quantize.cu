@@ -577,24 +577,13 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
   }
   if (m > 0) {
     const size_t row_smem = static_cast<size_t>(d) * sizeof(float);
-    static size_t attr_f = 0, attr_b = 0;
     if (q.w_bf16) {
-      if (row_smem > 48 * 1024 && row_smem > attr_b) {
-        GPTQ_CUDA(cudaFuncSetAttribute(gather_w_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(row_smem)));
-        attr_b = row_smem;
-      }
+      ensure_dynamic_smem(gather_w_kernel<__nv_bfloat16>, static_cast<int>(row_smem));
       GPTQ_LAUNCH(GPTQ_K_QUANT_GATHER, s, gather_w_kernel<__nv_bfloat16>, m, 256, row_smem,
                   static_cast<const __nv_bfloat16*>(q.W), d, q.perm, q.dead, q.Wp, q.loss_rows,
                   q.st);
     } else {
-      if (row_smem > 48 * 1024 && row_smem > attr_f) {
-        GPTQ_CUDA(cudaFuncSetAttribute(gather_w_kernel<float>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(row_smem)));
-        attr_f = row_smem;
-      }
+      ensure_dynamic_smem(gather_w_kernel<float>, static_cast<int>(row_smem));
       GPTQ_LAUNCH(GPTQ_K_QUANT_GATHER, s, gather_w_kernel<float>, m, 256, row_smem,
                   static_cast<const float*>(q.W), d, q.perm, q.dead, q.Wp, q.loss_rows, q.st);
     }
@@ -603,16 +592,8 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
     const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, 2 * kErrRows, q.uhi, q.ulo, q.Wp, m, d);
-    static bool loop_attr = false;
-    if (!loop_attr) {
-      GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kLoopSmemDynamic));
-      GPTQ_CUDA(cudaFuncSetAttribute(column_loop_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kLoopSmemStatic));
-      loop_attr = true;
-    }
+    ensure_dynamic_smem(column_loop_kernel<false>, kLoopSmemDynamic);
+    ensure_dynamic_smem(column_loop_kernel<true>, kLoopSmemStatic);
     const bool inblock_fit = !stat && q.group > 0 && q.group <= BLK;
     // Deferred updates in two levels: superblocks of kErrRows columns, unless a group that
     // starts inside a superblock would reach past its end (its fit must see every earlier

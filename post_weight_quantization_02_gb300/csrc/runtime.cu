@@ -117,6 +117,19 @@ void trace_discard() {
 
 void profile_enable(bool on) { g_enabled.store(on); }
 void profile_select(uint32_t mask) { g_mask.store(mask); }
+
+void ensure_dynamic_smem(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> limit;  // (device, kernel) -> bytes
+  int dev = 0;
+  GPTQ_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  int& cur = limit[{dev, func}];
+  if (bytes > cur) {
+    GPTQ_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    cur = bytes;
+  }
+}
 void profile_reset() {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int k = 0; k < GPTQ_K_COUNT; ++k) {
