@@ -20,7 +20,7 @@ triangular solve).  Sources, by page:
 * "GPTQ > ActOrder: Activation-Based Column Ordering" (mbrenndoerfer): the act-order
   permutation by descending Hessian diagonal.
 
-Readings where the pages are silent or disagree (all restated in the design doc):
+Readings where the pages are silent or disagree:
 
 * H is normalised as 2/n * sum(x x^T) (the streaming hook), not 2XX^T; every output but the
   loss is invariant to a positive scale of H because the damping is relative.
