@@ -11,6 +11,9 @@
  *                            lazy trailing update, group scales / zeros, g_idx and
  *                            bit packing
  *
+ * and two calls consume the packed checkpoint: gptq_dequant_matmul (y = x W_hat^T) and
+ * gptq_dequantize (the dense W_hat).
+ *
  * Conventions shared by every call
  * --------------------------------
  * - Device pointers are CUDA device memory on the current device, allocated and owned by
@@ -26,6 +29,10 @@
  * - On any status other than GPTQ_OK, gptq_last_error() (thread-local) describes it.
  *   Invalid arguments are detected before anything is enqueued; outputs are then
  *   untouched.
+ * - Calls may come from several host threads and for several devices in one process;
+ *   the library's own state (kernel attributes, internal streams) is kept per device.
+ *   gptq_prepare and gptq_quantize_layer(_ex) share internal streams, so concurrent
+ *   calls of those two run one after the other.
  */
 #ifndef GPTQ_GB300_H
 #define GPTQ_GB300_H

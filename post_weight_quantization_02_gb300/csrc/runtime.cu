@@ -151,7 +151,7 @@ int64_t launch_count() { return g_launches.load(); }
 int sm_count() {
   int dev = 0;
   cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
-  static int cached_dev = -1, cached = 0;
+  thread_local int cached_dev = -1, cached = 0;  // per host thread: no shared state
   if (dev != cached_dev) {
     cuda_check(cudaDeviceGetAttribute(&cached, cudaDevAttrMultiProcessorCount, dev),
                "cudaDeviceGetAttribute");
@@ -192,8 +192,8 @@ std::mutex& aux_mutex() {
 void make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                   uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encode == nullptr) {
+  // looked up once (a function-local static's initialisation is thread-safe)
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cuda_check(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
@@ -202,8 +202,8 @@ void make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
     if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
       fail(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     }
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
