@@ -595,6 +595,49 @@ def quadratic_loss(delta: np.ndarray, H: np.ndarray) -> np.ndarray:
     return 0.5 * np.einsum("ri,ij,rj->r", delta, np.asarray(H, dtype=F64), delta)
 
 
+def babai_nearest_plane(C, t) -> np.ndarray:
+    """Babai's nearest-plane algorithm for the closest vector problem: the integer
+    coefficients z of the lattice point sum_j z_j c_j that it returns for the basis
+    columns ``C`` ``[n, d]`` and the target ``t`` ``[n]``.
+
+    "04 - GPTQ", section 4 (GPTQ as Babai's nearest-plane algorithm on the lattice the
+    calibration Hessian defines).  With C = Q R (R upper triangular) and y = Q^T t, the
+    coefficients are fixed from the last to the first: z_j is the integer nearest to
+    (y_j - sum_{k>j} R_jk z_k) / R_jj, the hyperplane of the remaining sublattice that
+    lies nearest the target.
+    """
+    C = np.asarray(C, dtype=F64)
+    Qm, R = np.linalg.qr(C)
+    y = Qm.T @ np.asarray(t, dtype=F64)
+    d = C.shape[1]
+    z = np.zeros(d, dtype=F64)
+    for j in range(d - 1, -1, -1):
+        z[j] = np.rint((y[j] - R[j, j + 1:] @ z[j + 1:]) / R[j, j])
+    return z.astype(np.int64)
+
+
+def gptq_babai(Wp, Hd, scales) -> np.ndarray:
+    """GPTQ's codes on fixed, unclipped per-row grids s_r Z, computed as Babai's nearest
+    plane ("04 - GPTQ", section 4: GPTQ run back to front is that algorithm).
+
+    Row r minimises (what - w_r)^T Hd (what - w_r) over what in s_r Z^d.  With any B such
+    that B^T B = Hd (here from the eigendecomposition, so nothing is shared with the
+    Cholesky factor the column loop uses), the lattice has the basis vectors s_r B[:, j]
+    and the target is B w_r.  Babai's pass fixes the last basis vector first, so the
+    columns are handed over in reverse order and the pass visits column 0 first, as the
+    column loop does.  ``Wp`` ``[m, d]`` and ``Hd`` are in processing order; returns the
+    codes ``[m, d]`` in that order.
+    """
+    W = np.asarray(Wp, dtype=F64)
+    lam, V = np.linalg.eigh(np.asarray(Hd, dtype=F64))
+    B = np.sqrt(lam)[:, None] * V.T
+    s = np.asarray(scales, dtype=F64).reshape(-1)
+    codes = np.zeros(W.shape, dtype=np.int64)
+    for r in range(W.shape[0]):
+        codes[r] = babai_nearest_plane(s[r] * B[:, ::-1], B @ W[r])[::-1]
+    return codes
+
+
 def rtn_quantize(Wp, bits: int = 4, group: int = 128, sym: bool = False
                  ) -> Dict[str, np.ndarray]:
     """Round-to-nearest on the same groups, fitted on the uncompensated weights ("Same

@@ -481,12 +481,53 @@ def pin_block_pipeline(O):
     assert np.array_equal(steps[1]["inputs"]["qkv"], P.rmsnorm(steps[0]["y"]).reshape(B * S, h))
 
 
+def unclipped_grid(s):
+    """Fixed per-row grids s_r Z without clipping (the lattice of the Babai view)."""
+    def q(col_idx, w):
+        c = np.rint(w / s)
+        return c.astype(np.int64), c * s
+    return q
+
+
+def pin_babai(O):
+    """Babai's nearest plane ("04 - GPTQ", section 4).  On an orthogonal basis it rounds
+    each coordinate, which solves the closest vector problem exactly (brute force over a
+    box); GPTQ without clipping returns exactly its codes on random Hessians, blocked or
+    not; and each row's loss stays within the bound that rounding gives,
+    sum_q (s/2)^2 / (2 U_qq^2)."""
+    rng = np.random.default_rng(23)
+    for _ in range(5):
+        d = 4
+        Qb, _ = np.linalg.qr(rng.standard_normal((d, d)))
+        lens = np.exp(rng.standard_normal(d))
+        C = Qb * lens                                    # orthogonal columns
+        t = rng.standard_normal(d) * 3.0
+        z = O.babai_nearest_plane(C, t)
+        assert np.array_equal(z, np.rint(Qb.T @ t / lens).astype(np.int64))
+        box = np.stack(np.meshgrid(*[np.arange(-2, 3)] * d, indexing="ij"), -1)
+        box = box.reshape(-1, d) + z
+        dist = np.sum((box @ C.T - t) ** 2, axis=1)
+        assert np.sum((C @ z - t) ** 2) <= dist.min() * (1 + 1e-12) + 1e-15
+    for d, B in [(16, 10 ** 9), (24, 8), (40, 16), (32, 1)]:
+        H, _ = spd(rng, d)
+        Hd, _ = O.damping(H, 0.01)
+        U = O.inverse_cholesky_upper(Hd)
+        W = rng.standard_normal((4, d)) * 0.02
+        s = np.abs(W).max(axis=1) / 7.0
+        r = O.gptq_sweep(W, U, blocksize=B, column_quantizer=unclipped_grid(s))
+        assert np.array_equal(O.gptq_babai(W, Hd, s), r["codes"]), (d, B)
+        bound = 0.5 * (s / 2.0) ** 2 * np.sum(1.0 / np.diag(U) ** 2)
+        assert np.all(r["loss_rows"] <= bound * (1 + 1e-12))
+        assert np.allclose(r["loss_rows"], O.quadratic_loss(r["Q"] - W, Hd), rtol=1e-9)
+
+
 PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
         pin_cholesky_2x2, pin_cholesky_general, pin_obs_equals_cholesky,
         pin_blocked_equals_unblocked, pin_loss_identity, pin_brute_force_optimum,
         pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
         pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
-        pin_format_roundtrip, pin_static_groups, pin_dequantize, pin_block_pipeline]
+        pin_format_roundtrip, pin_static_groups, pin_dequantize, pin_block_pipeline,
+        pin_babai]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
