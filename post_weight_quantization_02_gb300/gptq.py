@@ -119,6 +119,30 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _buf(t: Optional[torch.Tensor], dtype, numel: Optional[int], name: str) -> Optional[int]:
+    """Device pointer of a caller buffer, after checking its element type and (when known)
+    its number of elements: the library reads raw memory and cannot check either."""
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+    return _ptr(t)
+
+
+def _ngroups(d: int, group: int) -> Optional[int]:
+    """Rows of scales / qzeros for a valid group size (None: left to the library)."""
+    if group == -1:
+        return 1
+    return -(-d // group) if group > 0 else None
+
+
+def _packed(bits: int, count: int) -> Optional[int]:
+    """32-bit words of `count` codes of `bits` bits (None: bits left to the library)."""
+    return bits * count // 32 if bits in (2, 3, 4, 8) else None
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -166,10 +190,11 @@ def gptq_hessian_accumulate(H: torch.Tensor, nseen: int, X: torch.Tensor,
     d = H.shape[0]
     if X.dim() != 2 or X.shape[1] != d:
         raise ValueError("X must be [ntok, d_in]")
+    pH = _buf(H, torch.float32, d * d, "H")
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_HESSIAN, X.shape[0], 0, d), H.device)
     n = ctypes.c_int64(int(nseen))
-    _check(lib().gptq_hessian_accumulate(_ptr(H), ctypes.byref(n), _ptr(X) if X.numel() else None,
+    _check(lib().gptq_hessian_accumulate(pH, ctypes.byref(n), _ptr(X) if X.numel() else None,
                                          _dtype_code(X), X.shape[0], d, _ptr(ws), ws.numel(),
                                          _stream(stream)))
     return int(n.value)
@@ -182,8 +207,9 @@ def gptq_hessian_accumulate_async(H: torch.Tensor, nseen: int, X: torch.Tensor,
     d = H.shape[0]
     if X.dim() != 2 or X.shape[1] != d:
         raise ValueError("X must be [ntok, d_in]")
+    pH = _buf(H, torch.float32, d * d, "H")
     n = ctypes.c_int64(int(nseen))
-    _check(lib().gptq_hessian_accumulate_async(_ptr(H), ctypes.byref(n),
+    _check(lib().gptq_hessian_accumulate_async(pH, ctypes.byref(n),
                                                _ptr(X) if X.numel() else None, _dtype_code(X),
                                                X.shape[0], d, _ptr(ws), ws.numel(),
                                                _stream(stream)))
@@ -200,11 +226,13 @@ def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tenso
                  stream=None) -> int:
     """Dead fix, act-order, damping, U; returns info (0, or the failing pivot)."""
     d = H.shape[0]
+    ptrs = (_buf(H, torch.float32, d * d, "H"), _buf(perm, torch.int32, d, "perm"),
+            _buf(dead, torch.uint8, d, "dead"), _buf(Hinv_chol, torch.float32, d * d, "Hinv_chol"))
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_PREPARE, 0, 0, d), H.device)
     info = ctypes.c_int32(0)
-    st = lib().gptq_prepare(_ptr(H), d, float(damp), int(bool(actorder)), _ptr(perm), _ptr(dead),
-                            _ptr(Hinv_chol), ctypes.byref(info), _ptr(ws), ws.numel(),
+    st = lib().gptq_prepare(ptrs[0], d, float(damp), int(bool(actorder)), ptrs[1], ptrs[2],
+                            ptrs[3], ctypes.byref(info), _ptr(ws), ws.numel(),
                             _stream(stream))
     if st != GPTQ_OK:
         err = GptqError(st, gptq_last_error())
@@ -222,14 +250,33 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional
     """The column loop and packing; ``static_groups`` fits the groups in the original
     column order before the loop (gptq_quantize_layer_ex, GPTQ_QUANT_STATIC_GROUPS)."""
     m, d = W.shape
+    G = _ngroups(d, group)
+    words = _packed(bits, d)
+    zwords = _packed(bits, m)
+    ptrs = (_buf(Hinv_chol, torch.float32, d * d, "Hinv_chol"),
+            _buf(perm, torch.int32, d, "perm"), _buf(dead, torch.uint8, d, "dead"),
+            _buf(qweight, torch.int32, None if words is None else words * m, "qweight"),
+            _buf(scales, torch.float32, None if G is None else G * m, "scales"),
+            _buf(qzeros, torch.int32, None if G is None or zwords is None else G * zwords,
+                 "qzeros"),
+            _buf(g_idx, torch.int32, d, "g_idx"), _buf(loss, torch.float64, 1, "loss"))
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_QUANTIZE, 0, m, d, bits, group), W.device)
     flags = GPTQ_QUANT_STATIC_GROUPS if static_groups else 0
-    _check(lib().gptq_quantize_layer_ex(_ptr(W), _dtype_code(W), _ptr(Hinv_chol), _ptr(perm),
-                                        _ptr(dead), m, d, bits, group, int(bool(sym)),
-                                        blocksize, flags, _ptr(qweight), _ptr(scales),
-                                        _ptr(qzeros), _ptr(g_idx), _ptr(loss), _ptr(ws),
-                                        ws.numel(), _stream(stream)))
+    _check(lib().gptq_quantize_layer_ex(_ptr(W), _dtype_code(W), ptrs[0], ptrs[1], ptrs[2], m, d,
+                                        bits, group, int(bool(sym)), blocksize, flags, *ptrs[3:],
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def _checkpoint_ptrs(qweight, scales, qzeros, g_idx, bits: int, m: int, d: int):
+    """Pointers of a packed checkpoint after checking types and sizes (G = rows of scales)."""
+    G = scales.shape[0] if scales.dim() == 2 else None
+    words, zwords = _packed(bits, d), _packed(bits, m)
+    return (_buf(qweight, torch.int32, None if words is None else words * m, "qweight"),
+            _buf(scales, torch.float32, None if G is None else G * m, "scales"),
+            _buf(qzeros, torch.int32, None if G is None or zwords is None else G * zwords,
+                 "qzeros"),
+            _buf(g_idx, torch.int32, d, "g_idx"))
 
 
 def gptq_dequant_matmul(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
@@ -243,11 +290,12 @@ def gptq_dequant_matmul(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
     m = qweight.shape[1]
     if y is None:
         y = torch.empty(n, m, dtype=torch.float32, device=x.device)
+    ptrs = _checkpoint_ptrs(qweight, scales, qzeros, g_idx, bits, m, d)
+    py = _buf(y, torch.float32, n * m, "y")
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, 0, m, d, bits, -1), x.device)
     _check(lib().gptq_dequant_matmul(_ptr(x) if x.numel() else None, _dtype_code(x), n, d, m,
-                                     bits, _ptr(qweight), _ptr(scales), _ptr(qzeros),
-                                     _ptr(g_idx), scales.shape[0], _ptr(y), _ptr(ws),
+                                     bits, *ptrs, scales.shape[0], py, _ptr(ws),
                                      ws.numel(), _stream(stream)))
     return y
 
@@ -261,12 +309,14 @@ def gptq_dequantize(qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.T
     d = qweight.shape[0] * 32 // bits
     if W is None:
         W = torch.empty(m, d, dtype=dtype, device=qweight.device)
+    ptrs = _checkpoint_ptrs(qweight, scales, qzeros, g_idx, bits, m, d)
+    if W.numel() != m * d:
+        raise ValueError(f"W must hold {m * d} elements, got {W.numel()}")
     if ws is None:
         ws = workspace(gptq_workspace_size(GPTQ_OP_DEQUANT_MATMUL, 0, m, d, bits, -1),
                        qweight.device)
-    _check(lib().gptq_dequantize(_ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx), m, d,
-                                 bits, scales.shape[0], _ptr(W), _dtype_code(W), _ptr(ws),
-                                 ws.numel(), _stream(stream)))
+    _check(lib().gptq_dequantize(*ptrs, m, d, bits, scales.shape[0], _ptr(W), _dtype_code(W),
+                                 _ptr(ws), ws.numel(), _stream(stream)))
     return W
 
 
