@@ -617,13 +617,15 @@ def babai_nearest_plane(C, t) -> np.ndarray:
 
 
 def gptq_babai(Wp, Hd, scales) -> np.ndarray:
-    """GPTQ's codes on fixed, unclipped per-row grids s_r Z, computed as Babai's nearest
-    plane ("04 - GPTQ", section 4: GPTQ run back to front is that algorithm).
+    """GPTQ's codes on fixed, unclipped grids, computed as Babai's nearest plane
+    ("04 - GPTQ", section 4: GPTQ run back to front is that algorithm).
 
-    Row r minimises (what - w_r)^T Hd (what - w_r) over what in s_r Z^d.  With any B such
-    that B^T B = Hd (here from the eigendecomposition, so nothing is shared with the
-    Cholesky factor the column loop uses), the lattice has the basis vectors s_r B[:, j]
-    and the target is B w_r.  Babai's pass fixes the last basis vector first, so the
+    ``scales`` is ``[m]`` (one step per row) or ``[m, d]`` (a step per row and column,
+    e.g. group-wise grids fixed before the loop).  Row r minimises
+    (what - w_r)^T Hd (what - w_r) over what_j in s_rj Z.  With any B such that
+    B^T B = Hd (here from the eigendecomposition, so nothing is shared with the Cholesky
+    factor the column loop uses), the lattice has the basis vectors s_rj B[:, j] and the
+    target is B w_r.  Babai's pass fixes the last basis vector first, so the
     columns are handed over in reverse order and the pass visits column 0 first, as the
     column loop does.  ``Wp`` ``[m, d]`` and ``Hd`` are in processing order; returns the
     codes ``[m, d]`` in that order.
@@ -631,10 +633,12 @@ def gptq_babai(Wp, Hd, scales) -> np.ndarray:
     W = np.asarray(Wp, dtype=F64)
     lam, V = np.linalg.eigh(np.asarray(Hd, dtype=F64))
     B = np.sqrt(lam)[:, None] * V.T
-    s = np.asarray(scales, dtype=F64).reshape(-1)
+    s = np.asarray(scales, dtype=F64)
+    if s.ndim == 1:
+        s = np.repeat(s[:, None], W.shape[1], axis=1)
     codes = np.zeros(W.shape, dtype=np.int64)
     for r in range(W.shape[0]):
-        codes[r] = babai_nearest_plane(s[r] * B[:, ::-1], B @ W[r])[::-1]
+        codes[r] = babai_nearest_plane((B * s[r][None, :])[:, ::-1], B @ W[r])[::-1]
     return codes
 
 

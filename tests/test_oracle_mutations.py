@@ -51,8 +51,12 @@ MUTATIONS = {
     "static_fit_on_permuted": ("sc, ze = static_group_fit(W, group, bits, sym,",
                                "sc, ze = static_group_fit(W[:, perm], group, bits, sym,"),
     "static_g_idx_permuted": ("if static and group != -1:", "if False:"),
-    "babai_natural_order": ("codes[r] = babai_nearest_plane(s[r] * B[:, ::-1], B @ W[r])[::-1]",
-                            "codes[r] = babai_nearest_plane(s[r] * B, B @ W[r])"),
+    "babai_natural_order": (
+        "codes[r] = babai_nearest_plane((B * s[r][None, :])[:, ::-1], B @ W[r])[::-1]",
+        "codes[r] = babai_nearest_plane(B * s[r][None, :], B @ W[r])"),
+    "babai_steps_reversed": (
+        "codes[r] = babai_nearest_plane((B * s[r][None, :])[:, ::-1], B @ W[r])[::-1]",
+        "codes[r] = babai_nearest_plane((B * s[r][::-1][None, :])[:, ::-1], B @ W[r])[::-1]"),
     "babai_floor": ("z[j] = np.rint((y[j] - R[j, j + 1:] @ z[j + 1:]) / R[j, j])",
                     "z[j] = np.floor((y[j] - R[j, j + 1:] @ z[j + 1:]) / R[j, j])"),
     "dequant_zero_dropped": ("return s * (codes.astype(F64) - z)", "return s * codes.astype(F64)"),

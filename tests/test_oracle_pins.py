@@ -482,10 +482,12 @@ def pin_block_pipeline(O):
 
 
 def unclipped_grid(s):
-    """Fixed per-row grids s_r Z without clipping (the lattice of the Babai view)."""
+    """Fixed grids without clipping (the lattice of the Babai view): s ``[m]`` per row,
+    or ``[m, d]`` per row and column."""
     def q(col_idx, w):
-        c = np.rint(w / s)
-        return c.astype(np.int64), c * s
+        sc = s if s.ndim == 1 else s[:, col_idx]
+        c = np.rint(w / sc)
+        return c.astype(np.int64), c * sc
     return q
 
 
@@ -519,6 +521,18 @@ def pin_babai(O):
         bound = 0.5 * (s / 2.0) ** 2 * np.sum(1.0 / np.diag(U) ** 2)
         assert np.all(r["loss_rows"] <= bound * (1 + 1e-12))
         assert np.allclose(r["loss_rows"], O.quadratic_loss(r["Q"] - W, Hd), rtol=1e-9)
+    # group-wise steps fixed before the loop (as with static groups), in act-order
+    d, g = 32, 8
+    H, _ = spd(rng, d)
+    W0 = rng.standard_normal((5, d)) * 0.02
+    perm = O.act_order(H)
+    Hd, _ = O.damping(H[np.ix_(perm, perm)], 0.01)
+    W = W0[:, perm]
+    sg = np.abs(W0).reshape(5, d // g, g).max(axis=2) / 7.0     # per original group
+    s = sg[:, perm // g]                                         # step of processed column
+    r = O.gptq_sweep(W, O.inverse_cholesky_upper(Hd), blocksize=8,
+                     column_quantizer=unclipped_grid(s))
+    assert np.array_equal(O.gptq_babai(W, Hd, s), r["codes"])
 
 
 PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
