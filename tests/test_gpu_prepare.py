@@ -6,7 +6,7 @@ import torch
 
 from oracle import gptq_oracle as O
 from tests.parity import U_REL_FRO, rel_fro, to_np
-from workloads import CONFIGS, make_tokens, make_tokens_chunk, channel_multipliers
+from workloads import CONFIGS, make_tokens, make_tokens_chunk
 
 pytestmark = pytest.mark.gpu
 
