@@ -578,7 +578,10 @@ def run_pipeline(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 100 for the layer path, about 0.6 s, so that "
+                         "the clock sampler sees the timed region several times; 10 for "
+                         "the other modes and the reference arm)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
@@ -595,6 +598,9 @@ def main(argv=None):
                     help="measure the block-sequential pipeline on a Llama-shaped block")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.steps is None:
+        layer_path = not (args.impl == "reference" or args.dequant_matmul or args.pipeline)
+        args.steps = 100 if layer_path else 10
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
