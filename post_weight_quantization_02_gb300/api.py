@@ -129,6 +129,8 @@ def quantize_layer_from_host(engine: LayerEngine, W_host: torch.Tensor,
         compute.wait_event(ready[b])
         engine.add_batch_async(bufs[b], compute)
         done[b].record(compute)
+    if engine.nseen == 0:
+        raise RuntimeError("no calibration tokens: X_chunks_host was empty")
     with torch.cuda.stream(copy):
         Wd = W_host.to(dev, non_blocking=True)
         wready = torch.cuda.Event()
