@@ -59,6 +59,19 @@ MUTATIONS = {
         "codes[r] = babai_nearest_plane((B * s[r][::-1][None, :])[:, ::-1], B @ W[r])[::-1]"),
     "babai_floor": ("z[j] = np.rint((y[j] - R[j, j + 1:] @ z[j + 1:]) / R[j, j])",
                     "z[j] = np.floor((y[j] - R[j, j + 1:] @ z[j + 1:]) / R[j, j])"),
+    # the replay rule of the GPU parity check: the near-tie band and the neighbour test
+    "hint_band_always_codes": ("near = np.abs(v - (fl + 0.5)) < tie_eps",
+                               "near = np.ones(v.shape, dtype=bool)"),
+    "hint_band_always_zeros": ("near = np.abs(u - (fl + 0.5)) < tie_eps",
+                               "near = np.ones(u.shape, dtype=bool)"),
+    "hint_neighbour_widened_codes": (
+        "take = near & (hint != own) & ((hint == lo_c) | (hint == hi_c))",
+        "take = near & (hint != own) & (np.abs(hint - own) <= 2)"),
+    "hint_neighbour_unclamped_codes": ("hi_c = np.clip(fl + 1 + z, lowest, maxq)",
+                                       "hi_c = fl + 1 + z"),
+    "hint_neighbour_widened_zeros": (
+        "take = near & (hint != r) & ((hint == fl) | (hint == fl + 1))",
+        "take = near & (hint != r) & (np.abs(hint - r) <= 2)"),
     "dequant_zero_dropped": ("return s * (codes.astype(F64) - z)", "return s * codes.astype(F64)"),
     "dequant_scale_of_position": ("s = np.asarray(scales, dtype=F64)[g].T",
                                   "s = np.asarray(scales, dtype=F64)[np.arange(g.size) * len(scales) // g.size].T"),

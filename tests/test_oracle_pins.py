@@ -324,6 +324,62 @@ def pin_fit_and_round(O):
     assert c.tolist() == [1, 15]
 
 
+def pin_replay_hint(O):
+    """The replay rule that lets a GPU code or zero differ from the oracle's own choice:
+    a hint is adopted only where the float32 pre-rounding value lies within tie_eps of a
+    rounding tie, and only for the other of the two neighbouring grid points (inside the
+    clamped grid).  Everything else keeps the oracle's own rounding (half to even)."""
+    s = np.float32([0.1])
+    z = np.array([0])
+
+    def code(w, hint, stats=None):
+        c, _ = O.round_to_grid(np.array([w]), s, z, 4, False, np.array([hint]), 1e-3, stats)
+        return int(c[0])
+
+    # w / s = 2.5 exactly in float32: half to even gives 2; the hint 3 is the other
+    # neighbour of the tie, so it is adopted and counted
+    assert abs(float(np.float32(0.25) / s[0]) - 2.5) < 1e-3
+    st = {}
+    assert code(0.25, 3, st) == 3 and st.get("codes") == 1
+    # the same hint just outside the band (|v - 2.5| = 2e-3 >= 1e-3) is refused
+    st = {}
+    assert code(0.2502, 2, st) == 3 and code(0.2498, 3, st) == 2 and st.get("codes", 0) == 0
+    # a hint two levels away (or on the far side) is refused even at an exact tie
+    st = {}
+    assert code(0.25, 4, st) == 2 and code(0.25, 1, st) == 2 and code(0.25, 0, st) == 2
+    assert st.get("codes", 0) == 0
+    # a hint equal to the oracle's own code changes nothing and is not counted
+    st = {}
+    assert code(0.25, 2, st) == 2 and st.get("codes", 0) == 0
+    # a hint outside the clamped grid is refused: at v = 15.5 both neighbours clamp to 15,
+    # at v = -0.5 both clamp to 0
+    st = {}
+    assert code(1.55, 16, st) == 15 and code(-0.05, -1, st) == 0 and st.get("codes", 0) == 0
+    # a code decided on the hint keeps its dequantised value consistent: what = s (c - z)
+    c, what = O.round_to_grid(np.array([0.25]), s, z, 4, False, np.array([3]), 1e-3, {})
+    assert c[0] == 3 and what[0] == np.float64(s[0]) * 3
+
+    # zero points: -lo / s = 2.5 for lo = -0.25, hi = 1.25 (s = 1.5 / 15 = 0.1)
+    def zero(wg, hint, stats=None):
+        _, zz = O.fit_group(np.array([wg]), 4, False, np.array([hint]), 1e-3, stats)
+        return int(zz[0])
+
+    st = {}
+    assert zero([-0.25, 1.25], 3, st) == 3 and st.get("zeros") == 1
+    st = {}
+    assert zero([-0.25, 1.25], 2, st) == 2 and st.get("zeros", 0) == 0
+    # off the band: -lo / s = 2.6 rounds to 3, the hint 2 is refused
+    st = {}
+    assert zero([-0.26, 1.24], 2, st) == 3 and st.get("zeros", 0) == 0
+    # two levels away at the tie: refused
+    st = {}
+    assert zero([-0.25, 1.25], 4, st) == 2 and zero([-0.25, 1.25], 0, st) == 2
+    assert st.get("zeros", 0) == 0
+    # no hint: plain half-to-even rounding
+    _, zz = O.fit_group(np.array([[-0.25, 1.25]]), 4, False)
+    assert int(zz[0]) == 2
+
+
 def pin_pack(O):
     codes = np.arange(1, 9)[None, :]
     w = O.pack_bitstream(codes, 4)
@@ -541,7 +597,7 @@ PINS = [pin_worked_example, pin_conditioned_example, pin_two_weight_closed_form,
         pin_gptq_beats_rtn_on_average, pin_act_order, pin_damping, pin_dead_columns,
         pin_hessian, pin_fit_and_round, pin_pack, pin_checkpoint_format,
         pin_format_roundtrip, pin_static_groups, pin_dequantize, pin_block_pipeline,
-        pin_babai]
+        pin_babai, pin_replay_hint]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
