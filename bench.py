@@ -3,13 +3,16 @@
 A step is one pass of the whole layer path over one synthetic workload: the Hessian hook
 over every calibration token, prepare (dead fix, act-order, damping, inverse Cholesky
 factor) and the column loop with the lazy update, group scales/zeros, g_idx and packing.
-The default workload is the q_proj-shaped layer (d_out = d_in = 4096, 128 x 2048 bf16
-tokens, 4-bit asymmetric, group 128, act-order).
+The default workload is the 70B-width down_proj-shaped layer (d_out = 8192, d_in =
+28672, 256 x 2048 bf16 tokens resident in HBM, 4-bit asymmetric, group 128, act-order),
+the largest configuration that fits one GPU.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 With N > 1 (torchrun) every rank quantises its own replica of the layer (weak scaling,
-no data-path collective); the step time is the maximum over ranks.  ``--impl
+no data-path collective); the step time is the maximum over ranks.  ``--shard`` splits
+one layer across the ranks instead (strong scaling: token-sharded Hessian with one
+all-reduce, replicated prepare, row-sharded quantize with one all-gather per output).  ``--impl
 reference`` times the float64 CPU oracle on bounded samples of the same workload.
 """
 
@@ -29,7 +32,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GPTQ per-layer time (ms) & weights/s at 4-bit g128; SYRK/GEMM TFLOP/s vs peak"
-DEFAULT_CONFIG = "q_proj_4096x4096"
+DEFAULT_CONFIG = "down_proj_8192x28672"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -154,10 +157,18 @@ def measured_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# the first line of the host-side part of the SYRK's source: the traffic figure depends
+# on the device code above it, not on edits below it
+HOST_PART_MARKER = "// CTAs' tiles per token split"
+
+
 def source_hash(path: str) -> str:
+    """Hash of a kernel file's device part (the text before HOST_PART_MARKER)."""
     import hashlib
     with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        text = f.read()
+    cut = text.find(HOST_PART_MARKER.encode())
+    return hashlib.sha256(text if cut < 0 else text[:cut]).hexdigest()[:16]
 
 
 def ncu_traffic(kernel_file: str, workload: str):
@@ -177,10 +188,92 @@ def ncu_traffic(kernel_file: str, workload: str):
 
 # ------------------------------------------------------------------------ our arm
 
+BLOCK = 128  # the engine's column block
+
+
+def algorithmic_work(cfg, n):
+    """The algorithmic work of each step of the layer path (flops or bytes per layer)."""
+    m, d = cfg.d_out, cfg.d_in
+    we = 2 if "bfloat16" in str(cfg.w_dtype) else 4
+    return {
+        "syrk_flops": float(d) * (d + 1) * n,              # upper triangle of X^T X
+        "cholesky_flops_pages": 4.0 * d ** 3 / 3,          # chol, cholesky_inverse, chol
+        "cholesky_flops_engine": 2.0 * d ** 3 / 3,         # one factor + one triangular inverse
+        "lazy_flops": float(m) * d * (d - BLOCK),          # sum over blocks of m x 128 x (d - i2)
+        "loop_bytes": 13.0 * m * d,                        # W r/w, errors, codes
+        "gather_bytes": float(m) * d * (we + 4),           # W in, permuted float32 copy out
+        "pack_bytes": float(m) * d * (1 + cfg.bits / 8),   # codes in, packed words out
+    }
+
+
+def layer_figures(cfg, n, step_ms, phase_ms, kern, hbm, bf16, bf16_sus):
+    """Achieved rates of each phase on its algorithmic work, as fractions of the measured
+    peaks, and the step time against the sum of the kernels' roofline times."""
+    w = algorithmic_work(cfg, n)
+
+    def rate(x, ms, scale):
+        return x / (ms * 1e-3) / scale if ms and ms > 0 else None
+
+    def kms(name):
+        k = kern.get(name)
+        return k["ms_per_step"] if k else None
+
+    def rnd(v, k=4):
+        return None if v is None else round(v, k)
+
+    prep_ms = phase_ms["prepare"]
+    lazy_ms, loop_ms = kms("quant_lazy"), kms("quant_loop")
+    gather_ms, pack_ms = kms("quant_gather"), kms("quant_pack")
+    tp = rate(w["cholesky_flops_pages"], prep_ms, 1e12)
+    te = rate(w["cholesky_flops_engine"], prep_ms, 1e12)
+    tl = rate(w["lazy_flops"], lazy_ms, 1e12)
+    gl = rate(w["loop_bytes"], loop_ms, 1e9)
+    gg = rate(w["gather_bytes"], gather_ms, 1e9)
+    gp = rate(w["pack_bytes"], pack_ms, 1e9)
+    loop_launches = kern.get("quant_loop", {}).get("launches_per_step")
+    figures = {
+        "phases_ms": {k: round(v, 3) for k, v in phase_ms.items()},
+        "prepare": {"ms": round(prep_ms, 3), "bound": "tensor (float32-accurate split products)",
+                    "tflops_on_4d3_over_3": rnd(tp, 1), "tflops_on_2d3_over_3": rnd(te, 1),
+                    "frac_of_bf16_burst": rnd(tp / bf16 if tp else None),
+                    "frac_of_bf16_sustained": rnd(tp / bf16_sus if tp else None),
+                    "note": "4d^3/3 is the pages' route (chol, inverse, chol); the engine's "
+                            "route does 2d^3/3 (one factor, one triangular inverse)"},
+        "lazy_update": {"kernel_ms": rnd(lazy_ms, 3), "bound": "tensor",
+                        "algorithmic_flops": w["lazy_flops"], "tflops": rnd(tl, 1),
+                        "frac_of_bf16_burst": rnd(tl / bf16 if tl else None),
+                        "frac_of_bf16_sustained": rnd(tl / bf16_sus if tl else None)},
+        "column_loop": {"kernel_ms": rnd(loop_ms, 3), "bound": "latency (column chain) / hbm",
+                        "algorithmic_bytes": w["loop_bytes"], "gbs": rnd(gl, 1),
+                        "frac_of_hbm": rnd(gl / hbm if gl else None),
+                        "us_per_block": rnd(loop_ms * 1e3 / loop_launches
+                                            if loop_ms and loop_launches else None, 2)},
+        "gather": {"kernel_ms": rnd(gather_ms, 3), "bound": "hbm",
+                   "algorithmic_bytes": w["gather_bytes"], "gbs": rnd(gg, 1),
+                   "frac_of_hbm": rnd(gg / hbm if gg else None)},
+        "pack": {"kernel_ms": rnd(pack_ms, 3), "bound": "hbm",
+                 "algorithmic_bytes": w["pack_bytes"], "gbs": rnd(gp, 1),
+                 "frac_of_hbm": rnd(gp / hbm if gp else None)},
+    }
+    # each kernel at its roofline (bf16 burst peak for the contractions, HBM for the rest)
+    roof = {
+        "syrk": w["syrk_flops"] / (bf16 * 1e12) * 1e3,
+        "cholesky_chain": w["cholesky_flops_pages"] / (bf16 * 1e12) * 1e3,
+        "lazy_update": w["lazy_flops"] / (bf16 * 1e12) * 1e3,
+        "column_loop": w["loop_bytes"] / (hbm * 1e9) * 1e3,
+        "gather": w["gather_bytes"] / (hbm * 1e9) * 1e3,
+        "pack": w["pack_bytes"] / (hbm * 1e9) * 1e3,
+    }
+    total = sum(roof.values())
+    figures["roofline_sum"] = {"ms": round(total, 3),
+                               "per_kernel_ms": {k: round(v, 4) for k, v in roof.items()},
+                               "step_frac_of_roofline_sum": round(total / step_ms, 4)}
+    return figures
+
+
 def run_ours(args, world, rank, local):
     import torch
-    from post_weight_quantization_02_gb300 import LayerEngine, QuantizedLayer, gptq as G
-    from post_weight_quantization_02_gb300 import quantize_layer_from_host
+    from post_weight_quantization_02_gb300 import LayerEngine, gptq as G
     from workloads import CONFIGS, channel_multipliers, make_tokens_chunk, make_weight
 
     if not torch.cuda.is_available():
@@ -193,10 +286,11 @@ def run_ours(args, world, rank, local):
         cfg = cfg.replace(n_tokens=args.tokens)
     m, d, n = cfg.d_out, cfg.d_in, cfg.n_tokens
 
-    # synthetic workload, resident in HBM
+    # synthetic workload, resident in HBM (chunks written straight into one tensor)
     mult = channel_multipliers(cfg, dev)
-    nch = -(-n // cfg.chunk)
-    X = torch.cat([make_tokens_chunk(cfg, i, dev, mult) for i in range(nch)])
+    X = torch.empty(n, d, dtype=cfg.x_dtype, device=dev)
+    for i, t0 in enumerate(range(0, n, cfg.chunk)):
+        X[t0:t0 + cfg.chunk] = make_tokens_chunk(cfg, i, dev, mult)
     W = make_weight(cfg, dev)
     eng = LayerEngine(m, d, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
                       cfg.blocksize, max_chunk_tokens=n, device=dev,
@@ -204,11 +298,19 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         eng.reset()
         eng.add_batch(X)
+        if ev is not None:
+            ev[1].record(stream)
         eng.prepare()
+        if ev is not None:
+            ev[2].record(stream)
         eng.quantize_weights(W)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -216,35 +318,36 @@ def run_ours(args, world, rank, local):
 
     # The timed steps trace the SYRK only (its CUDA-event duration is the roofline's
     # denominator); events around every kernel would cost time between the prepare's and
-    # the quantize's kernels and break their dependent launches.
+    # the quantize's kernels and break their dependent launches.  Four events per step,
+    # between the three calls, give the phase times.
     G.gptq_profile_reset()
     G.gptq_profile_select([G.GPTQ_K_SYRK_TC])
     G.gptq_profile_enable(True)
     launches0 = G.gptq_launch_count()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     with ClockSampler(dev.index) as clocks:
         barrier(dist, dev)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))              # evict L2 between steps (not timed)
-            starts[i].record(stream)
-            step()
-            stops[i].record(stream)
+            step(evs[i])
         torch.cuda.synchronize()
         barrier(dist, dev)
         wall = time.perf_counter() - wall0
     G.gptq_profile_enable(False)
     launches = G.gptq_launch_count() - launches0
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    phase_ms = {"hessian": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                "prepare": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+                "quantize": statistics.mean(e[2].elapsed_time(e[3]) for e in evs)}
     ms_local = statistics.mean(step_ms)
     ms = max_over_ranks(dist, ms_local, dev)
     syrk_t, syrk_c = G.gptq_profile_read(G.GPTQ_K_SYRK_TC)
 
     # per-kernel breakdown: a separate, untimed pass with every kind traced
     kern = {}
-    prof_steps = min(args.steps, 3)
+    prof_steps = max(1, min(args.steps, 2))
     G.gptq_profile_reset()
     G.gptq_profile_select(None)
     G.gptq_profile_enable(True)
@@ -271,11 +374,13 @@ def run_ours(args, world, rank, local):
                     # the measured power-capped figure (a GEMM run back to back), for context
                     "peak_sustained": bf16_sus,
                     "frac_of_sustained": round(achieved / bf16_sus, 4),
+                    "ms_per_launch": round(syrk_ms, 3),
                     "algorithmic_flops_per_launch": flops,
                     "traffic": ncu_traffic("post_weight_quantization_02_gb300/csrc/hessian_tc.cu",
-                                           args.config)}
+                                           cfg.name if not args.tokens else None)}
+    figures = layer_figures(cfg, n, ms, phase_ms, kern, hbm, bf16, bf16_sus)
 
-    # end to end through the public API from pinned host memory
+    # end to end through the C ABI's host-buffer call
     e2e = None
     if not args.skip_e2e:
         e2e = run_e2e(args, cfg, X, W, eng, dist, dev, world)
@@ -283,7 +388,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cfg, None, W, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(cfg)
 
     total_launches = sum_over_ranks(dist, float(launches), dev)
     if rank == 0:
@@ -314,6 +419,7 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "gpu_launches": int(total_launches),
             "roofline": roofline,
+            "figures": figures,
             "kernels": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in kern.items()},
             "cpu_baseline": cpu,
         }
@@ -322,87 +428,155 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def run_e2e(args, cfg, X, W, eng, dist, dev, world):
-    """The same metric through the public API from pinned host buffers: host-to-device
-    copies of every token chunk and of W, and the device-to-host copy of the packed
-    outputs, are inside the timed region."""
+def run_sharded(args, world, rank, local):
+    """--shard: one layer split across the ranks (strong scaling): each rank runs the
+    hook over its slice of the calibration tokens, the partial Hessians are rescaled and
+    summed by one all-reduce, every rank prepares, each quantises its slice of rows, and
+    one all-gather per output assembles the packed layer.  The step time is the maximum
+    over ranks; ``value`` is the one layer's weights per second."""
     import torch
-    from post_weight_quantization_02_gb300 import LayerEngine, QuantizedLayer
+    from post_weight_quantization_02_gb300 import LayerEngine, ShardedLayer, shard
+    from workloads import CONFIGS, channel_multipliers, make_tokens_chunk, make_weight
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the engine has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    cfg = CONFIGS[args.config]
+    if args.tokens:
+        cfg = cfg.replace(n_tokens=args.tokens)
+    m, d, n = cfg.d_out, cfg.d_in, cfg.n_tokens
+    t0, t1 = shard.token_range(rank, world, n)
+    r0, r1 = shard.row_range(rank, world, m)
+    mult = channel_multipliers(cfg, dev)
+    X = torch.empty(t1 - t0, d, dtype=cfg.x_dtype, device=dev)
+    for i, c0 in enumerate(range(0, n, cfg.chunk)):
+        a, b = max(c0, t0), min(c0 + cfg.chunk, t1)
+        if a < b:
+            X[a - t0:b - t0] = make_tokens_chunk(cfg, i, dev, mult)[a - c0:b - c0]
+    W = make_weight(cfg, dev)[r0:r1].contiguous()
+    eng = LayerEngine(r1 - r0, d, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
+                      cfg.blocksize, max_chunk_tokens=max(1, t1 - t0), device=dev)
+    sl = ShardedLayer(eng, m)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        sl.reset()
+        sl.add_batch(X)
+        sl.quantize(W)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            barrier(dist, dev)
+            torch.cuda.synchronize()
+            a = time.perf_counter()
+            step()
+            torch.cuda.synchronize()
+            times.append(max_over_ranks(dist, (time.perf_counter() - a) * 1e3, dev))
+    ms = statistics.mean(times)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(float(m) * d / (ms * 1e-3), 1),
+            "unit": "weights/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+            "config": {"workload": f"{cfg.name}: d_out={m} d_in={d}, {n} tokens, one layer "
+                                   f"split over {world} ranks",
+                       "split": "tokens for the Hessian (rescale + all-reduce), prepare "
+                                "replicated, rows for the quantize (all-gather)",
+                       "l2": "flushed between steps (256 MiB write, untimed)",
+                       "timing": "host wall clock per step, synchronised, max over ranks"},
+            "clocks": clocks.summary(),
+        }), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, cfg, X, W, eng, dist, dev, world):
+    """The same metric through the C ABI's host-buffer call (gptq_quantize_layer_host):
+    the host-to-device copies of every token chunk and of W, and the device-to-host copies
+    of the packed outputs, are inside the timed region."""
+    import torch
     from post_weight_quantization_02_gb300 import quantize_layer_from_host
     m, d, n = cfg.d_out, cfg.d_in, cfg.n_tokens
-    Xh = X.cpu().pin_memory()
-    Wh = W.cpu().pin_memory()
-    chunk = cfg.chunk
-    x_chunks = [Xh[i:i + chunk] for i in range(0, n, chunk)]
-    out = QuantizedLayer(*(t.cpu().pin_memory() for t in
-                           (eng.qweight, eng.scales, eng.qzeros, eng.g_idx, eng.perm, eng.loss)))
-    e_eng = LayerEngine(m, d, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
-                        cfg.blocksize, max_chunk_tokens=chunk, device=dev,
-                        static_groups=args.static_groups)
-    quantize_layer_from_host(e_eng, Wh, x_chunks, out)          # warm-up
-    e_steps = max(1, min(args.steps, 5))
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Xh.copy_(X)
+    Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+    Wh.copy_(W)
+    out = quantize_layer_from_host(eng, Wh, Xh, chunk_tokens=cfg.chunk)   # warm-up
+    e_steps = max(1, min(args.steps, 3))
     barrier(dist, dev)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e_steps):
-        quantize_layer_from_host(e_eng, Wh, x_chunks, out)
+        quantize_layer_from_host(eng, Wh, Xh, out, chunk_tokens=cfg.chunk)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / e_steps, dev)
     h2d = Xh.numel() * Xh.element_size() + Wh.numel() * Wh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in
-              (out.qweight, out.scales, out.qzeros, out.g_idx, out.perm, out.loss))
+              (out.qweight, out.scales, out.qzeros, out.g_idx, out.perm)) + 8
+    del Xh, Wh
     return {"value": round(world * float(m) * d / (e_ms * 1e-3), 1), "unit": "weights/s",
             "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": e_steps,
-            "path": f"quantize_layer_from_host, {len(x_chunks)} pinned chunks of {chunk} tokens"}
+            "path": f"gptq_quantize_layer_host (C ABI): page-locked X copied in "
+                    f"{-(-n // cfg.chunk)} chunks of {cfg.chunk} tokens overlapped with the "
+                    f"Hessian kernels, then W; packed outputs copied back"}
 
 
 # ------------------------------------------------------------------------ CPU oracle
 
-def oracle_layer_seconds(cfg, Xs, Ws, n_tokens_sample: int, rows_sample: int):
-    """Time the float64 oracle on a bounded sample and extrapolate to the whole layer.
+def oracle_sample(cfg, ds: int = 4096, ms: int = 256, ns: int = 4096):
+    """Time the float64 oracle, as it stands, on a bounded sample of the workload.
 
-    Hessian on ``n_tokens_sample`` tokens (scaled by n / sample: the product is linear in
-    tokens), the full prepare chain on the d_in x d_in matrix (not sampled), and the column
-    loop on ``rows_sample`` output rows (scaled by d_out / rows: rows are independent).
-    Returns (extrapolated seconds, measured seconds).
+    The sample is the same workload scaled down: d_in' = min(d_in, ds) channels, d_out' =
+    min(d_out, ms) rows and n' = min(n, ns) tokens drawn by the same generators.  Each
+    phase is timed and scaled to the full layer by its operation count: the Hessian by
+    (n/n') (d/d')^2, the prepare (dead fix, act-order, damping, inverse Cholesky factor) by
+    (d/d')^3, the column loop and packing by (m/m') (d/d')^2.  Returns (seconds per layer
+    extrapolated, seconds measured, description).
     """
-    from oracle import gptq_oracle as O
-    t0 = time.perf_counter()
-    H = O.hessian(Xs[:n_tokens_sample])
-    t1 = time.perf_counter()
-    prep = O.gptq_prepare(H, cfg.damp, cfg.actorder)
-    t2 = time.perf_counter()
-    O.gptq_quantize_layer(Ws[:rows_sample], prep["U"], prep["perm"], prep["dead"], cfg.bits,
-                          cfg.group, cfg.sym, cfg.blocksize, pack=False)
-    t3 = time.perf_counter()
-    full = ((t1 - t0) * cfg.n_tokens / n_tokens_sample + (t2 - t1)
-            + (t3 - t2) * cfg.d_out / rows_sample)
-    return full, t3 - t0
-
-
-def cpu_sample_inputs(cfg, X=None, W=None, n_tokens_sample=4096):
     import numpy as np
+    from oracle import gptq_oracle as O
     from workloads import make_tokens_chunk, make_weight
-    if X is None:
-        Xs = make_tokens_chunk(cfg, 0, "cpu")[:n_tokens_sample].float().numpy()
-    else:
-        Xs = X[:n_tokens_sample].float().cpu().numpy()
-    Wm = make_weight(cfg, "cpu") if W is None else W
-    return Xs.astype(np.float64), Wm.float().cpu().numpy().astype(np.float64)
+    sub = cfg.replace(d_in=min(ds, cfg.d_in), d_out=min(ms, cfg.d_out),
+                      n_tokens=min(ns, cfg.n_tokens), chunk=min(ns, cfg.n_tokens))
+    Xs = make_tokens_chunk(sub, 0, "cpu").float().numpy().astype(np.float64)
+    Ws = make_weight(sub, "cpu").float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    H = O.hessian(Xs)
+    t1 = time.perf_counter()
+    prep = O.gptq_prepare(H, sub.damp, sub.actorder)
+    t2 = time.perf_counter()
+    O.gptq_quantize_layer(Ws, prep["U"], prep["perm"], prep["dead"], sub.bits, sub.group,
+                          sub.sym, sub.blocksize, pack=True)
+    t3 = time.perf_counter()
+    rd = cfg.d_in / sub.d_in
+    full = ((t1 - t0) * (cfg.n_tokens / sub.n_tokens) * rd ** 2 + (t2 - t1) * rd ** 3
+            + (t3 - t2) * (cfg.d_out / sub.d_out) * rd ** 2)
+    exact = sub == cfg.replace(chunk=sub.chunk)
+    desc = (f"float64 numpy oracle on a scaled-down copy of the workload: d_in {sub.d_in} of "
+            f"{cfg.d_in}, d_out {sub.d_out} of {cfg.d_out}, {sub.n_tokens} of {cfg.n_tokens} "
+            f"tokens, same generators and quantiser; " +
+            ("the whole layer, not extrapolated" if exact else
+             "phases scaled by their operation counts (Hessian n d^2, prepare d^3, column "
+             "loop m d^2): extrapolated"))
+    return full, t3 - t0, desc
 
 
-def cpu_baseline(cfg, X=None, W=None, budget_s: float = 20.0):
+def cpu_baseline(cfg):
     """The oracle as it stands, on this host's cores, on a bounded sample of the workload."""
-    ntok, rows = 4096, 128
-    Xs, Ws = cpu_sample_inputs(cfg, X, W, ntok)
-    full, measured = oracle_layer_seconds(cfg, Xs, Ws, ntok, rows)
+    full, measured, desc = oracle_sample(cfg)
     return {"value": round(cfg.d_out * cfg.d_in / full, 1), "unit": "weights/s",
             "cores": os.cpu_count(), "kind": "oracle",
-            "sample": (f"float64 numpy oracle: Hessian on {ntok} of {cfg.n_tokens} tokens "
-                       f"(x{cfg.n_tokens // ntok}), full prepare on {cfg.d_in}^2, column loop "
-                       f"on {rows} of {cfg.d_out} rows (x{cfg.d_out // rows}); "
-                       f"{measured:.1f} s measured, {full:.1f} s extrapolated per layer"),
+            "sample": f"{desc}; {measured:.2f} s measured, {full:.1f} s per layer",
             "ms_per_layer_extrapolated": round(full * 1e3, 1)}
 
 
@@ -412,28 +586,31 @@ def run_reference(args, world, rank):
         return
     from workloads import CONFIGS
     cfg = CONFIGS[args.config]
-    ntok, rows = 2048, 64
-    Xs, Ws = cpu_sample_inputs(cfg, n_tokens_sample=ntok)
+    if args.tokens:
+        cfg = cfg.replace(n_tokens=args.tokens)
     for _ in range(args.warmup):
-        oracle_layer_seconds(cfg, Xs, Ws, ntok, rows)
-    fulls, measured = [], 0.0
+        oracle_sample(cfg)
+    fulls, walls = [], []
+    desc = ""
     for _ in range(args.steps):
-        f, mt = oracle_layer_seconds(cfg, Xs, Ws, ntok, rows)
+        f, mt, desc = oracle_sample(cfg)
         fulls.append(f)
-        measured += mt
+        walls.append(mt)
     sec = statistics.mean(fulls)
     value = round(cfg.d_out * cfg.d_in / sec, 1)
-    sample = (f"float64 numpy oracle per step: Hessian on {ntok} of {cfg.n_tokens} tokens, "
-              f"full prepare on {cfg.d_in}^2, column loop on {rows} of {cfg.d_out} rows, "
-              f"extrapolated to the whole layer")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "weights/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(sec * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(statistics.mean(walls) * 1e3, 1),
+        "ms_per_layer_extrapolated": round(sec * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": cfg.name, "measured_cpu_s": round(measured, 2)},
+        "config": {"workload": cfg.name,
+                   "step": "one bounded sample of the workload through the oracle; "
+                           "ms_per_step is the sample's measured time, value the layer "
+                           "throughput extrapolated from it"},
         "cpu_baseline": {"value": value, "unit": "weights/s", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -579,19 +756,21 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 100 for the layer path, about 0.6 s, so that "
-                         "the clock sampler sees the timed region several times; 10 for "
-                         "the other modes and the reference arm)")
+                    help="timed steps (default: 20 for the layer path, about 11 s on the "
+                         "default workload, so that the clock sampler sees the timed region "
+                         "many times; 10 for the other modes and the reference arm)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the calibration token count (small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--static-groups", action="store_true",
                     help="groups fixed in the original column order before the loop")
+    ap.add_argument("--shard", action="store_true",
+                    help="split one layer across the ranks (tokens for the Hessian, rows "
+                         "for the quantize) instead of one replica per rank")
     ap.add_argument("--dequant-matmul", action="store_true",
                     help="measure the packed checkpoint's consumer instead of the layer path")
     ap.add_argument("--pipeline", action="store_true",
@@ -599,8 +778,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.steps is None:
-        layer_path = not (args.impl == "reference" or args.dequant_matmul or args.pipeline)
-        args.steps = 100 if layer_path else 10
+        layer_path = not (args.impl == "reference" or args.dequant_matmul or args.pipeline
+                          or args.shard)
+        args.steps = 20 if layer_path else 10
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -608,6 +788,8 @@ def main(argv=None):
         run_dequant(args, world, rank, local)
     elif args.pipeline:
         run_pipeline(args, world, rank, local)
+    elif args.shard:
+        run_sharded(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

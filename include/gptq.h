@@ -17,9 +17,11 @@
  * Conventions shared by every call
  * --------------------------------
  * - Device pointers are CUDA device memory on the current device, allocated and owned by
- *   the caller.  The library never allocates device memory; scratch comes from the
- *   caller's workspace `ws` of `ws_bytes` bytes (size it with gptq_workspace_size; the
- *   base must be 256-byte aligned).  Host pointers are named as such below.
+ *   the caller.  The library allocates no device memory at run time: scratch comes from
+ *   the caller's workspace `ws` of `ws_bytes` bytes (size it with gptq_workspace_size; the
+ *   base must be 256-byte aligned).  The one exception is the fixed static array behind
+ *   gptq_hessian_accumulate_noalloc (16 MiB + 256 B per GPU that loads the library).
+ *   Host pointers are named as such below.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
  *   call enqueues its kernels on `stream`, then synchronises `stream` and returns the
  *   status of the work it enqueued (device-side failures such as a non-positive-definite
@@ -31,8 +33,8 @@
  *   untouched.
  * - Calls may come from several host threads and for several devices in one process;
  *   the library's own state (kernel attributes, internal streams) is kept per device.
- *   gptq_prepare and gptq_quantize_layer(_ex) share internal streams, so concurrent
- *   calls of those two run one after the other.
+ *   gptq_prepare and gptq_quantize_layer(_ex) (also inside gptq_quantize_layer_host)
+ *   share internal streams, so concurrent calls of those run one after the other.
  */
 #ifndef GPTQ_GB300_H
 #define GPTQ_GB300_H
@@ -65,7 +67,7 @@ typedef enum {
  * gptq_workspace_size -- bytes of workspace the call `op` wants for these sizes on the
  * current device.  Arguments that do not apply to `op` are ignored.  For GPTQ_OP_HESSIAN
  * the value is the size that lets the call split the token axis as it prefers; any ws of
- * at least d_in*d_in*4 + 4096 bytes is accepted (fewer splits).  Returns 0 for invalid
+ * at least d_in*d_in*4 + 256 bytes is accepted (fewer splits).  Returns 0 for invalid
  * sizes.
  */
 size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, int bits,
@@ -140,6 +142,26 @@ gptq_status gptq_hessian_accumulate_noalloc(float* H, int64_t* nseen, const void
 gptq_status gptq_hessian_accumulate_async(float* H, int64_t* nseen, const void* X,
                                           int xdtype, int64_t ntok, int32_t d_in, void* ws,
                                           size_t ws_bytes, void* stream);
+
+/*
+ * gptq_hessian_rescale -- H <- H * n_from / n_to on the upper 128-tile triangle.
+ *
+ * gptq_hessian_accumulate leaves H normalised by the tokens it has seen (2/n sum x x^T,
+ * "GPTQ Architecture, in depth", "The algorithm in code", HessianHook; "Same Ruler,
+ * Smarter Placement: GPTQ" section 1.4).  Rescaled from its n_from tokens to n_to, it
+ * becomes those tokens' share of the Hessian of an n_to-token stream: when a calibration
+ * stream is split across GPUs, each rank rescales its partial from its own token count
+ * to the total, and the sum of the partials (one all-reduce) is the Hessian of the whole
+ * stream.  The interface is an addition for that split; the pages run one GPU.
+ *
+ * H       device float32 [d_in, d_in], in/out (upper 128-tile triangle, as written by
+ *         gptq_hessian_accumulate; the rest is left as it was).  With n_from == 0 the
+ *         upper triangle is set to zero whatever it held (a rank that saw no tokens).
+ * d_in    > 0, multiple of 8.   n_from >= 0, n_to > 0.
+ * Synchronous on `stream`.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+gptq_status gptq_hessian_rescale(float* H, int32_t d_in, int64_t n_from, int64_t n_to,
+                                 void* stream);
 
 /*
  * gptq_hessian_status -- synchronise `stream` and return the status collected by the
@@ -248,6 +270,56 @@ gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_
                                    void* stream);
 
 /*
+ * gptq_layer_host_size -- bytes of device memory gptq_quantize_layer_host needs for these
+ * sizes and element types on the current device; 0 for invalid or unsupported values.
+ */
+size_t gptq_layer_host_size(int64_t chunk_tokens, int32_t d_out, int32_t d_in, int bits,
+                            int group, int xdtype, int wdtype);
+
+/*
+ * gptq_quantize_layer_host -- one linear layer end to end from host memory: the Hessian
+ * hook over every calibration token, gptq_prepare and gptq_quantize_layer_ex, with the
+ * inputs read from and the packed checkpoint written to host buffers.
+ *
+ * The method is the one the three device calls define ("GPTQ Architecture, in depth",
+ * "The algorithm in code": the hook over the calibration batches, then gptq; "Same
+ * Ruler, Smarter Placement: GPTQ", sections 1.4-1.9); the outputs equal those of the
+ * device calls run one after the other on the same inputs with the same chunking.  The
+ * interface itself is an addition: the pages run the method from PyTorch on device
+ * tensors.
+ *
+ * X      host [ntok, d_in] row-major, `xdtype`; ntok > 0.  It is copied to the device in
+ *        chunks of chunk_tokens tokens through two staging buffers, each copy overlapping
+ *        the Hessian kernels of the chunk before it.  Page-locked host memory (for example
+ *        from cudaHostAlloc) lets the copies run asynchronously; pageable memory works but
+ *        serialises them.
+ * W      host [d_out, d_in] row-major, `wdtype`; copied once, after the tokens.
+ * damp, actorder: as gptq_prepare.  bits, group, sym, blocksize, flags: as
+ *        gptq_quantize_layer_ex (d_out and d_in multiples of 32, d_out > 0).
+ * qweight, scales, qzeros, g_idx: host outputs with the layouts of gptq_quantize_layer.
+ * perm   host int32 [d_in], out: the processing order gptq_prepare chose.
+ * loss   host double, out: the OBS loss as in gptq_quantize_layer.
+ * info   host int32, out, may be NULL: as gptq_prepare.
+ * dev    device buffer of at least gptq_layer_host_size(chunk_tokens, d_out, d_in, bits,
+ *        group, xdtype, wdtype) bytes, 256-byte aligned, owned by the caller: it holds H,
+ *        U, the staging buffers, device copies of W and of the outputs, and the scratch
+ *        the three device calls use in turn.  Its contents afterwards are unspecified.
+ * stream as elsewhere; the host-to-device copies run on a library-internal copy stream of
+ *        the device, ordered after the work already queued on `stream`.  The call returns
+ *        after the outputs have arrived in host memory.  On every return no copy of this
+ *        call is still in flight.
+ * Errors: INVALID_ARG (also ntok == 0: nothing to prepare), UNSUPPORTED, WORKSPACE, and
+ *         those of the three device calls (NOT_PD, NONFINITE, CUDA, TIMEOUT).
+ */
+gptq_status gptq_quantize_layer_host(const void* X, int xdtype, int64_t ntok,
+                                     int64_t chunk_tokens, const void* W, int wdtype,
+                                     int32_t d_out, int32_t d_in, float damp, int actorder,
+                                     int bits, int group, int sym, int blocksize, int flags,
+                                     int32_t* qweight, float* scales, int32_t* qzeros,
+                                     int32_t* g_idx, int32_t* perm, double* loss, int32_t* info,
+                                     void* dev, size_t dev_bytes, void* stream);
+
+/*
  * gptq_dequant_matmul -- y = x W_hat^T from the packed checkpoint, the product a W4A16-
  * style serving kernel computes ("GPTQ Architecture, in depth", "Packing, tooling and
  * serving": codes are unpacked and dequantised with their group's scale and zero point
@@ -321,7 +393,7 @@ typedef enum {
   GPTQ_K_TRTRI_DIAG, GPTQ_K_TRTRI_UPDATE, GPTQ_K_PREP_REVERSE,
   GPTQ_K_QUANT_GATHER, GPTQ_K_QUANT_FIT, GPTQ_K_QUANT_LOOP, GPTQ_K_QUANT_LAZY,
   GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT, GPTQ_K_DEQUANT_MATMUL,
-  GPTQ_K_DEQUANTIZE,
+  GPTQ_K_DEQUANTIZE, GPTQ_K_HESSIAN_RESCALE,
   GPTQ_K_COUNT
 } gptq_kernel_kind;
 

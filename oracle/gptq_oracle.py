@@ -58,6 +58,7 @@ F64 = np.float64
 __all__ = [
     "hessian", "hessian_streaming", "hessian_block",
     "dead_columns", "fix_dead", "act_order", "damping", "inverse_cholesky_upper",
+    "inverse_cholesky_upper_rows",
     "grid", "fit_group", "round_to_grid",
     "gptq_sweep", "gptq_sweep_obs",
     "gptq_prepare", "gptq_quantize_layer", "gptq_layer",
@@ -175,6 +176,27 @@ def inverse_cholesky_upper(Hd) -> np.ndarray:
     Hinv = 0.5 * (Hinv + Hinv.T)                    # exact symmetry for the next factor
     Lh = np.linalg.cholesky(Hinv)                   # Hinv = Lh Lh^T
     return np.ascontiguousarray(Lh.T)               # U = Lh^T, Hinv = U^T U
+
+
+def inverse_cholesky_upper_rows(Hd, rows) -> np.ndarray:
+    """Rows ``rows`` of the same U, for matrices too large for the four steps on a CPU.
+
+    Section 1.7 of "Same Ruler" shows that row q of U holds the conditional inverse at
+    step q, i.e. it only depends on H_damp's trailing block from q on.  Ordering the
+    columns backwards (J the index reversal) turns those trailing blocks into leading
+    ones, so with Lr = chol(J H_damp J) (lower), U = J Lr^-1 J: row q of U is row
+    d-1-q of Lr^-1 read backwards, the solution y of Lr^T y = e_(d-1-q).  One Cholesky
+    factorisation and one triangular solve with the selected unit vectors; float64.
+    """
+    import scipy.linalg
+    Hd = np.asarray(Hd, dtype=F64)
+    d = Hd.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    Lr = np.linalg.cholesky(Hd[::-1, ::-1])          # J H_damp J = Lr Lr^T
+    E = np.zeros((d, rows.size), dtype=F64)
+    E[d - 1 - rows, np.arange(rows.size)] = 1.0
+    Y = scipy.linalg.solve_triangular(Lr, E, trans="T", lower=True)   # Lr^T Y = E
+    return np.ascontiguousarray(Y.T[:, ::-1])
 
 
 def _lower_inverse(L: np.ndarray) -> np.ndarray:

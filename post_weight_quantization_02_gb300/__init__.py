@@ -7,3 +7,4 @@ does, and fails loudly if it cannot.
 """
 
 from .api import LayerEngine, QuantizedLayer, quantize_layer_from_host  # noqa: F401
+from .shard import ShardedLayer, row_range, row_ranges, token_range  # noqa: F401

@@ -3,14 +3,15 @@
 ``LayerEngine`` owns the device buffers of one layer shape (torch allocates them; the
 library never does) and drives the three C-ABI calls: ``add_batch`` is the Hessian hook,
 ``quantize`` runs prepare and the column loop.  ``quantize_layer_from_host`` is the
-end-to-end path: pinned host activations and weights in, packed checkpoint tensors out,
-with the host-to-device copies of token chunks overlapped with the Hessian kernels.
+end-to-end path: host activations and weights in, packed checkpoint tensors out, in one
+call of the C ABI that copies token chunks to the device while the Hessian kernels of the
+previous chunk run.
 """
 
 from __future__ import annotations
 
 import dataclasses
-from typing import Iterable, Optional
+from typing import Optional
 
 import torch
 
@@ -81,6 +82,11 @@ class LayerEngine:
         """Wait for the enqueued Hessian steps and raise the first device-side failure."""
         G.gptq_hessian_status(self.ws_h, stream)
 
+    def rescale_hessian(self, n_from: int, n_to: int, stream=None) -> None:
+        """H <- H * n_from / n_to: this engine's partial as its share of an n_to-token
+        stream (the token-split combine; see ``shard``)."""
+        G.gptq_hessian_rescale(self.H, n_from, n_to, stream)
+
     def prepare(self, stream=None) -> int:
         return G.gptq_prepare(self.H, self.damp, self.actorder, self.perm, self.dead,
                               self.Hinv_chol, self.ws_p, stream)
@@ -101,47 +107,47 @@ class LayerEngine:
         return self.quantize_weights(W, stream)
 
 
-def quantize_layer_from_host(engine: LayerEngine, W_host: torch.Tensor,
-                             X_chunks_host: Iterable[torch.Tensor],
-                             out: Optional[QuantizedLayer] = None) -> QuantizedLayer:
-    """End to end from (pinned) host memory.
+def quantize_layer_from_host(engine: LayerEngine, W_host: torch.Tensor, X_host: torch.Tensor,
+                             out: Optional[QuantizedLayer] = None,
+                             chunk_tokens: int = 16384, stream=None) -> QuantizedLayer:
+    """End to end from host memory in one C-ABI call (gptq_quantize_layer_host).
 
-    Token chunks are copied host-to-device on a side stream, double buffered, while the
-    Hessian kernels of the previous chunk run (enqueued without waiting, so the host
-    issues the next copy at once); the weights follow; the packed outputs are copied back
-    into ``out`` (pinned host tensors) when given.
+    ``X_host`` ``[ntok, d_in]`` and ``W_host`` ``[d_out, d_in]`` are host tensors (page-
+    locked, e.g. ``.pin_memory()``, so that the library's chunked copies overlap the
+    Hessian kernels).  The engine supplies the quantiser settings and the device; the
+    library's device buffer is allocated here by torch, once per chunk size, and kept on
+    the engine.  The packed outputs land in ``out`` (host tensors, allocated pinned when
+    not given); ``out.loss`` is a float64 host scalar.
     """
-    dev = engine.device
-    compute = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
-    bufs = [None, None]
-    done = [torch.cuda.Event(), torch.cuda.Event()]
-    ready = [torch.cuda.Event(), torch.cuda.Event()]
-    engine.reset()
-    for i, xh in enumerate(X_chunks_host):
-        b = i % 2
-        if bufs[b] is None or bufs[b].shape != xh.shape or bufs[b].dtype != xh.dtype:
-            bufs[b] = torch.empty(xh.shape, dtype=xh.dtype, device=dev)
-        with torch.cuda.stream(copy):
-            copy.wait_event(done[b])
-            bufs[b].copy_(xh, non_blocking=True)
-            ready[b].record(copy)
-        compute.wait_event(ready[b])
-        engine.add_batch_async(bufs[b], compute)
-        done[b].record(compute)
-    if engine.nseen == 0:
-        raise RuntimeError("no calibration tokens: X_chunks_host was empty")
-    with torch.cuda.stream(copy):
-        Wd = W_host.to(dev, non_blocking=True)
-        wready = torch.cuda.Event()
-        wready.record(copy)
-    engine.hessian_status(compute)
-    engine.prepare(compute)
-    compute.wait_event(wready)
-    res = engine.quantize_weights(Wd, compute)
+    if X_host.dim() != 2 or X_host.shape[1] != engine.d_in:
+        raise ValueError("X_host must be [ntok, d_in]")
+    m, d, bits = engine.d_out, engine.d_in, engine.bits
     if out is None:
-        return res.to("cpu")
-    for f in dataclasses.fields(out):
-        getattr(out, f.name).copy_(getattr(res, f.name), non_blocking=True)
-    compute.synchronize()
+        ngroups = 1 if engine.group == -1 else -(-d // engine.group)
+        out = QuantizedLayer(
+            torch.empty(bits * d // 32, m, dtype=torch.int32).pin_memory(),
+            torch.empty(ngroups, m, dtype=torch.float32).pin_memory(),
+            torch.empty(ngroups, bits * m // 32, dtype=torch.int32).pin_memory(),
+            torch.empty(d, dtype=torch.int32).pin_memory(),
+            torch.empty(d, dtype=torch.int32).pin_memory(),
+            torch.empty((), dtype=torch.float64))
+    key = (int(chunk_tokens), _dtype_code(X_host), _dtype_code(W_host))
+    buf = getattr(engine, "_host_buf", None)
+    if buf is None or buf[0] != key:
+        nbytes = G.gptq_layer_host_size(chunk_tokens, m, d, bits, engine.group, key[1], key[2])
+        if nbytes == 0:
+            raise ValueError("unsupported sizes or element types for the host path")
+        engine._host_buf = (key, G.workspace(nbytes, engine.device))
+    dev = engine._host_buf[1]
+    with torch.cuda.device(engine.device):
+        loss, _ = G.gptq_quantize_layer_host(
+            X_host, W_host, chunk_tokens, engine.damp, engine.actorder, bits, engine.group,
+            engine.sym, engine.blocksize, out.qweight, out.scales, out.qzeros, out.g_idx,
+            out.perm, dev, stream, static_groups=engine.static_groups)
+    out.loss.fill_(loss)
     return out
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    """The library's element-type code of a tensor."""
+    return G.GPTQ_BF16 if t.dtype == torch.bfloat16 else G.GPTQ_F32

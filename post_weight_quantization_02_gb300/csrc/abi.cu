@@ -3,8 +3,8 @@
 // stream and returns the status of the work (see include/gptq.h).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -73,11 +73,8 @@ void raise_device_status(const DevStatus& h, const char* call) {
 
 // ------------------------------------------------------------------ Hessian
 
-bool use_tensor_cores(int xdtype) {
-  if (xdtype != GPTQ_BF16) return false;
-  const char* e = std::getenv("GPTQ_SYRK");
-  return !(e != nullptr && std::strcmp(e, "simt") == 0);
-}
+// bf16 tokens run on the tensor-core SYRK, float32 tokens on the float32 FMA kernel
+bool use_tensor_cores(int xdtype) { return xdtype == GPTQ_BF16; }
 
 int planning_sm_count() {
   int dev = 0, n = 0;
@@ -147,8 +144,8 @@ size_t quantize_ws_bytes(int m, int d, int G) {
   w.add<DevStatus>(1);
   w.add<float>(static_cast<size_t>(m) * d);    // Wp
   w.add<uint8_t>(static_cast<size_t>(m) * d);  // codesT
-  w.add<uint16_t>(static_cast<size_t>(2 * kErrRows) * m);  // errors, bf16 hi
-  w.add<uint16_t>(static_cast<size_t>(2 * kErrRows) * m);  // errors, bf16 lo
+  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 hi
+  w.add<uint16_t>(static_cast<size_t>(kErrRows) * m);  // errors, bf16 lo
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 hi
   w.add<uint16_t>(static_cast<size_t>(d) * d);    // U, bf16 lo
   w.add<int32_t>(static_cast<size_t>(G) * m);  // zeros
@@ -162,6 +159,42 @@ int groups_of(int d, int group) { return group == -1 ? 1 : static_cast<int>(ceil
 
 bool group_supported(int group) {
   return group == -1 || group == 16 || group == 32 || group == 64 || (group > 0 && group % 128 == 0);
+}
+
+// Device layout of gptq_quantize_layer_host: the layer's persistent buffers, two staging
+// buffers for token chunks, the device copies of W and of the outputs, and one scratch
+// region shared in turn by the Hessian, prepare and quantize workspaces.
+struct HostLayout {
+  size_t hess, prep, quant, scratch, total;
+};
+
+size_t hessian_ws_for(int64_t ntok, int d);
+
+HostLayout host_layout(int64_t chunk, int m, int d, int bits, int group, int xdtype,
+                       int wdtype) {
+  HostLayout L;
+  const int G = groups_of(d, group);
+  const size_t xe = (xdtype == GPTQ_BF16) ? 2 : 4, we = (wdtype == GPTQ_BF16) ? 2 : 4;
+  L.hess = hessian_ws_for(chunk, d);
+  L.prep = prepare_ws_bytes(d);
+  L.quant = quantize_ws_bytes(m, d, G);
+  L.scratch = std::max(L.hess, std::max(L.prep, L.quant));
+  WsPlan w;
+  w.add<float>(static_cast<size_t>(d) * d);                    // H
+  w.add<float>(static_cast<size_t>(d) * d);                    // U
+  w.add<int32_t>(d);                                           // perm
+  w.add<uint8_t>(d);                                           // dead
+  w.add<uint8_t>(static_cast<size_t>(m) * d * we);             // W
+  w.add<uint8_t>(static_cast<size_t>(chunk) * d * xe);         // token chunk, buffer 0
+  w.add<uint8_t>(static_cast<size_t>(chunk) * d * xe);         // token chunk, buffer 1
+  w.add<int32_t>(static_cast<size_t>(bits) * d / 32 * m);      // qweight
+  w.add<float>(static_cast<size_t>(G) * m);                    // scales
+  w.add<int32_t>(static_cast<size_t>(G) * bits * m / 32);      // qzeros
+  w.add<int32_t>(d);                                           // g_idx
+  w.add<double>(1);                                            // loss
+  w.add<uint8_t>(L.scratch);
+  L.total = w.bytes;
+  return L;
 }
 
 // The Hessian step behind gptq_hessian_accumulate (sync) and its enqueue-only form.
@@ -208,6 +241,27 @@ void hessian_step(float* H, int64_t* nseen, const void* X, int xdtype, int64_t n
   *nseen = n_old + ntok;
 }
 
+// The Hessian workspace gptq_workspace_size reports for a call of ntok tokens.
+size_t hessian_ws_for(int64_t ntok, int d) {
+  const int64_t t = ntok > 0 ? ntok : 1;
+  SplitPlan p = plan_splits(t, d, true, 16, planning_sm_count());
+  SplitPlan q = plan_splits(t, d, false, 16, planning_sm_count());
+  return hessian_ws_bytes(d, p.splits > q.splits ? p.splits : q.splits);
+}
+
+// Events of one gptq_quantize_layer_host call.  On every exit the copy stream is drained
+// first, so that no copy still reads the caller's host buffers or writes the device
+// buffer after the call returns.
+struct HostCallEvents {
+  cudaStream_t copy = nullptr;
+  cudaEvent_t ev[6] = {};
+  int n = 0;
+  ~HostCallEvents() {
+    if (copy != nullptr) cudaStreamSynchronize(copy);
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+};
+
 }  // namespace
 }  // namespace gptq
 
@@ -220,13 +274,9 @@ size_t gptq_workspace_size(int op, int64_t ntok, int32_t d_out, int32_t d_in, in
   (void)bits;
   if (d_in <= 0) return 0;
   switch (op) {
-    case GPTQ_OP_HESSIAN: {
+    case GPTQ_OP_HESSIAN:
       if (ntok < 0) return 0;
-      const int64_t t = ntok > 0 ? ntok : 1;
-      SplitPlan p = plan_splits(t, d_in, true, 16, planning_sm_count());
-      SplitPlan q = plan_splits(t, d_in, false, 16, planning_sm_count());
-      return hessian_ws_bytes(d_in, p.splits > q.splits ? p.splits : q.splits);
-    }
+      return hessian_ws_for(ntok, d_in);
     case GPTQ_OP_PREPARE:
       return prepare_ws_bytes(d_in);
     case GPTQ_OP_QUANTIZE:
@@ -262,6 +312,22 @@ gptq_status gptq_hessian_status(void* ws, size_t ws_bytes, void* stream) {
     GPTQ_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
     GPTQ_CUDA(cudaStreamSynchronize(s));
     raise_device_status(h, "gptq_hessian_accumulate_async");
+  });
+}
+
+gptq_status gptq_hessian_rescale(float* H, int32_t d_in, int64_t n_from, int64_t n_to,
+                                 void* stream) {
+  return guarded([&] {
+    require(H != nullptr, GPTQ_ERR_INVALID_ARG, "gptq_hessian_rescale: null H");
+    require(d_in > 0 && n_from >= 0 && n_to > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_hessian_rescale: need d_in > 0, n_from >= 0, n_to > 0");
+    require(d_in % 8 == 0, GPTQ_ERR_UNSUPPORTED, "gptq_hessian_rescale: d_in must be a multiple of 8");
+    require(aligned(H, 16), GPTQ_ERR_INVALID_ARG, "gptq_hessian_rescale: H must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float factor = static_cast<float>(static_cast<double>(n_from) / static_cast<double>(n_to));
+    launch_hessian_rescale(H, d_in, factor, s);
+    GPTQ_CUDA(cudaStreamSynchronize(s));
+    trace_flush();
   });
 }
 
@@ -344,8 +410,8 @@ gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_
     q.st = wc.take<DevStatus>(1);
     q.Wp = wc.take<float>(static_cast<size_t>(d_out) * d_in);
     q.codesT = wc.take<uint8_t>(static_cast<size_t>(d_out) * d_in);
-    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(2 * kErrRows) * d_out);
-    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(2 * kErrRows) * d_out);
+    q.ehi = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
+    q.elo = wc.take<__nv_bfloat16>(static_cast<size_t>(kErrRows) * d_out);
     q.uhi = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.ulo = wc.take<__nv_bfloat16>(static_cast<size_t>(d_in) * d_in);
     q.zeros = wc.take<int32_t>(static_cast<size_t>(G) * d_out);
@@ -369,7 +435,6 @@ gptq_status gptq_quantize_layer_ex(const void* W, int wdtype, const float* Hinv_
     q.qzeros = qzeros;
     q.g_idx = g_idx;
     q.loss = loss;
-    std::lock_guard<std::mutex> lk(aux_mutex());  // the internal streams are shared
     begin_call(q.st, s);
     launch_quantize(q, s);
     raise_device_status(finish_call(q.st, s), "gptq_quantize_layer");
@@ -385,6 +450,139 @@ gptq_status gptq_quantize_layer(const void* W, int wdtype, const float* Hinv_cho
   return gptq_quantize_layer_ex(W, wdtype, Hinv_chol, perm, dead, d_out, d_in, bits, group, sym,
                                 blocksize, 0, qweight, scales, qzeros, g_idx, loss, ws,
                                 ws_bytes, stream);
+}
+
+size_t gptq_layer_host_size(int64_t chunk_tokens, int32_t d_out, int32_t d_in, int bits,
+                            int group, int xdtype, int wdtype) {
+  if (chunk_tokens <= 0 || d_out <= 0 || d_in <= 0 || d_in % 32 != 0 || d_out % 32 != 0 ||
+      !(bits == 2 || bits == 3 || bits == 4 || bits == 8) || !group_supported(group) ||
+      !(xdtype == GPTQ_F32 || xdtype == GPTQ_BF16) || !(wdtype == GPTQ_F32 || wdtype == GPTQ_BF16)) {
+    return 0;
+  }
+  return host_layout(chunk_tokens, d_out, d_in, bits, group, xdtype, wdtype).total;
+}
+
+gptq_status gptq_quantize_layer_host(const void* X, int xdtype, int64_t ntok, int64_t chunk_tokens,
+                                     const void* W, int wdtype, int32_t d_out, int32_t d_in,
+                                     float damp, int actorder, int bits, int group, int sym,
+                                     int blocksize, int flags, int32_t* qweight, float* scales,
+                                     int32_t* qzeros, int32_t* g_idx, int32_t* perm, double* loss,
+                                     int32_t* info, void* dev, size_t dev_bytes, void* stream) {
+  if (info != nullptr) *info = 0;
+  int32_t pivot = 0;
+  gptq_status rc = guarded([&] {
+    const char* fn = "gptq_quantize_layer_host";
+    require(ntok > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: no calibration tokens (ntok must be positive)");
+    require(X != nullptr && W != nullptr && qweight != nullptr && scales != nullptr &&
+                qzeros != nullptr && g_idx != nullptr && perm != nullptr && loss != nullptr &&
+                dev != nullptr,
+            GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer_host: null pointer argument");
+    require(chunk_tokens > 0 && chunk_tokens < (int64_t(1) << 31), GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: chunk_tokens must be in 1 .. 2^31 - 1");
+    require(d_out > 0 && d_in > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: need d_out > 0 and d_in > 0");
+    require((xdtype == GPTQ_F32 || xdtype == GPTQ_BF16) && (wdtype == GPTQ_F32 || wdtype == GPTQ_BF16),
+            GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer_host: dtypes must be GPTQ_F32 or GPTQ_BF16");
+    require(std::isfinite(damp) && damp >= 0.0f, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: damp must be finite and >= 0");
+    require((flags & ~GPTQ_QUANT_STATIC_GROUPS) == 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: unknown flags");
+    require(sym == 0 || sym == 1, GPTQ_ERR_INVALID_ARG, "gptq_quantize_layer_host: sym must be 0 or 1");
+    require(blocksize >= 1 && blocksize <= 128, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: blocksize must be in 1..128");
+    require(group == -1 || group > 0, GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: group must be -1 or positive");
+    require(bits == 2 || bits == 3 || bits == 4 || bits == 8, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer_host: bits must be 2, 3, 4 or 8");
+    require(group_supported(group), GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer_host: group must be -1, 16, 32, 64 or a multiple of 128");
+    require(group == -1 || group % blocksize == 0 || blocksize % group == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer_host: group and blocksize must divide one another");
+    require(d_in % 32 == 0 && d_out % 32 == 0, GPTQ_ERR_UNSUPPORTED,
+            "gptq_quantize_layer_host: d_in and d_out must be multiples of 32");
+    require(aligned(dev, 256), GPTQ_ERR_INVALID_ARG,
+            "gptq_quantize_layer_host: the device buffer must be 256-byte aligned");
+    const HostLayout lay = host_layout(chunk_tokens, d_out, d_in, bits, group, xdtype, wdtype);
+    require(dev_bytes >= lay.total, GPTQ_ERR_WORKSPACE,
+            "gptq_quantize_layer_host: device buffer too small (see gptq_layer_host_size)");
+    const int m = d_out, d = d_in, G = groups_of(d, group);
+    const size_t xe = (xdtype == GPTQ_BF16) ? 2 : 4, we = (wdtype == GPTQ_BF16) ? 2 : 4;
+    WsCarver wc(dev, dev_bytes);
+    float* H = wc.take<float>(static_cast<size_t>(d) * d);
+    float* U = wc.take<float>(static_cast<size_t>(d) * d);
+    int32_t* perm_d = wc.take<int32_t>(d);
+    uint8_t* dead_d = wc.take<uint8_t>(d);
+    uint8_t* W_d = wc.take<uint8_t>(static_cast<size_t>(m) * d * we);
+    uint8_t* xs[2];
+    xs[0] = wc.take<uint8_t>(static_cast<size_t>(chunk_tokens) * d * xe);
+    xs[1] = wc.take<uint8_t>(static_cast<size_t>(chunk_tokens) * d * xe);
+    const size_t qw_words = static_cast<size_t>(bits) * d / 32 * m;
+    const size_t qz_words = static_cast<size_t>(G) * bits * m / 32;
+    int32_t* qw_d = wc.take<int32_t>(qw_words);
+    float* sc_d = wc.take<float>(static_cast<size_t>(G) * m);
+    int32_t* qz_d = wc.take<int32_t>(qz_words);
+    int32_t* gi_d = wc.take<int32_t>(d);
+    double* loss_d = wc.take<double>(1);
+    void* scratch = wc.take<uint8_t>(lay.scratch);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    HostCallEvents he;
+    {
+      std::lock_guard<std::mutex> lk(aux_mutex());
+      he.copy = copy_stream();
+    }
+    for (; he.n < 6; ++he.n) {
+      GPTQ_CUDA(cudaEventCreateWithFlags(&he.ev[he.n], cudaEventDisableTiming));
+    }
+    cudaEvent_t* done = he.ev;       // [2] the Hessian step that read staging buffer b
+    cudaEvent_t* ready = he.ev + 2;  // [2] the copy into staging buffer b
+    cudaEvent_t fork = he.ev[4], wready = he.ev[5];
+    // the copies follow whatever the caller queued on `stream` before this call
+    GPTQ_CUDA(cudaEventRecord(fork, s));
+    GPTQ_CUDA(cudaStreamWaitEvent(he.copy, fork, 0));
+    // the Hessian hook over the token stream: chunk c is copied into staging buffer c % 2
+    // while the Hessian kernels of chunk c - 1 run
+    int64_t nseen = 0;
+    const int64_t nchunks = (ntok + chunk_tokens - 1) / chunk_tokens;
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int b = static_cast<int>(c & 1);
+      const int64_t t = std::min(chunk_tokens, ntok - c * chunk_tokens);
+      if (c >= 2) GPTQ_CUDA(cudaStreamWaitEvent(he.copy, done[b], 0));
+      GPTQ_CUDA(cudaMemcpyAsync(xs[b], static_cast<const char*>(X) + c * chunk_tokens * d * xe,
+                                static_cast<size_t>(t) * d * xe, cudaMemcpyHostToDevice, he.copy));
+      GPTQ_CUDA(cudaEventRecord(ready[b], he.copy));
+      GPTQ_CUDA(cudaStreamWaitEvent(s, ready[b], 0));
+      hessian_step(H, &nseen, xs[b], xdtype, t, d, scratch, lay.hess, stream, false);
+      GPTQ_CUDA(cudaEventRecord(done[b], s));
+    }
+    // the weights follow the tokens on the copy stream
+    GPTQ_CUDA(cudaMemcpyAsync(W_d, W, static_cast<size_t>(m) * d * we, cudaMemcpyHostToDevice,
+                              he.copy));
+    GPTQ_CUDA(cudaEventRecord(wready, he.copy));
+    {
+      WsCarver hw(scratch, lay.hess);
+      raise_device_status(finish_call(hw.take<DevStatus>(1), s), fn);
+    }
+    gptq_status st = gptq_prepare(H, d, damp, actorder, perm_d, dead_d, U, &pivot, scratch,
+                                  lay.scratch, stream);
+    if (st != GPTQ_OK) fail(st, "%s", last_error().c_str());
+    GPTQ_CUDA(cudaStreamWaitEvent(s, wready, 0));
+    st = gptq_quantize_layer_ex(W_d, wdtype, U, perm_d, dead_d, m, d, bits, group, sym, blocksize,
+                                flags, qw_d, sc_d, qz_d, gi_d, loss_d, scratch, lay.scratch, stream);
+    if (st != GPTQ_OK) fail(st, "%s", last_error().c_str());
+    double loss_h = 0.0;
+    GPTQ_CUDA(cudaMemcpyAsync(qweight, qw_d, qw_words * 4, cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaMemcpyAsync(scales, sc_d, static_cast<size_t>(G) * m * 4, cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaMemcpyAsync(qzeros, qz_d, qz_words * 4, cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaMemcpyAsync(g_idx, gi_d, static_cast<size_t>(d) * 4, cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaMemcpyAsync(perm, perm_d, static_cast<size_t>(d) * 4, cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaMemcpyAsync(&loss_h, loss_d, sizeof(double), cudaMemcpyDeviceToHost, s));
+    GPTQ_CUDA(cudaStreamSynchronize(s));
+    *loss = loss_h;
+  });
+  if (info != nullptr) *info = pivot;
+  return rc;
 }
 
 gptq_status gptq_dequant_matmul(const void* x, int xdtype, int64_t n, int32_t d_in,
@@ -479,7 +677,7 @@ const char* gptq_kernel_name(int kind) {
       "syrk_tc", "syrk_simt", "syrk_reduce", "prep_diag", "prep_rank", "prep_mirror",
       "prep_gather", "potrf_panel", "potrf_trsm", "potrf_update", "trtri_diag", "trtri_update",
       "prep_reverse", "quant_gather", "quant_fit", "quant_loop", "quant_lazy", "quant_pack",
-      "quant_loss", "quant_split", "dequant_matmul", "dequantize"};
+      "quant_loss", "quant_split", "dequant_matmul", "dequantize", "hessian_rescale"};
   if (kind < 0 || kind >= GPTQ_K_COUNT) return "";
   return names[kind];
 }

@@ -161,8 +161,11 @@ struct AuxStreams {
   cudaStream_t b = nullptr;
   cudaStream_t c = nullptr;
   std::vector<cudaEvent_t> ev;
+  cudaStream_t copy = nullptr;  // host <-> device copies of gptq_quantize_layer_host
 };
 AuxStreams& aux_streams(int nevents);
 std::mutex& aux_mutex();
+// The current device's copy stream (created on first use); call with aux_mutex() held.
+cudaStream_t copy_stream();
 
 }  // namespace gptq

@@ -115,7 +115,29 @@ __global__ void syrk_reduce_kernel(float* __restrict__ H, const float* __restric
   *reinterpret_cast<float4*>(H + off) = h;
 }
 
+// H[i][j] = factor * H[i][j] on the upper 128-tile triangle (zeros when factor == 0, so
+// that a partial of no tokens contributes nothing whatever H held); same indexing as the
+// reduction, 16-byte accesses.
+__global__ void hessian_rescale_kernel(float* __restrict__ H, int d, float factor) {
+  const int i = blockIdx.y;
+  const int jstart = (i / 128) * 128;
+  const int j = jstart + 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (j >= d) return;
+  float4* p = reinterpret_cast<float4*>(H + (size_t)i * d + j);
+  float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (factor != 0.0f) {
+    h = *p;
+    h.x *= factor; h.y *= factor; h.z *= factor; h.w *= factor;
+  }
+  *p = h;
+}
+
 }  // namespace
+
+void launch_hessian_rescale(float* H, int d, float factor, cudaStream_t s) {
+  dim3 grid((unsigned)ceil_div(d / 4, 256), d);
+  GPTQ_LAUNCH(GPTQ_K_HESSIAN_RESCALE, s, hessian_rescale_kernel, grid, 256, 0, H, d, factor);
+}
 
 int syrk_simt_tiles(int d) {
   int nt = (d + kTile - 1) / kTile, n = 0;

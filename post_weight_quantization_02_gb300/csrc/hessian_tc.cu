@@ -31,6 +31,9 @@
 // alternate between chains, so the MMAs of one chain overlap the drain of the previous one.
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc_common.cuh"
@@ -67,17 +70,40 @@ struct SyrkArgs {
   DevStatus* st;
 };
 
-// pair p of column tile J: row tiles 2p and 2p + 1 (the second may lie past the last row
-// tile when a column tile has an odd count; its CTA then multiplies zeros and stores
-// nothing)
+// Unit order.  Pair p of column tile J covers row tiles 2p and 2p + 1 (the second may lie
+// past the last row tile when a column tile has an odd count; its CTA then multiplies
+// zeros and stores nothing); column tile J has min(J + 1, cap) pairs, cap = ceil(n_i / 2).
+// The pairs are taken in bands of kBand column tiles, and inside a band row pair by row
+// pair, so that the units in flight at once (one per cluster) read few distinct strips of
+// X: on a wide layer a wave of 76 units shares about 10 row strips and 8 column strips
+// instead of 76 row strips and one column strip, and the strips stay in L2 while every
+// unit of the wave walks the same tokens.
+constexpr int kBand = 8;
+
 __device__ __forceinline__ void decode_pair(int pair, int n_i, int n_j, int& P, int& J) {
+  const int cap = (n_i + 1) / 2;
   int rem = pair;
-  for (J = 0; J < n_j; ++J) {
-    const int cnt = (min(2 * J + 2, n_i) + 1) / 2;
-    if (rem < cnt) { P = rem; return; }
-    rem -= cnt;
+  for (int b0 = 0; b0 < n_j; b0 += kBand) {
+    const int b1 = min(b0 + kBand, n_j), w = b1 - b0;
+    const int p1 = min(b0, cap);  // pairs wholly above the band: every column tile of it
+    if (rem < p1 * w) {
+      P = rem / w;
+      J = b0 + rem % w;
+      return;
+    }
+    rem -= p1 * w;
+    for (int p = p1; p < min(b1, cap); ++p) {  // pairs meeting the diagonal: J >= p
+      const int k = b1 - p;
+      if (rem < k) {
+        P = p;
+        J = p + rem;
+        return;
+      }
+      rem -= k;
+    }
   }
   P = 0;
+  J = 0;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -291,6 +317,30 @@ int syrk_tc_tiles(int d) {
 
 int syrk_tc_token_granule() { return BK; }
 
+namespace {
+int resident_clusters() {
+  static std::mutex mu;
+  static std::map<int, int> per_dev;  // device -> co-resident clusters of the kernel
+  int dev = 0;
+  GPTQ_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  int& r = per_dev[dev];
+  if (r <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    r = n < sm_count() / 2 ? n : sm_count() / 2;
+  }
+  return r;
+}
+}  // namespace
+
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s) {
   ensure_dynamic_smem(syrk_tc_kernel, SMEM_BYTES);
@@ -309,20 +359,9 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.P = P;
   a.st = st;
   // one cluster of two CTAs per pair unit, no more clusters than can be resident at once
-  // (a cluster needs two SMs of one GPC, so that may be fewer than half the SMs)
-  static int resident = 0;
-  if (resident <= 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = sm_count() / 2;
-    }
-    resident = n < sm_count() / 2 ? n : sm_count() / 2;
-  }
+  // (a cluster needs two SMs of one GPC, so that may be fewer than half the SMs); the
+  // count is looked up once per device
+  const int resident = resident_clusters();
   const int64_t units = static_cast<int64_t>(a.n_pairs) * splits;
   const int64_t clusters = resident;
   const int grid = 2 * static_cast<int>(units < clusters ? units : clusters);

@@ -16,6 +16,8 @@ void launch_syrk_simt(const void* X, bool bf16, int64_t ntok, int d, int splits,
                       int64_t tok_per_split, float* P, cudaStream_t s);
 void launch_syrk_reduce(float* H, const float* P, int d, int splits, float alpha, float beta,
                         bool overwrite, cudaStream_t s);
+// H <- factor * H on the upper 128-tile triangle (d a multiple of 4)
+void launch_hessian_rescale(float* H, int d, float factor, cudaStream_t s);
 
 // hessian_tc.cu
 int syrk_tc_tiles(int d);
@@ -82,8 +84,7 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         cudaStream_t s, bool pdl);
 
 // lazy_tc.cu
-// ErrT rows kept for the deferred update: one 512-column superblock of the loop (the
-// workspace holds two, alternating between superblocks)
+// ErrT rows kept for the deferred update: one 512-column superblock of the loop
 constexpr int kErrRows = 512;
 
 struct LazyMaps {
@@ -99,7 +100,5 @@ void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, 
 // max_ctas > 0 caps the persistent grid (to leave SMs to concurrent work)
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
                     DevStatus* st, cudaStream_t s, int max_ctas);
-// CTAs of a far update's tail, which runs beside the column loop
-constexpr int kTailCtas = 24;
 
 }  // namespace gptq

@@ -591,7 +591,7 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
     GPTQ_LAUNCH(GPTQ_K_QUANT_SPLIT, s, ulayout_kernel, dim3((unsigned)ceil_div(d, BLK), BLK), 128,
                 0, q.U, d, q.Ublk);
     launch_usplit(q.U, d, q.uhi, q.ulo, s);
-    const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, 2 * kErrRows, q.uhi, q.ulo, q.Wp, m, d);
+    const LazyMaps maps = make_lazy_maps(q.ehi, q.elo, kErrRows, q.uhi, q.ulo, q.Wp, m, d);
     ensure_dynamic_smem(column_loop_kernel<false>, kLoopSmemDynamic);
     ensure_dynamic_smem(column_loop_kernel<true>, kLoopSmemStatic);
     const bool inblock_fit = !stat && q.group > 0 && q.group <= BLK;
@@ -601,25 +601,12 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
     const bool groups_nest = stat || q.group == -1 || q.group <= BLK ||
                              kErrRows % q.group == 0 || q.group % kErrRows == 0;
     const int sb_cols = groups_nest ? kErrRows : BLK;
-    // The far update of superblock S splits into a head, the next superblock's columns, on
-    // the call's stream (the next superblock's loop needs it) and a tail, every column after
-    // that, on an internal low-priority stream with a small grid, overlapping the next
-    // superblock's column loop.  The superblocks' errors alternate between two buffers so
-    // that the tail can still read them; each far update of a column waits for the
-    // previous one, so every W element receives its updates in the same order as in a
-    // sequential run.
-    const int nsup = static_cast<int>(ceil_div(d, sb_cols));
-    AuxStreams& aux = aux_streams(nsup + 2);
-    cudaStream_t st = aux.b;
-    cudaEvent_t ev_err = aux.ev[nsup];        // the superblock's errors are complete
-    cudaEvent_t ev_fork = aux.ev[nsup + 1];
-    GPTQ_CUDA(cudaEventRecord(ev_fork, s));
-    GPTQ_CUDA(cudaStreamWaitEvent(st, ev_fork, 0));
-    bool tail_pending = false;
-    int sup = 0;
-    for (int s0 = 0; s0 < d; s0 += sb_cols, ++sup) {
+    // The far update of superblock S (every later column) is one launch on the call's
+    // stream over the whole GPU: on wide layers it is most of the update's work, and a
+    // share of the SMs beside the next superblock's column loop left it on the critical
+    // path.  Every W element receives its updates in the sequential order of the blocks.
+    for (int s0 = 0; s0 < d; s0 += sb_cols) {
       const int s1 = (d - s0 < sb_cols) ? d : s0 + sb_cols;
-      const int ebase = (sup % 2) * kErrRows;  // this superblock's error buffer
       for (int i1 = s0; i1 < s1; i1 += BLK) {
         const int nb = (d - i1 < BLK) ? d - i1 : BLK;
         LoopArgs a;
@@ -637,8 +624,8 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
         a.scales = q.scales;
         a.zeros = q.zeros;
         a.codesT = q.codesT;
-        a.ehi = q.ehi + static_cast<size_t>(ebase + i1 - s0) * m;
-        a.elo = q.elo + static_cast<size_t>(ebase + i1 - s0) * m;
+        a.ehi = q.ehi + static_cast<size_t>(i1 - s0) * m;
+        a.elo = q.elo + static_cast<size_t>(i1 - s0) * m;
         a.loss_rows = q.loss_rows;
         if (!inblock_fit && !stat) {
           const bool start = (q.group == -1) ? (i1 == 0) : (i1 % q.group == 0);
@@ -658,26 +645,12 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                       LOOP_THREADS, kLoopSmemDynamic, a);
         }
         // near: the rest of the superblock, W[:, i2:s1] -= Err_block U[i1:i2, i2:s1]
-        if (i1 + nb < s1) launch_lazy_tc(maps, ebase + i1 - s0, i1, nb, i1 + nb, s1, q.st, s, 0);
+        if (i1 + nb < s1) launch_lazy_tc(maps, i1 - s0, i1, nb, i1 + nb, s1, q.st, s, 0);
       }
       if (s1 >= d) break;
-      // far: every later column, W[:, s1:] -= Err_superblock U[s0:s1, s1:]; the head waits
-      // for the previous superblock's tail, which also covered these columns
-      const int h1 = (d - s1 < sb_cols) ? d : s1 + sb_cols;
-      if (tail_pending) GPTQ_CUDA(cudaStreamWaitEvent(s, aux.ev[sup - 1], 0));
-      launch_lazy_tc(maps, ebase, s0, s1 - s0, s1, h1, q.st, s, 0);
-      tail_pending = false;
-      if (h1 < d) {
-        GPTQ_CUDA(cudaEventRecord(ev_err, s));
-        GPTQ_CUDA(cudaStreamWaitEvent(st, ev_err, 0));
-        launch_lazy_tc(maps, ebase, s0, s1 - s0, h1, d, q.st, st, kTailCtas);
-        GPTQ_CUDA(cudaEventRecord(aux.ev[sup], st));
-        tail_pending = true;
-      }
+      // far: every later column, W[:, s1:] -= Err_superblock U[s0:s1, s1:]
+      launch_lazy_tc(maps, 0, s0, s1 - s0, s1, d, q.st, s, 0);
     }
-    // join the internal stream back into the call's stream
-    GPTQ_CUDA(cudaEventRecord(ev_fork, st));
-    GPTQ_CUDA(cudaStreamWaitEvent(s, ev_fork, 0));
     dim3 gq((unsigned)ceil_div(m, 128), static_cast<unsigned>(q.bits * d / 32));
     GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_kernel, gq, 128, 0, q.codesT, q.pos, m, d,
                 q.bits, q.qweight);

@@ -175,6 +175,7 @@ AuxStreams& aux_streams(int nevents) {
                "cudaStreamCreateWithPriority");
     cuda_check(cudaStreamCreateWithPriority(&a.c, cudaStreamNonBlocking, (least + greatest) / 2),
                "cudaStreamCreateWithPriority");
+    cuda_check(cudaStreamCreateWithFlags(&a.copy, cudaStreamNonBlocking), "cudaStreamCreateWithFlags");
   }
   while (static_cast<int>(a.ev.size()) < nevents) {
     cudaEvent_t e;
@@ -183,6 +184,8 @@ AuxStreams& aux_streams(int nevents) {
   }
   return a;
 }
+
+cudaStream_t copy_stream() { return aux_streams(0).copy; }
 
 std::mutex& aux_mutex() {
   static std::mutex m;

@@ -22,12 +22,12 @@ __all__ = [
     "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul", "gptq_dequantize",
     "GptqError", "GptqLibraryError", "lib", "library_path",
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
-    "gptq_hessian_status", "gptq_prepare", "gptq_quantize_layer",
+    "gptq_hessian_status", "gptq_hessian_rescale", "gptq_prepare", "gptq_quantize_layer",
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
     "gptq_kernel_name",
     "gptq_launch_count", "KERNEL_KINDS", "GPTQ_K_SYRK_TC", "GPTQ_K_DEQUANT_MATMUL",
-    "GPTQ_QUANT_STATIC_GROUPS",
+    "GPTQ_QUANT_STATIC_GROUPS", "gptq_layer_host_size", "gptq_quantize_layer_host",
     "workspace",
 ]
 
@@ -35,7 +35,7 @@ GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 
 GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 6, 7
 GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE, GPTQ_OP_DEQUANT_MATMUL = 0, 1, 2, 3
-KERNEL_KINDS = 22
+KERNEL_KINDS = 23
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
 GPTQ_K_DEQUANT_MATMUL = 20
 GPTQ_QUANT_STATIC_GROUPS = 1
@@ -64,6 +64,7 @@ _SIGS = {
     "gptq_hessian_accumulate_async": (_c.c_int, [_vp, _c.POINTER(_i64), _vp, _c.c_int, _i64,
                                                  _i32, _vp, _sz, _vp]),
     "gptq_hessian_status": (_c.c_int, [_vp, _sz, _vp]),
+    "gptq_hessian_rescale": (_c.c_int, [_vp, _i32, _i64, _i64, _vp]),
     "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
                                 _vp, _sz, _vp]),
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
@@ -72,6 +73,12 @@ _SIGS = {
     "gptq_quantize_layer_ex": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
                                           _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp,
                                           _vp, _vp, _vp, _vp, _sz, _vp]),
+    "gptq_layer_host_size": (_sz, [_i64, _i32, _i32, _c.c_int, _c.c_int, _c.c_int, _c.c_int]),
+    "gptq_quantize_layer_host": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _vp, _c.c_int, _i32, _i32,
+                                            _f32, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                                            _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp,
+                                            _c.POINTER(_c.c_double), _c.POINTER(_i32), _vp, _sz,
+                                            _vp]),
     "gptq_dequant_matmul": (_c.c_int, [_vp, _c.c_int, _i64, _i32, _i32, _c.c_int, _vp, _vp,
                                        _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
     "gptq_dequantize": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _c.c_int, _i32, _vp,
@@ -221,6 +228,14 @@ def gptq_hessian_status(ws: torch.Tensor, stream=None) -> None:
     _check(lib().gptq_hessian_status(_ptr(ws), ws.numel(), _stream(stream)))
 
 
+def gptq_hessian_rescale(H: torch.Tensor, n_from: int, n_to: int, stream=None) -> None:
+    """H <- H * n_from / n_to on the upper tiles (a partial Hessian's share of a stream of
+    n_to tokens)."""
+    d = H.shape[0]
+    _check(lib().gptq_hessian_rescale(_buf(H, torch.float32, d * d, "H"), d, int(n_from),
+                                      int(n_to), _stream(stream)))
+
+
 def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tensor,
                  dead: torch.Tensor, Hinv_chol: torch.Tensor, ws: Optional[torch.Tensor] = None,
                  stream=None) -> int:
@@ -266,6 +281,61 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv_chol: torch.Tensor, perm: Optional
     _check(lib().gptq_quantize_layer_ex(_ptr(W), _dtype_code(W), ptrs[0], ptrs[1], ptrs[2], m, d,
                                         bits, group, int(bool(sym)), blocksize, flags, *ptrs[3:],
                                         _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def _hbuf(t: torch.Tensor, dtype, numel: int, name: str) -> int:
+    """Host pointer of a caller buffer (a contiguous CPU tensor) after checking its type
+    and size."""
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
+def gptq_layer_host_size(chunk_tokens: int, d_out: int, d_in: int, bits: int, group: int,
+                         xdtype: int, wdtype: int) -> int:
+    return int(lib().gptq_layer_host_size(chunk_tokens, d_out, d_in, bits, group, xdtype,
+                                          wdtype))
+
+
+def gptq_quantize_layer_host(X: torch.Tensor, W: torch.Tensor, chunk_tokens: int, damp: float,
+                             actorder: bool, bits: int, group: int, sym: bool, blocksize: int,
+                             qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor,
+                             g_idx: torch.Tensor, perm: torch.Tensor, dev: torch.Tensor,
+                             stream=None, static_groups: bool = False):
+    """The whole layer from host tensors X [ntok, d_in] and W [d_out, d_in] (page-locked
+    for overlapped copies) into host outputs; ``dev`` is the caller's device buffer of
+    gptq_layer_host_size bytes.  Returns (loss, info)."""
+    if X.dim() != 2 or W.dim() != 2 or X.shape[1] != W.shape[1]:
+        raise ValueError("X must be [ntok, d_in] and W [d_out, d_in]")
+    m, d = W.shape
+    G, words, zwords = _ngroups(d, group), _packed(bits, d), _packed(bits, m)
+    if G is None or words is None or zwords is None:
+        raise ValueError("unsupported bits or group")
+    px = _hbuf(X, X.dtype, X.numel(), "X")
+    pw = _hbuf(W, W.dtype, W.numel(), "W")
+    outs = (_hbuf(qweight, torch.int32, words * m, "qweight"),
+            _hbuf(scales, torch.float32, G * m, "scales"),
+            _hbuf(qzeros, torch.int32, G * zwords, "qzeros"),
+            _hbuf(g_idx, torch.int32, d, "g_idx"), _hbuf(perm, torch.int32, d, "perm"))
+    loss = ctypes.c_double(0.0)
+    info = ctypes.c_int32(0)
+    flags = GPTQ_QUANT_STATIC_GROUPS if static_groups else 0
+    st = lib().gptq_quantize_layer_host(px, _dtype_code(X), X.shape[0], int(chunk_tokens), pw,
+                                        _dtype_code(W), m, d, float(damp), int(bool(actorder)),
+                                        bits, group, int(bool(sym)), blocksize, flags, *outs,
+                                        ctypes.byref(loss), ctypes.byref(info), _ptr(dev),
+                                        dev.numel(), _stream(stream))
+    if st != GPTQ_OK:
+        err = GptqError(st, gptq_last_error())
+        err.info = int(info.value)
+        raise err
+    return float(loss.value), int(info.value)
 
 
 def _checkpoint_ptrs(qweight, scales, qzeros, g_idx, bits: int, m: int, d: int):

@@ -22,16 +22,13 @@ def _accumulate(lib, chunks, d, dev):
     return to_np(H), n
 
 
-@pytest.mark.parametrize("impl", ["tc", "simt"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("d,ntok", [(256, 128), (296, 1000), (1024, 4160)])
-def test_hessian_bf16_small(lib, cuda_device, impl, d, ntok, monkeypatch):
-    """Ragged column tiles (296) and token tails (1000, 4160) against the f64 oracle."""
-    if impl == "simt":
-        monkeypatch.setenv("GPTQ_SYRK", "simt")
-    else:
-        monkeypatch.delenv("GPTQ_SYRK", raising=False)
+def test_hessian_small(lib, cuda_device, dtype, d, ntok):
+    """Ragged column tiles (296) and token tails (1000, 4160) against the f64 oracle: bf16
+    tokens on the tensor-core SYRK, float32 tokens on the float32 FMA kernel."""
     g = torch.Generator().manual_seed(d + ntok)
-    X = (torch.randn(ntok, d, generator=g) * torch.exp(torch.randn(d, generator=g))).bfloat16()
+    X = (torch.randn(ntok, d, generator=g) * torch.exp(torch.randn(d, generator=g))).to(dtype)
     H, n = _accumulate(lib, [X], d, cuda_device)
     ref = O.hessian(X.float().numpy())
     mask = upper_tile_mask(d)

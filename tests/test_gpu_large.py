@@ -123,6 +123,9 @@ def test_prepare_down_proj_14336(lib, cuda_device):
     ("down_proj_8192x28672", 32, False),
     ("q_proj_4096x4096", 64, True),          # static groups
     ("down_proj_4096x14336", 32, True),
+    ("block_qkv_w4", 48, False),             # the Llama-3-8B block's stacked q/k/v, 6144 rows
+    ("block_o_w3", 48, False),               # 3-bit o_proj
+    ("block_down_w3", 32, False),            # 3-bit down_proj, d_in = 14336
 ])
 def test_quantize_large(lib, cuda_device, name, rows, static):
     """The column loop and packing at full size with a drawn inverse Cholesky factor and

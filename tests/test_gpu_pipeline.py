@@ -41,18 +41,40 @@ def test_layer_end_to_end(lib, cuda_device, name, override):
 
 
 def test_layer_from_host_matches_device_path(lib, cuda_device):
-    """The host-buffer path (pinned chunks, overlapped copies) gives the device path's
-    outputs bit for bit."""
+    """The host-buffer call (gptq_quantize_layer_host: chunked copies overlapped with the
+    Hessian kernels) gives the device path's outputs bit for bit with the same chunking."""
     cfg = CONFIGS["layer_256x256"].replace(chunk=512)
-    chunks = [c.pin_memory() for c in token_chunks(cfg)]
+    chunks = list(token_chunks(cfg))
+    X = torch.cat(chunks).pin_memory()
     W = make_weight(cfg).pin_memory()
     eng = LayerEngine(cfg.d_out, cfg.d_in, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
                       max_chunk_tokens=cfg.chunk, device=cuda_device)
-    host = quantize_layer_from_host(eng, W, chunks)
+    host = quantize_layer_from_host(eng, W, X, chunk_tokens=cfg.chunk)
     eng2 = LayerEngine(cfg.d_out, cfg.d_in, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
                        max_chunk_tokens=cfg.chunk, device=cuda_device)
     for c in chunks:
         eng2.add_batch(c.to(cuda_device))
     dev = eng2.quantize(W.to(cuda_device)).to("cpu")
-    for f in ("qweight", "scales", "qzeros", "g_idx", "loss"):
+    for f in ("qweight", "scales", "qzeros", "g_idx", "perm", "loss"):
         assert torch.equal(getattr(host, f), getattr(dev, f)), f
+    # a second call on the same buffers gives the same outputs; a ragged last chunk (300
+    # tokens per chunk) matches the device path fed the same chunks
+    again = quantize_layer_from_host(eng, W, X, chunk_tokens=cfg.chunk)
+    for f in ("qweight", "scales", "qzeros", "g_idx", "perm", "loss"):
+        assert torch.equal(getattr(again, f), getattr(dev, f)), f
+    ragged = quantize_layer_from_host(eng, W, X, chunk_tokens=300)
+    eng3 = LayerEngine(cfg.d_out, cfg.d_in, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
+                       max_chunk_tokens=300, device=cuda_device)
+    for t0 in range(0, X.shape[0], 300):
+        eng3.add_batch(X[t0:t0 + 300].to(cuda_device))
+    dev3 = eng3.quantize(W.to(cuda_device)).to("cpu")
+    for f in ("qweight", "scales", "qzeros", "g_idx", "perm", "loss"):
+        assert torch.equal(getattr(ragged, f), getattr(dev3, f)), f
+
+
+def test_layer_from_host_rejects_empty_tokens(lib, cuda_device):
+    cfg = CONFIGS["layer_256x256"]
+    eng = LayerEngine(cfg.d_out, cfg.d_in, cfg.bits, cfg.group, cfg.sym, cfg.actorder, cfg.damp,
+                      device=cuda_device)
+    with pytest.raises(lib.GptqError, match="no calibration tokens"):
+        quantize_layer_from_host(eng, make_weight(cfg), torch.empty(0, cfg.d_in))

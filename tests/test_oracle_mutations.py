@@ -72,6 +72,10 @@ MUTATIONS = {
     "hint_neighbour_widened_zeros": (
         "take = near & (hint != r) & ((hint == fl) | (hint == fl + 1))",
         "take = near & (hint != r) & (np.abs(hint - r) <= 2)"),
+    "rows_unreversed": ("    return np.ascontiguousarray(Y.T[:, ::-1])",
+                        "    return np.ascontiguousarray(Y.T)"),
+    "rows_wrong_index": ("E[d - 1 - rows, np.arange(rows.size)] = 1.0",
+                         "E[rows, np.arange(rows.size)] = 1.0"),
     "dequant_zero_dropped": ("return s * (codes.astype(F64) - z)", "return s * codes.astype(F64)"),
     "dequant_scale_of_position": ("s = np.asarray(scales, dtype=F64)[g].T",
                                   "s = np.asarray(scales, dtype=F64)[np.arange(g.size) * len(scales) // g.size].T"),

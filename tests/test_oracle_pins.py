@@ -155,6 +155,10 @@ def pin_cholesky_general(O):
     J = np.eye(d)[::-1]
     Lr = np.linalg.cholesky(J @ Hd @ J)
     assert np.allclose(J @ np.linalg.inv(Lr) @ J, U, rtol=1e-9, atol=1e-12)
+    # selected rows through the reversed factor and one triangular solve: the same rows
+    for rows in ([0], [d - 1], [0, 5, 11, d - 1], list(range(d))):
+        assert np.allclose(O.inverse_cholesky_upper_rows(Hd, rows), U[rows], rtol=1e-9,
+                           atol=1e-12), rows
 
 
 def _small_layer(rng, m, d, n=None):

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import gptq_oracle as O
 from tests.parity import H_REL_FRO, rel_fro, to_np, upper_tile_mask
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +24,8 @@ def _noalloc(lib, H, n, X):
     return int(c.value)
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 1024), (torch.float32, 256)])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 1024), (torch.float32, 256),
+                                     (torch.bfloat16, 2048)])    # 2048: one split fills the array
 def test_noalloc_matches_workspace_entry_point(lib, cuda_device, dtype, d):
     g = torch.Generator().manual_seed(d)
     X = (torch.randn(3000, d, generator=g) * torch.exp(torch.randn(d, generator=g))).to(dtype)
@@ -41,6 +43,9 @@ def test_noalloc_matches_workspace_entry_point(lib, cuda_device, dtype, d):
         a, b = to_np(H_new), to_np(H_ref)
         assert np.all(np.isfinite(a[mask]))
         assert rel_fro(a[mask], b[mask]) <= H_REL_FRO
+    # and directly against the float64 oracle's Hessian of every token so far
+    ref = O.hessian(X.float().cpu().numpy().astype(np.float64))
+    assert rel_fro(to_np(H_new)[mask], ref[mask]) <= H_REL_FRO
 
 
 def test_noalloc_rejects_large_d(lib, cuda_device):
