@@ -366,6 +366,24 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
                             int32_t G, void* W, int wdtype, void* ws, size_t ws_bytes,
                             void* stream);
 
+/*
+ * gptq_check_wait_timeout -- self-check of the library's failure path for device waits.
+ *
+ * Every wait of the tensor-core kernels on an mbarrier (a copy or a matrix operation that
+ * has not landed yet) is bounded: after a time limit it gives up, the kernel records
+ * GPTQ_ERR_TIMEOUT in the call's status word and returns, and the call reports it, so a
+ * wait that can never end does not hang the device.  This call runs that same bounded
+ * wait, for limit_ns nanoseconds, on an mbarrier nothing ever arrives on, in a kernel with
+ * nothing else in flight.  Not part of the method (the pages have no counterpart).
+ *
+ * limit_ns  1 .. 1e9 (at most one second).
+ * ws        device workspace of at least 256 bytes (the status word), 256-byte aligned.
+ * Returns GPTQ_ERR_TIMEOUT when the wait gave up as designed (gptq_last_error() says how
+ * many waits ran out); GPTQ_OK would mean the wait ended by itself, which it cannot.
+ * Errors: INVALID_ARG, CUDA.
+ */
+gptq_status gptq_check_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* gptq_last_error(void);
 
@@ -393,7 +411,7 @@ typedef enum {
   GPTQ_K_TRTRI_DIAG, GPTQ_K_TRTRI_UPDATE, GPTQ_K_PREP_REVERSE,
   GPTQ_K_QUANT_GATHER, GPTQ_K_QUANT_FIT, GPTQ_K_QUANT_LOOP, GPTQ_K_QUANT_LAZY,
   GPTQ_K_QUANT_PACK, GPTQ_K_QUANT_LOSS, GPTQ_K_QUANT_SPLIT, GPTQ_K_DEQUANT_MATMUL,
-  GPTQ_K_DEQUANTIZE, GPTQ_K_HESSIAN_RESCALE,
+  GPTQ_K_DEQUANTIZE, GPTQ_K_HESSIAN_RESCALE, GPTQ_K_SELFCHECK,
   GPTQ_K_COUNT
 } gptq_kernel_kind;
 

@@ -647,6 +647,21 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
   });
 }
 
+gptq_status gptq_check_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  return guarded([&] {
+    require(limit_ns >= 1 && limit_ns <= 1000000000ull, GPTQ_ERR_INVALID_ARG,
+            "gptq_check_wait_timeout: limit_ns must be in 1 .. 1e9");
+    require(ws != nullptr && aligned(ws, 256) && ws_bytes >= sizeof(DevStatus),
+            GPTQ_ERR_INVALID_ARG, "gptq_check_wait_timeout: null, unaligned or too small ws");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsCarver wc(ws, ws_bytes);
+    DevStatus* st = wc.take<DevStatus>(1);
+    begin_call(st, s);
+    launch_wait_timeout(st, limit_ns, s);
+    raise_device_status(finish_call(st, s), "gptq_check_wait_timeout");
+  });
+}
+
 const char* gptq_last_error(void) { return last_error().c_str(); }
 
 const char* gptq_status_string(int status) {
@@ -677,7 +692,8 @@ const char* gptq_kernel_name(int kind) {
       "syrk_tc", "syrk_simt", "syrk_reduce", "prep_diag", "prep_rank", "prep_mirror",
       "prep_gather", "potrf_panel", "potrf_trsm", "potrf_update", "trtri_diag", "trtri_update",
       "prep_reverse", "quant_gather", "quant_fit", "quant_loop", "quant_lazy", "quant_pack",
-      "quant_loss", "quant_split", "dequant_matmul", "dequantize", "hessian_rescale"};
+      "quant_loss", "quant_split", "dequant_matmul", "dequantize", "hessian_rescale",
+      "selfcheck"};
   if (kind < 0 || kind >= GPTQ_K_COUNT) return "";
   return names[kind];
 }

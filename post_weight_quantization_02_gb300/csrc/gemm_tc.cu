@@ -1,5 +1,5 @@
 // Float32-accurate tensor-core GEMM for the factorisation updates:
-//   C[i][j] = beta C[i][j] + alpha sum_{k<128} A[i][k] B[j][k],   beta in {0, 1},
+//   C[i][j] = beta C[i][j] + alpha sum_{k<K} A[i][k] B[j][k],   beta in {0, 1},
 // with both operands K-major (rows of 128 consecutive k), read through tensor maps that
 // cover whole matrices: the launch passes each operand's row and column offset.
 //
@@ -18,6 +18,12 @@
 // `lower` mode the entries of a diagonal tile above its diagonal are sent as zeros (C
 // unchanged).
 //
+// K is a multiple of 32 (128 for the panel steps, a superpanel's 1024 for the aggregated
+// trailing updates); the K-quarters stream through the same two buffers, and every four
+// quarters the TMEM sums are added into registers with round-to-nearest float32 adds.  In `lower` mode
+// only the tiles on or below the diagonal of C (tile column <= tile row) are computed:
+// with M > N that is a trapezoid, a triangle of N / 128 tile rows and whole rows below it.
+//
 // One CTA of 256 threads per 128 x 128 output tile, 96 KB of shared memory, two CTAs
 // per SM.
 #include <cuda.h>
@@ -30,7 +36,7 @@ namespace gptq {
 
 namespace {
 
-constexpr int TM = 128, TN = 128, TK = 128, KQ = 32;  // K-quarter per phase
+constexpr int TM = 128, TN = 128, KQ = 32;  // K-quarter per phase
 constexpr int THREADS = 256;
 constexpr int A_BYTES = TM * KQ * 4;                   // 16 KB
 constexpr int B_BYTES = TN * KQ * 4;                   // 16 KB
@@ -38,6 +44,10 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 // hi: two stages of (A, B) quarters; lo: one (A, B) quarter
 constexpr int SMEM_BYTES = 3 * STAGE_BYTES + 1024 + 128;
 constexpr int BOXB = 32 * 32 * 4;                      // one epilogue box: 32 x 32 float32
+// K-quarters per TMEM accumulation chain.  The tensor core's float32 accumulation does not
+// round to nearest, so its error grows with the chain; each chain covers K = 128 (as one
+// panel step) and is then added into registers with round-to-nearest float32 adds.
+constexpr int CHAIN_Q = 4;
 
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((b_mn ? 1u : 0u) << 16) |
@@ -51,7 +61,8 @@ struct TcGemmArgs {
   float alpha;
   int accumulate;  // beta = 1: reduce-add into C; beta = 0: store
   int lower;       // only tiles with row tile >= column tile; only entries j <= i change
-  int n_tiles;     // column tiles (non-lower enumeration)
+  int n_tiles;     // column tiles
+  int nq;          // K / 32
   DevStatus* st;
 };
 
@@ -92,10 +103,18 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
 
   int bi, bj;
   if (g.lower) {
-    int rem = blockIdx.x;
-    bi = 0;
-    while (rem > bi) { rem -= bi + 1; ++bi; }
-    bj = rem;
+    // the triangle of the first n_tiles tile rows, then whole tile rows
+    const int tri = g.n_tiles * (g.n_tiles + 1) / 2;
+    int rem = static_cast<int>(blockIdx.x);
+    if (rem < tri) {
+      bi = 0;
+      while (rem > bi) { rem -= bi + 1; ++bi; }
+      bj = rem;
+    } else {
+      rem -= tri;
+      bi = g.n_tiles + rem / g.n_tiles;
+      bj = rem % g.n_tiles;
+    }
   } else {
     bi = blockIdx.x / g.n_tiles;
     bj = blockIdx.x % g.n_tiles;
@@ -113,7 +132,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     tc::fence_mbar_init();
     griddep_wait();
     load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 0);
-    load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
+    if (g.nq > 1) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, 1);
   }
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, 128);
@@ -127,8 +146,14 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
   constexpr uint32_t IDESC = idesc_tf32(TM, TN, false);
   bool ok = true;
+  // warp w owns TMEM lanes (tile rows) 32 (w % 4) .. and columns 64 (w / 4) .. + 64
+  const int rq = warp % 4, ch = warp / 4;
+  const uint32_t tmem_w = tmem + (static_cast<uint32_t>(32 * rq) << 16) + 64 * ch;
+  float accr[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) accr[i] = 0.0f;
 
-  for (int ph = 0; ph < TK / KQ && ok; ++ph) {
+  for (int ph = 0; ph < g.nq && ok; ++ph) {
     uint8_t* a_hi = smem + (ph & 1) * STAGE_BYTES;
     uint8_t* b_hi = a_hi + A_BYTES;
     if (!tc::mbar_wait(bar_load + (ph & 1), (ph >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -168,7 +193,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
         const uint64_t dal = tc::smem_desc(al + 32 * kk, 16, 1024, tc::kSwizzle128B);
         const uint64_t dbh = tc::smem_desc(bh + 32 * kk, 16, 1024, tc::kSwizzle128B);
         const uint64_t dbl = tc::smem_desc(bl + 32 * kk, 16, 1024, tc::kSwizzle128B);
-        const uint32_t acc0 = (ph | kk) != 0 ? 1u : 0u;
+        const uint32_t acc0 = ((ph % CHAIN_Q) | kk) != 0 ? 1u : 0u;
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
@@ -190,30 +215,41 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     if (!tc::mbar_wait(bar_mma, ph & 1, abort_flag)) { ok = false; break; }
     tc::fence_after();
     // both buffers of this stage are free again: fetch the quarter after next into it
-    if (tid == 32 && ph + 2 < TK / KQ) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
+    if (tid == 32 && ph + 2 < g.nq) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
+    if (ph % CHAIN_Q == CHAIN_Q - 1 || ph == g.nq - 1) {
+      // end of a chain: its sums join the registers (the next chain's first MMAs
+      // overwrite TMEM only after the next quarter's CTA-wide barrier)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tmem_w + 32 * c, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          accr[32 * c + j] = __fadd_rn(accr[32 * c + j], __uint_as_float(r[j]));
+      }
+      tc::fence_before();
+    }
   }
 
   if (ok) {
-    // warp w: TMEM lanes (tile rows) 32 (w % 4) .., columns 64 (w / 4) .. + 64, as two
-    // 32 x 32 boxes, each staged in its own 4 KB buffer (the operand buffers are free)
-    const int rq = warp % 4, ch = warp / 4;
+    // warp w's rows and 64 columns as two 32 x 32 boxes, each staged in its own 4 KB
+    // buffer (the operand buffers are free)
     const int row = i0 + 32 * rq + lane;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int colt = 64 * ch + 32 * c;  // column inside the tile
       uint8_t* box = smem + (warp * 2 + c) * BOXB;
-      uint32_t r[32];
-      tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * rq) << 16) + colt, r);
-      tc::tmem_ld_wait();
+      const float* r = accr + 32 * c;
       uint8_t* srow = box + lane * 128;  // 128-byte swizzle: chunk j at (j ^ (lane % 8))
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int col = j0 + colt + 4 * j;
         float4 v;
-        v.x = (!g.lower || col <= row) ? g.alpha * __uint_as_float(r[4 * j]) : 0.0f;
-        v.y = (!g.lower || col + 1 <= row) ? g.alpha * __uint_as_float(r[4 * j + 1]) : 0.0f;
-        v.z = (!g.lower || col + 2 <= row) ? g.alpha * __uint_as_float(r[4 * j + 2]) : 0.0f;
-        v.w = (!g.lower || col + 3 <= row) ? g.alpha * __uint_as_float(r[4 * j + 3]) : 0.0f;
+        v.x = (!g.lower || col <= row) ? g.alpha * r[4 * j] : 0.0f;
+        v.y = (!g.lower || col + 1 <= row) ? g.alpha * r[4 * j + 1] : 0.0f;
+        v.z = (!g.lower || col + 2 <= row) ? g.alpha * r[4 * j + 2] : 0.0f;
+        v.w = (!g.lower || col + 3 <= row) ? g.alpha * r[4 * j + 3] : 0.0f;
         *reinterpret_cast<float4*>(srow + ((j ^ (lane & 7)) << 4)) = v;
       }
       tc::fence_proxy_async_shared();
@@ -255,12 +291,15 @@ void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int 
 }
 
 void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
-                        const CUtensorMap& mb, int b_row0, int b_k0, float* C, int ldc, int M,
-                        int N, float alpha, float beta, bool lower, DevStatus* st,
+                        const CUtensorMap& mb, int b_row0, int b_k0, int K, float* C, int ldc,
+                        int M, int N, float alpha, float beta, bool lower, DevStatus* st,
                         cudaStream_t s, bool pdl) {
   if (M <= 0 || N <= 0) return;
-  if ((beta != 0.0f && beta != 1.0f) || (lower && beta != 1.0f)) {
-    fail(GPTQ_ERR_INVALID_ARG, "launch_gemm_tf32x3: beta must be 0 or 1 (1 in lower mode)");
+  if ((beta != 0.0f && beta != 1.0f) || (lower && (beta != 1.0f || M < N)) || K <= 0 ||
+      K % KQ != 0) {
+    fail(GPTQ_ERR_INVALID_ARG,
+         "launch_gemm_tf32x3: beta must be 0 or 1 (1 and M >= N in lower mode), K a positive "
+         "multiple of 32");
   }
   ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
   // the M x N result, in boxes of 32 x 32 (128-byte rows, swizzled like the staging)
@@ -280,8 +319,9 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.lower = lower ? 1 : 0;
   const int tm = static_cast<int>(ceil_div(M, TM)), tn = static_cast<int>(ceil_div(N, TN));
   g.n_tiles = tn;
+  g.nq = K / KQ;
   g.st = st;
-  const unsigned grid = lower ? static_cast<unsigned>(tm * (tm + 1) / 2)
+  const unsigned grid = lower ? static_cast<unsigned>(tn * (tn + 1) / 2 + (tm - tn) * tn)
                               : static_cast<unsigned>(tm * tn);
   if (pdl) {
     GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);

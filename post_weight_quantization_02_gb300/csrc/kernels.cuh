@@ -19,6 +19,9 @@ void launch_syrk_reduce(float* H, const float* P, int d, int splits, float alpha
 // H <- factor * H on the upper 128-tile triangle (d a multiple of 4)
 void launch_hessian_rescale(float* H, int d, float factor, cudaStream_t s);
 
+// selfcheck.cu: one bounded wait on an mbarrier nothing arrives on
+void launch_wait_timeout(DevStatus* st, uint64_t limit_ns, cudaStream_t s);
+
 // hessian_tc.cu
 int syrk_tc_tiles(int d);
 int syrk_tc_token_granule();
@@ -74,13 +77,15 @@ void launch_dequant_matmul(const void* x, bool x_bf16, int64_t n, int d, int m, 
                            const int32_t* qweight, const float* scales, const int32_t* qzeros,
                            const int32_t* g_idx, float* y, DevStatus* st, cudaStream_t s);
 
-// gemm_tc.cu: C[i][j] = beta C[i][j] + alpha sum_{k<128} A[a_row0+i][a_k0+k]
-// B[b_row0+j][b_k0+k], float32-accurate (tf32 x3); maps from make_gemm_map.  pdl: launched
-// as a programmatic dependent of the kernel before it in the stream.
+// gemm_tc.cu: C[i][j] = beta C[i][j] + alpha sum_{k<K} A[a_row0+i][a_k0+k]
+// B[b_row0+j][b_k0+k], float32-accurate (tf32 x3), K a multiple of 32; maps from
+// make_gemm_map.  lower: only tiles with tile column <= tile row (M >= N), entries above the
+// diagonal of C unchanged.  pdl: launched as a programmatic dependent of the kernel before
+// it in the stream.
 void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int ld);
 void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
-                        const CUtensorMap& mb, int b_row0, int b_k0, float* C, int ldc, int M,
-                        int N, float alpha, float beta, bool lower, DevStatus* st,
+                        const CUtensorMap& mb, int b_row0, int b_k0, int K, float* C, int ldc,
+                        int M, int N, float alpha, float beta, bool lower, DevStatus* st,
                         cudaStream_t s, bool pdl);
 
 // lazy_tc.cu

@@ -12,6 +12,7 @@
 // Hr = J H_damp J directly, so both factorisations run on Hr and the last kernel
 // reverses the inverse into U.
 #include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -20,7 +21,8 @@ namespace gptq {
 
 namespace {
 
-constexpr int NB = 128;  // panel width of the blocked factorisation and inverse
+constexpr int NB = 128;    // panel width of the blocked factorisation and inverse
+constexpr int NBS = 1024;  // superpanel: panels whose update of later columns is grouped
 
 // ---------------------------------------------------------------- diagonal statistics
 
@@ -545,11 +547,14 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   make_gemm_map(&mS, S, d, d, d);
   make_gemm_map(&mDI, DI, static_cast<int>(ceil_div(d, NB)) * NB, NB, NB);
   const int nblk = static_cast<int>(ceil_div(d, NB));
-  AuxStreams& aux = aux_streams(2 * nblk + 3);
+  const int nsp = static_cast<int>(ceil_div(d, NBS));
+  AuxStreams& aux = aux_streams(2 * nblk + nsp + 3);
   cudaStream_t sa = aux.a, sb = aux.b, sc = aux.c;
-  cudaEvent_t* ev_panel = aux.ev.data();         // [nblk] panel kb factored and solved
-  cudaEvent_t* ev_far = aux.ev.data() + nblk;    // [nblk] far update of panel kb applied
-  cudaEvent_t ev_fork = aux.ev[2 * nblk], ev_b = aux.ev[2 * nblk + 1], ev_c = aux.ev[2 * nblk + 2];
+  cudaEvent_t* ev_panel = aux.ev.data();             // [nblk] panel kb factored and solved
+  cudaEvent_t* ev_far = ev_panel + nblk;             // [nblk] panel kb's far update applied
+  cudaEvent_t* ev_spfar = ev_far + nblk;             // [nsp] superpanel's far update applied
+  cudaEvent_t ev_fork = ev_spfar[nsp], ev_b = ev_spfar[nsp + 1], ev_c = ev_spfar[nsp + 2];
+  std::vector<char> far_done(nblk, 0), spfar_done(nsp, 0);
   GPTQ_CUDA(cudaEventRecord(ev_fork, s));
   GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_fork, 0));
   GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_fork, 0));
@@ -562,51 +567,90 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   for (int kb = 0; kb < nblk; ++kb) {
     const int k = kb * NB;
     const int rest = d - k - NB;
-    // block column kb is complete once the near update of panel kb - 1 is: that update
-    // waited for the far update of panel kb - 2, the last one that touches block column kb
-    // the factor's critical chain (diagonal block, panel solve, near update) runs on
-    // stream A as programmatic dependents, each launched during the kernel before it
+    const int sp = k / NBS;
+    const int sp0 = sp * NBS;                              // this panel's superpanel
+    const int sp_end = (d - sp0 < NBS) ? d : sp0 + NBS;
+    const int in_sp = sp_end - (k + NB);                   // its columns after this panel
+    // Block column kb is complete once the near update of panel kb - 1 is (that update
+    // waited for the far update of panel kb - 2, the last panel-level update of block
+    // column kb), and, for the first panel of a superpanel, once the near update of the
+    // previous superpanel is (which waited for the far update of the one before it).
+    // The factor's critical chain (diagonal block, panel solve, near update) runs on
+    // stream A as programmatic dependents, each launched during the kernel before it.
     GPTQ_LAUNCH_PDL(GPTQ_K_POTRF_PANEL, sa, chol_inv_diag_kernel, 1, 512, diag_smem, Hr, d, k,
                     DI, st, d);
     if (rest > 0) {
       // the panel below, in place: L[r, k:k+NB] = A[r, k:k+NB] L_kk^-T (rows r >= k + NB;
       // each CTA owns whole rows, loaded before it writes them)
-      launch_gemm_tf32x3(GPTQ_K_POTRF_TRSM, mHr, k + NB, k, mDI, k, 0,
+      launch_gemm_tf32x3(GPTQ_K_POTRF_TRSM, mHr, k + NB, k, mDI, k, 0, NB,
                          Hr + static_cast<size_t>(k + NB) * d + k, d, rest, NB, 1.0f, 0.0f,
                          false, st, sa, true);
     }
-    if (rest > 0) {
-      // near update, block column kb + 1: Hr[r][k+NB+j] -= L[r, panel] . L[k+NB+j, panel]
-      // (whole tiles; the entries it changes above the diagonal are never read).  It adds
-      // into block column kb + 1 after the far update of panel kb - 1 has, so that every
-      // entry receives its updates in panel order.
-      if (kb >= 1) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 1], 0));
-      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k,
+    if (in_sp > 0) {
+      // near update, block column kb + 1 (inside the superpanel), every row below it:
+      // Hr[r][k+NB+j] -= L[r, panel] . L[k+NB+j, panel] (whole tiles; the entries it
+      // changes above the diagonal are never read).  It adds into block column kb + 1
+      // after the far update of panel kb - 1 has, so that every entry receives its
+      // updates in panel order.
+      if (kb >= 1 && far_done[kb - 1]) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_far[kb - 1], 0));
+      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + NB, k, mHr, k + NB, k, NB,
                          Hr + static_cast<size_t>(k + NB) * d + k + NB, d, rest,
-                         rest < NB ? rest : NB, -1.0f, 1.0f, false, st, sa, true);
+                         in_sp < NB ? in_sp : NB, -1.0f, 1.0f, false, st, sa, true);
     }
     // panel kb is final (recorded after the near update, which keeps this stream's
     // kernel-to-kernel steps free of other stream operations where it can)
     GPTQ_CUDA(cudaEventRecord(ev_panel[kb], sa));
-    if (rest > NB) {
-      // far update, lower tiles of block columns >= kb + 2, on stream C
-      const int far = rest - NB;
+    if (in_sp > NB) {
+      // far update inside the superpanel, on stream C: block columns kb + 2 .. its end,
+      // every row below them (the triangle of those columns and whole rows beneath)
       GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_panel[kb], 0));
-      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + 2 * NB, k, mHr, k + 2 * NB, k,
-                         Hr + static_cast<size_t>(k + 2 * NB) * d + k + 2 * NB, d, far, far,
-                         -1.0f, 1.0f, true, st, sc, false);
+      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, k + 2 * NB, k, mHr, k + 2 * NB, k, NB,
+                         Hr + static_cast<size_t>(k + 2 * NB) * d + k + 2 * NB, d, rest - NB,
+                         in_sp - NB, -1.0f, 1.0f, true, st, sc, false);
       GPTQ_CUDA(cudaEventRecord(ev_far[kb], sc));
+      far_done[kb] = 1;
+    }
+    const bool sp_last = (k + NB >= sp_end);
+    if (sp_last && sp_end < d) {
+      // The superpanel's panels are factored and solved: every later column receives the
+      // superpanel's update at once, A[r][c] -= L[r, sp] . L[c, sp] with K = its width (the
+      // same sum as one update per panel, grouped).  The next superpanel's columns (every
+      // row below them) on stream A, which that superpanel's panels need next; the columns
+      // past it on stream C.  Each adds into columns that the previous superpanel's far
+      // update also wrote, after it.
+      const int spw = sp_end - sp0;
+      const int nxt = (d - sp_end < NBS) ? d - sp_end : NBS;
+      if (sp >= 1 && spfar_done[sp - 1]) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_spfar[sp - 1], 0));
+      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, sp_end, sp0, mHr, sp_end, sp0, spw,
+                         Hr + static_cast<size_t>(sp_end) * d + sp_end, d, d - sp_end, nxt,
+                         -1.0f, 1.0f, true, st, sa, true);
+      const int far = d - sp_end - nxt;
+      if (far > 0) {
+        // its operands, the superpanel's columns of L, are final since the last panel solve
+        GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_panel[kb], 0));
+        launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, sp_end + nxt, sp0, mHr, sp_end + nxt, sp0,
+                           spw, Hr + static_cast<size_t>(sp_end + nxt) * d + sp_end + nxt, d,
+                           far, far, -1.0f, 1.0f, true, st, sc, false);
+        GPTQ_CUDA(cudaEventRecord(ev_spfar[sp], sc));
+        spfar_done[sp] = 1;
+      }
     }
     // inverse, block column kb, on stream B once panel kb is final
     GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_panel[kb], 0));
     const int nbi = (d - k < NB) ? d - k : NB;
     // Y[c][k+t] = sum_j Y[c][k+j] DI[kb][t][j], rows c < k + nbi
-    launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, k, mDI, k, 0, S + k, d, k + nbi, nbi, 1.0f, 0.0f,
-                       false, st, sb, false);
-    if (rest > 0) {
-      // Y[c][r] -= sum_j Y[c][k+j] L[r][k+j], c < k + NB <= r
-      launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, k, mHr, k + NB, k, S + k + NB, d, k + NB,
-                         rest, -1.0f, 1.0f, false, st, sb, false);
+    launch_gemm_tf32x3(GPTQ_K_TRTRI_DIAG, mS, 0, k, mDI, k, 0, NB, S + k, d, k + nbi, nbi, 1.0f,
+                       0.0f, false, st, sb, false);
+    if (in_sp > 0) {
+      // Y[c][r] -= sum_j Y[c][k+j] L[r][k+j], c < k + NB <= r < the superpanel's end
+      launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, k, mHr, k + NB, k, NB, S + k + NB, d,
+                         k + NB, in_sp, -1.0f, 1.0f, false, st, sb, false);
+    }
+    if (sp_last && sp_end < d) {
+      // the superpanel's share at once: Y[c][r] -= sum_{j in sp} Y[c][j] L[r][j],
+      // c < sp_end <= r (rows c past a block column's end hold exact zeros there)
+      launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, sp0, mHr, sp_end, sp0, sp_end - sp0,
+                         S + sp_end, d, sp_end, d - sp_end, -1.0f, 1.0f, false, st, sb, false);
     }
   }
   GPTQ_CUDA(cudaEventRecord(ev_b, sb));

@@ -38,8 +38,35 @@ __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __bfloat162float(*p);
 }
 
-// Wp[r][k] = dead[perm[k]] ? 0 : W[r][perm[k]]; loss_rows[r] = 0.  One CTA per row,
-// the source row staged in shared memory.
+// 16 bytes of a row of W as float32 values (8 bf16 or 4 float32 elements).
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const float* p, float* v) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* v) {
+    const uint4 x = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);             // bf16 -> float32 is exact
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+
+// Wp[r][k] = dead[perm[k]] ? 0 : W[r][perm[k]]; loss_rows[r] = 0.  One CTA per row: the
+// source row is read with 16-byte loads into shared memory (dead columns zeroed there),
+// then written in processing order with 16-byte stores (d is a multiple of 32; W and Wp
+// are 16-byte aligned).
 template <typename T>
 __global__ void __launch_bounds__(256) gather_w_kernel(const T* __restrict__ W, int d,
                                                        const int32_t* __restrict__ perm,
@@ -48,19 +75,31 @@ __global__ void __launch_bounds__(256) gather_w_kernel(const T* __restrict__ W, 
                                                        double* __restrict__ loss_rows,
                                                        DevStatus* st) {
   extern __shared__ float srow[];
+  constexpr int VN = Vec16<T>::N;
   const int r = blockIdx.x;
   const T* src = W + static_cast<size_t>(r) * d;
   bool bad = false;
-  for (int j = threadIdx.x; j < d; j += 256) {
-    float v = ldf(src + j);
-    bad |= !isfinite(v);
-    if (dead != nullptr && dead[j]) v = 0.0f;
-    srow[j] = v;
+  for (int j = threadIdx.x * VN; j < d; j += 256 * VN) {
+    float v[VN];
+    Vec16<T>::load(src + j, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) {
+      bad |= !isfinite(v[i]);
+      if (dead != nullptr && dead[j + i]) v[i] = 0.0f;
+      srow[j + i] = v[i];
+    }
   }
   if (bad) dev_fail(st, GPTQ_ERR_NONFINITE, r + 1);
   __syncthreads();
-  float* dst = Wp + static_cast<size_t>(r) * d;
-  for (int k = threadIdx.x; k < d; k += 256) dst[k] = srow[perm ? perm[k] : k];
+  float4* dst = reinterpret_cast<float4*>(Wp + static_cast<size_t>(r) * d);
+  for (int k4 = threadIdx.x; k4 < d / 4; k4 += 256) {
+    int4 p = make_int4(4 * k4, 4 * k4 + 1, 4 * k4 + 2, 4 * k4 + 3);
+    if (perm != nullptr) {  // the caller's perm need not be 16-byte aligned
+      const int32_t* pp = perm + 4 * k4;
+      p = make_int4(pp[0], pp[1], pp[2], pp[3]);
+    }
+    dst[k4] = make_float4(srow[p.x], srow[p.y], srow[p.z], srow[p.w]);
+  }
   if (threadIdx.x == 0) loss_rows[r] = 0.0;
 }
 
@@ -506,10 +545,41 @@ __device__ __forceinline__ uint32_t stream_word(int wi, int bits, Get get) {
   return word;
 }
 
-// qweight[wi][r]: codes of row r in original column order, packed along d.
+// qweight[wi][r]: codes of row r in original column order, packed along d.  A thread
+// packs word wi of 16 consecutive rows: it reads each code row it needs (codesT[pos[k]]
+// at those 16 rows) with one 16-byte load and writes the 16 words with four 16-byte
+// stores (m is a multiple of 32; qweight is 16-byte aligned).
 __global__ void pack_qweight_kernel(const uint8_t* __restrict__ codesT,
                                     const int32_t* __restrict__ pos, int m, int d, int bits,
                                     int32_t* __restrict__ qweight) {
+  const int r0 = 16 * (blockIdx.x * blockDim.x + threadIdx.x);
+  const int wi = blockIdx.y;
+  if (r0 >= m) return;
+  uint32_t word[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) word[j] = 0;
+  const int b0 = wi * 32;
+  const int k_first = b0 / bits, k_last = (b0 + 31) / bits;
+  for (int k = k_first; k <= k_last && k < d; ++k) {
+    const uint4 c = *reinterpret_cast<const uint4*>(codesT + static_cast<size_t>(pos[k]) * m + r0);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    const int shift = k * bits - b0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t v = (cw[j / 4] >> (8 * (j % 4))) & 0xFFu;
+      word[j] |= (shift >= 0) ? (v << shift) : (v >> (-shift));
+    }
+  }
+  uint4* out = reinterpret_cast<uint4*>(qweight + static_cast<size_t>(wi) * m + r0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    out[q] = make_uint4(word[4 * q], word[4 * q + 1], word[4 * q + 2], word[4 * q + 3]);
+}
+
+// The same with 4-byte stores, for a qweight that is not 16-byte aligned.
+__global__ void pack_qweight_unaligned_kernel(const uint8_t* __restrict__ codesT,
+                                              const int32_t* __restrict__ pos, int m, int d,
+                                              int bits, int32_t* __restrict__ qweight) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   const int wi = blockIdx.y;
   if (r >= m) return;
@@ -651,9 +721,15 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
       // far: every later column, W[:, s1:] -= Err_superblock U[s0:s1, s1:]
       launch_lazy_tc(maps, 0, s0, s1 - s0, s1, d, q.st, s, 0);
     }
-    dim3 gq((unsigned)ceil_div(m, 128), static_cast<unsigned>(q.bits * d / 32));
-    GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_kernel, gq, 128, 0, q.codesT, q.pos, m, d,
-                q.bits, q.qweight);
+    if (reinterpret_cast<uintptr_t>(q.qweight) % 16 == 0) {
+      dim3 gq((unsigned)ceil_div(m, 16 * 64), static_cast<unsigned>(q.bits * d / 32));
+      GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_kernel, gq, 64, 0, q.codesT, q.pos, m, d,
+                  q.bits, q.qweight);
+    } else {
+      dim3 gq((unsigned)ceil_div(m, 128), static_cast<unsigned>(q.bits * d / 32));
+      GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qweight_unaligned_kernel, gq, 128, 0, q.codesT,
+                  q.pos, m, d, q.bits, q.qweight);
+    }
     const int nz = q.G * (m * q.bits / 32);
     GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, pack_qzeros_kernel, (unsigned)ceil_div(nz, 256), 256, 0,
                 q.zeros, m, q.G, q.bits, q.qzeros);

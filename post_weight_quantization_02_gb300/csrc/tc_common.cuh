@@ -61,9 +61,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete, polling with the non-blocking
 // test_wait (a suspended try_wait was observed to wake late).  Gives up (returns false)
-// when another role of the CTA raised *abort, or after kWaitLimitNs.
+// when another role of the CTA raised *abort, or after limit_ns (kWaitLimitNs unless a
+// caller says otherwise).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -71,7 +73,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_test_wait(a, parity)) return true;
     if ((it & 255) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -22,7 +22,7 @@ __all__ = [
     "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul", "gptq_dequantize",
     "GptqError", "GptqLibraryError", "lib", "library_path",
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
-    "gptq_hessian_status", "gptq_hessian_rescale", "gptq_prepare", "gptq_quantize_layer",
+    "gptq_hessian_status", "gptq_hessian_rescale", "gptq_check_wait_timeout", "gptq_prepare", "gptq_quantize_layer",
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
     "gptq_kernel_name",
@@ -35,7 +35,7 @@ GPTQ_OK, GPTQ_ERR_INVALID_ARG, GPTQ_ERR_UNSUPPORTED, GPTQ_ERR_NOT_PD = 0, 1, 2, 
 GPTQ_ERR_NONFINITE, GPTQ_ERR_CUDA, GPTQ_ERR_TIMEOUT, GPTQ_ERR_WORKSPACE = 4, 5, 6, 7
 GPTQ_F32, GPTQ_BF16 = 0, 1
 GPTQ_OP_HESSIAN, GPTQ_OP_PREPARE, GPTQ_OP_QUANTIZE, GPTQ_OP_DEQUANT_MATMUL = 0, 1, 2, 3
-KERNEL_KINDS = 23
+KERNEL_KINDS = 24
 GPTQ_K_SYRK_TC = 0  # the gptq_kernel_kind of the tensor-core SYRK
 GPTQ_K_DEQUANT_MATMUL = 20
 GPTQ_QUANT_STATIC_GROUPS = 1
@@ -65,6 +65,7 @@ _SIGS = {
                                                  _i32, _vp, _sz, _vp]),
     "gptq_hessian_status": (_c.c_int, [_vp, _sz, _vp]),
     "gptq_hessian_rescale": (_c.c_int, [_vp, _i32, _i64, _i64, _vp]),
+    "gptq_check_wait_timeout": (_c.c_int, [_c.c_uint64, _vp, _sz, _vp]),
     "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
                                 _vp, _sz, _vp]),
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
@@ -234,6 +235,12 @@ def gptq_hessian_rescale(H: torch.Tensor, n_from: int, n_to: int, stream=None) -
     d = H.shape[0]
     _check(lib().gptq_hessian_rescale(_buf(H, torch.float32, d * d, "H"), d, int(n_from),
                                       int(n_to), _stream(stream)))
+
+
+def gptq_check_wait_timeout(limit_ns: int, ws: torch.Tensor, stream=None) -> None:
+    """Run the library's bounded device wait on an mbarrier nothing arrives on; raises
+    GptqError with GPTQ_ERR_TIMEOUT when the wait gives up, as it must."""
+    _check(lib().gptq_check_wait_timeout(int(limit_ns), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tensor,

@@ -1,0 +1,46 @@
+"""Failure handling on the GPU without a fault: a bounded device wait that can never end
+gives up, the call reports GPTQ_ERR_TIMEOUT through the status word, and the context stays
+usable (the next calls succeed and match the oracle).  The failing pivot of a matrix that
+is not positive definite is covered in the prepare tests."""
+
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as O
+from tests.parity import H_REL_FRO, rel_fro, to_np, upper_tile_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("limit_ns", [1, 1_000_000, 50_000_000])
+def test_bounded_wait_times_out_and_context_survives(lib, cuda_device, limit_ns):
+    ws = lib.workspace(256, cuda_device)
+    t0 = time.perf_counter()
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_check_wait_timeout(limit_ns, ws)
+    elapsed = time.perf_counter() - t0
+    assert e.value.status == lib.GPTQ_ERR_TIMEOUT
+    assert "1 device-side wait(s) ran out" in str(e.value)
+    assert elapsed < 5.0
+    # the status word is per call: a normal call on the same workspace's device succeeds
+    d = 256
+    g = torch.Generator().manual_seed(limit_ns % 997)
+    X = (torch.randn(512, d, generator=g) * 2.0).bfloat16()
+    H = torch.empty(d, d, dtype=torch.float32, device=cuda_device)
+    assert lib.gptq_hessian_accumulate(H, 0, X.to(cuda_device)) == 512
+    torch.cuda.synchronize()
+    mask = upper_tile_mask(d)
+    assert rel_fro(to_np(H)[mask], O.hessian(X.float().numpy())[mask]) <= H_REL_FRO
+
+
+def test_wait_limit_is_checked(lib, cuda_device):
+    ws = lib.workspace(256, cuda_device)
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_check_wait_timeout(0, ws)
+    assert e.value.status == lib.GPTQ_ERR_INVALID_ARG
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_check_wait_timeout(2_000_000_000, ws)
+    assert e.value.status == lib.GPTQ_ERR_INVALID_ARG

