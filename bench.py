@@ -188,6 +188,16 @@ def ncu_traffic(kernel_file: str, workload: str):
 
 # ------------------------------------------------------------------------ our arm
 
+def workload(args):
+    """The configuration named by --config, with the --tokens / --shape overrides."""
+    from workloads import CONFIGS
+    cfg = CONFIGS[args.config]
+    if getattr(args, "tokens", 0):
+        cfg = cfg.replace(n_tokens=args.tokens)
+    if getattr(args, "shape", None):
+        cfg = cfg.replace(d_out=args.shape[0], d_in=args.shape[1])
+    return cfg
+
 BLOCK = 128  # the engine's column block
 
 
@@ -281,9 +291,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
-    cfg = CONFIGS[args.config]
-    if args.tokens:
-        cfg = cfg.replace(n_tokens=args.tokens)
+    cfg = workload(args)
     m, d, n = cfg.d_out, cfg.d_in, cfg.n_tokens
 
     # synthetic workload, resident in HBM (chunks written straight into one tensor)
@@ -377,7 +385,7 @@ def run_ours(args, world, rank, local):
                     "ms_per_launch": round(syrk_ms, 3),
                     "algorithmic_flops_per_launch": flops,
                     "traffic": ncu_traffic("post_weight_quantization_02_gb300/csrc/hessian_tc.cu",
-                                           cfg.name if not args.tokens else None)}
+                                           cfg.name if not (args.tokens or args.shape) else None)}
     figures = layer_figures(cfg, n, ms, phase_ms, kern, hbm, bf16, bf16_sus)
 
     # end to end through the C ABI's host-buffer call
@@ -443,9 +451,7 @@ def run_sharded(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
-    cfg = CONFIGS[args.config]
-    if args.tokens:
-        cfg = cfg.replace(n_tokens=args.tokens)
+    cfg = workload(args)
     m, d, n = cfg.d_out, cfg.d_in, cfg.n_tokens
     t0, t1 = shard.token_range(rank, world, n)
     r0, r1 = shard.row_range(rank, world, m)
@@ -585,9 +591,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from workloads import CONFIGS
-    cfg = CONFIGS[args.config]
-    if args.tokens:
-        cfg = cfg.replace(n_tokens=args.tokens)
+    cfg = workload(args)
     for _ in range(args.warmup):
         oracle_sample(cfg)
     fulls, walls = [], []
@@ -765,6 +769,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the calibration token count (small profiling cases)")
+    ap.add_argument("--shape", type=int, nargs=2, metavar=("D_OUT", "D_IN"), default=None,
+                    help="override the layer shape (small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--static-groups", action="store_true",
                     help="groups fixed in the original column order before the loop")

@@ -282,6 +282,255 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------------------------- long-K variant
+
+// For K >= 256 (a superpanel's aggregated updates, K = 1024) a warp-specialised kernel
+// keeps the tensor core fed: three ring stages of hi and lo parts, so that the copies and
+// the lo parts of the next quarters are formed while the MMAs of the current one run.
+//   warp 0       TMA producer: the A and B quarters into stage q % 3 (the hi halves)
+//   warp 1       TMEM owner (two 128-column accumulators) and MMA issuer
+//   warp 2       waits for a quarter's lo parts (and, at a chain start, for its accumulator
+//                to be drained) and releases warp 1 through a named barrier, so that the
+//                issuing warp never waits on an mbarrier
+//   warps 3..10  form the lo parts of every quarter; drain each finished chain from TMEM
+//                into registers one quarter later (round-to-nearest adds), while the next
+//                chain accumulates in the other TMEM half; then write the tile
+constexpr int WS_NS = 3;
+constexpr int WS_STAGE = 2 * A_BYTES + 2 * B_BYTES;   // A hi, B hi, A lo, B lo: 64 KB
+constexpr int WS_WORKERS = 8;
+constexpr int WS_THREADS = 32 * (3 + WS_WORKERS);
+constexpr int WS_SMEM = WS_NS * WS_STAGE + 1024 + 256;
+constexpr uint32_t kWsHandoff = 1;  // named barrier of warps 1 and 2
+static_assert(WS_SMEM <= 232448, "shared memory of one CTA");
+static_assert(2 * WS_WORKERS * BOXB <= WS_STAGE, "epilogue boxes fit in stage 0");
+
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tma,
+                          const __grid_constant__ CUtensorMap tmb,
+                          const __grid_constant__ CUtensorMap tmc, const TcGemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + WS_NS * WS_STAGE);  // [NS] copies
+  uint64_t* split = full + WS_NS;                                       // [NS] lo parts
+  uint64_t* empty = split + WS_NS;                                      // [NS] MMAs done
+  uint64_t* accfull = empty + WS_NS;                                    // [2]
+  uint64_t* accempty = accfull + 2;                                     // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  int bi, bj;
+  if (g.lower) {
+    const int tri = g.n_tiles * (g.n_tiles + 1) / 2;
+    int rem = static_cast<int>(blockIdx.x);
+    if (rem < tri) {
+      bi = 0;
+      while (rem > bi) { rem -= bi + 1; ++bi; }
+      bj = rem;
+    } else {
+      rem -= tri;
+      bi = g.n_tiles + rem / g.n_tiles;
+      bj = rem % g.n_tiles;
+    }
+  } else {
+    bi = blockIdx.x / g.n_tiles;
+    bj = blockIdx.x % g.n_tiles;
+  }
+  const int i0 = bi * TM, j0 = bj * TN;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WS_NS; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&split[s], WS_WORKERS);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accfull[b], 1);
+      tc::mbar_init(&accempty[b], WS_WORKERS);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_relinquish();
+  }
+  // no thread touches global memory before the previous kernel in the stream is done
+  griddep_wait();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr uint32_t IDESC = idesc_tf32(TM, TN, false);
+  const int nq = g.nq;
+  const int nchain = (nq + CHAIN_Q - 1) / CHAIN_Q;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int q = 0; q < nq; ++q) {
+        const int s = q % WS_NS;
+        const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* base = smem + s * WS_STAGE;
+        tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+        tc::tma_load_2d(base, &tma, &full[s], g.a_k0 + q * KQ, g.a_row0 + i0);
+        tc::tma_load_2d(base + A_BYTES, &tmb, &full[s], g.b_k0 + q * KQ, g.b_row0 + j0);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuer and waiter
+    const bool waiter = (warp == 2);
+    for (int q = 0; q < nq; ++q) {
+      const int s = q % WS_NS;
+      const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
+      const int chain = q / CHAIN_Q, acc = chain & 1;
+      bool bad = false;
+      if (waiter && lane == 0) {
+        if (q % CHAIN_Q == 0)
+          bad = !tc::mbar_wait(&accempty[acc], (static_cast<uint32_t>(chain >> 1) & 1u) ^ 1u,
+                               abort_flag);
+        if (!bad) bad = !tc::mbar_wait(&split[s], ph, abort_flag);
+      }
+      if (tc::handoff_or(kWsHandoff, 64, bad)) { ok = false; break; }
+      if (!waiter && lane == 0) {
+        tc::fence_after();
+        const uint32_t ah = tc::smem_u32(smem + s * WS_STAGE);
+        const uint32_t bh = ah + A_BYTES, al = ah + A_BYTES + B_BYTES, bl = al + A_BYTES;
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TN);
+#pragma unroll
+        for (int kk = 0; kk < KQ / 8; ++kk) {
+          const uint64_t dah = tc::smem_desc(ah + 32 * kk, 16, 1024, tc::kSwizzle128B);
+          const uint64_t dal = tc::smem_desc(al + 32 * kk, 16, 1024, tc::kSwizzle128B);
+          const uint64_t dbh = tc::smem_desc(bh + 32 * kk, 16, 1024, tc::kSwizzle128B);
+          const uint64_t dbl = tc::smem_desc(bl + 32 * kk, 16, 1024, tc::kSwizzle128B);
+          const uint32_t acc0 = ((q % CHAIN_Q) | kk) != 0 ? 1u : 0u;
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "l"(dah), "l"(dbh), "r"(IDESC), "r"(acc0)
+              : "memory");
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "l"(dah), "l"(dbl), "r"(IDESC), "r"(1u)
+              : "memory");
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "l"(dal), "l"(dbh), "r"(IDESC), "r"(1u)
+              : "memory");
+        }
+        tc::mma_commit(&empty[s]);
+        if (q % CHAIN_Q == CHAIN_Q - 1 || q == nq - 1) tc::mma_commit(&accfull[acc]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ workers
+    const int wk = warp - 3;                       // 0 .. WS_WORKERS - 1
+    const int wt = threadIdx.x - 96;               // 0 .. 32 * WS_WORKERS - 1
+    const int rq = warp % 4, half = wk / 4;        // TMEM lane quarter, column half
+    const uint32_t tmem_w = tmem_base + (static_cast<uint32_t>(32 * rq) << 16) + 64 * half;
+    float accr[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) accr[i] = 0.0f;
+    for (int q = 0; q <= nq && ok; ++q) {
+      if (q < nq) {
+        const int s = q % WS_NS;
+        const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
+        if (!tc::mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+        // lo = x - trunc_tf32(x), elementwise in the same swizzled layout
+        const float4* src = reinterpret_cast<const float4*>(smem + s * WS_STAGE);
+        float4* dst = reinterpret_cast<float4*>(smem + s * WS_STAGE + A_BYTES + B_BYTES);
+#pragma unroll
+        for (int e = wt; e < (A_BYTES + B_BYTES) / 16; e += 32 * WS_WORKERS) {
+          float4 x = src[e];
+          x.x -= __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+          x.y -= __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+          x.z -= __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+          x.w -= __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+          dst[e] = x;
+        }
+        tc::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&split[s]);
+      }
+      // a chain that ended with the previous quarter (or the last one): TMEM -> registers
+      if (q > 0 && (q % CHAIN_Q == 0 || q == nq)) {
+        const int chain = (q - 1) / CHAIN_Q, acc = chain & 1;
+        if (!tc::mbar_wait(&accfull[acc], static_cast<uint32_t>(chain >> 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tmem_w + static_cast<uint32_t>(acc * TN) + 32 * c, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            accr[32 * c + j] = __fadd_rn(accr[32 * c + j], __uint_as_float(r[j]));
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+      }
+    }
+    (void)nchain;
+    if (ok) {
+      // every MMA has completed (the last chain's commit) and every copy was consumed:
+      // stage 0 holds the epilogue's boxes, two 32 x 32 per worker warp
+      const int row = i0 + 32 * rq + lane;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int colt = 64 * half + 32 * c;
+        uint8_t* box = smem + (wk * 2 + c) * BOXB;
+        const float* r = accr + 32 * c;
+        uint8_t* srow = box + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int col = j0 + colt + 4 * j;
+          float4 v;
+          v.x = (!g.lower || col <= row) ? g.alpha * r[4 * j] : 0.0f;
+          v.y = (!g.lower || col + 1 <= row) ? g.alpha * r[4 * j + 1] : 0.0f;
+          v.z = (!g.lower || col + 2 <= row) ? g.alpha * r[4 * j + 2] : 0.0f;
+          v.w = (!g.lower || col + 3 <= row) ? g.alpha * r[4 * j + 3] : 0.0f;
+          *reinterpret_cast<float4*>(srow + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        tc::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && i0 + 32 * rq < g.M && j0 + colt < g.N) {
+          if (g.accumulate) tc::tma_reduce_add_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
+          else tma_store_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
+          tc::bulk_commit_group();
+        }
+      }
+      if (lane == 0) tc::bulk_wait_group_read0();
+    }
+  }
+
+  if (!ok) {
+    *abort_flag = 1;
+    if (lane == 0) {
+      dev_fail(g.st, GPTQ_ERR_TIMEOUT, 0);
+      atomicAdd(&g.st->timeouts, 1);
+    }
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 200000ull) {
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_base, 256);
+  }
+}
+
 }  // namespace
 
 void make_gemm_map(CUtensorMap* map, const float* base, int rows, int cols, int ld) {
@@ -301,7 +550,6 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
          "launch_gemm_tf32x3: beta must be 0 or 1 (1 and M >= N in lower mode), K a positive "
          "multiple of 32");
   }
-  ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
   // the M x N result, in boxes of 32 x 32 (128-byte rows, swizzled like the staging)
   CUtensorMap mc;
   make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
@@ -323,10 +571,21 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.st = st;
   const unsigned grid = lower ? static_cast<unsigned>(tn * (tn + 1) / 2 + (tm - tn) * tn)
                               : static_cast<unsigned>(tm * tn);
-  if (pdl) {
-    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+  if (g.nq >= 8) {
+    // long K: the warp-specialised kernel, one CTA per SM
+    ensure_dynamic_smem(gemm_tf32x3_ws_kernel, WS_SMEM);
+    if (pdl) {
+      GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_ws_kernel, grid, WS_THREADS, WS_SMEM, ma, mb, mc, g);
+    } else {
+      GPTQ_LAUNCH(kind, s, gemm_tf32x3_ws_kernel, grid, WS_THREADS, WS_SMEM, ma, mb, mc, g);
+    }
   } else {
-    GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+    ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
+    if (pdl) {
+      GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+    } else {
+      GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
+    }
   }
 }
 
