@@ -136,6 +136,7 @@ size_t prepare_ws_bytes(int d) {
   w.add<float>(d);                           // fixed diagonal
   w.add<float>(1);                           // lambda
   w.add<float>(static_cast<size_t>(ceil_div(d, 128)) * 128 * 128);  // diagonal-block inverses
+  w.add<float>(static_cast<size_t>(2) * d * kSuperpanel);  // lo parts of two superpanels
   return w.bytes;
 }
 
@@ -356,10 +357,11 @@ gptq_status gptq_prepare(const float* H, int32_t d_in, float damp, int actorder,
     float* diag = wc.take<float>(d_in);
     float* lam = wc.take<float>(1);
     float* DI = wc.take<float>(static_cast<size_t>(ceil_div(d_in, 128)) * 128 * 128);
+    float* Lo = wc.take<float>(static_cast<size_t>(2) * d_in * kSuperpanel);
     std::lock_guard<std::mutex> lk(aux_mutex());  // the internal streams are shared
     begin_call(st, s);
     launch_prepare(H, d_in, damp, actorder ? 1 : 0, perm, dead, Hinv_chol, S, Hr, diag, lam, DI,
-                   st, s);
+                   Lo, st, s);
     DevStatus h = finish_call(st, s);
     if (h.code == GPTQ_ERR_NOT_PD) pivot = h.info;
     raise_device_status(h, "gptq_prepare");

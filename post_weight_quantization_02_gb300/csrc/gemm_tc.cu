@@ -28,6 +28,8 @@
 // per SM.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc_common.cuh"
@@ -284,76 +286,91 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
 
 // ---------------------------------------------------------------- long-K variant
 
-// For K >= 256 (a superpanel's aggregated updates, K = 1024) a warp-specialised kernel
-// keeps the tensor core fed: three ring stages of hi and lo parts, so that the copies and
-// the lo parts of the next quarters are formed while the MMAs of the current one run.
-//   warp 0       TMA producer: the A and B quarters into stage q % 3 (the hi halves)
-//   warp 1       TMEM owner (two 128-column accumulators) and MMA issuer
-//   warp 2       waits for a quarter's lo parts (and, at a chain start, for its accumulator
-//                to be drained) and releases warp 1 through a named barrier, so that the
-//                issuing warp never waits on an mbarrier
-//   warps 3..10  form the lo parts of every quarter; drain each finished chain from TMEM
-//                into registers one quarter later (round-to-nearest adds), while the next
-//                chain accumulates in the other TMEM half; then write the tile
-constexpr int WS_NS = 3;
-constexpr int WS_STAGE = 2 * A_BYTES + 2 * B_BYTES;   // A hi, B hi, A lo, B lo: 64 KB
-constexpr int WS_WORKERS = 8;
-constexpr int WS_THREADS = 32 * (3 + WS_WORKERS);
-constexpr int WS_SMEM = WS_NS * WS_STAGE + 1024 + 256;
-constexpr uint32_t kWsHandoff = 1;  // named barrier of warps 1 and 2
-static_assert(WS_SMEM <= 232448, "shared memory of one CTA");
-static_assert(2 * WS_WORKERS * BOXB <= WS_STAGE, "epilogue boxes fit in stage 0");
+// For K >= 256 (a superpanel's aggregated updates, K = 1024) the lo parts of both
+// operands come precomputed from global memory (each operand element is split once, not
+// once per tile that reads it), and a warp-specialised kernel keeps the tensor core fed.
+// Shared memory is the bound of the tf32x3 product: per K-quarter the MMAs read hi and lo
+// of A and B three times over, so with the split done elsewhere the traffic per quarter
+// is the TMA's writes plus those reads; a 128 x 256 tile (TNX = 256) reuses each A
+// quarter over twice the columns.
+//   warp 0       TMA producer: A hi, A lo, B hi, B lo quarters into stage q % NS
+//   warp 1       TMEM owner (two TNX-column accumulators) and MMA issuer
+//   warp 2       waits for each quarter's copies (and, at a chain start, for its
+//                accumulator to be drained) and releases warp 1 through a named barrier,
+//                so that the issuing warp never waits on an mbarrier
+//   warps 3..10  drain each finished chain from TMEM into registers (round-to-nearest
+//                adds) while the next chain accumulates in the other half; write the tile
+template <int TNX>
+struct Presplit {
+  static constexpr int A_B = TM * KQ * 4;                   // 16 KB per part
+  static constexpr int B_B = TNX * KQ * 4;                  // 16 or 32 KB per part
+  static constexpr int STAGE = 2 * A_B + 2 * B_B;           // A hi, A lo, B hi, B lo
+  static constexpr int NS = (TNX == 128) ? 3 : 2;
+  static constexpr int WORKERS = 8;
+  static constexpr int COLS = TNX / 2;                      // columns per worker thread
+  static constexpr int THREADS = 32 * (3 + WORKERS);
+  static constexpr int SMEM = NS * STAGE + 1024 + 256;
+  static_assert(SMEM <= 232448, "shared memory of one CTA");
+  static_assert(WORKERS * (COLS / 32) * BOXB <= NS * STAGE, "epilogue boxes fit");
+};
+constexpr uint32_t kPsHandoff = 1;  // named barrier of warps 1 and 2
 
-__global__ void __launch_bounds__(WS_THREADS, 1)
-    gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tma,
-                          const __grid_constant__ CUtensorMap tmb,
-                          const __grid_constant__ CUtensorMap tmc, const TcGemmArgs g) {
+struct PresplitArgs {
+  TcGemmArgs g;
+  int a_lo_row0, a_lo_k0;  // the lo parts' offsets in their own maps
+  int b_lo_row0, b_lo_k0;
+};
+
+template <int TNX>
+__global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
+    gemm_tf32x3_presplit_kernel(const __grid_constant__ CUtensorMap tma,
+                                const __grid_constant__ CUtensorMap tma_lo,
+                                const __grid_constant__ CUtensorMap tmb,
+                                const __grid_constant__ CUtensorMap tmb_lo,
+                                const __grid_constant__ CUtensorMap tmc, const PresplitArgs pa) {
+  using P = Presplit<TNX>;
+  const TcGemmArgs& g = pa.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + WS_NS * WS_STAGE);  // [NS] copies
-  uint64_t* split = full + WS_NS;                                       // [NS] lo parts
-  uint64_t* empty = split + WS_NS;                                      // [NS] MMAs done
-  uint64_t* accfull = empty + WS_NS;                                    // [2]
-  uint64_t* accempty = accfull + 2;                                     // [2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::NS * P::STAGE);  // [NS] copies
+  uint64_t* empty = full + P::NS;                                         // [NS] MMAs done
+  uint64_t* accfull = empty + P::NS;                                      // [2]
+  uint64_t* accempty = accfull + 2;                                       // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  int bi, bj;
+  // tile: row tile bi (128 rows), column tile bj (TNX columns); in lower mode only the
+  // tiles that reach the diagonal or below it (bj * TNX <= bi * 128 + 127)
+  int bi = 0, bj = 0;
   if (g.lower) {
-    const int tri = g.n_tiles * (g.n_tiles + 1) / 2;
     int rem = static_cast<int>(blockIdx.x);
-    if (rem < tri) {
-      bi = 0;
-      while (rem > bi) { rem -= bi + 1; ++bi; }
-      bj = rem;
-    } else {
-      rem -= tri;
-      bi = g.n_tiles + rem / g.n_tiles;
-      bj = rem % g.n_tiles;
+    for (;; ++bi) {
+      const int cnt = min((bi * TM + TM - 1) / TNX + 1, g.n_tiles);
+      if (rem < cnt) { bj = rem; break; }
+      rem -= cnt;
     }
   } else {
     bi = blockIdx.x / g.n_tiles;
     bj = blockIdx.x % g.n_tiles;
   }
-  const int i0 = bi * TM, j0 = bj * TN;
+  const int i0 = bi * TM, j0 = bj * TNX;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < WS_NS; ++s) {
+    for (int s = 0; s < P::NS; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&split[s], WS_WORKERS);
       tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
-      tc::mbar_init(&accempty[b], WS_WORKERS);
+      tc::mbar_init(&accempty[b], P::WORKERS);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_alloc(tmem_slot, 2 * TNX);
     tc::tmem_relinquish();
   }
   // no thread touches global memory before the previous kernel in the stream is done
@@ -362,44 +379,50 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  constexpr uint32_t IDESC = idesc_tf32(TM, TN, false);
+  constexpr uint32_t IDESC = idesc_tf32(TM, TNX, false);
   const int nq = g.nq;
-  const int nchain = (nq + CHAIN_Q - 1) / CHAIN_Q;
   bool ok = true;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int q = 0; q < nq; ++q) {
-        const int s = q % WS_NS;
-        const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
+        const int s = q % P::NS;
+        const uint32_t ph = static_cast<uint32_t>(q / P::NS) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-        uint8_t* base = smem + s * WS_STAGE;
-        tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+        uint8_t* base = smem + s * P::STAGE;
+        tc::mbar_arrive_expect_tx(&full[s], P::STAGE);
         tc::tma_load_2d(base, &tma, &full[s], g.a_k0 + q * KQ, g.a_row0 + i0);
-        tc::tma_load_2d(base + A_BYTES, &tmb, &full[s], g.b_k0 + q * KQ, g.b_row0 + j0);
+        tc::tma_load_2d(base + P::A_B, &tma_lo, &full[s], pa.a_lo_k0 + q * KQ, pa.a_lo_row0 + i0);
+#pragma unroll
+        for (int h = 0; h < TNX / 128; ++h) {
+          tc::tma_load_2d(base + 2 * P::A_B + h * A_BYTES, &tmb, &full[s], g.b_k0 + q * KQ,
+                          g.b_row0 + j0 + 128 * h);
+          tc::tma_load_2d(base + 2 * P::A_B + P::B_B + h * A_BYTES, &tmb_lo, &full[s],
+                          pa.b_lo_k0 + q * KQ, pa.b_lo_row0 + j0 + 128 * h);
+        }
       }
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuer and waiter
     const bool waiter = (warp == 2);
     for (int q = 0; q < nq; ++q) {
-      const int s = q % WS_NS;
-      const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
+      const int s = q % P::NS;
+      const uint32_t ph = static_cast<uint32_t>(q / P::NS) & 1u;
       const int chain = q / CHAIN_Q, acc = chain & 1;
       bool bad = false;
       if (waiter && lane == 0) {
         if (q % CHAIN_Q == 0)
           bad = !tc::mbar_wait(&accempty[acc], (static_cast<uint32_t>(chain >> 1) & 1u) ^ 1u,
                                abort_flag);
-        if (!bad) bad = !tc::mbar_wait(&split[s], ph, abort_flag);
+        if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag);
       }
-      if (tc::handoff_or(kWsHandoff, 64, bad)) { ok = false; break; }
+      if (tc::handoff_or(kPsHandoff, 64, bad)) { ok = false; break; }
       if (!waiter && lane == 0) {
         tc::fence_after();
-        const uint32_t ah = tc::smem_u32(smem + s * WS_STAGE);
-        const uint32_t bh = ah + A_BYTES, al = ah + A_BYTES + B_BYTES, bl = al + A_BYTES;
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TN);
+        const uint32_t ah = tc::smem_u32(smem + s * P::STAGE);
+        const uint32_t al = ah + P::A_B, bh = ah + 2 * P::A_B, bl = bh + P::B_B;
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TNX);
 #pragma unroll
         for (int kk = 0; kk < KQ / 8; ++kk) {
           const uint64_t dah = tc::smem_desc(ah + 32 * kk, 16, 1024, tc::kSwizzle128B);
@@ -429,65 +452,42 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ workers
-    const int wk = warp - 3;                       // 0 .. WS_WORKERS - 1
-    const int wt = threadIdx.x - 96;               // 0 .. 32 * WS_WORKERS - 1
+    const int wk = warp - 3;                       // 0 .. WORKERS - 1
     const int rq = warp % 4, half = wk / 4;        // TMEM lane quarter, column half
-    const uint32_t tmem_w = tmem_base + (static_cast<uint32_t>(32 * rq) << 16) + 64 * half;
-    float accr[64];
+    const uint32_t tmem_w =
+        tmem_base + (static_cast<uint32_t>(32 * rq) << 16) + static_cast<uint32_t>(P::COLS * half);
+    float accr[P::COLS];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) accr[i] = 0.0f;
-    for (int q = 0; q <= nq && ok; ++q) {
-      if (q < nq) {
-        const int s = q % WS_NS;
-        const uint32_t ph = static_cast<uint32_t>(q / WS_NS) & 1u;
-        if (!tc::mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
-        // lo = x - trunc_tf32(x), elementwise in the same swizzled layout
-        const float4* src = reinterpret_cast<const float4*>(smem + s * WS_STAGE);
-        float4* dst = reinterpret_cast<float4*>(smem + s * WS_STAGE + A_BYTES + B_BYTES);
-#pragma unroll
-        for (int e = wt; e < (A_BYTES + B_BYTES) / 16; e += 32 * WS_WORKERS) {
-          float4 x = src[e];
-          x.x -= __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
-          x.y -= __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
-          x.z -= __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
-          x.w -= __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
-          dst[e] = x;
-        }
-        tc::fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&split[s]);
+    for (int i = 0; i < P::COLS; ++i) accr[i] = 0.0f;
+    const int nchain = (nq + CHAIN_Q - 1) / CHAIN_Q;
+    for (int chain = 0; chain < nchain; ++chain) {
+      const int acc = chain & 1;
+      if (!tc::mbar_wait(&accfull[acc], static_cast<uint32_t>(chain >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
       }
-      // a chain that ended with the previous quarter (or the last one): TMEM -> registers
-      if (q > 0 && (q % CHAIN_Q == 0 || q == nq)) {
-        const int chain = (q - 1) / CHAIN_Q, acc = chain & 1;
-        if (!tc::mbar_wait(&accfull[acc], static_cast<uint32_t>(chain >> 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
+      tc::fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(tmem_w + static_cast<uint32_t>(acc * TN) + 32 * c, r);
-          tc::tmem_ld_wait();
+      for (int c = 0; c < P::COLS / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tmem_w + static_cast<uint32_t>(acc * TNX) + 32 * c, r);
+        tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            accr[32 * c + j] = __fadd_rn(accr[32 * c + j], __uint_as_float(r[j]));
-        }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+        for (int j = 0; j < 32; ++j)
+          accr[32 * c + j] = __fadd_rn(accr[32 * c + j], __uint_as_float(r[j]));
       }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&accempty[acc]);
     }
-    (void)nchain;
     if (ok) {
       // every MMA has completed (the last chain's commit) and every copy was consumed:
-      // stage 0 holds the epilogue's boxes, two 32 x 32 per worker warp
+      // the stages hold the epilogue's boxes, COLS / 32 per worker warp
       const int row = i0 + 32 * rq + lane;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int colt = 64 * half + 32 * c;
-        uint8_t* box = smem + (wk * 2 + c) * BOXB;
+      for (int c = 0; c < P::COLS / 32; ++c) {
+        const int colt = P::COLS * half + 32 * c;
+        uint8_t* box = smem + (wk * (P::COLS / 32) + c) * BOXB;
         const float* r = accr + 32 * c;
         uint8_t* srow = box + lane * 128;
 #pragma unroll
@@ -527,8 +527,23 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
-    tc::tmem_dealloc(tmem_base, 256);
+    tc::tmem_dealloc(tmem_base, 2 * TNX);
   }
+}
+
+// lo = x - trunc_tf32(x) for a rows x cols block (cols a multiple of 4, rows 16-byte
+// aligned); one thread per 4 elements
+__global__ void split_lo_kernel(const float* __restrict__ src, int ld, int rows, int cols,
+                                float* __restrict__ lo, int ld_lo) {
+  const int r = blockIdx.y;
+  const int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (r >= rows || c >= cols) return;
+  float4 x = *reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * ld + c);
+  x.x -= __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+  x.y -= __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+  x.z -= __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+  x.w -= __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+  *reinterpret_cast<float4*>(lo + static_cast<size_t>(r) * ld_lo + c) = x;
 }
 
 }  // namespace
@@ -571,22 +586,82 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.st = st;
   const unsigned grid = lower ? static_cast<unsigned>(tn * (tn + 1) / 2 + (tm - tn) * tn)
                               : static_cast<unsigned>(tm * tn);
-  if (g.nq >= 8) {
-    // long K: the warp-specialised kernel, one CTA per SM
-    ensure_dynamic_smem(gemm_tf32x3_ws_kernel, WS_SMEM);
-    if (pdl) {
-      GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_ws_kernel, grid, WS_THREADS, WS_SMEM, ma, mb, mc, g);
-    } else {
-      GPTQ_LAUNCH(kind, s, gemm_tf32x3_ws_kernel, grid, WS_THREADS, WS_SMEM, ma, mb, mc, g);
-    }
+  ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
+  if (pdl) {
+    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
   } else {
-    ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
-    if (pdl) {
-      GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
-    } else {
-      GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
-    }
+    GPTQ_LAUNCH(kind, s, gemm_tf32x3_kernel, grid, THREADS, SMEM_BYTES, ma, mb, mc, g);
   }
+}
+
+void launch_split_lo(const float* src, int ld, int rows, int cols, float* lo, int ld_lo,
+                     cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return;
+  dim3 grid(static_cast<unsigned>(ceil_div(cols / 4, 256)), static_cast<unsigned>(rows));
+  GPTQ_LAUNCH(GPTQ_K_POTRF_UPDATE, s, split_lo_kernel, grid, 256, 0, src, ld, rows, cols, lo,
+              ld_lo);
+}
+
+namespace {
+template <int TNX>
+void launch_presplit_t(int kind, const CUtensorMap& ma, const CUtensorMap& ma_lo,
+                       const CUtensorMap& mb, const CUtensorMap& mb_lo, const CUtensorMap& mc,
+                       const PresplitArgs& pa, int tm, cudaStream_t s, bool pdl) {
+  using P = Presplit<TNX>;
+  const int tn = pa.g.n_tiles;
+  unsigned grid = 0;
+  if (pa.g.lower) {
+    for (int bi = 0; bi < tm; ++bi) grid += static_cast<unsigned>(std::min((bi * TM + TM - 1) / TNX + 1, tn));
+  } else {
+    grid = static_cast<unsigned>(tm * tn);
+  }
+  ensure_dynamic_smem(gemm_tf32x3_presplit_kernel<TNX>, P::SMEM);
+  if (pdl) {
+    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_presplit_kernel<TNX>, grid, P::THREADS, P::SMEM, ma,
+                    ma_lo, mb, mb_lo, mc, pa);
+  } else {
+    GPTQ_LAUNCH(kind, s, gemm_tf32x3_presplit_kernel<TNX>, grid, P::THREADS, P::SMEM, ma, ma_lo,
+                mb, mb_lo, mc, pa);
+  }
+}
+}  // namespace
+
+void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
+                                 const CUtensorMap& ma_lo, int a_lo_row0, int a_lo_k0,
+                                 const CUtensorMap& mb, int b_row0, int b_k0,
+                                 const CUtensorMap& mb_lo, int b_lo_row0, int b_lo_k0, int K,
+                                 float* C, int ldc, int M, int N, float alpha, float beta,
+                                 bool lower, DevStatus* st, cudaStream_t s, bool pdl) {
+  if (M <= 0 || N <= 0) return;
+  if ((beta != 0.0f && beta != 1.0f) || (lower && (beta != 1.0f || M < N)) || K <= 0 ||
+      K % KQ != 0) {
+    fail(GPTQ_ERR_INVALID_ARG,
+         "launch_gemm_tf32x3_presplit: beta must be 0 or 1 (1 and M >= N in lower mode), K a "
+         "positive multiple of 32");
+  }
+  CUtensorMap mc;
+  make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
+               static_cast<uint64_t>(M), static_cast<uint64_t>(ldc) * 4, 32, 32,
+               CU_TENSOR_MAP_SWIZZLE_128B);
+  PresplitArgs pa;
+  pa.g.a_row0 = a_row0;
+  pa.g.a_k0 = a_k0;
+  pa.g.b_row0 = b_row0;
+  pa.g.b_k0 = b_k0;
+  pa.g.M = M;
+  pa.g.N = N;
+  pa.g.alpha = alpha;
+  pa.g.accumulate = (beta != 0.0f) ? 1 : 0;
+  pa.g.lower = lower ? 1 : 0;
+  pa.g.nq = K / KQ;
+  pa.g.st = st;
+  pa.a_lo_row0 = a_lo_row0;
+  pa.a_lo_k0 = a_lo_k0;
+  pa.b_lo_row0 = b_lo_row0;
+  pa.b_lo_k0 = b_lo_k0;
+  const int tm = static_cast<int>(ceil_div(M, TM));
+  pa.g.n_tiles = static_cast<int>(ceil_div(N, kPresplitTN));
+  launch_presplit_t<kPresplitTN>(kind, ma, ma_lo, mb, mb_lo, mc, pa, tm, s, pdl);
 }
 
 }  // namespace gptq

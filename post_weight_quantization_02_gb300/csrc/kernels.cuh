@@ -37,7 +37,7 @@ constexpr int kLoopUblkFloats = 128 * kLoopLanesPerRow * (128 / kLoopLanesPerRow
 // prepare.cu
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, DevStatus* st, cudaStream_t s);
+                    float* lam, float* DI, float* Lo, DevStatus* st, cudaStream_t s);
 
 // quantize.cu
 struct QuantArgs {
@@ -87,6 +87,21 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         const CUtensorMap& mb, int b_row0, int b_k0, int K, float* C, int ldc,
                         int M, int N, float alpha, float beta, bool lower, DevStatus* st,
                         cudaStream_t s, bool pdl);
+
+// gemm_tc.cu, long K: the same product with the lo parts of both operands precomputed
+// (lo = x - tf32(x), read through their own maps at their own offsets); tiles of 128 x
+// kPresplitTN.  launch_split_lo writes those lo parts for a rows x cols block.
+constexpr int kPresplitTN = 256;
+void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
+                                 const CUtensorMap& ma_lo, int a_lo_row0, int a_lo_k0,
+                                 const CUtensorMap& mb, int b_row0, int b_k0,
+                                 const CUtensorMap& mb_lo, int b_lo_row0, int b_lo_k0, int K,
+                                 float* C, int ldc, int M, int N, float alpha, float beta,
+                                 bool lower, DevStatus* st, cudaStream_t s, bool pdl);
+void launch_split_lo(const float* src, int ld, int rows, int cols, float* lo, int ld_lo,
+                     cudaStream_t s);
+// superpanel width of the prepare (panels whose update of later columns is grouped)
+constexpr int kSuperpanel = 1024;
 
 // lazy_tc.cu
 // ErrT rows kept for the deferred update: one 512-column superblock of the loop

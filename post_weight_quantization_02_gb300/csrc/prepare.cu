@@ -22,7 +22,7 @@ namespace gptq {
 namespace {
 
 constexpr int NB = 128;    // panel width of the blocked factorisation and inverse
-constexpr int NBS = 1024;  // superpanel: panels whose update of later columns is grouped
+constexpr int NBS = kSuperpanel;  // superpanel: panels whose update of later columns is grouped
 
 // ---------------------------------------------------------------- diagonal statistics
 
@@ -502,7 +502,7 @@ __global__ void reverse_transpose_kernel(const float* __restrict__ Y, int d, flo
 
 void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* perm,
                     uint8_t* dead, float* U, float* S, float* Hr, float* diag_fixed,
-                    float* lam, float* DI, DevStatus* st, cudaStream_t s) {
+                    float* lam, float* DI, float* Lo, DevStatus* st, cudaStream_t s) {
   GPTQ_LAUNCH(GPTQ_K_PREP_DIAG, s, prep_diag_kernel, 1, 1024, 0, H, d, damp, dead, diag_fixed,
               lam, st);
   GPTQ_LAUNCH(GPTQ_K_PREP_RANK, s, prep_rank_kernel, (unsigned)ceil_div(d, 8), 256, 0,
@@ -542,19 +542,25 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   const int diag_smem = std::max(kDiagSmemFloats * static_cast<int>(sizeof(float)),
                                  smem_optin - static_cast<int>(diag_attr.sharedSizeBytes));
   ensure_dynamic_smem(chol_inv_diag_kernel, diag_smem);
-  CUtensorMap mHr, mS, mDI;
+  CUtensorMap mHr, mS, mDI, mLo[2];
   make_gemm_map(&mHr, Hr, d, d, d);
   make_gemm_map(&mS, S, d, d, d);
   make_gemm_map(&mDI, DI, static_cast<int>(ceil_div(d, NB)) * NB, NB, NB);
+  // lo parts (x - tf32(x)) of a superpanel's columns, two buffers [d][NBS] that
+  // alternate between superpanels: rows past the superpanel from L (Hr), rows before it
+  // from the inverse (S)
+  for (int b = 0; b < 2; ++b) make_gemm_map(&mLo[b], Lo + static_cast<size_t>(b) * d * NBS, d, NBS, NBS);
   const int nblk = static_cast<int>(ceil_div(d, NB));
   const int nsp = static_cast<int>(ceil_div(d, NBS));
-  AuxStreams& aux = aux_streams(2 * nblk + nsp + 3);
+  AuxStreams& aux = aux_streams(2 * nblk + 3 * nsp + 3);
   cudaStream_t sa = aux.a, sb = aux.b, sc = aux.c;
   cudaEvent_t* ev_panel = aux.ev.data();             // [nblk] panel kb factored and solved
   cudaEvent_t* ev_far = ev_panel + nblk;             // [nblk] panel kb's far update applied
   cudaEvent_t* ev_spfar = ev_far + nblk;             // [nsp] superpanel's far update applied
-  cudaEvent_t ev_fork = ev_spfar[nsp], ev_b = ev_spfar[nsp + 1], ev_c = ev_spfar[nsp + 2];
-  std::vector<char> far_done(nblk, 0), spfar_done(nsp, 0);
+  cudaEvent_t* ev_lo = ev_spfar + nsp;               // [nsp] its lo parts of L written
+  cudaEvent_t* ev_sptri = ev_lo + nsp;               // [nsp] its inverse update applied
+  cudaEvent_t ev_fork = ev_sptri[nsp], ev_b = ev_sptri[nsp + 1], ev_c = ev_sptri[nsp + 2];
+  std::vector<char> far_done(nblk, 0), spfar_done(nsp, 0), sptri_done(nsp, 0);
   GPTQ_CUDA(cudaEventRecord(ev_fork, s));
   GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_fork, 0));
   GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_fork, 0));
@@ -620,17 +626,27 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
       // update also wrote, after it.
       const int spw = sp_end - sp0;
       const int nxt = (d - sp_end < NBS) ? d - sp_end : NBS;
+      const int lb = sp % 2;  // this superpanel's lo buffer
+      float* lo = Lo + static_cast<size_t>(lb) * d * NBS;
+      // the lo parts of L[sp_end:, sp] (final since the last panel solve); the buffer was
+      // last read by the far and inverse updates of superpanel sp - 2 (the far one is
+      // already ordered before this stream by the wait below of sp - 1's near update)
+      if (sp >= 2 && sptri_done[sp - 2]) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_sptri[sp - 2], 0));
       if (sp >= 1 && spfar_done[sp - 1]) GPTQ_CUDA(cudaStreamWaitEvent(sa, ev_spfar[sp - 1], 0));
-      launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, sp_end, sp0, mHr, sp_end, sp0, spw,
-                         Hr + static_cast<size_t>(sp_end) * d + sp_end, d, d - sp_end, nxt,
-                         -1.0f, 1.0f, true, st, sa, true);
+      launch_split_lo(Hr + static_cast<size_t>(sp_end) * d + sp0, d, d - sp_end, spw,
+                      lo + static_cast<size_t>(sp_end) * NBS, NBS, sa);
+      GPTQ_CUDA(cudaEventRecord(ev_lo[sp], sa));
+      launch_gemm_tf32x3_presplit(GPTQ_K_POTRF_UPDATE, mHr, sp_end, sp0, mLo[lb], sp_end, 0, mHr,
+                                  sp_end, sp0, mLo[lb], sp_end, 0, spw,
+                                  Hr + static_cast<size_t>(sp_end) * d + sp_end, d, d - sp_end,
+                                  nxt, -1.0f, 1.0f, true, st, sa, false);
       const int far = d - sp_end - nxt;
       if (far > 0) {
-        // its operands, the superpanel's columns of L, are final since the last panel solve
-        GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_panel[kb], 0));
-        launch_gemm_tf32x3(GPTQ_K_POTRF_UPDATE, mHr, sp_end + nxt, sp0, mHr, sp_end + nxt, sp0,
-                           spw, Hr + static_cast<size_t>(sp_end + nxt) * d + sp_end + nxt, d,
-                           far, far, -1.0f, 1.0f, true, st, sc, false);
+        GPTQ_CUDA(cudaStreamWaitEvent(sc, ev_lo[sp], 0));
+        launch_gemm_tf32x3_presplit(GPTQ_K_POTRF_UPDATE, mHr, sp_end + nxt, sp0, mLo[lb],
+                                    sp_end + nxt, 0, mHr, sp_end + nxt, sp0, mLo[lb], sp_end + nxt,
+                                    0, spw, Hr + static_cast<size_t>(sp_end + nxt) * d + sp_end + nxt,
+                                    d, far, far, -1.0f, 1.0f, true, st, sc, false);
         GPTQ_CUDA(cudaEventRecord(ev_spfar[sp], sc));
         spfar_done[sp] = 1;
       }
@@ -648,9 +664,20 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
     }
     if (sp_last && sp_end < d) {
       // the superpanel's share at once: Y[c][r] -= sum_{j in sp} Y[c][j] L[r][j],
-      // c < sp_end <= r (rows c past a block column's end hold exact zeros there)
-      launch_gemm_tf32x3(GPTQ_K_TRTRI_UPDATE, mS, 0, sp0, mHr, sp_end, sp0, sp_end - sp0,
-                         S + sp_end, d, sp_end, d - sp_end, -1.0f, 1.0f, false, st, sb, false);
+      // c < sp_end <= r (rows c past a block column's end hold exact zeros there).  The
+      // lo parts of Y[:sp_end, sp] go to rows 0 .. sp_end of the superpanel's buffer, once
+      // the far update of superpanel sp - 2, which read those rows, is done; the lo parts
+      // of L come from stream A.
+      const int lb = sp % 2;
+      float* lo = Lo + static_cast<size_t>(lb) * d * NBS;
+      if (sp >= 2 && spfar_done[sp - 2]) GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_spfar[sp - 2], 0));
+      launch_split_lo(S + sp0, d, sp_end, sp_end - sp0, lo, NBS, sb);
+      GPTQ_CUDA(cudaStreamWaitEvent(sb, ev_lo[sp], 0));
+      launch_gemm_tf32x3_presplit(GPTQ_K_TRTRI_UPDATE, mS, 0, sp0, mLo[lb], 0, 0, mHr, sp_end, sp0,
+                                  mLo[lb], sp_end, 0, sp_end - sp0, S + sp_end, d, sp_end,
+                                  d - sp_end, -1.0f, 1.0f, false, st, sb, false);
+      GPTQ_CUDA(cudaEventRecord(ev_sptri[sp], sb));
+      sptri_done[sp] = 1;
     }
   }
   GPTQ_CUDA(cudaEventRecord(ev_b, sb));
