@@ -23,6 +23,9 @@ namespace {
 
 constexpr int NB = 128;    // panel width of the blocked factorisation and inverse
 constexpr int NBS = kSuperpanel;  // superpanel: panels whose update of later columns is grouped
+// Superpanels pay off where the trailing matrix is large: below this width the prepare is
+// a short latency chain, and the superpanel updates would lengthen it.
+constexpr int kSuperpanelFrom = 8192;
 
 // ---------------------------------------------------------------- diagonal statistics
 
@@ -551,7 +554,9 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   // from the inverse (S)
   for (int b = 0; b < 2; ++b) make_gemm_map(&mLo[b], Lo + static_cast<size_t>(b) * d * NBS, d, NBS, NBS);
   const int nblk = static_cast<int>(ceil_div(d, NB));
-  const int nsp = static_cast<int>(ceil_div(d, NBS));
+  // superpanel width: NBS on wide layers, the whole matrix (no superpanel updates) below
+  const int nbs = (d >= kSuperpanelFrom) ? NBS : static_cast<int>(ceil_div(d, NB)) * NB;
+  const int nsp = static_cast<int>(ceil_div(d, nbs));
   AuxStreams& aux = aux_streams(2 * nblk + 3 * nsp + 3);
   cudaStream_t sa = aux.a, sb = aux.b, sc = aux.c;
   cudaEvent_t* ev_panel = aux.ev.data();             // [nblk] panel kb factored and solved
@@ -573,9 +578,9 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   for (int kb = 0; kb < nblk; ++kb) {
     const int k = kb * NB;
     const int rest = d - k - NB;
-    const int sp = k / NBS;
-    const int sp0 = sp * NBS;                              // this panel's superpanel
-    const int sp_end = (d - sp0 < NBS) ? d : sp0 + NBS;
+    const int sp = k / nbs;
+    const int sp0 = sp * nbs;                              // this panel's superpanel
+    const int sp_end = (d - sp0 < nbs) ? d : sp0 + nbs;
     const int in_sp = sp_end - (k + NB);                   // its columns after this panel
     // Block column kb is complete once the near update of panel kb - 1 is (that update
     // waited for the far update of panel kb - 2, the last panel-level update of block
@@ -625,7 +630,7 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
       // past it on stream C.  Each adds into columns that the previous superpanel's far
       // update also wrote, after it.
       const int spw = sp_end - sp0;
-      const int nxt = (d - sp_end < NBS) ? d - sp_end : NBS;
+      const int nxt = (d - sp_end < nbs) ? d - sp_end : nbs;
       const int lb = sp % 2;  // this superpanel's lo buffer
       float* lo = Lo + static_cast<size_t>(lb) * d * NBS;
       // the lo parts of L[sp_end:, sp] (final since the last panel solve); the buffer was
