@@ -376,12 +376,15 @@ def run_ours(args, world, rank, local):
         syrk_ms = syrk_t / syrk_c                       # live, over the timed steps
         flops = float(d) * (d + 1) * n                  # upper triangle of X^T X, 2 flop/MAC
         achieved = flops / (syrk_ms * 1e-3) / 1e12
+        # The SYRK is timed inside a long run of steps (seconds of back-to-back work under
+        # the power cap), so its roofline is the measured sustained bf16 figure; the burst
+        # figure (a GEMM timed alone) is reported beside it.
         roofline = {"bound": "tensor", "kernel": "syrk_tc", "achieved": round(achieved, 1),
-                    "peak": bf16, "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
-                    "peak_source": f"{peak_src} bf16 dense burst",
-                    # the measured power-capped figure (a GEMM run back to back), for context
-                    "peak_sustained": bf16_sus,
-                    "frac_of_sustained": round(achieved / bf16_sus, 4),
+                    "peak": bf16_sus, "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
+                    "peak_source": f"{peak_src} bf16 dense sustained (GEMM back to back under "
+                                   f"the power cap)",
+                    "peak_burst": bf16,
+                    "frac_of_burst": round(achieved / bf16, 4),
                     "ms_per_launch": round(syrk_ms, 3),
                     "algorithmic_flops_per_launch": flops,
                     "traffic": ncu_traffic("post_weight_quantization_02_gb300/csrc/hessian_tc.cu",
