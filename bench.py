@@ -709,8 +709,8 @@ def run_dequant(args, world, rank, local):
 
 
 def run_pipeline(args, world, rank, local):
-    """The block-sequential pipeline on a Llama-shaped block (hidden 4096, MLP 14336, 32
-    heads, the 8B-class shapes of the survey's block configuration): Hessians of the four
+    """The block-sequential pipeline on a Llama-3-8B-shaped block (hidden 4096, MLP 14336,
+    32 query heads, 8 key/value heads: k and v are 1024 x 4096): Hessians of the four
     input groups over every calibration token, prepare, all seven linears quantised, and
     the re-forward with the dequantised weights.  One JSON line."""
     import torch
@@ -721,14 +721,16 @@ def run_pipeline(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
-    hidden, inter, heads, seq = 4096, 14336, 32, 2048
+    hidden, inter, heads, kv_heads, seq = 4096, 14336, 32, 8, 2048
+    kv_dim = hidden * kv_heads // heads
     tokens = args.tokens if args.tokens else 262144
     B = max(1, tokens // seq)
     g = torch.Generator(device="cpu").manual_seed(11)
     x = torch.randn(B, seq, hidden, generator=g).to(device=dev, dtype=torch.bfloat16)
-    W = make_block_weights(hidden, inter, 1, dev)
+    W = make_block_weights(hidden, inter, 1, dev, kv_dim=kv_dim)
     bq = BlockQuantizer(hidden, inter, heads, bits=4, group=128, static_groups=args.static_groups,
-                        seqs_per_chunk=8, max_chunk_tokens=8 * seq, device=dev)
+                        seqs_per_chunk=8, max_chunk_tokens=8 * seq, device=dev,
+                        kv_heads=kv_heads)
     for _ in range(max(1, args.warmup - 2)):
         bq.quantize_block(x, W)
     torch.cuda.synchronize()
@@ -741,7 +743,7 @@ def run_pipeline(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(dist, dev)
         ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / steps, dev)
-    weights = 4 * hidden * hidden + 3 * hidden * inter
+    weights = 2 * hidden * hidden + 2 * kv_dim * hidden + 3 * hidden * inter
     if rank == 0:
         print(json.dumps({
             "metric": "block-sequential GPTQ, ms per Llama-shaped block (and weights/s)",
@@ -749,7 +751,8 @@ def run_pipeline(args, world, rank, local):
             "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random-init block, seeded calibration tokens)",
-            "config": {"workload": f"block hidden {hidden}, MLP {inter}, {heads} heads, "
+            "config": {"workload": f"block hidden {hidden}, MLP {inter}, {heads} heads "
+                                   f"({kv_heads} key/value heads), "
                                    f"{B * seq} tokens ({B} x {seq}), 4-bit group 128, act-order"
                                    + (", static groups" if args.static_groups else ""),
                        "step": "forward (4 Hessian groups) + 4 prepares + 7 quantisations "

@@ -18,7 +18,9 @@ gate, up and down projections; "Worked example: a 7B model"):
 Readings (the pages give no block formula; these are the plainest Llama-style ones):
 rmsnorm without a learned gain (random init: gain 1), eps 1e-6; softmax attention scaled
 by 1/sqrt(head_dim) with a causal mask; no rotary position encoding; the linears have no
-bias.  Inputs of the four Hessians: q, k and v share h1 (one H, as the pages' 7B example
+bias.  With grouped-query attention (``kv_heads`` < ``heads``, as in the Llama-3-8B block:
+32 query heads, 8 key/value heads, k and v projections of 1024 rows) key/value head j
+serves the query heads j*r .. j*r + r - 1, r = heads / kv_heads.  Inputs of the four Hessians: q, k and v share h1 (one H, as the pages' 7B example
 shares one Hessian for q, k and v); o sees the attention output; gate and up share h2;
 down sees a.  All four come from one forward with the block's own weights, and the block
 is re-run once with every linear quantised.
@@ -47,13 +49,19 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (1.0 + np.exp(-x))
 
 
-def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, heads: int) -> np.ndarray:
-    """Causal multi-head softmax attention; q, k, v ``[B, S, h]`` -> ``[B, S, h]``."""
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, heads: int,
+              kv_heads: int = None) -> np.ndarray:
+    """Causal multi-head softmax attention; q ``[B, S, h]``, k and v ``[B, S, kv_heads *
+    h / heads]`` -> ``[B, S, h]``."""
     B, S, h = q.shape
     hd = h // heads
-    def split(t):
-        return t.reshape(B, S, heads, hd).transpose(0, 2, 1, 3)     # [B, heads, S, hd]
-    qh, kh, vh = split(q), split(k), split(v)
+    kv = heads if kv_heads is None else kv_heads
+    def split(t, n):
+        return t.reshape(B, S, n, hd).transpose(0, 2, 1, 3)         # [B, n, S, hd]
+    qh = split(q, heads)
+    # key/value head j serves query heads j*r .. j*r + r - 1
+    kh = np.repeat(split(k, kv), heads // kv, axis=1)
+    vh = np.repeat(split(v, kv), heads // kv, axis=1)
     scores = qh @ kh.transpose(0, 1, 3, 2) / np.sqrt(hd)            # [B, heads, S, S]
     mask = np.triu(np.ones((S, S), dtype=bool), 1)
     scores = np.where(mask, -np.inf, scores)
@@ -63,13 +71,13 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, heads: int) -> np.nda
     return (p @ vh).transpose(0, 2, 1, 3).reshape(B, S, h)
 
 
-def block_forward(x: np.ndarray, W: Dict[str, np.ndarray], heads: int
+def block_forward(x: np.ndarray, W: Dict[str, np.ndarray], heads: int, kv_heads: int = None
                   ) -> Tuple[np.ndarray, Dict[str, np.ndarray]]:
     """The block's output and the inputs of its four Hessian groups (``[B*S, dim]``)."""
     x = np.asarray(x, dtype=F64)
     B, S, h = x.shape
     h1 = rmsnorm(x)
-    o = attention(h1 @ W["wq"].T, h1 @ W["wk"].T, h1 @ W["wv"].T, heads)
+    o = attention(h1 @ W["wq"].T, h1 @ W["wk"].T, h1 @ W["wv"].T, heads, kv_heads)
     y1 = x + o @ W["wo"].T
     h2 = rmsnorm(y1)
     a = silu(h2 @ W["wg"].T) * (h2 @ W["wu"].T)
@@ -80,10 +88,10 @@ def block_forward(x: np.ndarray, W: Dict[str, np.ndarray], heads: int
 
 def quantize_block(x: np.ndarray, W: Dict[str, np.ndarray], heads: int, bits: int = 4,
                    group: int = 128, sym: bool = False, actorder: bool = True,
-                   damp: float = 0.01) -> Dict:
+                   damp: float = 0.01, kv_heads: int = None) -> Dict:
     """One pipeline step: Hessians from the block's own forward, every linear quantised
     (gptq_layer), then the re-forward with the dequantised weights."""
-    _, inputs = block_forward(x, W, heads)
+    _, inputs = block_forward(x, W, heads, kv_heads)
     out: Dict = {"inputs": inputs, "H": {}, "layers": {}, "W_hat": {}}
     for gname, names in GROUPS:
         H = O.hessian(inputs[gname])
@@ -94,7 +102,7 @@ def quantize_block(x: np.ndarray, W: Dict[str, np.ndarray], heads: int, bits: in
             Q = np.empty_like(res["Q"])
             Q[:, res["perm"]] = res["Q"]                 # original column order
             out["W_hat"][name] = Q
-    out["y"], _ = block_forward(x, out["W_hat"], heads)
+    out["y"], _ = block_forward(x, out["W_hat"], heads, kv_heads)
     return out
 
 

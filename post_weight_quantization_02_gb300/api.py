@@ -92,12 +92,27 @@ class LayerEngine:
                               self.Hinv_chol, self.ws_p, stream)
 
     def quantize_weights(self, W: torch.Tensor, stream=None) -> QuantizedLayer:
+        """The column loop and packing of W with this engine's U and perm.  W may have
+        fewer rows than the engine's d_out (layers that share the Hessian but not the
+        output size, such as grouped-query k and v beside q); its outputs are then
+        allocated for its own rows."""
+        m = W.shape[0]
+        if m == self.d_out:
+            out = (self.qweight, self.scales, self.qzeros, self.g_idx, self.loss)
+        elif 0 < m < self.d_out:
+            ngroups = self.scales.shape[0]
+            dev = self.device
+            out = (torch.empty(self.bits * self.d_in // 32, m, dtype=torch.int32, device=dev),
+                   torch.empty(ngroups, m, dtype=torch.float32, device=dev),
+                   torch.empty(ngroups, self.bits * m // 32, dtype=torch.int32, device=dev),
+                   torch.empty(self.d_in, dtype=torch.int32, device=dev),
+                   torch.empty((), dtype=torch.float64, device=dev))
+        else:
+            raise ValueError(f"W has {m} rows; this engine quantises at most {self.d_out}")
         G.gptq_quantize_layer(W, self.Hinv_chol, self.perm, self.dead, self.bits, self.group,
-                              self.sym, self.blocksize, self.qweight, self.scales, self.qzeros,
-                              self.g_idx, self.loss, self.ws_q, stream,
+                              self.sym, self.blocksize, *out, self.ws_q, stream,
                               static_groups=self.static_groups)
-        return QuantizedLayer(self.qweight, self.scales, self.qzeros, self.g_idx, self.perm,
-                              self.loss)
+        return QuantizedLayer(out[0], out[1], out[2], out[3], self.perm, out[4])
 
     def quantize(self, W: torch.Tensor, stream=None) -> QuantizedLayer:
         """Prepare (damping, act-order, inverse Cholesky factor) then the column loop."""

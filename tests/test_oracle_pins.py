@@ -539,6 +539,19 @@ def pin_block_pipeline(O):
     assert np.allclose(st["H"]["qkv"], O.hessian(inputs["qkv"]))
     steps = P.pipeline(x, [W, W], heads, bits=4, group=32)
     assert np.array_equal(steps[1]["inputs"]["qkv"], P.rmsnorm(steps[0]["y"]).reshape(B * S, h))
+    # grouped-query attention is multi-head attention whose key / value heads are repeated:
+    # with k and v weights of 2 heads (16 rows), expanding each head's rows to its query
+    # heads gives the same block
+    kvh = 2
+    hd = h // heads
+    Wg = dict(W, wk=W["wk"][:kvh * hd], wv=W["wv"][:kvh * hd])
+    expand = lambda w: np.concatenate([np.tile(w[j * hd:(j + 1) * hd], (heads // kvh, 1))
+                                       for j in range(kvh)])
+    Wm = dict(W, wk=expand(Wg["wk"]), wv=expand(Wg["wv"]))
+    yg, ig = P.block_forward(x, Wg, heads, kvh)
+    ym, im = P.block_forward(x, Wm, heads)
+    assert np.allclose(yg, ym, rtol=1e-12, atol=1e-14)
+    assert np.allclose(ig["o"], im["o"], rtol=1e-12, atol=1e-14)
 
 
 def unclipped_grid(s):
