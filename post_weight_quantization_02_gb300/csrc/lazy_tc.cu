@@ -4,8 +4,8 @@
 // depth", "The algorithm in code": after a block of columns is quantised, its
 // accumulated errors are pushed into every later column as one matrix product.  The
 // driver defers in two levels: after each 128-column block only the rest of its
-// 512-column superblock is updated (K = 128); after the superblock, every later column
-// at once (K = 512), so the far columns of W are rewritten a quarter as often.  W is
+// 1024-column superblock is updated (K = 128); after the superblock, every later column
+// at once (K = 1024), so the far columns of W are rewritten an eighth as often.  W is
 // float32 and the update must keep float32 accuracy (the next blocks round these
 // values), so each operand is split into two bf16 parts, x = hi + lo, and the product is
 // accumulated in float32 TMEM as hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-16

@@ -9,10 +9,10 @@
 //       e = (w_q - what) / U_qq; W[:, q+1:i2] -= e U[q, q+1:i2]; Err[:, q-i1] = e
 //     W[:, i2:] -= Err U[i1:i2, i2:]          (the lazy update)
 // The lazy update is deferred in two levels (same product, fewer passes over W): after a
-// block only the rest of its 512-column superblock, after the superblock every later
+// block only the rest of its 1024-column superblock, after the superblock every later
 // column.  Layouts in the workspace: Wp [m][d] float32 (processing order), codesT [d][m]
 // uint8 (column-major codes, so that a step's codes are one coalesced row), the
-// superblock's errors as bf16 halves ehi/elo [512][m] (e = hi + lo), U's bf16 halves
+// superblock's errors as bf16 halves ehi/elo [1024][m] (e = hi + lo), U's bf16 halves
 // [d][d], the loop's
 // per-block layout of U, zeros [G][m] int32, loss_rows [m] float64 and pos [d] int32
 // (the inverse permutation).
@@ -280,7 +280,7 @@ struct LoopArgs {
   float* scales;       // [G][m]
   int32_t* zeros;      // [G][m]
   uint8_t* codesT;     // [d][m]
-  __nv_bfloat16* ehi;  // [128][m] rows of the superblock's [512][m]: e = hi + lo, bf16
+  __nv_bfloat16* ehi;  // [128][m] rows of the superblock's [1024][m]: e = hi + lo, bf16
   __nv_bfloat16* elo;
   double* loss_rows;   // [m]
 };
