@@ -520,6 +520,16 @@ def run_e2e(args, cfg, X, W, eng, dist, dev, world):
     Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
     Wh.copy_(W)
     out = quantize_layer_from_host(eng, Wh, Xh, chunk_tokens=cfg.chunk)   # warm-up
+    # the host-to-device link's rate on this machine (untimed): one chunk copied 8 times
+    stage = torch.empty(min(cfg.chunk, n), d, dtype=X.dtype, device=dev)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(8):
+        stage.copy_(Xh[:stage.shape[0]], non_blocking=True)
+    a1.record()
+    torch.cuda.synchronize()
+    link_gbs = 8 * stage.numel() * stage.element_size() / (a0.elapsed_time(a1) * 1e-3) / 1e9
+    del stage
     e_steps = max(1, min(args.steps, 3))
     barrier(dist, dev)
     torch.cuda.synchronize()
@@ -535,6 +545,8 @@ def run_e2e(args, cfg, X, W, eng, dist, dev, world):
     return {"value": round(world * float(m) * d / (e_ms * 1e-3), 1), "unit": "weights/s",
             "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": e_steps,
+            "h2d_link_gbs": round(link_gbs, 1),
+            "h2d_copy_ms_at_link_rate": round(h2d / (link_gbs * 1e9) * 1e3, 1),
             "path": f"gptq_quantize_layer_host (C ABI): page-locked X copied in "
                     f"{-(-n // cfg.chunk)} chunks of {cfg.chunk} tokens overlapped with the "
                     f"Hessian kernels, then W; packed outputs copied back"}
