@@ -137,3 +137,59 @@ def test_quantize_flags_and_dequant_workspace():
     assert G.lib().gptq_quantize_layer_ex(P, 1, P, None, None, 64, 256, 4, 128, 0, 128, 2, P,
                                           P, P, P, P, P, 1 << 30, None) == \
         G.GPTQ_ERR_INVALID_ARG
+
+
+def _call_host(**kw):
+    a = dict(X=P, xt=1, ntok=4096, chunk=1024, W=P, wt=1, m=64, d=256, damp=0.01, act=1,
+             bits=4, group=128, sym=0, block=128, flags=0, qw=P, sc=P, qz=P, gi=P, perm=P,
+             dev=P, devb=1 << 40)
+    a.update(kw)
+    loss = ctypes.c_double(0.0)
+    info = ctypes.c_int32(0)
+    return G.lib().gptq_quantize_layer_host(
+        a["X"], a["xt"], a["ntok"], a["chunk"], a["W"], a["wt"], a["m"], a["d"], a["damp"],
+        a["act"], a["bits"], a["group"], a["sym"], a["block"], a["flags"], a["qw"], a["sc"],
+        a["qz"], a["gi"], a["perm"], ctypes.byref(loss), ctypes.byref(info), a["dev"],
+        a["devb"], None)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(ntok=0, X=None), G.GPTQ_ERR_INVALID_ARG, "no calibration tokens"),
+    (dict(W=None), G.GPTQ_ERR_INVALID_ARG, "null"),
+    (dict(chunk=0), G.GPTQ_ERR_INVALID_ARG, "chunk_tokens"),
+    (dict(xt=7), G.GPTQ_ERR_INVALID_ARG, "dtypes"),
+    (dict(damp=-1.0), G.GPTQ_ERR_INVALID_ARG, "damp"),
+    (dict(flags=4), G.GPTQ_ERR_INVALID_ARG, "flags"),
+    (dict(bits=5), G.GPTQ_ERR_UNSUPPORTED, "bits"),
+    (dict(group=96), G.GPTQ_ERR_UNSUPPORTED, "group"),
+    (dict(group=256, block=96), G.GPTQ_ERR_UNSUPPORTED, "divide"),
+    (dict(m=48), G.GPTQ_ERR_UNSUPPORTED, "multiples of 32"),
+    (dict(dev=P + 16), G.GPTQ_ERR_INVALID_ARG, "256-byte aligned"),
+    (dict(devb=4096), G.GPTQ_ERR_WORKSPACE, "too small"),
+])
+def test_layer_host_argument_checks(kw, status, msg):
+    """gptq_quantize_layer_host rejects bad arguments before any copy or kernel."""
+    assert _call_host(**kw) == status
+    assert msg in G.gptq_last_error()
+
+
+def test_layer_host_size_and_the_other_additions():
+    lib = G.lib()
+    n = G.gptq_layer_host_size(16384, 8192, 28672, 4, 128, G.GPTQ_BF16, G.GPTQ_BF16)
+    # at least H, U, two staging chunks and W, and the largest of the three scratch uses
+    assert n >= 2 * 28672 ** 2 * 4 + 2 * 16384 * 28672 * 2 + 8192 * 28672 * 2 + \
+        G.gptq_workspace_size(G.GPTQ_OP_PREPARE, 0, 0, 28672)
+    assert G.gptq_layer_host_size(16384, 8192, 28672, 4, 128, G.GPTQ_F32, G.GPTQ_BF16) > n
+    assert G.gptq_layer_host_size(0, 64, 256, 4, 128, 1, 1) == 0
+    assert G.gptq_layer_host_size(1024, 64, 250, 4, 128, 1, 1) == 0
+    assert G.gptq_layer_host_size(1024, 64, 256, 5, 128, 1, 1) == 0
+    # gptq_hessian_rescale and gptq_check_wait_timeout check their arguments first
+    assert lib.gptq_hessian_rescale(None, 256, 1, 2, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_rescale(P, 256, 1, 0, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_rescale(P, 256, -1, 2, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_rescale(P, 100, 1, 2, None) == G.GPTQ_ERR_UNSUPPORTED
+    assert lib.gptq_hessian_rescale(P + 4, 256, 1, 2, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_check_wait_timeout(0, P, 256, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_check_wait_timeout(2 * 10 ** 9, P, 256, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_check_wait_timeout(1000, P + 8, 256, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_check_wait_timeout(1000, P, 16, None) == G.GPTQ_ERR_INVALID_ARG
