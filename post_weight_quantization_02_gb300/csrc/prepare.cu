@@ -518,21 +518,26 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
               Hr);
 
   // Cholesky of Hr (lower, in place) by NB-wide panels, right-looking with one panel of
-  // look-ahead.  Stream A carries the critical chain: factor and invert the diagonal
-  // block, solve the panel below it, apply the panel's update to the next block column
-  // only (the near update).  Stream C applies the rest of the panel's update (the far
-  // update, block columns >= kb + 2) behind it.  Ordering: block column kb is final
-  // once the near update of kb - 1 (stream A, in order) and the far update of kb - 2 have
-  // run; the near update of kb writes block column kb + 1, which the far update of
-  // kb - 1 also writes, so it waits for that one.  A failing pivot at reversed position
-  // a reports processing position d - a (1-based).
+  // look-ahead, the panels grouped into superpanels of nbs columns (NBS on wide layers,
+  // the whole matrix below kSuperpanelFrom).  Stream A carries the critical chain: factor
+  // and invert the diagonal block, solve the panel below it, apply the panel's update to
+  // the next block column only (the near update).  Stream C applies the rest of the
+  // panel's update inside its superpanel (the far update) behind it.  Ordering: block
+  // column kb is final once the near update of kb - 1 (stream A, in order) and the far
+  // update of kb - 2 have run; the near update of kb writes block column kb + 1, which the
+  // far update of kb - 1 also writes, so it waits for that one.  At a superpanel's end its
+  // panels' update of every later column is applied at once (K = the superpanel's width):
+  // the next superpanel's columns on stream A, the rest on stream C, each after the
+  // previous superpanel's far update that wrote the same columns.  A failing pivot at
+  // reversed position a reports processing position d - a (1-based).
   //
   // Stream B inverts the factor meanwhile: block column kb of the inverse needs only L's
   // first kb + 1 block columns, so it runs as soon as panel kb is final.  The inverse
   // X = L^-1 is kept transposed as Y = X^T in S so that both GEMM operands are K-major:
   // block column i of Y is Y[:, i] = R DI[i]^T (R = the accumulated right-hand side,
-  // initially I), after which every later block column loses Y[:, i] L[r, i]^T.
-  // Finally U = J X J = (J Y J)^T.
+  // initially I), after which every later block column loses Y[:, i] L[r, i]^T (inside
+  // the superpanel per panel, past it once per superpanel).  Finally U = J X J =
+  // (J Y J)^T.
   // The diagonal block's CTA asks for all of an SM's shared memory, so that no GEMM CTA
   // of the other streams shares its SM: its chain of dependent steps runs about 15 %
   // slower beside one.
