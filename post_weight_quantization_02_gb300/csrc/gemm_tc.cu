@@ -288,26 +288,32 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
 
 // For K >= 256 (a superpanel's aggregated updates, K = 1024) the lo parts of both
 // operands come precomputed from global memory (each operand element is split once, not
-// once per tile that reads it), and a warp-specialised kernel keeps the tensor core fed.
-// Shared memory is the bound of the tf32x3 product: per K-quarter the MMAs read hi and lo
-// of A and B three times over, so with the split done elsewhere the traffic per quarter
-// is the TMA's writes plus those reads; a 128 x 256 tile (TNX = 256) reuses each A
-// quarter over twice the columns.
-//   warp 0       TMA producer: A hi, A lo, B hi, B lo quarters into stage q % NS
-//   warp 1       TMEM owner (two TNX-column accumulators) and MMA issuer
-//   warp 2       waits for each quarter's copies (and, at a chain start, for its
-//                accumulator to be drained) and releases warp 1 through a named barrier,
-//                so that the issuing warp never waits on an mbarrier
-//   warps 3..10  drain each finished chain from TMEM into registers (round-to-nearest
-//                adds) while the next chain accumulates in the other half; write the tile
-template <int TNX>
-struct Presplit {
-  static constexpr int A_B = TM * KQ * 4;                   // 16 KB per part
-  static constexpr int B_B = TNX * KQ * 4;                  // 16 or 32 KB per part
-  static constexpr int STAGE = 2 * A_B + 2 * B_B;           // A hi, A lo, B hi, B lo
-  static constexpr int NS = (TNX == 128) ? 3 : 2;
+// once per tile that reads it), and a warp-specialised kernel on pairs of SMs keeps the
+// tensor core fed.  What bounds the tf32x3 product is the operand bytes that must reach
+// an SM per MMA cycle: a unit is one 256 x 256 tile of C computed by a cluster of two
+// CTAs with paired-SM MMAs (tcgen05.mma.cta_group::2, M = 256): the even CTA's TMEM holds
+// rows 0..127 of the tile and the odd CTA's rows 128..255, each CTA's shared memory holds
+// its own 128 rows of A and one half (128 rows) of B, hi and lo, and the tensor cores of
+// the pair read each other's half of B.  Per K-quarter an SM then receives 64 KB for
+// 1536 MMA cycles, two thirds of what a one-SM 128 x 256 tile needs.
+//   warp 0       TMA producer (both CTAs): A hi, A lo, B hi, B lo quarters into stage
+//                q % NS, completion counted on the even CTA's barrier
+//   warp 1       TMEM owner (both CTAs, paired allocation of two 256-column
+//                accumulators); in the even CTA also the MMA issuer
+//   warp 2       in the even CTA: waits for each quarter's copies (and, at a chain start,
+//                for its accumulator to be drained by both CTAs) and releases warp 1
+//                through a named barrier, so that the issuing warp never waits on an
+//                mbarrier
+//   warps 3..10  (both CTAs) drain each finished chain from TMEM into registers
+//                (round-to-nearest adds) while the next chain accumulates in the other
+//                accumulator; write the CTA's 128 x 256 part of the tile
+struct PresplitPair {
+  static constexpr int PART = TM * KQ * 4;   // 16 KB: 128 rows x one K-quarter
+  static constexpr int STAGE = 4 * PART;     // A hi, A lo, B hi, B lo (this CTA's half)
+  static constexpr int NS = 3;
+  static constexpr int TNP = 256;            // columns of a unit
   static constexpr int WORKERS = 8;
-  static constexpr int COLS = TNX / 2;                      // columns per worker thread
+  static constexpr int COLS = TNP / 2;       // columns per worker thread
   static constexpr int THREADS = 32 * (3 + WORKERS);
   static constexpr int SMEM = NS * STAGE + 1024 + 256;
   static_assert(SMEM <= 232448, "shared memory of one CTA");
@@ -316,19 +322,18 @@ struct Presplit {
 constexpr uint32_t kPsHandoff = 1;  // named barrier of warps 1 and 2
 
 struct PresplitArgs {
-  TcGemmArgs g;
+  TcGemmArgs g;            // n_tiles: column tiles of 256
   int a_lo_row0, a_lo_k0;  // the lo parts' offsets in their own maps
   int b_lo_row0, b_lo_k0;
 };
 
-template <int TNX>
-__global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREADS, 1)
     gemm_tf32x3_presplit_kernel(const __grid_constant__ CUtensorMap tma,
                                 const __grid_constant__ CUtensorMap tma_lo,
                                 const __grid_constant__ CUtensorMap tmb,
                                 const __grid_constant__ CUtensorMap tmb_lo,
                                 const __grid_constant__ CUtensorMap tmc, const PresplitArgs pa) {
-  using P = Presplit<TNX>;
+  using P = PresplitPair;
   const TcGemmArgs& g = pa.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -340,46 +345,51 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // tile: row tile bi (128 rows), column tile bj (TNX columns); in lower mode only the
-  // tiles that reach the diagonal or below it (bj * TNX <= bi * 128 + 127)
-  int bi = 0, bj = 0;
+  // unit: row pair pi (256 rows), column tile bj (256 columns); in lower mode only the
+  // units that reach the diagonal or below it (bj <= pi)
+  const int unit = static_cast<int>(blockIdx.x / 2);
+  int pi = 0, bj = 0;
   if (g.lower) {
-    int rem = static_cast<int>(blockIdx.x);
-    for (;; ++bi) {
-      const int cnt = min((bi * TM + TM - 1) / TNX + 1, g.n_tiles);
+    int rem = unit;
+    for (;; ++pi) {
+      const int cnt = min(pi + 1, g.n_tiles);
       if (rem < cnt) { bj = rem; break; }
       rem -= cnt;
     }
   } else {
-    bi = blockIdx.x / g.n_tiles;
-    bj = blockIdx.x % g.n_tiles;
+    pi = unit / g.n_tiles;
+    bj = unit % g.n_tiles;
   }
-  const int i0 = bi * TM, j0 = bj * TNX;
+  const int crank = static_cast<int>(tc::cluster_ctarank());
+  const int i0 = pi * 2 * TM + crank * TM;   // this CTA's rows of C
+  const int j0 = bj * P::TNP;                // the unit's columns of C
+  const int jb = j0 + crank * (P::TNP / 2);  // this CTA's half of B
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::NS; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&full[s], 1);   // the even CTA's: both CTAs' bytes
+      tc::mbar_init(&empty[s], 1);  // the pair's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
-      tc::mbar_init(&accempty[b], P::WORKERS);
+      tc::mbar_init(&accempty[b], 2 * P::WORKERS);  // the even CTA's: both CTAs' workers
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 2 * TNX);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(tmem_slot, 2 * P::TNP);
+    tc::tmem_relinquish_pair();
   }
   // no thread touches global memory before the previous kernel in the stream is done
   griddep_wait();
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // both CTAs' barriers exist before either copies into them
   tc::fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  constexpr uint32_t IDESC = idesc_tf32(TM, TNX, false);
+  constexpr uint32_t IDESC = idesc_tf32(2 * TM, P::TNP, false);  // paired: M = 256
   const int nq = g.nq;
   bool ok = true;
 
@@ -391,19 +401,17 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
         const uint32_t ph = static_cast<uint32_t>(q / P::NS) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* base = smem + s * P::STAGE;
-        tc::mbar_arrive_expect_tx(&full[s], P::STAGE);
-        tc::tma_load_2d(base, &tma, &full[s], g.a_k0 + q * KQ, g.a_row0 + i0);
-        tc::tma_load_2d(base + P::A_B, &tma_lo, &full[s], pa.a_lo_k0 + q * KQ, pa.a_lo_row0 + i0);
-#pragma unroll
-        for (int h = 0; h < TNX / 128; ++h) {
-          tc::tma_load_2d(base + 2 * P::A_B + h * A_BYTES, &tmb, &full[s], g.b_k0 + q * KQ,
-                          g.b_row0 + j0 + 128 * h);
-          tc::tma_load_2d(base + 2 * P::A_B + P::B_B + h * A_BYTES, &tmb_lo, &full[s],
-                          pa.b_lo_k0 + q * KQ, pa.b_lo_row0 + j0 + 128 * h);
-        }
+        const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[s]), 0);
+        if (crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * P::STAGE);
+        tc::tma_load_2d_pair(base, &tma, bar, g.a_k0 + q * KQ, g.a_row0 + i0);
+        tc::tma_load_2d_pair(base + P::PART, &tma_lo, bar, pa.a_lo_k0 + q * KQ,
+                             pa.a_lo_row0 + i0);
+        tc::tma_load_2d_pair(base + 2 * P::PART, &tmb, bar, g.b_k0 + q * KQ, g.b_row0 + jb);
+        tc::tma_load_2d_pair(base + 3 * P::PART, &tmb_lo, bar, pa.b_lo_k0 + q * KQ,
+                             pa.b_lo_row0 + jb);
       }
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (crank == 0 && (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------ MMA issuer and waiter
     const bool waiter = (warp == 2);
     for (int q = 0; q < nq; ++q) {
@@ -421,8 +429,8 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
       if (!waiter && lane == 0) {
         tc::fence_after();
         const uint32_t ah = tc::smem_u32(smem + s * P::STAGE);
-        const uint32_t al = ah + P::A_B, bh = ah + 2 * P::A_B, bl = bh + P::B_B;
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TNX);
+        const uint32_t al = ah + P::PART, bh = ah + 2 * P::PART, bl = ah + 3 * P::PART;
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P::TNP);
 #pragma unroll
         for (int kk = 0; kk < KQ / 8; ++kk) {
           const uint64_t dah = tc::smem_desc(ah + 32 * kk, 16, 1024, tc::kSwizzle128B);
@@ -432,25 +440,26 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
           const uint32_t acc0 = ((q % CHAIN_Q) | kk) != 0 ? 1u : 0u;
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
               "l"(dah), "l"(dbh), "r"(IDESC), "r"(acc0)
               : "memory");
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
               "l"(dah), "l"(dbl), "r"(IDESC), "r"(1u)
               : "memory");
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+              "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
               "l"(dal), "l"(dbh), "r"(IDESC), "r"(1u)
               : "memory");
         }
-        tc::mma_commit(&empty[s]);
-        if (q % CHAIN_Q == CHAIN_Q - 1 || q == nq - 1) tc::mma_commit(&accfull[acc]);
+        tc::mma_commit_pair(&empty[s], static_cast<uint16_t>(0x3));
+        if (q % CHAIN_Q == CHAIN_Q - 1 || q == nq - 1)
+          tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3));
       }
     }
-  } else {
+  } else if (warp >= 3) {
     // ------------------------------------------------------------ workers
     const int wk = warp - 3;                       // 0 .. WORKERS - 1
     const int rq = warp % 4, half = wk / 4;        // TMEM lane quarter, column half
@@ -468,21 +477,21 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
       }
       tc::fence_after();
 #pragma unroll
-      for (int c = 0; c < P::COLS / 32; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld_32x32b_x32(tmem_w + static_cast<uint32_t>(acc * TNX) + 32 * c, r);
+      for (int c = 0; c < P::COLS / 16; ++c) {
+        uint32_t r[16];
+        tc::tmem_ld_32x32b_x16(tmem_w + static_cast<uint32_t>(acc * P::TNP) + 16 * c, r);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          accr[32 * c + j] = __fadd_rn(accr[32 * c + j], __uint_as_float(r[j]));
+        for (int j = 0; j < 16; ++j)
+          accr[16 * c + j] = __fadd_rn(accr[16 * c + j], __uint_as_float(r[j]));
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+      if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&accempty[acc]), 0));
     }
     if (ok) {
-      // every MMA has completed (the last chain's commit) and every copy was consumed:
-      // the stages hold the epilogue's boxes, COLS / 32 per worker warp
+      // every MMA of the pair has completed (the last chain's commit) and every copy was
+      // consumed: this CTA's stages hold the epilogue's boxes, COLS / 32 per worker warp
       const int row = i0 + 32 * rq + lane;
 #pragma unroll
       for (int c = 0; c < P::COLS / 32; ++c) {
@@ -502,7 +511,9 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
         }
         tc::fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0 && i0 + 32 * rq < g.M && j0 + colt < g.N) {
+        // in lower mode a box wholly above the diagonal adds only zeros: skip it
+        const bool live = !g.lower || j0 + colt <= i0 + 32 * rq + 31;
+        if (lane == 0 && live && i0 + 32 * rq < g.M && j0 + colt < g.N) {
           if (g.accumulate) tc::tma_reduce_add_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
           else tma_store_2d(&tmc, box, j0 + colt, i0 + 32 * rq);
           tc::bulk_commit_group();
@@ -518,16 +529,18 @@ __global__ void __launch_bounds__(Presplit<TNX>::THREADS, 1)
       dev_fail(g.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&g.st->timeouts, 1);
     }
+    // let copies and MMAs already in flight land before the CTA's memory goes away
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
   }
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
-    tc::tmem_dealloc(tmem_base, 2 * TNX);
+    tc::tmem_dealloc_pair(tmem_base, 2 * P::TNP);
   }
 }
 
@@ -602,30 +615,6 @@ void launch_split_lo(const float* src, int ld, int rows, int cols, float* lo, in
               ld_lo);
 }
 
-namespace {
-template <int TNX>
-void launch_presplit_t(int kind, const CUtensorMap& ma, const CUtensorMap& ma_lo,
-                       const CUtensorMap& mb, const CUtensorMap& mb_lo, const CUtensorMap& mc,
-                       const PresplitArgs& pa, int tm, cudaStream_t s, bool pdl) {
-  using P = Presplit<TNX>;
-  const int tn = pa.g.n_tiles;
-  unsigned grid = 0;
-  if (pa.g.lower) {
-    for (int bi = 0; bi < tm; ++bi) grid += static_cast<unsigned>(std::min((bi * TM + TM - 1) / TNX + 1, tn));
-  } else {
-    grid = static_cast<unsigned>(tm * tn);
-  }
-  ensure_dynamic_smem(gemm_tf32x3_presplit_kernel<TNX>, P::SMEM);
-  if (pdl) {
-    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_presplit_kernel<TNX>, grid, P::THREADS, P::SMEM, ma,
-                    ma_lo, mb, mb_lo, mc, pa);
-  } else {
-    GPTQ_LAUNCH(kind, s, gemm_tf32x3_presplit_kernel<TNX>, grid, P::THREADS, P::SMEM, ma, ma_lo,
-                mb, mb_lo, mc, pa);
-  }
-}
-}  // namespace
-
 void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                                  const CUtensorMap& ma_lo, int a_lo_row0, int a_lo_k0,
                                  const CUtensorMap& mb, int b_row0, int b_k0,
@@ -659,9 +648,25 @@ void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, in
   pa.a_lo_k0 = a_lo_k0;
   pa.b_lo_row0 = b_lo_row0;
   pa.b_lo_k0 = b_lo_k0;
-  const int tm = static_cast<int>(ceil_div(M, TM));
-  pa.g.n_tiles = static_cast<int>(ceil_div(N, kPresplitTN));
-  launch_presplit_t<kPresplitTN>(kind, ma, ma_lo, mb, mb_lo, mc, pa, tm, s, pdl);
+  using P = PresplitPair;
+  const int tp = static_cast<int>(ceil_div(M, 2 * TM));  // row pairs
+  const int tn = static_cast<int>(ceil_div(N, P::TNP));
+  pa.g.n_tiles = tn;
+  unsigned units = 0;
+  if (lower) {
+    for (int p = 0; p < tp; ++p) units += static_cast<unsigned>(std::min(p + 1, tn));
+  } else {
+    units = static_cast<unsigned>(tp * tn);
+  }
+  const unsigned grid = 2 * units;  // one cluster of two CTAs per unit
+  ensure_dynamic_smem(gemm_tf32x3_presplit_kernel, P::SMEM);
+  if (pdl) {
+    GPTQ_LAUNCH_PDL(kind, s, gemm_tf32x3_presplit_kernel, grid, P::THREADS, P::SMEM, ma, ma_lo,
+                    mb, mb_lo, mc, pa);
+  } else {
+    GPTQ_LAUNCH(kind, s, gemm_tf32x3_presplit_kernel, grid, P::THREADS, P::SMEM, ma, ma_lo, mb,
+                mb_lo, mc, pa);
+  }
 }
 
 }  // namespace gptq

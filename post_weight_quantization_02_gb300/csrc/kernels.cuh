@@ -89,9 +89,8 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                         cudaStream_t s, bool pdl);
 
 // gemm_tc.cu, long K: the same product with the lo parts of both operands precomputed
-// (lo = x - tf32(x), read through their own maps at their own offsets); tiles of 128 x
-// kPresplitTN.  launch_split_lo writes those lo parts for a rows x cols block.
-constexpr int kPresplitTN = 256;
+// (lo = x - tf32(x), read through their own maps at their own offsets); units of 256 x 256
+// on pairs of SMs.  launch_split_lo writes those lo parts for a rows x cols block.
 void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
                                  const CUtensorMap& ma_lo, int a_lo_row0, int a_lo_k0,
                                  const CUtensorMap& mb, int b_row0, int b_k0,
