@@ -5,30 +5,38 @@
 // Placement: GPTQ", section 1.4) for bf16 X, with float32 accumulation in TMEM.  Only
 // tiles that touch the upper 128-tile triangle are computed.
 //
-// Persistent, warp-specialised kernel, one CTA per SM, the CTAs in pairs (clusters of
-// two) that run paired-SM MMAs: a unit is one 256 x 256 tile of H (row tiles 2p, 2p+1 of
-// 128, column tile J of 256) for one token split s.  The even CTA's TMEM holds rows
-// 256p .. + 127, the odd CTA's the next 128; each CTA's shared memory holds its own 128
-// rows' operand and half of the 256-column operand, so an SM reads 32 KB of operands per
-// 64-token stage (48 KB for a one-SM 128 x 256 tile), which keeps the tensor core fed.
-//   warp 0      TMA producer (both CTAs): X tiles [64 tokens x 128 | 128 columns] into a
-//               6-stage ring; completion is counted on the even CTA's barrier
-//   warp 1      TMEM owner (both CTAs, paired allocation); in the even CTA also the MMA
+// Persistent, warp-specialised kernel, one CTA per SM, the CTAs in pairs that run
+// paired-SM MMAs, NP pairs per cluster (NP = 2 on wide layers, else 1).  A unit is a
+// 256 NP x 256 block of H (row tiles 2 NP Q .. 2 NP Q + 2 NP - 1 of 128, column tile J of
+// 256) for one token split s: pair p of the cluster computes the 256 x 256 tile of row
+// tiles 2 NP Q + 2p, + 1.  In a pair the even CTA's TMEM holds the first 128 rows and the
+// odd CTA's the next 128; each CTA's shared memory holds its own 128 rows' operand and
+// half of the 256-column operand, so an SM takes in 32 KB of operands per 64-token stage
+// (48 KB for a one-SM 128 x 256 tile).  With NP = 2 both pairs need the same column
+// strip: CTAs 0 and 2 hold its first half, CTAs 1 and 3 its second, and each half is read
+// from L2 once, by two multicast copies of one 64-column box each (a quarter less L2
+// traffic than two separate pairs; under the power cap the clock rises with it).
+//   warp 0      TMA producer (every CTA): its own X rows [64 tokens x 128 columns] and its
+//               column half (NP = 2: one box of it, multicast to the same-parity CTA of
+//               the other pair) into a 6-stage ring; completion is counted on the even CTA
+//               of each pair
+//   warp 1      TMEM owner (every CTA, paired allocation); in the even CTAs also the MMA
 //               issuer: tcgen05.mma.cta_group::2 256x256x16, both operands MN-major (the
 //               column index of X is contiguous in memory)
-//   warps 2..9  epilogue (both CTAs): drain finished TMEM accumulators into float32
-//               registers, then store the CTA's 128 x 256 part of the unit's tile of P[s]
-//   warp 10     in the even CTA: waits for two stages' data (and, at a chain start, for
+//   warps 2..9  epilogue (every CTA): drain finished TMEM accumulators into float32
+//               registers, then store the CTA's 128 x 256 part of its pair's tile of P[s]
+//   warp 10     in the even CTAs: waits for two stages' data (and, at a chain start, for
 //               the accumulator) and releases warp 1 through a named barrier.  The issuing
 //               warp never waits on an mbarrier: such a wait holds it until its
 //               outstanding MMAs have read their operands, which empties the tensor pipe.
 //               Two stages (8 MMAs) per hand-off keep the pipe fed across it.
-// A stage is refilled when the pair's MMAs have consumed it (the commit arrives on both
-// CTAs' barriers).  The tensor core's float32 accumulation does not round to nearest, so
-// its error grows with the length of an accumulation chain; each chain therefore covers
-// only a few stages (512 tokens) and is then added, with round-to-nearest float32 adds in
-// a fixed order, into the epilogue warps' registers.  Two 256-column TMEM accumulators
-// alternate between chains, so the MMAs of one chain overlap the drain of the previous one.
+// A stage is refilled when every pair's MMAs have consumed it (each pair's commit arrives
+// on every CTA's barrier of the cluster), since a multicast writes into the other pair's
+// ring.  The tensor core's float32 accumulation does not round to nearest, so its error
+// grows with the length of an accumulation chain; each chain therefore covers only a few
+// stages (512 tokens) and is then added, with round-to-nearest float32 adds in a fixed
+// order, into the epilogue warps' registers.  Two 256-column TMEM accumulators alternate
+// between chains, so the MMAs of one chain overlap the drain of the previous one.
 #include <cuda_bf16.h>
 
 #include <map>
@@ -64,28 +72,33 @@ struct SyrkArgs {
   int64_t tok_per_split;
   int n_i;       // row tiles of 128
   int n_j;       // column tiles of 256
-  int n_pairs;   // row-tile pairs of the tiles intersecting the upper 128-tile triangle
+  int n_units;   // units (NP pairs of row tiles) intersecting the upper 128-tile triangle
   int splits;
   float* P;      // [splits][d][d]
   DevStatus* st;
 };
 
-// pair p of column tile J: row tiles 2p and 2p + 1 (the second may lie past the last row
-// tile when a column tile has an odd count; its CTA then multiplies zeros and stores
-// nothing).  Units go column tile by column tile, so the units in flight at once share
-// their column strip of X.  (A banded order, 8 column tiles by row pair, which reads
-// fewer distinct strips per wave, measured 1.5-2 % slower at d_in = 28672.)
-__device__ __forceinline__ void decode_pair(int pair, int n_i, int n_j, int& P, int& J) {
-  int rem = pair;
+// unit Q of column tile J: row tiles 2 NP Q .. 2 NP Q + 2 NP - 1.  Row tiles past 2J + 1
+// (below the upper triangle, when NP = 2 and a column tile has an odd number of row-tile
+// pairs) or past the last row tile are computed all the same, on the matrix or on zeros,
+// so that every pair walks the same stages; the former land in the lower part of P[s],
+// which nothing reads, the latter are not stored.  Units go column tile by column tile, so
+// the units in flight at once share their column strip of X.  (A banded order of the
+// one-pair kernel, 8 column tiles by row pair, which read fewer distinct strips per wave,
+// measured 1.5-2 % slower at d_in = 28672.)
+template <int NP>
+__device__ __forceinline__ void decode_unit(int unit, int n_i, int n_j, int& Q, int& J) {
+  int rem = unit;
   for (J = 0; J < n_j; ++J) {
-    const int cnt = (min(2 * J + 2, n_i) + 1) / 2;
-    if (rem < cnt) { P = rem; return; }
+    const int cnt = ((min(2 * J + 2, n_i) + 1) / 2 + NP - 1) / NP;
+    if (rem < cnt) { Q = rem; return; }
     rem -= cnt;
   }
-  P = 0;
+  Q = 0;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+template <int NP>
+__global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
     syrk_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SyrkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -100,13 +113,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int crank = static_cast<int>(tc::cluster_ctarank());
-  const int64_t n_units = static_cast<int64_t>(a.n_pairs) * a.splits;
-  const int64_t unit0 = blockIdx.x / 2, unit_step = gridDim.x / 2;
+  const uint32_t lead = static_cast<uint32_t>(crank & ~1);  // the pair's even CTA
+  const int64_t n_units = static_cast<int64_t>(a.n_units) * a.splits;
+  const int64_t unit0 = blockIdx.x / (2 * NP), unit_step = gridDim.x / (2 * NP);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       tc::mbar_init(&full[s], 1);   // the even CTA's: both CTAs' bytes
-      tc::mbar_init(&empty[s], 1);  // the pair's MMA commit
+      tc::mbar_init(&empty[s], NP);  // every pair's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
@@ -132,10 +146,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
-      const int s = static_cast<int>(u / a.n_pairs);
-      int pp, J;
-      decode_pair(static_cast<int>(u % a.n_pairs), a.n_i, a.n_j, pp, J);
-      const int I = 2 * pp + crank;
+      const int s = static_cast<int>(u / a.n_units);
+      int qq, J;
+      decode_unit<NP>(static_cast<int>(u % a.n_units), a.n_i, a.n_j, qq, J);
+      const int I = 2 * NP * qq + crank;
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
@@ -144,17 +158,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         // both CTAs' 32 KB land on the even CTA's barrier
-        const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
-        if (crank == 0) tc::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+        const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[stage]), lead);
+        if ((crank & 1) == 0) tc::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
         const int tok = static_cast<int>(t0 + static_cast<int64_t>(kb) * BK);
         tc::tma_load_2d_pair(sa, &tmap, bar, I * BM, tok);
         tc::tma_load_2d_pair(sa + BOX_BYTES, &tmap, bar, I * BM + 64, tok);
-        tc::tma_load_2d_pair(sb, &tmap, bar, J * BN + 128 * crank, tok);
-        tc::tma_load_2d_pair(sb + BOX_BYTES, &tmap, bar, J * BN + 128 * crank + 64, tok);
+        if constexpr (NP == 1) {
+          tc::tma_load_2d_pair(sb, &tmap, bar, J * BN + 128 * crank, tok);
+          tc::tma_load_2d_pair(sb + BOX_BYTES, &tmap, bar, J * BN + 128 * crank + 64, tok);
+        } else {
+          // the CTAs 0, 2 (1, 3) share their half of the column strip: each loads one box
+          // of it into both
+          const int hb = crank >> 1;
+          tc::tma_load_2d_pair_mc(sb + hb * BOX_BYTES, &tmap, bar,
+                                  J * BN + 128 * (crank & 1) + 64 * hb, tok,
+                                  static_cast<uint16_t>(0x5u << (crank & 1)));
+        }
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
       }
     }
-  } else if (crank == 0 && (warp == 1 || warp == WAITER_WARP)) {
+  } else if ((crank & 1) == 0 && (warp == 1 || warp == WAITER_WARP)) {
     // ---------------------------------------------------------------- MMA issuer and its
     // waiter (even CTA): both walk the same stages, two per hand-off; the waiter's lane 0
     // waits, then both warps meet at the named barrier, which also carries a failed wait
@@ -164,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t accphase = 0;
     for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
-      const int s = static_cast<int>(u / a.n_pairs);
+      const int s = static_cast<int>(u / a.n_units);
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
@@ -197,9 +220,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const uint64_t bd = tc::smem_desc(bbase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
               tc::mma_f16_pair(d_tmem, ad, bd, IDESC, (kc | kk) != 0 ? 1u : 0u);
             }
-            tc::mma_commit_pair(&empty[stage], static_cast<uint16_t>(0x3));
+            tc::mma_commit_pair(&empty[stage], static_cast<uint16_t>((1u << (2 * NP)) - 1));
             if (kc == CHAIN - 1 || kq == nk - 1)
-              tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3));
+              tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3u << lead));
           }
           if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
           if (kc == CHAIN - 1 || kq == nk - 1) {
@@ -216,10 +239,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t accphase = 0;
     for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
-      const int s = static_cast<int>(u / a.n_pairs);
-      int pp, J;
-      decode_pair(static_cast<int>(u % a.n_pairs), a.n_i, a.n_j, pp, J);
-      const int I = 2 * pp + crank;
+      const int s = static_cast<int>(u / a.n_units);
+      int qq, J;
+      decode_unit<NP>(static_cast<int>(u % a.n_units), a.n_i, a.n_j, qq, J);
+      const int I = 2 * NP * qq + crank;
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
@@ -243,7 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&accempty[acc]), 0));
+        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&accempty[acc]), lead));
         acc ^= 1;
         if (acc == 0) accphase ^= 1u;
       }
@@ -286,17 +309,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-// CTAs' tiles per token split (pairs of row tiles, the odd tile of a column padded)
+// CTAs' tiles per token split (units of NP pairs of row tiles, a column's last unit
+// padded).  Wide layers take clusters of two pairs (NP = 2): their Hessian streams run for
+// seconds under the power cap, where the shared column strip's multicast (a quarter less
+// L2 traffic) buys clock (70B-width down_proj: 337 against 350 ms per 524,288 tokens).  A
+// cluster of four needs four SMs of one GPC, which leaves 8 of the 152 SMs idle, so the
+// short Hessians of narrower layers, which run at full clock, keep one pair per cluster
+// (q_proj: 2.74 against 2.83 ms).
+static int syrk_pairs_per_cluster(int d) { return d >= 8192 ? 2 : 1; }
+
 int syrk_tc_tiles(int d) {
+  const int np = syrk_pairs_per_cluster(d);
   const int n_i = (d + BM - 1) / BM, n_j = (d + BN - 1) / BN;
   int n = 0;
-  for (int J = 0; J < n_j; ++J) n += 2 * ((((2 * J + 2 < n_i) ? 2 * J + 2 : n_i) + 1) / 2);
+  for (int J = 0; J < n_j; ++J) {
+    const int pairs = (((2 * J + 2 < n_i) ? 2 * J + 2 : n_i) + 1) / 2;
+    n += 2 * np * ((pairs + np - 1) / np);
+  }
   return n;
 }
 
 int syrk_tc_token_granule() { return BK; }
 
 namespace {
+template <int NP>
 int resident_clusters() {
   static std::mutex mu;
   static std::map<int, int> per_dev;  // device -> co-resident clusters of the kernel
@@ -304,25 +340,38 @@ int resident_clusters() {
   GPTQ_CUDA(cudaGetDevice(&dev));
   std::lock_guard<std::mutex> lock(mu);
   int& r = per_dev[dev];
+  const int most = sm_count() / (2 * NP);
   if (r <= 0) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * NP * most));
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel<NP>, &cfg) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
-      n = sm_count() / 2;
+      n = most;
     }
-    r = n < sm_count() / 2 ? n : sm_count() / 2;
+    r = n < most ? n : most;
   }
   return r;
+}
+
+template <int NP>
+void launch_syrk_np(const CUtensorMap& tmap, SyrkArgs a, cudaStream_t s) {
+  ensure_dynamic_smem(syrk_tc_kernel<NP>, SMEM_BYTES);
+  a.n_units = syrk_tc_tiles(a.d) / (2 * NP);
+  // one cluster of 2 NP CTAs per unit, no more clusters than can be resident at once (a
+  // cluster needs 2 NP SMs of one GPC, so that may be fewer than the SMs allow); the
+  // count is looked up once per device
+  const int64_t units = static_cast<int64_t>(a.n_units) * a.splits;
+  const int64_t clusters = resident_clusters<NP>();
+  const int grid = 2 * NP * static_cast<int>(units < clusters ? units : clusters);
+  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel<NP>, grid, THREADS, SMEM_BYTES, tmap, a);
 }
 }  // namespace
 
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s) {
-  ensure_dynamic_smem(syrk_tc_kernel, SMEM_BYTES);
   CUtensorMap tmap;
   make_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(d),
                static_cast<uint64_t>(ntok), static_cast<uint64_t>(d) * 2, 64, BK,
@@ -333,18 +382,12 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.tok_per_split = tok_per_split;
   a.n_i = (d + BM - 1) / BM;
   a.n_j = (d + BN - 1) / BN;
-  a.n_pairs = syrk_tc_tiles(d) / 2;
+  a.n_units = 0;
   a.splits = splits;
   a.P = P;
   a.st = st;
-  // one cluster of two CTAs per pair unit, no more clusters than can be resident at once
-  // (a cluster needs two SMs of one GPC, so that may be fewer than half the SMs); the
-  // count is looked up once per device
-  const int resident = resident_clusters();
-  const int64_t units = static_cast<int64_t>(a.n_pairs) * splits;
-  const int64_t clusters = resident;
-  const int grid = 2 * static_cast<int>(units < clusters ? units : clusters);
-  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel, grid, THREADS, SMEM_BYTES, tmap, a);
+  if (syrk_pairs_per_cluster(d) == 2) launch_syrk_np<2>(tmap, a, s);
+  else launch_syrk_np<1>(tmap, a, s);
 }
 
 }  // namespace gptq

@@ -172,6 +172,19 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// The same load multicast to the CTAs of cta_mask (the same shared-memory offset in each);
+// every destination's bytes are counted on the barrier at bar_cluster's offset in that
+// destination's own pair (its even CTA when bar_cluster names the issuer's even CTA).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
+                                                    uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

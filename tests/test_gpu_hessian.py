@@ -37,6 +37,43 @@ def test_hessian_small(lib, cuda_device, dtype, d, ntok):
     assert np.all(np.isfinite(H[mask]))
 
 
+@pytest.mark.parametrize("d,ntok", [(8264, 6000), (8192, 5000)])
+def test_hessian_wide_clusters(lib, cuda_device, d, ntok):
+    """Wide layers (d_in >= 8192) run the SYRK in clusters of two SM pairs that share the
+    column strip by multicast: a ragged last row and column tile (8264 = 64 * 128 + 72),
+    the padded units of column tiles with an odd number of row-tile pairs, and two token
+    splits added by the reduction (8192).  Sampled 128-blocks (the first, the last on the
+    diagonal, blocks of the last column tile and of padded units) against the float64
+    Hessian of their columns; the whole diagonal and two quadratic forms against the
+    float64 sums."""
+    g = torch.Generator().manual_seed(d + ntok)
+    X = (torch.randn(ntok, d, generator=g) * torch.exp(0.5 * torch.randn(d, generator=g)))
+    X = X.bfloat16()
+    H, n = _accumulate(lib, [X], d, cuda_device)
+    assert n == ntok
+    Xd = X.double().numpy()
+    nb = -(-d // 128)
+    picks = [(0, 0), (1, 1), (nb - 1, nb - 1), (0, nb - 1), (nb - 2, nb - 1), (2, 2), (3, 4),
+             (4, 5), (5, 5), (1, 60), (62, 63), (30, 31)]
+    mask = upper_tile_mask(d)
+    num = den = 0.0
+    for bi, bj in picks:
+        r, c = slice(128 * bi, min(d, 128 * bi + 128)), slice(128 * bj, min(d, 128 * bj + 128))
+        ref = (2.0 / ntok) * (Xd[:, r].T @ Xd[:, c])
+        got = H[r, c].astype(np.float64)
+        assert np.all(mask[r, c]) and np.all(np.isfinite(got))
+        num += float(np.sum((got - ref) ** 2))
+        den += float(np.sum(ref ** 2))
+    assert np.sqrt(num / den) <= H_REL_FRO
+    diag_ref = (2.0 / ntok) * np.sum(Xd * Xd, axis=0)
+    assert np.max(np.abs(np.diag(H) - diag_ref) / diag_ref) <= 1e-5
+    Hs = np.where(mask, H, H.T).astype(np.float64)  # the symmetric H from its upper tiles
+    for seed in range(2):
+        v = np.random.default_rng(seed).standard_normal(d)
+        ref = (2.0 / ntok) * float(np.sum((Xd @ v) ** 2))
+        assert abs(float(v @ Hs @ v) - ref) <= 1e-5 * abs(ref)
+
+
 def test_hessian_streaming_chunks(lib, cuda_device):
     """Three uneven calls follow the hook's recurrence (H <- H n/(n+t) + 2/(n+t) X^T X)."""
     d = 384
