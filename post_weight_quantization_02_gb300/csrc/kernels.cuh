@@ -116,6 +116,8 @@ struct LazyMaps {
 LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int erows,
                         const __nv_bfloat16* uhi, const __nv_bfloat16* ulo, float* W, int m,
                         int d);
+// bf16 halves of U (x = hi + lo) on the blocks the lazy updates read: row i, columns from
+// the 128-column block after row i's block on (d a multiple of 8)
 void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s);
 // W[:, c_begin:c_end] -= ErrT[e_row0 : e_row0 + k]^T U[u_row0 : u_row0 + k, c_begin:c_end];
 // max_ctas > 0 caps the persistent grid (to leave SMs to concurrent work)

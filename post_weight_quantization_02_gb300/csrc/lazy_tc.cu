@@ -243,24 +243,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// hi = bf16(x), lo = bf16(x - hi) for the strict upper triangle of U (0 elsewhere).
-__global__ void usplit_kernel(const float* __restrict__ U, int d, __nv_bfloat16* __restrict__ hi,
-                              __nv_bfloat16* __restrict__ lo) {
-  const int i = blockIdx.y;
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
-  const size_t o = static_cast<size_t>(i) * d + j;
-  const float x = (j > i) ? U[o] : 0.0f;
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  hi[o] = h;
-  lo[o] = __float2bfloat16_rn(x - __bfloat162float(h));
+// hi = bf16(x), lo = bf16(x - hi) for the part of U that the lazy updates read: row i,
+// columns from the first 128-column block past row i's block (an update takes U rows of
+// its blocks and columns of later blocks only).  The rest of hi and lo is left unwritten.
+// One CTA per row, 8 elements per thread and step: two 16-byte loads, two 16-byte stores
+// (d a multiple of 8, rows 16-byte aligned).
+__global__ void __launch_bounds__(256) usplit_kernel(const float* __restrict__ U, int d,
+                                                     __nv_bfloat16* __restrict__ hi,
+                                                     __nv_bfloat16* __restrict__ lo) {
+  const int i = blockIdx.x;
+  const size_t row = static_cast<size_t>(i) * d;
+  for (int j = (i / 128 + 1) * 128 + 8 * static_cast<int>(threadIdx.x); j < d; j += 8 * 256) {
+    const float4 x0 = *reinterpret_cast<const float4*>(U + row + j);
+    const float4 x1 = *reinterpret_cast<const float4*>(U + row + j + 4);
+    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    __align__(16) __nv_bfloat16 h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      h[k] = __float2bfloat16_rn(x[k]);
+      l[k] = __float2bfloat16_rn(x[k] - __bfloat162float(h[k]));
+    }
+    *reinterpret_cast<uint4*>(hi + row + j) = *reinterpret_cast<const uint4*>(h);
+    *reinterpret_cast<uint4*>(lo + row + j) = *reinterpret_cast<const uint4*>(l);
+  }
 }
 
 }  // namespace
 
 void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s) {
-  dim3 grid((unsigned)ceil_div(d, 256), d);
-  GPTQ_LAUNCH(GPTQ_K_QUANT_SPLIT, s, usplit_kernel, grid, 256, 0, U, d, hi, lo);
+  if (d % 8 != 0) fail(GPTQ_ERR_INVALID_ARG, "launch_usplit: d must be a multiple of 8");
+  GPTQ_LAUNCH(GPTQ_K_QUANT_SPLIT, s, usplit_kernel, static_cast<unsigned>(d), 256, 0, U, d, hi,
+              lo);
 }
 
 LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int erows,
