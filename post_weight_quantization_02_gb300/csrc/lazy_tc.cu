@@ -11,20 +11,31 @@
 // accumulated in float32 TMEM as hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-16
 // relative, is dropped).
 //
-// Persistent kernel, one CTA per SM, one output tile (128 rows x 256 columns) per unit,
-// K in chunks of 64 through a two-stage operand pipeline:
-//   warp 0      TMA: ErrT hi/lo [64 k x 128 rows] and U hi/lo [64 k x 256 columns] per
-//               chunk, both MN-major, 96 KB per stage
-//   warp 1      TMEM owner and MMA issuer: 4 k-steps x 3 tcgen05.mma 128x256x16 per chunk
-//   warp 10     waits for each chunk's data (and, per tile, for the accumulator) and
-//               releases warp 1 through a named barrier, so that the issuing warp never
-//               waits on an mbarrier (which would drain the tensor pipe each chunk)
-//   warps 2..9  epilogue: TMEM -> registers -> -D into a swizzled shared box -> TMA
-//               reduce-add into W.  The memory system applies W += (-D) (one rounding,
-//               as a float32 subtraction); the SM never reads W.
+// Persistent kernel on pairs of SMs (clusters of two CTAs, one per SM) running paired
+// MMAs: a unit is one 256 x 256 tile of W, the even CTA's TMEM holding rows 0..127 of it
+// and the odd CTA's rows 128..255.  K goes in chunks of 64 through a three-stage operand
+// pipeline; each CTA's stage holds its own 128 rows of ErrT and one half (128 columns) of
+// U, hi and lo, 64 KB, and the tensor cores of the pair read each other's half of U.  Per
+// chunk an SM so takes in 64 KB for 1536 MMA cycles, two thirds of what a one-SM
+// 128 x 256 tile needs (the operand bytes that reach an SM per MMA cycle bound this
+// product).
+//   warp 0      TMA (both CTAs): ErrT hi/lo [64 k x 128 rows] and U hi/lo [64 k x 128
+//               columns] per chunk, both MN-major; completion on the even CTA's barrier
+//   warp 1      TMEM owner (both CTAs, paired allocation); in the even CTA also the MMA
+//               issuer: 4 k-steps x 3 tcgen05.mma.cta_group::2 256x256x16 per chunk
+//   warp 10     in the even CTA: waits for each chunk's data (and, per tile, for the
+//               accumulator) and releases warp 1 through a named barrier, so that the
+//               issuing warp never waits on an mbarrier (which would drain the tensor pipe
+//               each chunk)
+//   warps 2..9  epilogue (both CTAs): TMEM -> registers -> -D into a swizzled shared box
+//               -> TMA reduce-add into W.  The memory system applies W += (-D) (one
+//               rounding, as a float32 subtraction); the SM never reads W.
 // Two 256-column TMEM accumulators let the epilogue of one tile overlap the MMAs of the
 // next.
 #include <cuda_bf16.h>
+
+#include <map>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -34,19 +45,19 @@ namespace gptq {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BN = 256, BK = 64;      // BM rows per CTA, 2 BM per unit
 constexpr int BOX = 64 * 64 * 2;                 // one TMA box: 64 x 64 bf16
 constexpr int A_PART = BM * BK * 2;              // per part (hi or lo): 16 KB
-constexpr int B_PART = BN * BK * 2;              // 32 KB
-constexpr int STAGE = 2 * A_PART + 2 * B_PART;   // 96 KB
-constexpr int NSTAGE = 2;
+constexpr int B_PART = (BN / 2) * BK * 2;        // this CTA's half of U: 16 KB
+constexpr int STAGE = 2 * A_PART + 2 * B_PART;   // 64 KB
+constexpr int NSTAGE = 3;
 constexpr int EPI_WARPS = 8;
 constexpr int STG_BYTES = 32 * 32 * 4;           // per epilogue warp: 32 rows x 32 columns
 constexpr int SMEM_BYTES = NSTAGE * STAGE + EPI_WARPS * STG_BYTES + 1024 + 256;
 constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
 constexpr int WAITER_WARP = 2 + EPI_WARPS;
 constexpr uint32_t kHandoffBarrier = 1;  // named barrier of warps 1 and WAITER_WARP
-constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, true, true);
+constexpr uint32_t IDESC = tc::idesc_bf16_f32(2 * BM, BN, true, true);  // paired: M = 256
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 
 struct LazyArgs {
@@ -56,7 +67,7 @@ struct LazyArgs {
   int nk;          // K / 64
   int c_begin;     // first W column updated
   int c_end;       // columns >= c_end are left alone
-  int n_mt, n_nt;  // row tiles, column tiles
+  int n_mt, n_nt;  // row-tile pairs (256 rows), column tiles
   DevStatus* st;
 };
 
@@ -68,7 +79,7 @@ __device__ __forceinline__ uint32_t b_off(int p, int h) {
   return static_cast<uint32_t>(2 * A_PART + p * B_PART + h * BOX);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     lazy_tc_kernel(const __grid_constant__ CUtensorMap tm_ehi, const __grid_constant__ CUtensorMap tm_elo,
                    const __grid_constant__ CUtensorMap tm_uhi, const __grid_constant__ CUtensorMap tm_ulo,
                    const __grid_constant__ CUtensorMap tm_w, const LazyArgs a) {
@@ -84,26 +95,29 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int crank = static_cast<int>(tc::cluster_ctarank());
   const int n_units = a.n_mt * a.n_nt;
+  const int unit0 = static_cast<int>(blockIdx.x / 2), unit_step = static_cast<int>(gridDim.x / 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&full[s], 1);   // the even CTA's: both CTAs' bytes
+      tc::mbar_init(&empty[s], 1);  // the pair's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accfull[b], 1);
-      tc::mbar_init(&accempty[b], EPI_WARPS);
+      tc::mbar_init(&accempty[b], 2 * EPI_WARPS);  // the even CTA's: both CTAs' epilogues
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 512);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(tmem_slot, 512);
+    tc::tmem_relinquish_pair();
   }
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // both CTAs' barriers exist before either copies into them
   tc::fence_after();
   const uint32_t tmem_base = *tmem_slot;
   bool ok = true;
@@ -111,27 +125,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < n_units && ok; u += unit_step) {
       const int mt = u % a.n_mt, nt = u / a.n_mt;
-      const int r0 = mt * BM, c0 = a.c_begin + nt * BN;
+      const int r0 = mt * 2 * BM + crank * BM;                 // this CTA's rows of W
+      const int c0 = a.c_begin + nt * BN + crank * (BN / 2);   // this CTA's half of U
       for (int kc = 0; kc < a.nk; ++kc, ++it) {
         const int s = static_cast<int>(it % NSTAGE);
         const uint32_t ph = (it / NSTAGE) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* base = smem + s * STAGE;
-        tc::mbar_arrive_expect_tx(&full[s], STAGE);
+        const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[s]), 0);
+        if (crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);
         const int ke = a.e_row0 + kc * BK, ku = a.u_row0 + kc * BK;
         for (int h = 0; h < 2; ++h) {
-          tc::tma_load_2d(base + a_off(0, h), &tm_ehi, &full[s], r0 + 64 * h, ke);
-          tc::tma_load_2d(base + a_off(1, h), &tm_elo, &full[s], r0 + 64 * h, ke);
-        }
-        for (int h = 0; h < 4; ++h) {
-          tc::tma_load_2d(base + b_off(0, h), &tm_uhi, &full[s], c0 + 64 * h, ku);
-          tc::tma_load_2d(base + b_off(1, h), &tm_ulo, &full[s], c0 + 64 * h, ku);
+          tc::tma_load_2d_pair(base + a_off(0, h), &tm_ehi, bar, r0 + 64 * h, ke);
+          tc::tma_load_2d_pair(base + a_off(1, h), &tm_elo, bar, r0 + 64 * h, ke);
+          tc::tma_load_2d_pair(base + b_off(0, h), &tm_uhi, bar, c0 + 64 * h, ku);
+          tc::tma_load_2d_pair(base + b_off(1, h), &tm_ulo, bar, c0 + 64 * h, ku);
         }
       }
     }
-  } else if (warp == 1 || warp == WAITER_WARP) {
+  } else if (crank == 0 && (warp == 1 || warp == WAITER_WARP)) {
     // ------------------------------------------------------------ MMA issuer and its
     // waiter: both walk the same chunks; the waiter's lane 0 waits, then both warps meet
     // at the named barrier, which also carries a failed wait
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t accphase = 0;
     const uint32_t sbase = tc::smem_u32(smem);
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < n_units && ok; u += unit_step) {
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kc = 0; kc < a.nk; ++kc, ++it) {
         const int s = static_cast<int>(it % NSTAGE);
@@ -161,12 +175,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t alo = tc::smem_desc(base + a_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
             const uint64_t bhi = tc::smem_desc(base + b_off(0, 0) + ko, BOX, 1024, tc::kSwizzle128B);
             const uint64_t blo = tc::smem_desc(base + b_off(1, 0) + ko, BOX, 1024, tc::kSwizzle128B);
-            tc::mma_f16(d_tmem, ahi, bhi, IDESC, (kc | kk) != 0 ? 1u : 0u);
-            tc::mma_f16(d_tmem, ahi, blo, IDESC, 1u);
-            tc::mma_f16(d_tmem, alo, bhi, IDESC, 1u);
+            tc::mma_f16_pair(d_tmem, ahi, bhi, IDESC, (kc | kk) != 0 ? 1u : 0u);
+            tc::mma_f16_pair(d_tmem, ahi, blo, IDESC, 1u);
+            tc::mma_f16_pair(d_tmem, alo, bhi, IDESC, 1u);
           }
-          tc::mma_commit(&empty[s]);
-          if (kc == a.nk - 1) tc::mma_commit(&accfull[acc]);
+          tc::mma_commit_pair(&empty[s], static_cast<uint16_t>(0x3));
+          if (kc == a.nk - 1) tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3));
         }
       }
       if (!ok) break;
@@ -180,11 +194,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* stg = stg_base + (warp - 2) * STG_BYTES;
     int acc = 0;
     uint32_t accphase = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < n_units && ok; u += unit_step) {
       const int mt = u % a.n_mt, nt = u / a.n_mt;
       if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag)) { ok = false; break; }
       tc::fence_after();
-      const int row0 = mt * BM + 32 * q;
+      const int row0 = mt * 2 * BM + crank * BM + 32 * q;
       const int col0 = a.c_begin + nt * BN + half * 128;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN + half * 128);
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&accempty[acc]);
+      if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&accempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) accphase ^= 1u;
     }
@@ -230,16 +244,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       dev_fail(a.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&a.st->timeouts, 1);
     }
+    // let copies and MMAs already in flight land before the CTA's memory goes away
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
   }
   tc::fence_before();
-  __syncthreads();
+  __syncwarp();
+  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
-    tc::tmem_dealloc(tmem_base, 512);
+    tc::tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -296,6 +312,32 @@ LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int 
   return mp;
 }
 
+namespace {
+// co-resident clusters of the kernel on the current device, looked up once per device
+int resident_pairs() {
+  static std::mutex mu;
+  static std::map<int, int> per_dev;
+  int dev = 0;
+  GPTQ_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  int& r = per_dev[dev];
+  const int most = sm_count() / 2;
+  if (r <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * most));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, lazy_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = most;
+    }
+    r = n < most ? n : most;
+  }
+  return r;
+}
+}  // namespace
+
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,
                     DevStatus* st, cudaStream_t s, int max_ctas) {
   if (k <= 0 || c_end <= c_begin || mp.m <= 0) return;
@@ -308,12 +350,14 @@ void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_beg
   a.nk = static_cast<int>(ceil_div(k, BK));
   a.c_begin = c_begin;
   a.c_end = c_end;
-  a.n_mt = static_cast<int>(ceil_div(mp.m, BM));
+  a.n_mt = static_cast<int>(ceil_div(mp.m, 2 * BM));
   a.n_nt = static_cast<int>(ceil_div(c_end - c_begin, BN));
   a.st = st;
   const int units = a.n_mt * a.n_nt;
-  int grid = units < sm_count() ? units : sm_count();
-  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  // one cluster of two CTAs per pair of SMs that can hold one at once
+  int clusters = resident_pairs();
+  if (max_ctas > 0 && clusters > max_ctas / 2) clusters = max_ctas / 2 > 0 ? max_ctas / 2 : 1;
+  const int grid = 2 * (units < clusters ? units : clusters);
   GPTQ_LAUNCH(GPTQ_K_QUANT_LAZY, s, lazy_tc_kernel, grid, THREADS, SMEM_BYTES, mp.ehi, mp.elo,
               mp.uhi, mp.ulo, mp.w, a);
 }
