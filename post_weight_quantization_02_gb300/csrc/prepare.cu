@@ -483,21 +483,41 @@ __global__ void identity_kernel(float* __restrict__ S, int d) {
   if (j < d) S[static_cast<size_t>(i) * d + j] = (i == j) ? 1.0f : 0.0f;
 }
 
-// U[i][j] = X[d-1-i][d-1-j] = Y[d-1-j][d-1-i] for j >= i, 0 below the diagonal; 32x32
-// tiles transposed through shared memory.
-__global__ void reverse_transpose_kernel(const float* __restrict__ Y, int d, float* __restrict__ U) {
-  __shared__ float t[32][33];
-  const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
-  const bool below = j0 + 31 < i0;  // a tile of zeros: nothing to read
-  for (int jj = threadIdx.y; jj < 32; jj += 8) {
-    const int j = j0 + jj, ii = threadIdx.x, i = i0 + ii;
-    t[jj][ii] = (!below && i < d && j < d) ? Y[static_cast<size_t>(d - 1 - j) * d + (d - 1 - i)]
-                                           : 0.0f;
+// U[i][j] = X[d-1-i][d-1-j] = Y[d-1-j][d-1-i] for j >= i, 0 below the diagonal.  64x64
+// tiles transposed through shared memory with 16-byte global accesses (d a multiple of 8,
+// so a 4-float piece is wholly inside the matrix or wholly outside): tile row jj reads
+// Y[d-1-(j0+jj)] at columns d-64-i0 .. d-1-i0, which hold i = i0+63 .. i0 in reverse.
+__global__ void __launch_bounds__(256) reverse_transpose_kernel(const float* __restrict__ Y,
+                                                                int d, float* __restrict__ U) {
+  __shared__ float t[64][65];  // t[j - j0][i - i0]
+  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const bool below = j0 + 63 < i0;  // a tile of zeros: nothing to read
+  if (!below) {
+    const int cbase = d - 64 - i0;
+    for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+      const int jj = e / 16, k = e % 16;
+      const int j = j0 + jj, c = cbase + 4 * k;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < d && c >= 0)
+        v = *reinterpret_cast<const float4*>(Y + static_cast<size_t>(d - 1 - j) * d + c);
+      const int ii = d - 1 - i0 - c;  // the tile column of v.x; v.y .. v.w go down from it
+      if (ii < 64) t[jj][ii] = v.x;
+      if (ii - 1 >= 0 && ii - 1 < 64) t[jj][ii - 1] = v.y;
+      if (ii - 2 >= 0 && ii - 2 < 64) t[jj][ii - 2] = v.z;
+      if (ii - 3 >= 0 && ii - 3 < 64) t[jj][ii - 3] = v.w;
+    }
   }
   __syncthreads();
-  for (int ii = threadIdx.y; ii < 32; ii += 8) {
-    const int i = i0 + ii, jj = threadIdx.x, j = j0 + jj;
-    if (i < d && j < d) U[static_cast<size_t>(i) * d + j] = (j >= i) ? t[jj][ii] : 0.0f;
+  for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+    const int ii = e / 16, k = e % 16;
+    const int i = i0 + ii, j = j0 + 4 * k;
+    if (i >= d || j >= d) continue;
+    float4 v;
+    v.x = (!below && j >= i) ? t[4 * k][ii] : 0.0f;
+    v.y = (!below && j + 1 >= i) ? t[4 * k + 1][ii] : 0.0f;
+    v.z = (!below && j + 2 >= i) ? t[4 * k + 2][ii] : 0.0f;
+    v.w = (!below && j + 3 >= i) ? t[4 * k + 3][ii] : 0.0f;
+    *reinterpret_cast<float4*>(U + static_cast<size_t>(i) * d + j) = v;
   }
 }
 
@@ -697,8 +717,8 @@ void launch_prepare(const float* H, int d, float damp, int actorder, int32_t* pe
   GPTQ_CUDA(cudaEventRecord(ev_fork, sa));
   GPTQ_CUDA(cudaStreamWaitEvent(s, ev_fork, 0));
   {
-    dim3 grid((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
-    GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_transpose_kernel, grid, dim3(32, 8), 0, S, d, U);
+    dim3 grid((unsigned)ceil_div(d, 64), (unsigned)ceil_div(d, 64));
+    GPTQ_LAUNCH(GPTQ_K_PREP_REVERSE, s, reverse_transpose_kernel, grid, 256, 0, S, d, U);
   }
 }
 
