@@ -76,6 +76,7 @@ struct SyrkArgs {
   int splits;
   float* P;      // [splits][d][d]
   DevStatus* st;
+  uint64_t wait_ns;  // limit of each pipeline wait (the exit's drain waits use kWaitLimitNs)
 };
 
 // unit Q of column tile J: row tiles 2 NP Q .. 2 NP Q + 2 NP - 1.  Row tiles past 2J + 1
@@ -109,6 +110,9 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* accempty = accfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [0]: stages this CTA's producer issued; [1] (even CTAs): stages the waiter saw land
+  int* counts = const_cast<int*>(abort_flag) + 1;
+  uint64_t* mma_drain = reinterpret_cast<uint64_t*>(counts + 2);  // the issuer's last commit
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -126,7 +130,9 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
       tc::mbar_init(&accfull[b], 1);
       tc::mbar_init(&accempty[b], 2 * EPI_WARPS);  // the even CTA's: both CTAs' epilogues
     }
+    tc::mbar_init(mma_drain, 1);
     *abort_flag = 0;
+    counts[0] = counts[1] = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmap);
   }
@@ -145,6 +151,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- producer
     int stage = 0;
     uint32_t phase = 0;
+    int issued = 0;
     for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
       const int s = static_cast<int>(u / a.n_units);
       int qq, J;
@@ -154,7 +161,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
       for (int kb = 0; kb < nk; ++kb) {
-        if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         // both CTAs' 32 KB land on the even CTA's barrier
@@ -174,9 +181,11 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
                                   J * BN + 128 * (crank & 1) + 64 * hb, tok,
                                   static_cast<uint16_t>(0x5u << (crank & 1)));
         }
+        ++issued;
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
       }
     }
+    counts[0] = issued;
   } else if ((crank & 1) == 0 && (warp == 1 || warp == WAITER_WARP)) {
     // ---------------------------------------------------------------- MMA issuer and its
     // waiter (even CTA): both walk the same stages, two per hand-off; the waiter's lane 0
@@ -186,6 +195,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t accphase = 0;
+    int seen = 0;  // stages whose copies the waiter saw land
     for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
       const int s = static_cast<int>(u / a.n_units);
       const int64_t t0 = s * a.tok_per_split;
@@ -195,12 +205,15 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
         const int nst = (kb + 1 < nk) ? 2 : 1;
         bool bad = false;
         if (waiter && lane == 0) {
-          if ((kb % CHAIN) == 0) bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag);
-          if (!bad) bad = !tc::mbar_wait(&full[stage], phase, abort_flag);
+          if ((kb % CHAIN) == 0)
+            bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag, a.wait_ns);
+          if (!bad) bad = !tc::mbar_wait(&full[stage], phase, abort_flag, a.wait_ns);
+          if (!bad) ++seen;
           if (!bad && nst == 2) {
             const int s2 = (stage + 1 == NSTAGE) ? 0 : stage + 1;
             bad = !tc::mbar_wait(&full[s2], (stage + 1 == NSTAGE) ? (phase ^ 1u) : phase,
-                                 abort_flag);
+                                 abort_flag, a.wait_ns);
+            if (!bad) ++seen;
           }
         }
         if (tc::handoff_or(kHandoffBarrier, 64, bad)) { ok = false; break; }
@@ -232,6 +245,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
+    if (waiter && lane == 0) counts[1] = seen;
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp % 4;            // TMEM lane quarter this warp may access
@@ -251,7 +265,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 128; ++k) sum[k] = 0.0f;
       for (int ch = 0; ch < nchain; ++ch) {
-        if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag, a.wait_ns)) { ok = false; break; }
         tc::fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                static_cast<uint32_t>(acc * BN + half * 128);
@@ -292,14 +306,62 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
       dev_fail(a.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&a.st->timeouts, 1);
     }
-    // let copies and MMAs already in flight land before the CTA's memory goes away
+  }
+  // Drain, on every exit, so that nothing is in flight when the CTAs' memory goes away.
+  // First the issuer's MMAs: one more commit, which arrives once every earlier MMA of the
+  // pair has completed (read its operands, written TMEM).
+  bool drained = true;
+  if ((crank & 1) == 0 && warp == 1 && lane == 0) {
+    tc::mma_commit_pair(mma_drain, static_cast<uint16_t>(1u << crank));
+    drained = tc::mbar_wait_for(mma_drain, 0, kWaitLimitNs);
+  }
+  tc::fence_before();
+  __syncwarp();
+  tc::cluster_sync();  // every producer has stopped; its count is visible cluster-wide
+  if ((crank & 1) == 0 && threadIdx.x == 0) {
+    // Then the copies: each pair's copies complete on its even CTA's barriers.  Stage k
+    // (of every CTA's common sequence) sits in slot k % NSTAGE; the waiter saw stages
+    // below counts[1] land, and no producer runs more than NSTAGE stages ahead of it, so
+    // each later stage up to the largest count has a slot of its own, whose current phase
+    // is that stage's.  A stage this CTA's producer did not arm is armed here, and the
+    // bytes of every copy that was never issued are counted here, so the phase completes
+    // exactly when the copies that were issued have landed.
+    int cnt[2 * NP];
+    int kmax = counts[1];
+    for (int r = 0; r < 2 * NP; ++r) {
+      cnt[r] = (r == crank) ? counts[0]
+                            : static_cast<int>(tc::ld_shared_cluster_u32(
+                                  tc::mapa_shared(tc::smem_u32(counts), static_cast<uint32_t>(r))));
+      kmax = max(kmax, cnt[r]);
+    }
+    for (int k = counts[1]; k < kmax; ++k) {
+      uint32_t missing = 0;  // bytes of this stage's copies that no producer issued
+      for (int r = 0; r < 2 * NP; ++r) {
+        if (k < cnt[r]) continue;
+        // a CTA of this pair copies its rows and its box of the column half here; a CTA of
+        // the other pair only its multicast box
+        missing += ((r & ~1) == crank) ? static_cast<uint32_t>(NP == 1 ? STAGE_BYTES : A_BYTES + BOX_BYTES)
+                                       : static_cast<uint32_t>(BOX_BYTES);
+      }
+      uint64_t* bar = &full[k % NSTAGE];
+      if (k >= cnt[crank]) tc::mbar_arrive_expect_tx(bar, 2 * STAGE_BYTES);
+      if (missing != 0) tc::mbar_complete_tx(bar, missing);
+      if (!tc::mbar_wait_for(bar, static_cast<uint32_t>(k / NSTAGE) & 1u, kWaitLimitNs))
+        drained = false;
+    }
+  }
+  if (!drained) {
+    // a drain wait ran out (nothing should be left to land): record it, and give whatever
+    // is still in flight time to land before the memory goes away
+    dev_fail(a.st, GPTQ_ERR_TIMEOUT, 1);
+    atomicAdd(&a.st->timeouts, 1);
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
   }
   tc::fence_before();
   __syncwarp();
-  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
+  tc::cluster_sync();  // every pair's copies have landed; no CTA signals another any more
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
@@ -386,6 +448,7 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.splits = splits;
   a.P = P;
   a.st = st;
+  a.wait_ns = hessian_wait_limit_ns();
   if (syrk_pairs_per_cluster(d) == 2) launch_syrk_np<2>(tmap, a, s);
   else launch_syrk_np<1>(tmap, a, s);
 }

@@ -148,6 +148,15 @@ int64_t launch_count() { return g_launches.load(); }
 
 // ------------------------------------------------------------------ device facts
 
+namespace {
+std::atomic<uint64_t> g_hessian_wait_ns{kWaitLimitNs};
+}
+
+uint64_t hessian_wait_limit_ns() { return g_hessian_wait_ns.load(std::memory_order_relaxed); }
+void set_hessian_wait_limit_ns(uint64_t ns) {
+  g_hessian_wait_ns.store(ns == 0 ? kWaitLimitNs : ns, std::memory_order_relaxed);
+}
+
 int sm_count() {
   int dev = 0;
   cuda_check(cudaGetDevice(&dev), "cudaGetDevice");

@@ -62,20 +62,46 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete, polling with the non-blocking
 // test_wait (a suspended try_wait was observed to wake late).  Gives up (returns false)
 // when another role of the CTA raised *abort, or after limit_ns (kWaitLimitNs unless a
-// caller says otherwise).
+// caller says otherwise).  The clock and the flag are read every 256 polls, or on every
+// poll under a limit below a millisecond (so that a tiny limit gives up at the first wait
+// that is not already satisfied).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag,
                                           uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
+  const uint32_t mask = limit_ns < 1000000ull ? 0u : 255u;
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait(a, parity)) return true;
-    if ((it & 255) == 0) {
+    if ((it & mask) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+// The same wait for a drain at a kernel's exit: no abort flag, only the time limit.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_test_wait(a, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Counts `bytes` of the barrier's current phase as arrived, as a copy's completion would.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// A 32-bit load from the shared memory of a CTA of the cluster (a shared::cluster address).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 
 // Hand-off through a hardware named barrier: every thread of the participating warps

@@ -44,3 +44,40 @@ def test_wait_limit_is_checked(lib, cuda_device):
     with pytest.raises(lib.GptqError) as e:
         lib.gptq_check_wait_timeout(2_000_000_000, ws)
     assert e.value.status == lib.GPTQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d,ntok", [(256, 4096), (1024, 20000), (8192, 1024)])
+def test_hessian_timeout_drains_and_context_survives(lib, cuda_device, d, ntok):
+    """The SYRK itself: with a wait limit of 1 ns its pipeline waits run out while copies
+    and matrix operations are in flight; the kernel drains them before it returns (one SM
+    pair per cluster at 256 and 1024, two at 8192 with multicast copies) and the call reports
+    GPTQ_ERR_TIMEOUT.  Then, with the default limit, the same call succeeds and matches
+    the float64 Hessian."""
+    g = torch.Generator().manual_seed(d + ntok)
+    X = (torch.randn(ntok, d, generator=g) * 2.0).bfloat16()
+    Xd = X.to(cuda_device)
+    H = torch.empty(d, d, dtype=torch.float32, device=cuda_device)
+    lib.gptq_set_hessian_wait_limit(1)
+    try:
+        t0 = time.perf_counter()
+        with pytest.raises(lib.GptqError) as e:
+            lib.gptq_hessian_accumulate(H, 0, Xd)
+        assert time.perf_counter() - t0 < 5.0
+    finally:
+        lib.gptq_set_hessian_wait_limit(0)
+    assert e.value.status == lib.GPTQ_ERR_TIMEOUT
+    assert lib.gptq_hessian_accumulate(H, 0, Xd) == ntok
+    torch.cuda.synchronize()
+    Hn = to_np(H)
+    Xn = X.double().numpy()
+    for bi, bj in [(0, 0), (0, d // 128 - 1), (d // 128 - 1, d // 128 - 1)]:
+        r, c = slice(128 * bi, 128 * bi + 128), slice(128 * bj, 128 * bj + 128)
+        ref = (2.0 / ntok) * (Xn[:, r].T @ Xn[:, c])
+        assert rel_fro(Hn[r, c], ref) <= H_REL_FRO
+
+
+def test_hessian_wait_limit_is_checked(lib, cuda_device):
+    with pytest.raises(lib.GptqError) as e:
+        lib.gptq_set_hessian_wait_limit(20_000_000_000)
+    assert e.value.status == lib.GPTQ_ERR_INVALID_ARG
+    lib.gptq_set_hessian_wait_limit(0)
