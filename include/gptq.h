@@ -385,20 +385,22 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
 gptq_status gptq_check_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * gptq_set_hessian_wait_limit -- the time limit of the Hessian SYRK's device waits, for
- * every later call in this process (all threads, all devices).  Not part of the method:
- * a diagnostic that lets a test make the SYRK's pipeline waits run out on purpose.
+ * gptq_set_wait_limit -- the time limit of the tensor-core kernels' device waits (the
+ * Hessian SYRK, the prepare's tf32x3 GEMMs, the lazy update), for every later call in
+ * this process (all threads, all devices).  Not part of the method: a diagnostic that lets
+ * a test make the kernels' pipeline waits run out on purpose.
  *
- * The SYRK's producer, MMA and epilogue waits give up after limit_ns nanoseconds (2 s by
- * default): the kernel records GPTQ_ERR_TIMEOUT in the call's status word and drains
- * before it returns.  The drain waits for every matrix operation and every copy the
- * kernel issued to complete (it does not use this limit), so the device memory and the
- * context stay usable, and the Hessian call reports GPTQ_ERR_TIMEOUT; H is then unset.
+ * A pipeline wait (for a copy, a matrix operation or an accumulator) gives up after
+ * limit_ns nanoseconds (2 s by default); the kernel then records GPTQ_ERR_TIMEOUT in the
+ * call's status word and drains before it returns: it waits for every matrix operation
+ * and every copy it issued to complete (the drain does not use this limit), so the device
+ * memory and the context stay usable, and the call reports GPTQ_ERR_TIMEOUT; its outputs
+ * are then unset.
  *
  * limit_ns  0 restores the default; else 1 .. 1e10.
  * Errors: INVALID_ARG.
  */
-gptq_status gptq_set_hessian_wait_limit(uint64_t limit_ns);
+gptq_status gptq_set_wait_limit(uint64_t limit_ns);
 
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* gptq_last_error(void);

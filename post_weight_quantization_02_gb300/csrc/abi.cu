@@ -649,11 +649,11 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
   });
 }
 
-gptq_status gptq_set_hessian_wait_limit(uint64_t limit_ns) {
+gptq_status gptq_set_wait_limit(uint64_t limit_ns) {
   return guarded([&] {
     require(limit_ns <= 10000000000ull, GPTQ_ERR_INVALID_ARG,
-            "gptq_set_hessian_wait_limit: limit_ns must be 0 (the default) or 1 .. 1e10");
-    set_hessian_wait_limit_ns(limit_ns);
+            "gptq_set_wait_limit: limit_ns must be 0 (the default) or 1 .. 1e10");
+    set_wait_limit_ns(limit_ns);
   });
 }
 

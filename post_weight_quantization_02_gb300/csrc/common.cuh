@@ -153,10 +153,10 @@ void launch_pdl(const char* name, void (*kernel)(P...), dim3 grid, dim3 block, s
 // Number of SMs of the current device.
 int sm_count();
 
-// Limit of the Hessian SYRK's pipeline waits for the launches that follow (process-wide;
-// kWaitLimitNs unless gptq_set_hessian_wait_limit changed it).
-uint64_t hessian_wait_limit_ns();
-void set_hessian_wait_limit_ns(uint64_t ns);
+// Limit of the tensor-core kernels' pipeline waits for the launches that follow
+// (process-wide; kWaitLimitNs unless gptq_set_wait_limit changed it).
+uint64_t wait_limit_ns();
+void set_wait_limit_ns(uint64_t ns);
 
 // Three library-internal streams of the current device (a: highest priority, c: middle,
 // b: lowest) and at least `nevents` timing-free events, created on first use and kept for the life

@@ -66,6 +66,7 @@ struct TcGemmArgs {
   int n_tiles;     // column tiles
   int nq;          // K / 32
   DevStatus* st;
+  uint64_t wait_ns;  // limit of each pipeline wait (the exit's drain waits use kWaitLimitNs)
 };
 
 // TMA of K-quarter ph of the A and B tiles into stage ph % 2
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
   uint8_t* b_lo = a_lo + A_BYTES;
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + 3 * STAGE_BYTES);  // [2]
   uint64_t* bar_mma = bar_load + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  uint64_t* mma_drain = bar_mma + 1;  // the issuer's last commit at the exit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int bi, bj;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     tc::mbar_init(bar_load, 1);
     tc::mbar_init(bar_load + 1, 1);
     tc::mbar_init(bar_mma, 1);
+    tc::mbar_init(mma_drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     griddep_wait();
@@ -155,12 +158,16 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
 #pragma unroll
   for (int i = 0; i < 64; ++i) accr[i] = 0.0f;
 
+  // Every wait's outcome is made CTA-wide (__syncthreads_or) so that all threads leave the
+  // loop at the same point; `landed` counts the quarters whose copies were seen to land and
+  // `mmas_done` the quarters whose MMAs completed (quarters below mmas_done + 2 were loaded).
+  int landed = 0, mmas_done = 0;
   for (int ph = 0; ph < g.nq && ok; ++ph) {
     uint8_t* a_hi = smem + (ph & 1) * STAGE_BYTES;
     uint8_t* b_hi = a_hi + A_BYTES;
-    if (!tc::mbar_wait(bar_load + (ph & 1), (ph >> 1) & 1, abort_flag)) { ok = false; break; }
+    const bool bad_load = !tc::mbar_wait(bar_load + (ph & 1), (ph >> 1) & 1, abort_flag, g.wait_ns);
     // lo = x - trunc_tf32(x), elementwise in the same swizzled layout
-    {
+    if (!bad_load) {
       const float4* src_a = reinterpret_cast<const float4*>(a_hi);
       float4* dst_a = reinterpret_cast<float4*>(a_lo);
       const float4* src_b = reinterpret_cast<const float4*>(b_hi);
@@ -183,7 +190,8 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
     }
     tc::fence_proxy_async_shared();
     tc::fence_before();
-    __syncthreads();
+    if (__syncthreads_or(bad_load)) { ok = false; break; }
+    landed = ph + 1;
     if (tid == 0) {
       tc::fence_after();
       const uint32_t ah = tc::smem_u32(a_hi), al = tc::smem_u32(a_lo);
@@ -214,7 +222,9 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
       }
       tc::mma_commit(bar_mma);
     }
-    if (!tc::mbar_wait(bar_mma, ph & 1, abort_flag)) { ok = false; break; }
+    const bool bad_mma = !tc::mbar_wait(bar_mma, ph & 1, abort_flag, g.wait_ns);
+    if (__syncthreads_or(bad_mma)) { ok = false; break; }
+    mmas_done = ph + 1;
     tc::fence_after();
     // both buffers of this stage are free again: fetch the quarter after next into it
     if (tid == 32 && ph + 2 < g.nq) load_quarter(smem, bar_load, &tma, &tmb, g, i0, j0, ph + 2);
@@ -271,6 +281,27 @@ __global__ void __launch_bounds__(THREADS) gemm_tf32x3_kernel(const __grid_const
       dev_fail(g.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&g.st->timeouts, 1);
     }
+  }
+  // Drain, on every exit, so that nothing is in flight when the CTA's memory goes away:
+  // the MMAs (one more commit, which arrives once every earlier MMA has completed) and the
+  // copies of the quarters loaded but not seen to land (at most two, one per stage; the
+  // slot's previous quarter was seen, so its current phase is this quarter's).
+  bool drained = true;
+  if (tid == 0) {
+    tc::mma_commit(mma_drain);
+    drained = tc::mbar_wait_for(mma_drain, 0, kWaitLimitNs);
+  }
+  if (tid == 32) {
+    const int loaded = min(g.nq, mmas_done + 2);
+    for (int q = landed; q < loaded; ++q)
+      if (!tc::mbar_wait_for(bar_load + (q & 1), static_cast<uint32_t>(q >> 1) & 1u, kWaitLimitNs))
+        drained = false;
+  }
+  if (!drained) {
+    // a drain wait ran out (nothing should be left to land): record it, and give whatever
+    // is still in flight time to land before the memory goes away
+    dev_fail(g.st, GPTQ_ERR_TIMEOUT, 1);
+    atomicAdd(&g.st->timeouts, 1);
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
@@ -344,6 +375,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
   uint64_t* accempty = accfull + 2;                                       // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [0]: quarters this CTA's producer issued; [1] (even CTA): quarters the waiter saw land
+  int* counts = const_cast<int*>(abort_flag) + 1;
+  uint64_t* mma_drain = reinterpret_cast<uint64_t*>(counts + 2);  // the issuer's last commit
 
   // unit: row pair pi (256 rows), column tile bj (256 columns); in lower mode only the
   // units that reach the diagonal or below it (bj <= pi)
@@ -375,7 +409,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
       tc::mbar_init(&accfull[b], 1);
       tc::mbar_init(&accempty[b], 2 * P::WORKERS);  // the even CTA's: both CTAs' workers
     }
+    tc::mbar_init(mma_drain, 1);
     *abort_flag = 0;
+    counts[0] = counts[1] = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
@@ -396,10 +432,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int q = 0; q < nq; ++q) {
+      int q = 0;
+      for (; q < nq; ++q) {
         const int s = q % P::NS;
         const uint32_t ph = static_cast<uint32_t>(q / P::NS) & 1u;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.wait_ns)) { ok = false; break; }
         uint8_t* base = smem + s * P::STAGE;
         const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[s]), 0);
         if (crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * P::STAGE);
@@ -410,10 +447,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
         tc::tma_load_2d_pair(base + 3 * P::PART, &tmb_lo, bar, pa.b_lo_k0 + q * KQ,
                              pa.b_lo_row0 + jb);
       }
+      counts[0] = q;  // the quarters below q were issued
     }
   } else if (crank == 0 && (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------ MMA issuer and waiter
     const bool waiter = (warp == 2);
+    int seen = 0;  // quarters whose copies the waiter saw land
     for (int q = 0; q < nq; ++q) {
       const int s = q % P::NS;
       const uint32_t ph = static_cast<uint32_t>(q / P::NS) & 1u;
@@ -422,8 +461,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
       if (waiter && lane == 0) {
         if (q % CHAIN_Q == 0)
           bad = !tc::mbar_wait(&accempty[acc], (static_cast<uint32_t>(chain >> 1) & 1u) ^ 1u,
-                               abort_flag);
-        if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag);
+                               abort_flag, g.wait_ns);
+        if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag, g.wait_ns);
+        if (!bad) ++seen;
       }
       if (tc::handoff_or(kPsHandoff, 64, bad)) { ok = false; break; }
       if (!waiter && lane == 0) {
@@ -459,6 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
           tc::mma_commit_pair(&accfull[acc], static_cast<uint16_t>(0x3));
       }
     }
+    if (waiter && lane == 0) counts[1] = seen;
   } else if (warp >= 3) {
     // ------------------------------------------------------------ workers
     const int wk = warp - 3;                       // 0 .. WORKERS - 1
@@ -471,7 +512,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
     const int nchain = (nq + CHAIN_Q - 1) / CHAIN_Q;
     for (int chain = 0; chain < nchain; ++chain) {
       const int acc = chain & 1;
-      if (!tc::mbar_wait(&accfull[acc], static_cast<uint32_t>(chain >> 1) & 1u, abort_flag)) {
+      if (!tc::mbar_wait(&accfull[acc], static_cast<uint32_t>(chain >> 1) & 1u, abort_flag,
+                         g.wait_ns)) {
         ok = false;
         break;
       }
@@ -529,14 +571,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PresplitPair::THREAD
       dev_fail(g.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&g.st->timeouts, 1);
     }
-    // let copies and MMAs already in flight land before the CTA's memory goes away
+  }
+  // Drain, on every exit, so that nothing is in flight when the CTAs' memory goes away:
+  // the issuer's MMAs (one more commit, which arrives once every earlier MMA of the pair
+  // has completed), then, once both producers have stopped, the pair's copies.
+  bool drained = true;
+  if (crank == 0 && warp == 1 && lane == 0) {
+    tc::mma_commit_pair(mma_drain, static_cast<uint16_t>(1u));
+    drained = tc::mbar_wait_for(mma_drain, 0, kWaitLimitNs);
+  }
+  tc::fence_before();
+  __syncwarp();
+  tc::cluster_sync();  // both producers have stopped; their counts are visible
+  if (crank == 0 && threadIdx.x == 0) {
+    const int odd = static_cast<int>(
+        tc::ld_shared_cluster_u32(tc::mapa_shared(tc::smem_u32(counts), 1u)));
+    drained = tc::drain_pair_stages(full, P::NS, counts[1], counts[0], odd, P::STAGE);
+  }
+  if (!drained) {
+    // a drain wait ran out (nothing should be left to land): record it, and give whatever
+    // is still in flight time to land before the memory goes away
+    dev_fail(g.st, GPTQ_ERR_TIMEOUT, 1);
+    atomicAdd(&g.st->timeouts, 1);
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
   }
   tc::fence_before();
   __syncwarp();
-  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
+  tc::cluster_sync();  // the pair's copies have landed; neither CTA signals the other any more
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
@@ -597,6 +660,7 @@ void launch_gemm_tf32x3(int kind, const CUtensorMap& ma, int a_row0, int a_k0,
   g.n_tiles = tn;
   g.nq = K / KQ;
   g.st = st;
+  g.wait_ns = wait_limit_ns();
   const unsigned grid = lower ? static_cast<unsigned>(tn * (tn + 1) / 2 + (tm - tn) * tn)
                               : static_cast<unsigned>(tm * tn);
   ensure_dynamic_smem(gemm_tf32x3_kernel, SMEM_BYTES);
@@ -644,6 +708,7 @@ void launch_gemm_tf32x3_presplit(int kind, const CUtensorMap& ma, int a_row0, in
   pa.g.lower = lower ? 1 : 0;
   pa.g.nq = K / KQ;
   pa.g.st = st;
+  pa.g.wait_ns = wait_limit_ns();
   pa.a_lo_row0 = a_lo_row0;
   pa.a_lo_k0 = a_lo_k0;
   pa.b_lo_row0 = b_lo_row0;

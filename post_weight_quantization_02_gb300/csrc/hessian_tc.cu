@@ -448,7 +448,7 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
   a.splits = splits;
   a.P = P;
   a.st = st;
-  a.wait_ns = hessian_wait_limit_ns();
+  a.wait_ns = wait_limit_ns();
   if (syrk_pairs_per_cluster(d) == 2) launch_syrk_np<2>(tmap, a, s);
   else launch_syrk_np<1>(tmap, a, s);
 }

@@ -69,6 +69,7 @@ struct LazyArgs {
   int c_end;       // columns >= c_end are left alone
   int n_mt, n_nt;  // row-tile pairs (256 rows), column tiles
   DevStatus* st;
+  uint64_t wait_ns;  // limit of each pipeline wait (the exit's drain waits use kWaitLimitNs)
 };
 
 // offsets inside a stage of part p (0 hi, 1 lo), box h
@@ -93,6 +94,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* accempty = accfull + 2;                                                // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [0]: stages this CTA's producer issued; [1] (even CTA): stages the waiter saw land
+  int* counts = const_cast<int*>(abort_flag) + 1;
+  uint64_t* mma_drain = reinterpret_cast<uint64_t*>(counts + 2);  // the issuer's last commit
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int crank = static_cast<int>(tc::cluster_ctarank());
@@ -108,7 +112,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc::mbar_init(&accfull[b], 1);
       tc::mbar_init(&accempty[b], 2 * EPI_WARPS);  // the even CTA's: both CTAs' epilogues
     }
+    tc::mbar_init(mma_drain, 1);
     *abort_flag = 0;
+    counts[0] = counts[1] = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
@@ -132,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int kc = 0; kc < a.nk; ++kc, ++it) {
         const int s = static_cast<int>(it % NSTAGE);
         const uint32_t ph = (it / NSTAGE) & 1u;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
         uint8_t* base = smem + s * STAGE;
         const uint32_t bar = tc::mapa_shared(tc::smem_u32(&full[s]), 0);
         if (crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);
@@ -145,6 +151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
+    counts[0] = static_cast<int>(it);  // the stage counter stops at the first one not issued
   } else if (crank == 0 && (warp == 1 || warp == WAITER_WARP)) {
     // ------------------------------------------------------------ MMA issuer and its
     // waiter: both walk the same chunks; the waiter's lane 0 waits, then both warps meet
@@ -153,6 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t it = 0;
     int acc = 0;
     uint32_t accphase = 0;
+    int seen = 0;  // stages whose copies the waiter saw land
     const uint32_t sbase = tc::smem_u32(smem);
     for (int u = unit0; u < n_units && ok; u += unit_step) {
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -161,8 +169,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t ph = (it / NSTAGE) & 1u;
         bool bad = false;
         if (waiter && lane == 0) {
-          if (kc == 0) bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag);
-          if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag);
+          if (kc == 0) bad = !tc::mbar_wait(&accempty[acc], accphase ^ 1u, abort_flag, a.wait_ns);
+          if (!bad) bad = !tc::mbar_wait(&full[s], ph, abort_flag, a.wait_ns);
+          if (!bad) ++seen;
         }
         if (tc::handoff_or(kHandoffBarrier, 64, bad)) { ok = false; break; }
         if (!waiter && lane == 0) {
@@ -187,6 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       acc ^= 1;
       if (acc == 0) accphase ^= 1u;
     }
+    if (waiter && lane == 0) counts[1] = seen;
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int q = warp % 4;             // TMEM lane quarter = tile rows 32q..32q+31
@@ -196,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t accphase = 0;
     for (int u = unit0; u < n_units && ok; u += unit_step) {
       const int mt = u % a.n_mt, nt = u / a.n_mt;
-      if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag)) { ok = false; break; }
+      if (!tc::mbar_wait(&accfull[acc], accphase, abort_flag, a.wait_ns)) { ok = false; break; }
       tc::fence_after();
       const int row0 = mt * 2 * BM + crank * BM + 32 * q;
       const int col0 = a.c_begin + nt * BN + half * 128;
@@ -244,14 +254,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       dev_fail(a.st, GPTQ_ERR_TIMEOUT, 0);
       atomicAdd(&a.st->timeouts, 1);
     }
-    // let copies and MMAs already in flight land before the CTA's memory goes away
+  }
+  // Drain, on every exit, so that nothing is in flight when the CTAs' memory goes away:
+  // the issuer's MMAs (one more commit, which arrives once every earlier MMA of the pair
+  // has completed), then, once both producers have stopped, the pair's copies.
+  bool drained = true;
+  if (crank == 0 && warp == 1 && lane == 0) {
+    tc::mma_commit_pair(mma_drain, static_cast<uint16_t>(1u));
+    drained = tc::mbar_wait_for(mma_drain, 0, kWaitLimitNs);
+  }
+  tc::fence_before();
+  __syncwarp();
+  tc::cluster_sync();  // both producers have stopped; their counts are visible
+  if (crank == 0 && threadIdx.x == 0) {
+    const int odd = static_cast<int>(
+        tc::ld_shared_cluster_u32(tc::mapa_shared(tc::smem_u32(counts), 1u)));
+    drained = tc::drain_pair_stages(full, NSTAGE, counts[1], counts[0], odd, STAGE);
+  }
+  if (!drained) {
+    // a drain wait ran out (nothing should be left to land): record it, and give whatever
+    // is still in flight time to land before the memory goes away
+    dev_fail(a.st, GPTQ_ERR_TIMEOUT, 1);
+    atomicAdd(&a.st->timeouts, 1);
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 200000ull) {
     }
   }
   tc::fence_before();
   __syncwarp();
-  tc::cluster_sync();  // neither CTA exits while the other may still signal or fill it
+  tc::cluster_sync();  // the pair's copies have landed; neither CTA signals the other any more
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
@@ -353,6 +384,7 @@ void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_beg
   a.n_mt = static_cast<int>(ceil_div(mp.m, 2 * BM));
   a.n_nt = static_cast<int>(ceil_div(c_end - c_begin, BN));
   a.st = st;
+  a.wait_ns = wait_limit_ns();
   const int units = a.n_mt * a.n_nt;
   // one cluster of two CTAs per pair of SMs that can hold one at once
   int clusters = resident_pairs();

@@ -149,12 +149,12 @@ int64_t launch_count() { return g_launches.load(); }
 // ------------------------------------------------------------------ device facts
 
 namespace {
-std::atomic<uint64_t> g_hessian_wait_ns{kWaitLimitNs};
+std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};
 }
 
-uint64_t hessian_wait_limit_ns() { return g_hessian_wait_ns.load(std::memory_order_relaxed); }
-void set_hessian_wait_limit_ns(uint64_t ns) {
-  g_hessian_wait_ns.store(ns == 0 ? kWaitLimitNs : ns, std::memory_order_relaxed);
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+void set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kWaitLimitNs : ns, std::memory_order_relaxed);
 }
 
 int sm_count() {

@@ -104,6 +104,31 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
   return v;
 }
 
+// Exit drain of the copies of a pair of CTAs whose copies complete on the even CTA's
+// barriers full[0 .. nstage) (stage k in slot k % nstage), each CTA copying stage_bytes
+// per stage.  Run by one thread of the even CTA once neither producer issues any more:
+// the waiter saw stages below `seen` land; the producers issued the stages below
+// issued_even and issued_odd, never more than nstage ahead of the waiter, so every later
+// stage up to the larger count has a slot of its own whose current phase is that stage's.
+// A stage the even producer did not arm is armed here, and the bytes of a copy that was
+// never issued are counted here, so each phase completes exactly when the copies that
+// were issued have landed.  Returns false if a wait ran out (then something is still in
+// flight).
+__device__ __forceinline__ bool drain_pair_stages(uint64_t* full, int nstage, int seen,
+                                                  int issued_even, int issued_odd,
+                                                  uint32_t stage_bytes) {
+  bool drained = true;
+  const int kmax = max(seen, max(issued_even, issued_odd));
+  for (int k = seen; k < kmax; ++k) {
+    uint64_t* bar = &full[k % nstage];
+    const uint32_t missing = (k >= issued_even ? stage_bytes : 0u) + (k >= issued_odd ? stage_bytes : 0u);
+    if (k >= issued_even) mbar_arrive_expect_tx(bar, 2 * stage_bytes);
+    if (missing != 0) mbar_complete_tx(bar, missing);
+    if (!mbar_wait_for(bar, static_cast<uint32_t>(k / nstage) & 1u, kWaitLimitNs)) drained = false;
+  }
+  return drained;
+}
+
 // Hand-off through a hardware named barrier: every thread of the participating warps
 // executes it once per step; returns whether any of them passed `flag`.  An MMA-issuing
 // warp synchronises with its waiting warp this way because an mbarrier wait executed by

@@ -194,6 +194,6 @@ def test_layer_host_size_and_the_other_additions():
     assert lib.gptq_check_wait_timeout(1000, P + 8, 256, None) == G.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_check_wait_timeout(1000, P, 16, None) == G.GPTQ_ERR_INVALID_ARG
     # the SYRK's wait limit: 0 (the default) or 1 .. 1e10 ns, a host-side setting
-    assert lib.gptq_set_hessian_wait_limit(2 * 10 ** 10) == G.GPTQ_ERR_INVALID_ARG
-    assert lib.gptq_set_hessian_wait_limit(5) == G.GPTQ_OK
-    assert lib.gptq_set_hessian_wait_limit(0) == G.GPTQ_OK
+    assert lib.gptq_set_wait_limit(2 * 10 ** 10) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_set_wait_limit(5) == G.GPTQ_OK
+    assert lib.gptq_set_wait_limit(0) == G.GPTQ_OK

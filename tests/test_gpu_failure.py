@@ -10,7 +10,8 @@ import pytest
 import torch
 
 from oracle import gptq_oracle as O
-from tests.parity import H_REL_FRO, rel_fro, to_np, upper_tile_mask
+from tests.parity import H_REL_FRO, gpu_quantize, rel_fro, to_np, upper_tile_mask
+from workloads import make_permutation, make_upper_factor
 
 pytestmark = pytest.mark.gpu
 
@@ -57,14 +58,14 @@ def test_hessian_timeout_drains_and_context_survives(lib, cuda_device, d, ntok):
     X = (torch.randn(ntok, d, generator=g) * 2.0).bfloat16()
     Xd = X.to(cuda_device)
     H = torch.empty(d, d, dtype=torch.float32, device=cuda_device)
-    lib.gptq_set_hessian_wait_limit(1)
+    lib.gptq_set_wait_limit(1)
     try:
         t0 = time.perf_counter()
         with pytest.raises(lib.GptqError) as e:
             lib.gptq_hessian_accumulate(H, 0, Xd)
         assert time.perf_counter() - t0 < 5.0
     finally:
-        lib.gptq_set_hessian_wait_limit(0)
+        lib.gptq_set_wait_limit(0)
     assert e.value.status == lib.GPTQ_ERR_TIMEOUT
     assert lib.gptq_hessian_accumulate(H, 0, Xd) == ntok
     torch.cuda.synchronize()
@@ -76,8 +77,63 @@ def test_hessian_timeout_drains_and_context_survives(lib, cuda_device, d, ntok):
         assert rel_fro(Hn[r, c], ref) <= H_REL_FRO
 
 
-def test_hessian_wait_limit_is_checked(lib, cuda_device):
+def _prepare(lib, H, dev):
+    d = H.shape[0]
+    perm = torch.empty(d, dtype=torch.int32, device=dev)
+    dead = torch.empty(d, dtype=torch.uint8, device=dev)
+    U = torch.empty(d, d, dtype=torch.float32, device=dev)
+    lib.gptq_prepare(H, 0.01, True, perm, dead, U)
+    torch.cuda.synchronize()
+    return to_np(perm), to_np(U)
+
+
+@pytest.mark.parametrize("d", [1024, 8192])
+def test_prepare_timeout_drains_and_context_survives(lib, cuda_device, d):
+    """The prepare's tf32x3 GEMMs (the K = 128 panel steps on one SM; from 8192 also the
+    paired-SM superpanel updates) with a wait limit of 1 ns: the call reports
+    GPTQ_ERR_TIMEOUT, and with the default limit the same prepare then gives the same
+    permutation and factor, bit for bit, as before the failure."""
+    g = torch.Generator(device=cuda_device).manual_seed(d)
+    X = torch.randn(2 * d, d, generator=g, device=cuda_device) * (
+        1.0 + torch.rand(d, generator=g, device=cuda_device))
+    H = (2.0 / X.shape[0]) * (X.T @ X)
+    perm0, U0 = _prepare(lib, H, cuda_device)
+    lib.gptq_set_wait_limit(1)
+    try:
+        with pytest.raises(lib.GptqError) as e:
+            _prepare(lib, H, cuda_device)
+    finally:
+        lib.gptq_set_wait_limit(0)
+    assert e.value.status == lib.GPTQ_ERR_TIMEOUT
+    perm1, U1 = _prepare(lib, H, cuda_device)
+    assert np.array_equal(perm0, perm1)
+    assert np.array_equal(U0, U1)
+
+
+def test_quantize_timeout_drains_and_context_survives(lib, cuda_device):
+    """The lazy update (paired-SM bf16x3 MMAs) with a wait limit of 1 ns: the quantize
+    reports GPTQ_ERR_TIMEOUT, and with the default limit it then gives the same outputs,
+    bit for bit, as before the failure."""
+    m, d = 512, 2304
+    g = torch.Generator(device=cuda_device).manual_seed(7)
+    W = torch.randn(m, d, generator=g, device=cuda_device) * 0.02
+    U = make_upper_factor(d, 7, cuda_device)
+    perm = make_permutation(d, 7, cuda_device)
+    ref = gpu_quantize(lib, W, U, perm, None, 4, 128, False)
+    lib.gptq_set_wait_limit(1)
+    try:
+        with pytest.raises(lib.GptqError) as e:
+            gpu_quantize(lib, W, U, perm, None, 4, 128, False)
+    finally:
+        lib.gptq_set_wait_limit(0)
+    assert e.value.status == lib.GPTQ_ERR_TIMEOUT
+    again = gpu_quantize(lib, W, U, perm, None, 4, 128, False)
+    for k in ref:
+        assert np.array_equal(ref[k], again[k]), k
+
+
+def test_wait_limit_is_checked_host_side(lib, cuda_device):
     with pytest.raises(lib.GptqError) as e:
-        lib.gptq_set_hessian_wait_limit(20_000_000_000)
+        lib.gptq_set_wait_limit(20_000_000_000)
     assert e.value.status == lib.GPTQ_ERR_INVALID_ARG
-    lib.gptq_set_hessian_wait_limit(0)
+    lib.gptq_set_wait_limit(0)
