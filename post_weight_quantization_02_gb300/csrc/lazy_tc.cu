@@ -121,6 +121,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc::tmem_alloc_pair(tmem_slot, 512);
     tc::tmem_relinquish_pair();
   }
+  // launched as a programmatic dependent of the column loop before it: the set-up above
+  // overlaps its tail, and no global memory is touched before it has completed
+  griddep_launch_dependents();
+  griddep_wait();
   tc::fence_before();
   __syncwarp();
   tc::cluster_sync();  // both CTAs' barriers exist before either copies into them
@@ -390,7 +394,7 @@ void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_beg
   int clusters = resident_pairs();
   if (max_ctas > 0 && clusters > max_ctas / 2) clusters = max_ctas / 2 > 0 ? max_ctas / 2 : 1;
   const int grid = 2 * (units < clusters ? units : clusters);
-  GPTQ_LAUNCH(GPTQ_K_QUANT_LAZY, s, lazy_tc_kernel, grid, THREADS, SMEM_BYTES, mp.ehi, mp.elo,
+  GPTQ_LAUNCH_PDL(GPTQ_K_QUANT_LAZY, s, lazy_tc_kernel, grid, THREADS, SMEM_BYTES, mp.ehi, mp.elo,
               mp.uhi, mp.ulo, mp.w, a);
 }
 

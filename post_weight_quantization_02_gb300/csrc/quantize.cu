@@ -401,6 +401,12 @@ __global__ void __launch_bounds__(LOOP_THREADS) column_loop_kernel(const LoopArg
   __nv_bfloat16* elo_s = ehi_s + BLK * RPC;                                          // [128][RPC]
   float* sz_s = reinterpret_cast<float*>(elo_s + BLK * RPC);  // static: [3][128][RPC], [128]
   const int i1 = a.i1, nb = a.nb;
+  // the lazy update after this kernel is launched as its programmatic dependent: let it
+  // set up while this block's loop runs (it waits for this grid before touching memory).
+  // This kernel itself is an ordinary launch (launched as a dependent, its CTAs would
+  // crowd onto the SMs a small update leaves free), so the wait returns at once.
+  griddep_launch_dependents();
+  griddep_wait();
   {
     const float4* src = reinterpret_cast<const float4*>(a.Ulay + static_cast<size_t>(i1 / BLK) * kUlayFloats);
     float4* dst = reinterpret_cast<float4*>(smem_f);
