@@ -367,6 +367,23 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
                             void* stream);
 
 /*
+ * gptq_scales_fp16 -- the checkpoint's fp16 copy of the group scales.
+ *
+ * The checkpoint format stores the scales as fp16 ("GPTQ Architecture, in depth",
+ * "Packing, tooling and serving"; the bytes of "04 - GPTQ" section 8 count 2 bytes per
+ * scale).  The column loop fits and uses them in float32; this call converts the scales
+ * of gptq_quantize_layer to fp16 with round to nearest, ties to even (overflow to
+ * infinity, underflow to subnormals or zero; a scale of an all-zero group, 1e-8, becomes
+ * 0, which dequantizes that group to zeros as before).
+ *
+ * scales  device float32 [n], in.
+ * out     device binary16 [n] (uint16 bit patterns), out; may not overlap scales.
+ * n       number of scales (G * d_out), >= 0.
+ * Errors: INVALID_ARG (null pointer with n > 0, n < 0), CUDA.
+ */
+gptq_status gptq_scales_fp16(const float* scales, int64_t n, uint16_t* out, void* stream);
+
+/*
  * gptq_check_wait_timeout -- self-check of the library's failure path for device waits.
  *
  * Every wait of the tensor-core kernels on an mbarrier (a copy or a matrix operation that

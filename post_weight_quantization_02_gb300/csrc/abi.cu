@@ -649,6 +649,15 @@ gptq_status gptq_dequantize(const int32_t* qweight, const float* scales, const i
   });
 }
 
+gptq_status gptq_scales_fp16(const float* scales, int64_t n, uint16_t* out, void* stream) {
+  return guarded([&] {
+    require(n >= 0, GPTQ_ERR_INVALID_ARG, "gptq_scales_fp16: n must be >= 0");
+    require(n == 0 || (scales != nullptr && out != nullptr), GPTQ_ERR_INVALID_ARG,
+            "gptq_scales_fp16: null pointer");
+    launch_scales_fp16(scales, n, out, static_cast<cudaStream_t>(stream));
+  });
+}
+
 gptq_status gptq_set_wait_limit(uint64_t limit_ns) {
   return guarded([&] {
     require(limit_ns <= 10000000000ull, GPTQ_ERR_INVALID_ARG,

@@ -119,6 +119,8 @@ LazyMaps make_lazy_maps(const __nv_bfloat16* ehi, const __nv_bfloat16* elo, int 
 // bf16 halves of U (x = hi + lo) on the blocks the lazy updates read: row i, columns from
 // the 128-column block after row i's block on (d a multiple of 8)
 void launch_usplit(const float* U, int d, __nv_bfloat16* hi, __nv_bfloat16* lo, cudaStream_t s);
+// quantize.cu: the checkpoint's fp16 copy of n float32 scales (round to nearest even)
+void launch_scales_fp16(const float* scales, int64_t n, uint16_t* out, cudaStream_t s);
 // W[:, c_begin:c_end] -= ErrT[e_row0 : e_row0 + k]^T U[u_row0 : u_row0 + k, c_begin:c_end];
 // max_ctas > 0 caps the persistent grid (to leave SMs to concurrent work)
 void launch_lazy_tc(const LazyMaps& mp, int e_row0, int u_row0, int k, int c_begin, int c_end,

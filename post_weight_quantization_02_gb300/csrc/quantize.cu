@@ -17,6 +17,7 @@
 // per-block layout of U, zeros [G][m] int32, loss_rows [m] float64 and pos [d] int32
 // (the inverse permutation).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -741,6 +742,31 @@ void launch_quantize(const QuantArgs& q, cudaStream_t s) {
                 q.zeros, m, q.G, q.bits, q.qzeros);
   }
   GPTQ_LAUNCH(GPTQ_K_QUANT_LOSS, s, loss_sum_kernel, 1, 1024, 0, q.loss_rows, m, q.loss);
+}
+
+namespace {
+// The checkpoint's fp16 copy of the scales: round to nearest, ties to even, as a
+// checkpoint writer's float32 -> float16 conversion (overflow to inf, underflow to
+// subnormals or zero).  Four scales per thread.
+__global__ void scales_fp16_kernel(const float* __restrict__ s, int64_t n, __half* __restrict__ h) {
+  const int64_t i = 4 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i + 3 < n && (reinterpret_cast<uintptr_t>(s) % 16) == 0 &&
+      (reinterpret_cast<uintptr_t>(h) % 8) == 0) {
+    const float4 v = *reinterpret_cast<const float4*>(s + i);
+    __align__(8) __half o[4] = {__float2half_rn(v.x), __float2half_rn(v.y),
+                                __float2half_rn(v.z), __float2half_rn(v.w)};
+    *reinterpret_cast<uint2*>(h + i) = *reinterpret_cast<const uint2*>(o);
+  } else {
+    for (int64_t k = i; k < n && k < i + 4; ++k) h[k] = __float2half_rn(s[k]);
+  }
+}
+}  // namespace
+
+void launch_scales_fp16(const float* scales, int64_t n, uint16_t* out, cudaStream_t s) {
+  if (n <= 0) return;
+  const unsigned grid = static_cast<unsigned>((n + 4 * 256 - 1) / (4 * 256));
+  GPTQ_LAUNCH(GPTQ_K_QUANT_PACK, s, scales_fp16_kernel, grid, 256, 0, scales, n,
+              reinterpret_cast<__half*>(out));
 }
 
 }  // namespace gptq

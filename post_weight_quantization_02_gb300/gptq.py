@@ -22,7 +22,7 @@ __all__ = [
     "GPTQ_OP_DEQUANT_MATMUL", "gptq_dequant_matmul", "gptq_dequantize",
     "GptqError", "GptqLibraryError", "lib", "library_path",
     "gptq_workspace_size", "gptq_hessian_accumulate", "gptq_hessian_accumulate_async",
-    "gptq_hessian_status", "gptq_hessian_rescale", "gptq_check_wait_timeout", "gptq_set_wait_limit",
+    "gptq_hessian_status", "gptq_hessian_rescale", "gptq_check_wait_timeout", "gptq_set_wait_limit", "gptq_scales_fp16",
     "gptq_prepare", "gptq_quantize_layer",
     "gptq_last_error", "gptq_status_string", "gptq_abi_version",
     "gptq_profile_enable", "gptq_profile_select", "gptq_profile_read", "gptq_profile_reset",
@@ -68,6 +68,7 @@ _SIGS = {
     "gptq_hessian_rescale": (_c.c_int, [_vp, _i32, _i64, _i64, _vp]),
     "gptq_check_wait_timeout": (_c.c_int, [_c.c_uint64, _vp, _sz, _vp]),
     "gptq_set_wait_limit": (_c.c_int, [_c.c_uint64]),
+    "gptq_scales_fp16": (_c.c_int, [_vp, _i64, _vp, _vp]),
     "gptq_prepare": (_c.c_int, [_vp, _i32, _f32, _c.c_int, _vp, _vp, _vp, _c.POINTER(_i32),
                                 _vp, _sz, _vp]),
     "gptq_quantize_layer": (_c.c_int, [_vp, _c.c_int, _vp, _vp, _vp, _i32, _i32, _c.c_int,
@@ -250,6 +251,19 @@ def gptq_set_wait_limit(limit_ns: int) -> None:
     the default, 2 s).  A diagnostic: with a limit of a few nanoseconds the waits run out,
     the kernel drains what it issued and the call raises GptqError(GPTQ_ERR_TIMEOUT)."""
     _check(lib().gptq_set_wait_limit(int(limit_ns)))
+
+
+def gptq_scales_fp16(scales: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """The checkpoint's fp16 copy of float32 scales (device tensors), rounded to nearest
+    even; returns ``out`` (allocated like ``scales`` when not given)."""
+    if out is None:
+        out = torch.empty(scales.shape, dtype=torch.float16, device=scales.device)
+    n = scales.numel()
+    ps = _buf(scales, torch.float32, n, "scales")
+    po = _buf(out, torch.float16, n, "out")
+    _check(lib().gptq_scales_fp16(ps, n, po, _stream(stream)))
+    return out
 
 
 def gptq_prepare(H: torch.Tensor, damp: float, actorder: bool, perm: torch.Tensor,

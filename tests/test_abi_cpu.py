@@ -193,6 +193,11 @@ def test_layer_host_size_and_the_other_additions():
     assert lib.gptq_check_wait_timeout(2 * 10 ** 9, P, 256, None) == G.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_check_wait_timeout(1000, P + 8, 256, None) == G.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_check_wait_timeout(1000, P, 16, None) == G.GPTQ_ERR_INVALID_ARG
+    # the fp16 scale copy checks its arguments before any launch; n = 0 does nothing
+    assert lib.gptq_scales_fp16(P, -1, P, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_scales_fp16(None, 8, P, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_scales_fp16(P, 8, None, None) == G.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_scales_fp16(None, 0, None, None) == G.GPTQ_OK
     # the SYRK's wait limit: 0 (the default) or 1 .. 1e10 ns, a host-side setting
     assert lib.gptq_set_wait_limit(2 * 10 ** 10) == G.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_set_wait_limit(5) == G.GPTQ_OK

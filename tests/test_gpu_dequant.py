@@ -119,3 +119,26 @@ def test_dequantize_dense(lib, cuda_device, bits, group, static):
     torch.cuda.synchronize()
     assert np.array_equal(to_np(W32), ref.astype(np.float32))
     assert torch.equal(Wbf, torch.from_numpy(ref.astype(np.float32)).to(cuda_device).bfloat16())
+
+
+@pytest.mark.parametrize("n,offset", [(4096, 0), (1001, 0), (1001, 1), (3, 2)])
+def test_scales_fp16_matches_round_to_nearest_even(lib, cuda_device, n, offset):
+    """The checkpoint's fp16 copy of the scales, bit for bit against numpy's float32 ->
+    float16 conversion (round to nearest, ties to even): drawn scales across the fp16
+    range, exact ties, the all-zero group's 1e-8 (to zero), subnormals, overflow to inf;
+    ragged lengths and unaligned starts take the element-wise path."""
+    rng = np.random.default_rng(n + offset)
+    s = (10.0 ** rng.uniform(-9, 5.5, n)).astype(np.float32)
+    special = np.array([1e-8, 6.0e-8, 3.0e-5, 1.0009765625, 1.00048828125, 65504.0, 65520.0,
+                        1e6, 2.0 ** -24, 2.0 ** -25], dtype=np.float32)
+    k = min(n, special.size)
+    s[:k] = special[:k]
+    buf = torch.zeros(n + offset, dtype=torch.float32, device=cuda_device)
+    buf[offset:] = torch.from_numpy(s).to(cuda_device)
+    out = torch.zeros(n + offset, dtype=torch.float16, device=cuda_device)
+    lib.gptq_scales_fp16(buf[offset:], out[offset:])
+    torch.cuda.synchronize()
+    got = out[offset:].cpu().numpy().view(np.uint16)
+    with np.errstate(over="ignore"):  # the overflow to infinity is part of the check
+        ref = s.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
