@@ -94,7 +94,7 @@ struct SplitPlan {
 // Splits of the token axis: enough units to fill the SMs evenly, at least 8 token
 // stages per unit, and no more partials than the workspace holds.
 SplitPlan plan_splits(int64_t ntok, int d, bool tc, int64_t max_splits, int nsm) {
-  const int granule = tc ? syrk_tc_token_granule() : 16;
+  const int granule = tc ? syrk_tc_token_granule(d) : 16;
   const int64_t tiles = tc ? syrk_tc_tiles(d) : syrk_simt_tiles(d);
   const int64_t slots = tc ? nsm : 4LL * nsm;  // the SIMT kernel keeps ~4 CTAs per SM
   int64_t smax = ntok / (8LL * granule);

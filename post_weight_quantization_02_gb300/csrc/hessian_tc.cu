@@ -11,25 +11,25 @@
 // 256) for one token split s: pair p of the cluster computes the 256 x 256 tile of row
 // tiles 2 NP Q + 2p, + 1.  In a pair the even CTA's TMEM holds the first 128 rows and the
 // odd CTA's the next 128; each CTA's shared memory holds its own 128 rows' operand and
-// half of the 256-column operand, so an SM takes in 32 KB of operands per 64-token stage
-// (48 KB for a one-SM 128 x 256 tile).  With NP = 2 both pairs need the same column
-// strip: CTAs 0 and 2 hold its first half, CTAs 1 and 3 its second, and each half is read
-// from L2 once, by two multicast copies of one 64-column box each (a quarter less L2
-// traffic than two separate pairs; under the power cap the clock rises with it).
-//   warp 0      TMA producer (every CTA): its own X rows [64 tokens x 128 columns] and its
+// half of the 256-column operand, so an SM takes in 512 bytes of operands per token (768
+// for a one-SM 128 x 256 tile).  With NP = 2 both pairs need the same column strip: CTAs 0
+// and 2 hold its first half, CTAs 1 and 3 its second, and each half is read from L2 once,
+// by two multicast copies of one 64-column box each (a quarter less L2 traffic than two
+// separate pairs; under the power cap the clock rises with it).
+//   warp 0      TMA producer (every CTA): its own X rows [BK tokens x 128 columns] and its
 //               column half (NP = 2: one box of it, multicast to the same-parity CTA of
-//               the other pair) into a 6-stage ring; completion is counted on the even CTA
-//               of each pair
+//               the other pair) into a 192 KB ring of BK-token stages (Stages below);
+//               completion is counted on the even CTA of each pair
 //   warp 1      TMEM owner (every CTA, paired allocation); in the even CTAs also the MMA
 //               issuer: tcgen05.mma.cta_group::2 256x256x16, both operands MN-major (the
 //               column index of X is contiguous in memory)
 //   warps 2..9  epilogue (every CTA): drain finished TMEM accumulators into float32
 //               registers, then store the CTA's 128 x 256 part of its pair's tile of P[s]
-//   warp 10     in the even CTAs: waits for two stages' data (and, at a chain start, for
+//   warp 10     in the even CTAs: waits for each stage's data (and, at a chain start, for
 //               the accumulator) and releases warp 1 through a named barrier.  The issuing
 //               warp never waits on an mbarrier: such a wait holds it until its
 //               outstanding MMAs have read their operands, which empties the tensor pipe.
-//               Two stages (8 MMAs) per hand-off keep the pipe fed across it.
+//               128 tokens (8 MMAs) per hand-off keep the pipe fed across it.
 // A stage is refilled when every pair's MMAs have consumed it (each pair's commit arrives
 // on every CTA's barrier of the cluster), since a multicast writes into the other pair's
 // ring.  The tensor core's float32 accumulation does not round to nearest, so its error
@@ -52,14 +52,23 @@ namespace {
 
 constexpr int BM = 128;  // rows of H per CTA
 constexpr int BN = 256;  // columns of H per unit (128 in each CTA's shared memory)
-constexpr int BK = 64;   // tokens per stage
-constexpr int NSTAGE = 6;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = (BN / 2) * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int BOX_BYTES = 64 * BK * 2;  // one TMA box: 64 columns x 64 tokens
-constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024 + 256;
-constexpr int CHAIN = 8;            // stages per TMEM accumulation chain (512 tokens), even
+// Stages by pairs per cluster: one pair (narrower layers, short Hessians at full clock,
+// where moving operands into the SMs bounds the kernel) copies 128-token stages, 16 KB
+// per TMA copy (q_proj: 2.55 against 2.81 ms with 64-token stages); two pairs (wide layers
+// under the power cap) keep 64-token stages (128-token ones measured 1-3 % slower per
+// clock there).  The ring holds the same 192 KB either way, and a TMEM accumulation chain
+// covers 512 tokens.
+template <int NP>
+struct Stages {
+  static constexpr int BK = NP == 1 ? 128 : 64;      // tokens per stage
+  static constexpr int NSTAGE = NP == 1 ? 3 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BOX_BYTES = 64 * BK * 2;      // one TMA box: 64 columns x BK tokens
+  static constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + 1024 + 256;
+  static constexpr int CHAIN = 512 / BK;             // stages per TMEM accumulation chain
+};
 constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, 128 columns each
 constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
 constexpr int WAITER_WARP = 2 + EPI_WARPS;
@@ -101,6 +110,10 @@ __device__ __forceinline__ void decode_unit(int unit, int n_i, int n_j, int& Q, 
 template <int NP>
 __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
     syrk_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SyrkArgs a) {
+  constexpr int BK = Stages<NP>::BK, NSTAGE = Stages<NP>::NSTAGE, CHAIN = Stages<NP>::CHAIN;
+  constexpr int A_BYTES = Stages<NP>::A_BYTES, STAGE_BYTES = Stages<NP>::STAGE_BYTES;
+  constexpr int BOX_BYTES = Stages<NP>::BOX_BYTES;
+  constexpr int HS = 128 / BK;  // stages per hand-off
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -188,7 +201,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
     counts[0] = issued;
   } else if ((crank & 1) == 0 && (warp == 1 || warp == WAITER_WARP)) {
     // ---------------------------------------------------------------- MMA issuer and its
-    // waiter (even CTA): both walk the same stages, two per hand-off; the waiter's lane 0
+    // waiter (even CTA): both walk the same stages, 128 tokens per hand-off; the waiter's lane 0
     // waits, then both warps meet at the named barrier, which also carries a failed wait
     const bool waiter = (warp == WAITER_WARP);
     int stage = 0;
@@ -201,8 +214,10 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
       const int64_t t0 = s * a.tok_per_split;
       const int64_t t1 = min(a.ntok, t0 + a.tok_per_split);
       const int nk = static_cast<int>((t1 - t0 + BK - 1) / BK);
-      for (int kb = 0; kb < nk; kb += 2) {
-        const int nst = (kb + 1 < nk) ? 2 : 1;
+      // HS stages (128 tokens, 8 MMAs) per hand-off; the loop keeps the two-stage form's
+      // expressions, which measured faster than a general count
+      for (int kb = 0; kb < nk; kb += HS) {
+        const int nst = (HS == 2 && kb + 1 < nk) ? 2 : 1;
         bool bad = false;
         if (waiter && lane == 0) {
           if ((kb % CHAIN) == 0)
@@ -219,7 +234,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
         if (tc::handoff_or(kHandoffBarrier, 64, bad)) { ok = false; break; }
         for (int q = 0; q < nst; ++q) {
           const int kq = kb + q;
-          const int kc = kq % CHAIN;
+          const int kc = kq % CHAIN;  // position in the accumulation chain
           if (!waiter && lane == 0) {
             tc::fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -228,7 +243,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // 16 tokens = two 8-row core groups of 1024 B; 64-column atoms are one TMA
-              // box (8192 B) apart.
+              // box (BOX_BYTES) apart.
               const uint64_t ad = tc::smem_desc(abase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
               const uint64_t bd = tc::smem_desc(bbase + kk * 2048, BOX_BYTES, 1024, tc::kSwizzle128B);
               tc::mma_f16_pair(d_tmem, ad, bd, IDESC, (kc | kk) != 0 ? 1u : 0u);
@@ -391,7 +406,9 @@ int syrk_tc_tiles(int d) {
   return n;
 }
 
-int syrk_tc_token_granule() { return BK; }
+int syrk_tc_token_granule(int d) {
+  return syrk_pairs_per_cluster(d) == 2 ? Stages<2>::BK : Stages<1>::BK;
+}
 
 namespace {
 template <int NP>
@@ -407,7 +424,7 @@ int resident_clusters() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * NP * most));
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = Stages<NP>::SMEM_BYTES;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, syrk_tc_kernel<NP>, &cfg) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
@@ -420,7 +437,7 @@ int resident_clusters() {
 
 template <int NP>
 void launch_syrk_np(const CUtensorMap& tmap, SyrkArgs a, cudaStream_t s) {
-  ensure_dynamic_smem(syrk_tc_kernel<NP>, SMEM_BYTES);
+  ensure_dynamic_smem(syrk_tc_kernel<NP>, Stages<NP>::SMEM_BYTES);
   a.n_units = syrk_tc_tiles(a.d) / (2 * NP);
   // one cluster of 2 NP CTAs per unit, no more clusters than can be resident at once (a
   // cluster needs 2 NP SMs of one GPC, so that may be fewer than the SMs allow); the
@@ -428,7 +445,8 @@ void launch_syrk_np(const CUtensorMap& tmap, SyrkArgs a, cudaStream_t s) {
   const int64_t units = static_cast<int64_t>(a.n_units) * a.splits;
   const int64_t clusters = resident_clusters<NP>();
   const int grid = 2 * NP * static_cast<int>(units < clusters ? units : clusters);
-  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel<NP>, grid, THREADS, SMEM_BYTES, tmap, a);
+  GPTQ_LAUNCH(GPTQ_K_SYRK_TC, s, syrk_tc_kernel<NP>, grid, THREADS, Stages<NP>::SMEM_BYTES, tmap,
+              a);
 }
 }  // namespace
 
@@ -436,8 +454,8 @@ void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_
                     float* P, DevStatus* st, cudaStream_t s) {
   CUtensorMap tmap;
   make_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(d),
-               static_cast<uint64_t>(ntok), static_cast<uint64_t>(d) * 2, 64, BK,
-               CU_TENSOR_MAP_SWIZZLE_128B);
+               static_cast<uint64_t>(ntok), static_cast<uint64_t>(d) * 2, 64,
+               static_cast<uint32_t>(syrk_tc_token_granule(d)), CU_TENSOR_MAP_SWIZZLE_128B);
   SyrkArgs a;
   a.d = d;
   a.ntok = ntok;

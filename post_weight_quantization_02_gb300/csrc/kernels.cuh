@@ -24,7 +24,7 @@ void launch_wait_timeout(DevStatus* st, uint64_t limit_ns, cudaStream_t s);
 
 // hessian_tc.cu
 int syrk_tc_tiles(int d);
-int syrk_tc_token_granule();
+int syrk_tc_token_granule(int d);  // tokens per pipeline stage at this width
 void launch_syrk_tc(const void* X, int64_t ntok, int d, int splits, int64_t tok_per_split,
                     float* P, DevStatus* st, cudaStream_t s);
 
