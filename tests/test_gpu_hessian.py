@@ -23,10 +23,12 @@ def _accumulate(lib, chunks, d, dev):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("d,ntok", [(256, 128), (296, 1000), (1024, 4160)])
+@pytest.mark.parametrize("d,ntok", [(256, 128), (296, 1000), (1024, 4160), (2056, 6000)])
 def test_hessian_small(lib, cuda_device, dtype, d, ntok):
-    """Ragged column tiles (296) and token tails (1000, 4160) against the f64 oracle: bf16
-    tokens on the tensor-core SYRK, float32 tokens on the float32 FMA kernel."""
+    """Ragged column tiles (296, 2056 = 16 * 128 + 8) and token tails (1000, 4160, 6000)
+    against the f64 oracle: bf16 tokens on the tensor-core SYRK (128-token stages below
+    d_in = 8192; 4160 and 6000 tokens take several token splits, the last one short of a
+    whole stage), float32 tokens on the float32 FMA kernel."""
     g = torch.Generator().manual_seed(d + ntok)
     X = (torch.randn(ntok, d, generator=g) * torch.exp(torch.randn(d, generator=g))).to(dtype)
     H, n = _accumulate(lib, [X], d, cuda_device)
