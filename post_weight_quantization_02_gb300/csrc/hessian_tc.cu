@@ -392,7 +392,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(THREADS, 1)
 // L2 traffic) buys clock (70B-width down_proj: 337 against 350 ms per 524,288 tokens).  A
 // cluster of four needs four SMs of one GPC, which leaves 8 of the 152 SMs idle, so the
 // short Hessians of narrower layers, which run at full clock, keep one pair per cluster
-// (q_proj: 2.74 against 2.83 ms).
+// (q_proj, both with 64-token stages: 2.74 against 2.83 ms).
 static int syrk_pairs_per_cluster(int d) { return d >= 8192 ? 2 : 1; }
 
 int syrk_tc_tiles(int d) {
