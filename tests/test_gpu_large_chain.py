@@ -1,7 +1,8 @@
 """The prepare at the wide layers' full widths, the whole GPU chain at q_proj size, and
 the column loop as Babai's nearest plane, through the C ABI against the float64 oracle.
 
-* Prepare at d_in = 14336 and 28672 on the Hessian of a token sample (the GPU's own
+* Prepare at d_in = 14336 and 28672 (and at 8264, whose last superpanel and panel are
+  ragged) on the Hessian of a token sample (the GPU's own
   Hessian, checked against the oracle): perm bit-exact against the oracle's act-order of
   that Hessian, and rows of U taken across the whole factor (the first, middle and last
   row panels) against the oracle's rows of the factor of the same damped, permuted
@@ -84,6 +85,44 @@ def test_prepare_rows_across_the_factor(lib, cuda_device, name, ntok):
         err = rel_fro(got[k * 64:(k + 1) * 64], ref[k * 64:(k + 1) * 64])
         assert err <= U_REL_FRO, (k, err)
     assert np.all(np.tril(got[:64, :64], -1) == 0.0)
+
+
+@pytest.mark.slow
+def test_prepare_ragged_wide(lib, cuda_device):
+    """A wide layer whose width is a whole number of neither superpanels (1024 columns)
+    nor panels (128): d_in = 8264 = 8 * 1024 + 72, so the last superpanel and the last
+    panel are 72 columns wide.  Perm bit-exact against the oracle's act-order of the
+    GPU's Hessian; rows of U across the factor (the first, a middle one, those around the
+    ragged superpanel's start, the last) against the oracle's rows of the factor of the
+    same damped, permuted Hessian.  16,384 tokens give a full-rank Hessian: with 4096 the
+    first rows of U, which condition on the whole matrix, carry 1.3e-4 of rounding at
+    d_in = 8192 and 8264 alike (the tail rows 1e-7)."""
+    d, ntok, damp = 8264, 16384, 0.01
+    g = torch.Generator().manual_seed(d)
+    X = (torch.randn(ntok, d, generator=g) * torch.exp(0.5 * torch.randn(d, generator=g)))
+    X = X.bfloat16().to(cuda_device)
+    H = torch.empty(d, d, dtype=torch.float32, device=cuda_device)
+    assert lib.gptq_hessian_accumulate(H, 0, X) == ntok
+    del X
+    perm, dead, U = _gpu_prepare(lib, H, damp, cuda_device)
+    Hs = _sym(to_np(H))
+    Hf, dead_ref = O.fix_dead(Hs)
+    perm_np = to_np(perm).astype(np.int64)
+    assert np.array_equal(perm_np, O.act_order(Hf))
+    assert np.array_equal(to_np(dead).astype(bool), dead_ref)
+    Hd, _ = O.damping(Hf[np.ix_(perm_np, perm_np)], damp)
+    del Hf, Hs
+    panels = [np.arange(0, 64), np.arange(4100, 4164), np.arange(8160, 8224),
+              np.arange(d - 64, d)]
+    rows = np.concatenate(panels)
+    assert rows.min() >= 0 and rows.max() < d
+    ref = O.inverse_cholesky_upper_rows(Hd, rows)
+    got = to_np(U[torch.from_numpy(rows).to(cuda_device)])
+    for k, p in enumerate(panels):
+        err = rel_fro(got[k * 64:(k + 1) * 64], ref[k * 64:(k + 1) * 64])
+        assert err <= U_REL_FRO, (k, err)
+    assert np.all(np.tril(got[:64, :64], -1) == 0.0)
+    assert np.all(np.tril(got[-64:, d - 64:], -1) == 0.0)
 
 
 @pytest.mark.slow
