@@ -43,13 +43,19 @@ CASES = [
     (64, 640, 4, 256, False, True),     # groups wider than a block, ragged
     (128, 512, 4, 16, True, True),
     (160, 1024, 4, 128, False, True),   # several blocks and row tiles
+    (64, 2080, 4, 128, False, True),    # three 1024-column superblocks, the last one a
+                                        # ragged block of 32 columns (superblock-end updates)
+    (64, 2304, 4, 384, True, True),     # 384-column groups do not nest in a superblock:
+                                        # every block is its own, fits outside the loop
 ]
 
 
 @pytest.mark.parametrize("m,d,bits,group,sym,actorder", CASES)
 def test_quantize_cases(lib, cuda_device, m, d, bits, group, sym, actorder):
     rng = np.random.default_rng(m * 7 + d + bits)
-    W, U32, perm, dead = _inputs(rng, m, d, actorder=actorder, dead=(5,))
+    # wider layers: a full-rank token sample of d + 256 rows keeps the float64 Hessian cheap
+    n = None if d <= 1024 else d + 256
+    W, U32, perm, dead = _inputs(rng, m, d, n=n, actorder=actorder, dead=(5,))
     rep = _run(lib, cuda_device, W, U32, perm, dead, bits, group, sym)
     assert rep["n_codes"] == m * d
 
@@ -61,6 +67,7 @@ STATIC_CASES = [
     (64, 640, 4, 256, False),       # groups wider than a block, ragged
     (128, 512, 2, 16, False),
     (64, 256, 4, -1, False),        # one group per row: the dynamic mode
+    (64, 2080, 4, 128, False),      # three superblocks, the last a ragged block
 ]
 
 
@@ -68,7 +75,8 @@ STATIC_CASES = [
 def test_quantize_static_groups(lib, cuda_device, m, d, bits, group, sym):
     """Static groups (fixed in the original order before the loop) against the oracle."""
     rng = np.random.default_rng(m * 5 + d + bits + 3)
-    W, U32, perm, dead = _inputs(rng, m, d, actorder=True, dead=(5,))
+    n = None if d <= 1024 else d + 256
+    W, U32, perm, dead = _inputs(rng, m, d, n=n, actorder=True, dead=(5,))
     Wt = torch.from_numpy(W).to(cuda_device)
     gpu = gpu_quantize(lib, Wt, torch.from_numpy(U32).to(cuda_device),
                        torch.from_numpy(perm.astype(np.int32)).to(cuda_device),
