@@ -23,9 +23,10 @@ def _accumulate(lib, chunks, d, dev):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("d,ntok", [(256, 128), (296, 1000), (1024, 4160), (2056, 6000)])
+@pytest.mark.parametrize("d,ntok", [(256, 3), (256, 128), (296, 1000), (1024, 4160),
+                                   (2056, 6000)])
 def test_hessian_small(lib, cuda_device, dtype, d, ntok):
-    """Ragged column tiles (296, 2056 = 16 * 128 + 8) and token tails (1000, 4160, 6000)
+    """Ragged column tiles (296, 2056 = 16 * 128 + 8) and token tails (3, 1000, 4160, 6000)
     against the f64 oracle: bf16 tokens on the tensor-core SYRK (128-token stages below
     d_in = 8192; 4160 and 6000 tokens take several token splits, the last one short of a
     whole stage), float32 tokens on the float32 FMA kernel."""
@@ -39,12 +40,12 @@ def test_hessian_small(lib, cuda_device, dtype, d, ntok):
     assert np.all(np.isfinite(H[mask]))
 
 
-@pytest.mark.parametrize("d,ntok", [(8264, 6000), (8192, 5000)])
+@pytest.mark.parametrize("d,ntok", [(8264, 6000), (8192, 5000), (8192, 7)])
 def test_hessian_wide_clusters(lib, cuda_device, d, ntok):
     """Wide layers (d_in >= 8192) run the SYRK in clusters of two SM pairs that share the
     column strip by multicast: a ragged last row and column tile (8264 = 64 * 128 + 72),
-    the padded units of column tiles with an odd number of row-tile pairs, and two token
-    splits added by the reduction (8192).  Sampled 128-blocks (the first, the last on the
+    the padded units of column tiles with an odd number of row-tile pairs, two token
+    splits added by the reduction (8192, 5000 tokens) and one stage holding 7 tokens.  Sampled 128-blocks (the first, the last on the
     diagonal, blocks of the last column tile and of padded units) against the float64
     Hessian of their columns; the whole diagonal and two quadratic forms against the
     float64 sums."""
